@@ -110,6 +110,7 @@ class Workload:
     norm_topk_prob: int = 1
     group_size: int = 64
     chained: bool = False        # RMSNorm chaining between layers
+    chain_center: bool = True    # the chaining norm removes the row mean first
     seed: int = 0
 
     @property
@@ -151,25 +152,21 @@ def _bf16_bits(v64: torch.Tensor) -> torch.Tensor:
 
 def gen_x(w: Workload, layer: int, tokens: int, attempts: Optional[torch.Tensor] = None,
           device="cpu", token_offset: int = 0) -> torch.Tensor:
-    """Hidden rows x[t] ~ N(0,1) as bf16 [tokens, d].  attempts[t] re-draws row t."""
+    """Hidden rows x[t] ~ N(0,1) as bf16 [tokens, d].  attempts[t] > 0 re-draws row t from
+    another stream (used to pick rows whose router logits are well separated)."""
     d = w.d_model
-    rows = []
     if attempts is None:
-        key = stream_key(w.seed, layer, T_X)
-        idx = _indices(tokens * d, device) + token_offset * d
-        u1 = ((stream_bits(key, 2 * idx) >> 8).to(torch.float64) + 0.5) * (1.0 / 16777216.0)
-        u2 = (stream_bits(key, 2 * idx + 1) >> 8).to(torch.float64) * (1.0 / 16777216.0)
-        z = torch.sqrt(-2.0 * torch.log(u1)) * torch.cos((2.0 * math.pi) * u2)
-        return _bf16_bits(z).reshape(tokens, d)
-    for t in range(tokens):
-        a = int(attempts[t])
-        key = stream_key(w.seed, layer, T_X, 0, a)
-        idx = _indices(d, device) + (token_offset + t) * d
-        u1 = ((stream_bits(key, 2 * idx) >> 8).to(torch.float64) + 0.5) * (1.0 / 16777216.0)
-        u2 = (stream_bits(key, 2 * idx + 1) >> 8).to(torch.float64) * (1.0 / 16777216.0)
-        z = torch.sqrt(-2.0 * torch.log(u1)) * torch.cos((2.0 * math.pi) * u2)
-        rows.append(_bf16_bits(z))
-    return torch.stack(rows, 0)
+        attempts = torch.zeros(tokens, dtype=torch.int64)
+    keys = [stream_key(w.seed, layer, T_X, 0, int(a)) for a in attempts.tolist()]
+    k = torch.tensor(keys, dtype=torch.int64, device=device).unsqueeze(1)
+    k2 = torch.tensor([hash32_int(q ^ 0x27D4EB2F) for q in keys], dtype=torch.int64, device=device).unsqueeze(1)
+    idx = (_indices(tokens, device).unsqueeze(1) + token_offset) * d + _indices(d, device).unsqueeze(0)
+    h1 = hash32(hash32(((2 * idx) + k) & MASK32) ^ k2)
+    h2 = hash32(hash32(((2 * idx + 1) + k) & MASK32) ^ k2)
+    u1 = ((h1 >> 8).to(torch.float64) + 0.5) * (1.0 / 16777216.0)
+    u2 = (h2 >> 8).to(torch.float64) * (1.0 / 16777216.0)
+    z = torch.sqrt(-2.0 * torch.log(u1)) * torch.cos((2.0 * math.pi) * u2)
+    return _bf16_bits(z)
 
 
 def gen_gate(w: Workload, layer: int, device="cpu") -> torch.Tensor:

@@ -210,12 +210,13 @@ def moe_layer(layer: Layer, x_bf16, idx, w64, residual, mode: str = "layer", thr
     return out, out64, ys
 
 
-def rmsnorm_bf16(h, eps: float = 1e-6) -> np.ndarray:
-    """bf16 bits (uint16) of h / sqrt(mean(h^2) + eps), computed in double."""
+def rmsnorm_bf16(h, eps: float = 1e-6, center: bool = False) -> np.ndarray:
+    """bf16 bits (uint16) of (h - c) / sqrt(mean((h - c)^2) + eps), c = row mean if center else 0,
+    computed in double."""
     h = _np(h, np.float32)
     B, d = h.shape
     out = np.empty((B, d), np.uint16)
-    rc = lib().oracle_rmsnorm_bf16(_ptr(h), B, d, ctypes.c_double(eps), _ptr(out))
+    rc = lib().oracle_rmsnorm_bf16(_ptr(h), B, d, ctypes.c_double(eps), int(bool(center)), _ptr(out))
     if rc:
         raise ValueError(f"oracle_rmsnorm_bf16 rc={rc}")
     return out
@@ -243,6 +244,6 @@ def _setup_signatures(L):
                                      [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_int32])
     L.oracle_rmsnorm_bf16.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
-                                      ctypes.c_void_p]
+                                      ctypes.c_int32, ctypes.c_void_p]
     L.oracle_to_bf16.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
 

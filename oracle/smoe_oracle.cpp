@@ -341,18 +341,25 @@ int oracle_moe_combine(const Desc* D, const Weights* W, const uint16_t* x, int32
     return 0;
 }
 
-// x_out[t] = bf16( h[t] / sqrt(mean_i h[t][i]^2 + eps) )  (unit norm weight), double inside.
-int oracle_rmsnorm_bf16(const float* h, int32_t B, int32_t d, double eps, uint16_t* x_out) {
+// x_out[t] = bf16( (h[t] - c) / sqrt(mean_i (h[t][i] - c)^2 + eps) ), unit norm weight,
+// c = row mean when center != 0 else 0; double inside.
+int oracle_rmsnorm_bf16(const float* h, int32_t B, int32_t d, double eps, int32_t center, uint16_t* x_out) {
     if (!h || !x_out || B < 0 || d <= 0) return 1;
     for (int32_t t = 0; t < B; ++t) {
+        const float* row = h + static_cast<int64_t>(t) * d;
+        double c = 0.0;
+        if (center) {
+            for (int32_t i = 0; i < d; ++i) c += row[i];
+            c /= d;
+        }
         double ss = 0.0;
         for (int32_t i = 0; i < d; ++i) {
-            double v = h[static_cast<int64_t>(t) * d + i];
+            double v = row[i] - c;
             ss += v * v;
         }
         double inv = 1.0 / std::sqrt(ss / d + eps);
         for (int32_t i = 0; i < d; ++i)
-            x_out[static_cast<int64_t>(t) * d + i] = double_to_bf16(h[static_cast<int64_t>(t) * d + i] * inv);
+            x_out[static_cast<int64_t>(t) * d + i] = double_to_bf16((row[i] - c) * inv);
     }
     return 0;
 }

@@ -365,6 +365,19 @@ def test_rmsnorm_closed_forms():
     assert x[2].tolist() == [0x3F35] * 4
 
 
+def test_centred_rmsnorm_closed_form():
+    """Centring removes the row mean first: [5,3,5,3] -> [1,-1,1,-1]; [2,2,2,10] -> mean 4,
+    deviations [-2,-2,-2,6], RMS sqrt(12): -1/sqrt(3) = -0.57735 lies between the bf16 values
+    -0.57421875 (0xBF13) and -0.578125 (0xBF14), nearer the latter; sqrt(3) = 1.73205 between
+    1.7265625 (0x3FDD) and 1.734375 (0x3FDE), nearer the latter."""
+    h = np.array([[5.0, 3.0, 5.0, 3.0], [2.0, 2.0, 2.0, 10.0]], np.float32)
+    x = oracle.rmsnorm_bf16(h, 1e-9, center=True)
+    assert x[0].tolist() == [0x3F80, 0xBF80, 0x3F80, 0xBF80]
+    assert x[1].tolist() == [0xBF14, 0xBF14, 0xBF14, 0x3FDE]
+    # without centring the same rows keep their offset
+    assert oracle.rmsnorm_bf16(h, 1e-9)[0].tolist() != x[0].tolist()
+
+
 def test_oracle_row_subset_matches_full():
     w, x, layer, idx, w64, res = _toy_case()
     full = oracle.moe_layer(layer, x, idx, w64, res)[1]
