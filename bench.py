@@ -1,0 +1,359 @@
+"""Benchmark of the per-layer MoE block (route -> union -> 4-bit SwiGLU experts -> combine).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
+
+A step is one pass of the whole hot path over one batch: for every layer of the workload's
+stack, RMSNorm glue (chained stacks), exact routing, the expert union, the expert FFN and
+the weighted combine, all through libsmoe's C ABI.  Inputs are seeded and synthetic (the
+workload generator), resident in HBM when the timed region starts; the expert weights of a
+stack are far larger than L2, so no flush is needed between steps.
+
+The JSON line reports MoE-layer tokens/s (token-layers per second) for the whole job, the
+union-expert bytes/s, the roofline of the expert FFN step, the end-to-end figure through
+host buffers, and the CPU oracle timed on a bounded sample (`cpu_baseline`).
+`--impl reference` times the oracle alone on the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s and union-expert GB/s at 1 GB300; % of roofline"
+UNIT = "token-layers/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.idx = gpu_index
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(gpu_index), "-lms", "200"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in out.splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(smax), "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _traffic_from_profile(kernel_src: str):
+    """DRAM bytes per FFN-step launch recorded in the committed ncu summary, if the kernel
+    source is unchanged since the capture (sha256 of csrc/ffn.cu must match)."""
+    path = os.path.join(ROOT, "profiles", "expert_ffn_prefill64.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"ffn\.cu sha256:\s*([0-9a-f]{64})", text)
+    m_b = re.search(r"dram bytes per smoe_moe_ffn_batch launch:\s*([0-9]+)", text)
+    if not m_sha or not m_b:
+        return None
+    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    return int(m_b.group(1)) if sha == m_sha.group(1) else None
+
+
+# ------------------------------------------------------------------------------ oracle timing
+def oracle_sample(w, layer, x, gate, bias, wts_cpu, rows, threads=0):
+    """Time the oracle (layer-major, all host cores) on `rows` of one layer: (seconds, cores)."""
+    import oracle
+    lay = oracle.Layer.from_workload(w, wts_cpu)
+    t0 = time.perf_counter()
+    idx, w64, _, _ = oracle.route(x[rows], gate, bias, w.top_k, w.norm_topk_prob)
+    xs = x[rows]
+    oracle.moe_layer(lay, xs, idx, w64, xs.float(), threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, (threads if threads > 0 else oracle.hardware_threads())
+
+
+def _sample_rows(w, budget_s: float = 15.0):
+    """Rows of one layer the oracle finishes in about budget_s on the host (rough model)."""
+    macs_per_token = 3 * w.d_model * w.ffn_dim * w.top_k
+    return max(1, min(w.tokens, int(budget_s * 2.0e9 / macs_per_token)))
+
+
+def run_reference(args, w):
+    import torch
+    from moe_expert_routing_gb300 import workload as W
+
+    gdev = "cuda" if torch.cuda.is_available() else "cpu"
+    n = _sample_rows(w, budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
+    rows = list(range(n))
+    gate = W.gen_gate(w, 0)
+    bias = W.gen_gate_bias(w, 0)
+    x = W.gen_x(w, 0, w.tokens)
+    wts = {k: v.cpu() for k, v in W.gen_layer_weights(w, 0, device=gdev).items()}
+    for _ in range(args.warmup):
+        oracle_sample(w, 0, x, gate, bias, wts, rows)
+    times, cores = [], 0
+    for _ in range(args.steps):
+        dt, cores = oracle_sample(w, 0, x, gate, bias, wts, rows)
+        times.append(dt)
+    t = sum(times) / len(times)
+    value = n / t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.tokens, "layers": w.layers, "sample_tokens": n},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"layer 0, first {n} of {w.tokens} tokens, layer-major oracle (fp64)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------ GPU arm
+def run_gpu(args, w, world, rank, local):
+    import torch
+    import torch.distributed as dist
+    from moe_expert_routing_gb300 import smoe
+    from moe_expert_routing_gb300 import workload as W
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    smoe.load_library()
+    B, L, K, E, d, F = w.tokens, w.layers, w.top_k, w.num_experts, w.d_model, w.ffn_dim
+    desc = smoe.make_desc(d, E, K, F, w.layout, w.norm_topk_prob)
+
+    layers = []
+    for l in range(L):
+        wts = W.gen_layer_weights(w, l, device=dev)
+        bias = W.gen_gate_bias(w, l)
+        layers.append({
+            "weights": smoe.Weights(wts), "wts": wts, "gate": W.gen_gate(w, l, device=dev).contiguous(),
+            "bias": None if bias is None else bias.to(dev),
+            "uid": torch.zeros(E, dtype=torch.int32, device=dev), "nu": torch.zeros(1, dtype=torch.int32, device=dev),
+            "off": torch.zeros(E + 1, dtype=torch.int32, device=dev),
+            "tl": torch.zeros(B * K, dtype=torch.int32, device=dev),
+            "sl": torch.zeros(B * K, dtype=torch.int32, device=dev),
+        })
+    x_in = W.gen_x(w, 0, B, device=dev).view(torch.int16).contiguous()
+    ws = smoe.alloc_workspace(desc, B, dev)
+    h = torch.empty(B, d, dtype=torch.float32, device=dev)
+    xb = torch.empty(B, d, dtype=torch.int16, device=dev)
+    idx = torch.empty(B, K, dtype=torch.int32, device=dev)
+    wt = torch.empty(B, K, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    launches_per_layer = (1 if w.chained else 0) + 2 + 1 + 4
+
+    def step(x_dev, ev=None):
+        h.copy_(x_dev.view(torch.bfloat16))
+        for l, ly in enumerate(layers):
+            if w.chained:
+                smoe.smoe_rmsnorm_bf16(h, xb, 1e-6, center=int(w.chain_center))
+                xl = xb
+            else:
+                xl = x_dev
+            smoe.smoe_route(desc, xl, ly["gate"], ly["bias"], idx, wt, ws)
+            smoe.smoe_expert_union(desc, idx, ly["uid"], ly["nu"], ly["off"], ly["tl"], ly["sl"], ws)
+            if ev is not None:
+                ev[l][0].record(stream)
+            smoe.smoe_moe_ffn_batch(desc, ly["weights"], xl, ly["uid"], ly["nu"], ly["off"], ly["tl"], ly["sl"], wt,
+                                    h, ws)
+            if ev is not None:
+                ev[l][1].record(stream)
+
+    smoe.smoe_clear_device_status(ws)
+    for _ in range(max(3, args.warmup)):
+        step(x_in)
+    bits = smoe.smoe_read_device_status(ws)
+    if bits:
+        raise RuntimeError(f"device status {bits:#x} during warm-up")
+
+    # ---- timed region: inputs resident in HBM
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(L)]
+           for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = Clocks(local) if rank == 0 else None
+    time.sleep(0.3 if clocks else 0.0)
+    t_start.record(stream)
+    for s in range(args.steps):
+        step(x_in, evs[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    if world > 1:
+        dist.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    ffn_ms = [evs[s][l][0].elapsed_time(evs[s][l][1]) for s in range(args.steps) for l in range(L)]
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    bits = smoe.smoe_read_device_status(ws)
+    if bits:
+        raise RuntimeError(f"device status {bits:#x} in the timed region")
+
+    # ---- algorithmic work (measured union sizes)
+    U = [int(ly["nu"].item()) for ly in layers]
+    eb = w.expert_bytes
+    hbm, tf_burst, tf_sus, peak_kind = _peaks()
+    ffn_bytes = [u * eb + B * d * 2 + 2 * B * d * 4 for u in U]
+    layer_bytes = [fb + E * d * 4 for fb in ffn_bytes]
+    layer_flops = 6 * B * K * d * F + 2 * B * d * E
+    t_roof_step = sum(max(bb / (hbm * 1e9), layer_flops / (tf_sus * 1e12)) for bb in layer_bytes)
+    ffn_ms_mean = sum(ffn_ms) / len(ffn_ms)
+    ffn_bytes_mean = sum(ffn_bytes) / len(ffn_bytes)
+    achieved = ffn_bytes_mean / (ffn_ms_mean * 1e-3) / 1e9
+    value = world * B * L / (ms_step * 1e-3)
+    union_gbs = world * sum(U) * eb / (ms_step * 1e-3) / 1e9
+
+    # ---- end to end through host buffers: pinned H2D of x, D2H of the final hidden state
+    x_host = x_in.cpu().pin_memory()
+    out_host = torch.empty(B, d, dtype=torch.float32).pin_memory()
+    x_dev2 = torch.empty_like(x_in)
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(2):
+        x_dev2.copy_(x_host, non_blocking=True)
+        step(x_dev2)
+        out_host.copy_(h, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 10))
+    e_s.record(stream)
+    for _ in range(e2e_steps):
+        x_dev2.copy_(x_host, non_blocking=True)
+        step(x_dev2)
+        out_host.copy_(h, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    e_e.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_s.elapsed_time(e_e) / e2e_steps
+    e2e_value = world * B * L / (e2e_ms * 1e-3)
+
+    if rank != 0:
+        return
+    # ---- CPU oracle on a bounded sample of the same workload (host cores, rank 0, N=1 only)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        n = _sample_rows(w)
+        ly = layers[0]
+        wts_cpu = {k: v.cpu() for k, v in ly["wts"].items()}
+        xs = (x_in.view(torch.bfloat16) if not w.chained else None)
+        if xs is None:   # chained stacks: layer 0 consumes RMSNorm(x); use the device's own glue output
+            h.copy_(x_in.view(torch.bfloat16))
+            smoe.smoe_rmsnorm_bf16(h, xb, 1e-6, center=int(w.chain_center))
+            xs = xb.view(torch.bfloat16)
+        xs = xs.cpu()
+        dt, cores = oracle_sample(w, 0, xs, ly["gate"].cpu(), None if ly["bias"] is None else ly["bias"].cpu(),
+                                  wts_cpu, list(range(n)))
+        cpu = {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"layer 0, first {n} of {B} tokens ({n} token-layers), layer-major fp64 oracle, "
+                         f"{dt:.1f} s"}
+    traffic = _traffic_from_profile(os.path.join(ROOT, "moe_expert_routing_gb300", "csrc", "ffn.cu"))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": B, "layers": L, "d_model": d, "experts": E, "top_k": K,
+                   "ffn_dim": F, "layout": w.layout, "weights": "4-bit affine g64, bf16 scales/biases",
+                   "l2": f"inputs larger than L2: {L * E * eb / 1e9:.1f} GB of expert weights per step",
+                   "parallelism": f"replicas x{world}"},
+        "union_expert_gbs": union_gbs,
+        "union_sizes": U,
+        "step_roofline_frac": t_roof_step / (ms_step * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": traffic,
+                     "kernel": "expert FFN step (smoe_moe_ffn_batch: gather, gate/up+SwiGLU, down, combine)",
+                     "peak_kind": f"{peak_kind} copy bandwidth"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": B * d * 2, "d2h_bytes_per_step": B * d * 4},
+        "gpu_launches": launches_per_layer * L * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="prefill64")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="profiling only: run the first N layers of the stack")
+    args = ap.parse_args()
+    from moe_expert_routing_gb300 import workload as W
+    w = W.WORKLOADS[args.workload]
+    if args.layers:
+        w = W.scaled(w, layers=args.layers)
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        run_gpu(args, w, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * smoe.h -- C ABI of libsmoe, the GB300 (sm_103a) per-layer MoE block.
+ *
+ * One MoE layer of exact-routing, layer-major batched prefill and decode, in four steps:
+ *   1. route   router gate matvec on each token's hidden state, softmax, top-k and
+ *              norm_topk_prob re-normalisation
+ *              (page "Layer-Major Batched Prefill", "Choreography Per Chunk" step 5;
+ *               page "Surface Scout", "The Model Config": norm_topk_prob)
+ *   2. union   the chunk's routed experts deduplicated into a union, with a per-expert
+ *              token list        (page "Layer-Major Batched Prefill", "The Inversion")
+ *   3. FFN     each union expert applied once to all of its tokens:
+ *              y = down(silu(gate(x)) * up(x)) on 4-bit affine, group-64 weights
+ *              (page "SSD Streaming Expert Layers", "Math Contract" and "Quantized Layout";
+ *               "Layer-Major Batched Prefill", "Choreography Per Chunk" step 6)
+ *   4. combine residual[t] += sum_k w[t][k] * y_{idx[t][k]}(x[t])
+ *              (page "Data Flow", "Serial Step Trace", FFN block: outputs x routing
+ *               weights into the residual)
+ *
+ * Conventions for every call
+ *   - All data pointers are DEVICE pointers unless stated otherwise; the caller owns every
+ *     buffer, including the workspace.  The library never allocates or frees memory and
+ *     keeps no state between calls other than per-device attributes it caches once.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *     Nothing is read back to the host: counts such as the union size stay on the device.
+ *     Only smoe_read_device_status synchronises.
+ *   - Argument errors are found on the host before anything is launched: the call returns
+ *     an error status and enqueues nothing.  Faults found on the device (an expert index
+ *     outside [0, E), an fp16 overflow of the SwiGLU activation) set bits in the status word
+ *     kept at the start of the workspace; the kernels then skip the bad work and return,
+ *     they never trap.  smoe_read_device_status reports them.
+ *   - bf16 values are passed as uint16_t bit patterns.
+ *   - Supported shapes: group_size 64; d_model and ffn_dim multiples of 256; 1 <= top_k
+ *     <= 16; top_k <= num_experts <= 256.  Weight, scale, bias, x and residual pointers
+ *     16-byte aligned.  Other shapes return SMOE_ERR_UNSUPPORTED.
+ */
+#ifndef SMOE_H
+#define SMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SMOE_API __attribute__((visibility("default")))
+#else
+#define SMOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SMOE_OK = 0,
+    SMOE_ERR_INVALID_ARG = 1,   /* NULL pointer, negative size, inconsistent descriptor   */
+    SMOE_ERR_UNSUPPORTED = 2,   /* shape or alignment outside what the kernels support   */
+    SMOE_ERR_WORKSPACE = 3,     /* workspace NULL, misaligned or smaller than required   */
+    SMOE_ERR_CUDA = 4,          /* a CUDA runtime call failed (launch or synchronise)    */
+    SMOE_ERR_DEVICE_FAULT = 5   /* the device status word has a fault bit set           */
+} smoe_status;
+
+typedef enum {
+    SMOE_LAYOUT_SEPARATE = 0,       /* up, gate, down as three tensors                  */
+    SMOE_LAYOUT_FUSED_GATE_UP = 1   /* gate_up [E, 2F, d/8]: per expert, gate rows
+                                       0..F-1 on top, up rows F..2F-1 below ("Math
+                                       Contract", fused gate+up; "Why Whole-Layer Loading
+                                       Is Also Fast": per-expert interleave)             */
+} smoe_layout;
+
+/* Device status bits (smoe_read_device_status). */
+#define SMOE_FAULT_EXPERT_INDEX 0x1u  /* a routed expert id outside [0, num_experts)      */
+#define SMOE_FAULT_FP16_RANGE   0x2u  /* |silu(g) * v| exceeded the fp16 range           */
+#define SMOE_FAULT_TIMEOUT      0x4u  /* a bounded wait for an async weight copy gave up   */
+#define SMOE_FAULT_TOKEN_INDEX  0x8u  /* a token list entry outside [0, B)                 */
+
+/* Layer descriptor: the subset of the model config the MoE block needs
+ * (page "Surface Scout", "The Model Config": d_model, ffn_dim, max_experts_per_layer,
+ * norm_topk_prob).  top_k is the number of routed experts per token. */
+typedef struct {
+    int32_t d_model;
+    int32_t num_experts;
+    int32_t top_k;
+    int32_t ffn_dim;
+    int32_t group_size;      /* must be 64 */
+    int32_t norm_topk_prob;  /* 1: top-k weights re-normalised to sum 1; 0: full softmax p */
+    int32_t layout;          /* smoe_layout */
+} smoe_layer_desc;
+
+/* Expert weights of one layer ("SSD Streaming Expert Layers", "Quantized Layout"):
+ *   packed words u32 [E, out, in/8], element i of a row = bits 4*(i%8).. of word i/8
+ *   scales, biases bf16 [E, out, in/64];  weight = scale * q + bias
+ * up/gate: out = ffn_dim, in = d_model;  down: out = d_model, in = ffn_dim.
+ * SEPARATE layout uses w_up/w_gate (+ scales, biases) and leaves the gate_up fields NULL;
+ * FUSED_GATE_UP uses w_gate_up/s_gate_up/b_gate_up [E, 2*ffn_dim, ...] and leaves the
+ * up/gate fields NULL.  The down fields are always used.  Device pointers, read only. */
+typedef struct {
+    const uint32_t* w_up;      const uint16_t* s_up;      const uint16_t* b_up;
+    const uint32_t* w_gate;    const uint16_t* s_gate;    const uint16_t* b_gate;
+    const uint32_t* w_gate_up; const uint16_t* s_gate_up; const uint16_t* b_gate_up;
+    const uint32_t* w_down;    const uint16_t* s_down;    const uint16_t* b_down;
+} smoe_expert_weights;
+
+/* Bytes of device workspace the calls below need for up to `max_tokens` tokens per call
+ * (0 on an invalid descriptor).  The workspace must be 256-byte aligned.  Its first 256
+ * bytes hold the device status word; the caller clears it with smoe_clear_device_status
+ * once after allocation (and after reading a fault). */
+SMOE_API size_t smoe_workspace_bytes(const smoe_layer_desc* desc, int32_t max_tokens);
+
+/* Step 1, exact routing.
+ *   x        bf16 [B, d_model], row-major: the tokens' hidden states
+ *   gate_w   fp32 [num_experts, d_model], row-major: router gate
+ *   gate_bias fp32 [num_experts] added to the logits, or NULL
+ *   topk_idx int32 [B, top_k] out: experts by descending probability, equal
+ *            probabilities ordered by the lower expert id
+ *   topk_w   fp32 [B, top_k] out: routing weights (softmax of the logits; with
+ *            norm_topk_prob, divided by the sum over the selected experts)
+ * Logits accumulate in fp32.  B == 0 is a no-op. */
+SMOE_API smoe_status smoe_route(const smoe_layer_desc* desc, const uint16_t* x, const float* gate_w,
+                       const float* gate_bias, int32_t B, int32_t* topk_idx, float* topk_w,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Step 2, the expert union of a chunk.
+ *   topk_idx   int32 [B, top_k] in
+ *   union_ids  int32 [num_experts] out: ascending routed expert ids, first n_union valid
+ *   n_union    int32 [1] out
+ *   offsets    int32 [num_experts + 1] out: entries offsets[u]..offsets[u+1]-1 of
+ *              token_list/slot_list belong to union_ids[u]; offsets[n_union] = B*top_k
+ *   token_list int32 [B*top_k] out: token rows, ascending within each expert
+ *   slot_list  int32 [B*top_k] out: rank k of that expert in the token's top-k
+ * An id outside [0, num_experts) sets SMOE_FAULT_EXPERT_INDEX and n_union = 0. */
+SMOE_API smoe_status smoe_expert_union(const smoe_layer_desc* desc, const int32_t* topk_idx, int32_t B,
+                              int32_t* union_ids, int32_t* n_union, int32_t* offsets,
+                              int32_t* token_list, int32_t* slot_list,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Steps 3 + 4: every union expert applied once to its token list, outputs weighted by
+ * topk_w and added to the residual in rank order k = 0..top_k-1.
+ *   x         bf16 [B, d_model] (the same rows that were routed)
+ *   union ... slot_list: as produced by smoe_expert_union
+ *   topk_w    fp32 [B, top_k]
+ *   residual  fp32 [B, d_model], updated in place
+ * Dequantised weights, x and the SwiGLU activation are fp16 on the tensor cores with fp32
+ * accumulation. */
+SMOE_API smoe_status smoe_moe_ffn_batch(const smoe_layer_desc* desc, const smoe_expert_weights* weights,
+                               const uint16_t* x, int32_t B, const int32_t* union_ids,
+                               const int32_t* n_union, const int32_t* offsets,
+                               const int32_t* token_list, const int32_t* slot_list,
+                               const float* topk_w, float* residual,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* The whole MoE block (steps 1-4) for B tokens: residual += MoE(x).
+ * topk_idx / topk_w may be NULL (the routing then lives in the workspace only) or device
+ * buffers [B, top_k] that receive it. */
+SMOE_API smoe_status smoe_moe_layer(const smoe_layer_desc* desc, const smoe_expert_weights* weights,
+                           const uint16_t* x, const float* gate_w, const float* gate_bias,
+                           int32_t B, float* residual, int32_t* topk_idx, float* topk_w,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Chaining glue between stacked layers (page "Data Flow", "Serial Step Trace": RMS norm
+ * before the FFN block), unit norm weight:
+ *   c = center ? mean_i h[t][i] : 0
+ *   x_out[t][i] = bf16( (h[t][i] - c) / sqrt(mean_i (h[t][i] - c)^2 + eps) )
+ *   h fp32 [B, d], x_out bf16 [B, d].  fp32 arithmetic, bf16 round to nearest even.
+ * center = 0 is the pages' RMS norm; center = 1 first removes the row mean (used to chain
+ * synthetic layers whose weights are not zero-mean, see the design notes). */
+SMOE_API smoe_status smoe_rmsnorm_bf16(const float* h, float eps, int32_t center, int32_t B, int32_t d,
+                                       uint16_t* x_out, void* stream);
+
+/* Zero the device status word (asynchronous). */
+SMOE_API smoe_status smoe_clear_device_status(void* workspace, void* stream);
+
+/* Synchronise `stream` and read the device status word.  SMOE_OK if it is zero, else
+ * SMOE_ERR_DEVICE_FAULT with the bits stored to *bits_out (may be NULL). */
+SMOE_API smoe_status smoe_read_device_status(void* workspace, void* stream, uint32_t* bits_out);
+
+/* Static description of a status code. */
+SMOE_API const char* smoe_status_string(smoe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SMOE_H */

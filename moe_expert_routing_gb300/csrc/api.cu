@@ -1,0 +1,261 @@
+// libsmoe C ABI: argument validation, workspace layout and the kernel sequence of a layer.
+// Declarations and the contract of every call are in include/smoe.h.
+#include "smoe_internal.cuh"
+
+#include <cudaTypedefs.h>
+#include <stddef.h>
+
+namespace smoe {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Descriptor checks shared by every call.  INVALID_ARG for values that make no sense,
+// UNSUPPORTED for sensible shapes the kernels do not handle.
+smoe_status check_desc(const smoe_layer_desc* D) {
+    if (!D) return SMOE_ERR_INVALID_ARG;
+    if (D->d_model <= 0 || D->num_experts <= 0 || D->top_k <= 0 || D->ffn_dim <= 0 || D->group_size <= 0)
+        return SMOE_ERR_INVALID_ARG;
+    if (D->top_k > D->num_experts) return SMOE_ERR_INVALID_ARG;
+    if (D->layout != SMOE_LAYOUT_SEPARATE && D->layout != SMOE_LAYOUT_FUSED_GATE_UP) return SMOE_ERR_INVALID_ARG;
+    if (D->norm_topk_prob != 0 && D->norm_topk_prob != 1) return SMOE_ERR_INVALID_ARG;
+    if (D->group_size != kGroup) return SMOE_ERR_UNSUPPORTED;
+    if (D->d_model % 256 || D->ffn_dim % 256) return SMOE_ERR_UNSUPPORTED;
+    if (D->num_experts > kMaxExperts || D->top_k > kMaxTopK) return SMOE_ERR_UNSUPPORTED;
+    if ((int64_t)D->d_model * D->ffn_dim > (int64_t)1 << 30) return SMOE_ERR_UNSUPPORTED;
+    return SMOE_OK;
+}
+
+smoe_status check_ws(const smoe_layer_desc& D, int B, void* ws, size_t ws_bytes, WsLayout* L) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return SMOE_ERR_WORKSPACE;
+    *L = ws_layout(D, B);
+    if (ws_bytes < L->total) return SMOE_ERR_WORKSPACE;
+    return SMOE_OK;
+}
+
+// 2-D u32 view [rows, in/8] of a packed weight tensor; box 32 words (4 groups) x box_rows,
+// 128-byte swizzle.
+bool encode_weight_map(CUtensorMap* map, const uint32_t* words, int64_t rows, int64_t in, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)(in / 8), (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(in / 2)};
+    cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(words), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+smoe_status check_weights(const smoe_layer_desc& D, const smoe_expert_weights* W, FfnPointers* P) {
+    if (!W) return SMOE_ERR_INVALID_ARG;
+    const int64_t F = D.ffn_dim, d = D.d_model, E = D.num_experts;
+    const bool sep = D.layout == SMOE_LAYOUT_SEPARATE;
+    // pointers and alignment first: nothing touches CUDA before the arguments are known good
+    if (!W->w_down || !W->s_down || !W->b_down) return SMOE_ERR_INVALID_ARG;
+    if (sep && (!W->w_up || !W->s_up || !W->b_up || !W->w_gate || !W->s_gate || !W->b_gate))
+        return SMOE_ERR_INVALID_ARG;
+    if (!sep && (!W->w_gate_up || !W->s_gate_up || !W->b_gate_up)) return SMOE_ERR_INVALID_ARG;
+    if (!aligned16(W->w_down) || !aligned16(W->s_down) || !aligned16(W->b_down)) return SMOE_ERR_UNSUPPORTED;
+    if (sep && (!aligned16(W->w_up) || !aligned16(W->s_up) || !aligned16(W->b_up) || !aligned16(W->w_gate) ||
+                !aligned16(W->s_gate) || !aligned16(W->b_gate)))
+        return SMOE_ERR_UNSUPPORTED;
+    if (!sep && (!aligned16(W->w_gate_up) || !aligned16(W->s_gate_up) || !aligned16(W->b_gate_up)))
+        return SMOE_ERR_UNSUPPORTED;
+    P->sd = W->s_down; P->bd = W->b_down;
+    if (sep) {
+        P->sg = W->s_gate; P->bg = W->b_gate; P->g_rows_per_expert = F;
+        P->su = W->s_up;   P->bu = W->b_up;   P->u_rows_per_expert = F; P->u_row_offset = 0;
+    } else {
+        // per expert 2F rows: gate rows 0..F-1, up rows F..2F-1
+        P->sg = W->s_gate_up; P->bg = W->b_gate_up; P->g_rows_per_expert = 2 * F;
+        P->su = W->s_gate_up; P->bu = W->b_gate_up; P->u_rows_per_expert = 2 * F; P->u_row_offset = F;
+    }
+    if (!encode_weight_map(&P->map_down, W->w_down, E * d, F, 256)) return SMOE_ERR_CUDA;
+    if (sep) {
+        if (!encode_weight_map(&P->map_gate, W->w_gate, E * F, d, 128)) return SMOE_ERR_CUDA;
+        if (!encode_weight_map(&P->map_up, W->w_up, E * F, d, 128)) return SMOE_ERR_CUDA;
+    } else {
+        if (!encode_weight_map(&P->map_gate, W->w_gate_up, E * 2 * F, d, 128)) return SMOE_ERR_CUDA;
+        P->map_up = P->map_gate;
+    }
+    return SMOE_OK;
+}
+
+smoe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SMOE_OK : SMOE_ERR_CUDA; }
+
+}  // namespace
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+WsLayout ws_layout(const smoe_layer_desc& D, int max_tokens) {
+    const size_t B = max_tokens > 0 ? (size_t)max_tokens : 1, E = D.num_experts, K = D.top_k;
+    const size_t d = D.d_model, F = D.ffn_dim, BK = B * K;
+    // max over b <= B of splits(b) * b; splits(b) is constant between multiples of 16
+    size_t max_split_rows = 0;
+    for (size_t b = 16; b < B + 16; b += 16) {
+        const size_t bb = b < B ? b : B;
+        const size_t v = (size_t)route_splits((int)bb, (int)E, (int)d) * bb;
+        if (v > max_split_rows) max_split_rows = v;
+    }
+    WsLayout L{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
+    L.status = take(4);
+    L.logits = take(max_split_rows * E * 4);
+    L.topk_idx = take(BK * 4);
+    L.topk_w = take(BK * 4);
+    L.union_ids = take(E * 4);
+    L.n_union = take(4);
+    L.offsets = take((E + 1) * 4);
+    L.token_list = take(BK * 4);
+    L.slot_list = take(BK * 4);
+    L.xg = take(BK * d * 2);
+    L.sx = take(BK * (d / kGroup) * 4);
+    L.h = take(BK * F * 2);
+    L.sh = take(BK * (F / kGroup) * 4);
+    L.y = take(BK * d * 4);
+    L.total = o;
+    return L;
+}
+
+}  // namespace smoe
+
+using namespace smoe;
+
+extern "C" {
+
+size_t smoe_workspace_bytes(const smoe_layer_desc* desc, int32_t max_tokens) {
+    if (check_desc(desc) != SMOE_OK || max_tokens < 0) return 0;
+    return ws_layout(*desc, max_tokens).total;
+}
+
+smoe_status smoe_route(const smoe_layer_desc* desc, const uint16_t* x, const float* gate_w, const float* gate_bias,
+                       int32_t B, int32_t* topk_idx, float* topk_w, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+    smoe_status st = check_desc(desc);
+    if (st != SMOE_OK) return st;
+    if (B < 0) return SMOE_ERR_INVALID_ARG;
+    if (B == 0) return SMOE_OK;
+    if (!x || !gate_w || !topk_idx || !topk_w) return SMOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(gate_w)) return SMOE_ERR_UNSUPPORTED;
+    WsLayout L;
+    if ((st = check_ws(*desc, B, workspace, workspace_bytes, &L)) != SMOE_OK) return st;
+    return cuda_status(launch_route(*desc, x, gate_w, gate_bias, B, topk_idx, topk_w,
+                                    ws_ptr<float>(workspace, L.logits), static_cast<cudaStream_t>(stream)));
+}
+
+smoe_status smoe_expert_union(const smoe_layer_desc* desc, const int32_t* topk_idx, int32_t B, int32_t* union_ids,
+                              int32_t* n_union, int32_t* offsets, int32_t* token_list, int32_t* slot_list,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+    smoe_status st = check_desc(desc);
+    if (st != SMOE_OK) return st;
+    if (B < 0) return SMOE_ERR_INVALID_ARG;
+    if (!topk_idx || !union_ids || !n_union || !offsets || !token_list || !slot_list) return SMOE_ERR_INVALID_ARG;
+    WsLayout L;
+    if ((st = check_ws(*desc, B, workspace, workspace_bytes, &L)) != SMOE_OK) return st;
+    return cuda_status(launch_union(*desc, topk_idx, B, union_ids, n_union, offsets, token_list, slot_list,
+                                    ws_ptr<uint32_t>(workspace, L.status), static_cast<cudaStream_t>(stream)));
+}
+
+smoe_status smoe_moe_ffn_batch(const smoe_layer_desc* desc, const smoe_expert_weights* weights, const uint16_t* x,
+                               int32_t B, const int32_t* union_ids, const int32_t* n_union, const int32_t* offsets,
+                               const int32_t* token_list, const int32_t* slot_list, const float* topk_w,
+                               float* residual, void* workspace, size_t workspace_bytes, void* stream) {
+    smoe_status st = check_desc(desc);
+    if (st != SMOE_OK) return st;
+    if (B < 0) return SMOE_ERR_INVALID_ARG;
+    if (B == 0) return SMOE_OK;
+    if (!x || !union_ids || !n_union || !offsets || !token_list || !slot_list || !topk_w || !residual)
+        return SMOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(residual)) return SMOE_ERR_UNSUPPORTED;
+    FfnPointers P{};
+    if ((st = check_weights(*desc, weights, &P)) != SMOE_OK) return st;
+    WsLayout L;
+    if ((st = check_ws(*desc, B, workspace, workspace_bytes, &L)) != SMOE_OK) return st;
+    return cuda_status(launch_ffn(*desc, P, x, B, union_ids, n_union, offsets, token_list, slot_list, topk_w,
+                                  residual, workspace, L, static_cast<cudaStream_t>(stream)));
+}
+
+smoe_status smoe_moe_layer(const smoe_layer_desc* desc, const smoe_expert_weights* weights, const uint16_t* x,
+                           const float* gate_w, const float* gate_bias, int32_t B, float* residual,
+                           int32_t* topk_idx, float* topk_w, void* workspace, size_t workspace_bytes, void* stream) {
+    smoe_status st = check_desc(desc);
+    if (st != SMOE_OK) return st;
+    if (B < 0) return SMOE_ERR_INVALID_ARG;
+    if (B == 0) return SMOE_OK;
+    if (!x || !gate_w || !residual) return SMOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(gate_w) || !aligned16(residual)) return SMOE_ERR_UNSUPPORTED;
+    FfnPointers P{};
+    if ((st = check_weights(*desc, weights, &P)) != SMOE_OK) return st;
+    WsLayout L;
+    if ((st = check_ws(*desc, B, workspace, workspace_bytes, &L)) != SMOE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t* idx = topk_idx ? topk_idx : ws_ptr<int32_t>(workspace, L.topk_idx);
+    float* w = topk_w ? topk_w : ws_ptr<float>(workspace, L.topk_w);
+    int32_t* uid = ws_ptr<int32_t>(workspace, L.union_ids);
+    int32_t* nu = ws_ptr<int32_t>(workspace, L.n_union);
+    int32_t* off = ws_ptr<int32_t>(workspace, L.offsets);
+    int32_t* tl = ws_ptr<int32_t>(workspace, L.token_list);
+    int32_t* sl = ws_ptr<int32_t>(workspace, L.slot_list);
+    cudaError_t e = launch_route(*desc, x, gate_w, gate_bias, B, idx, w, ws_ptr<float>(workspace, L.logits), s);
+    if (e == cudaSuccess)
+        e = launch_union(*desc, idx, B, uid, nu, off, tl, sl, ws_ptr<uint32_t>(workspace, L.status), s);
+    if (e == cudaSuccess) e = launch_ffn(*desc, P, x, B, uid, nu, off, tl, sl, w, residual, workspace, L, s);
+    return cuda_status(e);
+}
+
+smoe_status smoe_rmsnorm_bf16(const float* h, float eps, int32_t center, int32_t B, int32_t d, uint16_t* x_out,
+                              void* stream) {
+    if (B < 0 || d <= 0 || !(eps >= 0.f) || (center != 0 && center != 1)) return SMOE_ERR_INVALID_ARG;
+    if (B == 0) return SMOE_OK;
+    if (!h || !x_out) return SMOE_ERR_INVALID_ARG;
+    if (d % 4 || !aligned16(h) || (reinterpret_cast<uintptr_t>(x_out) & 7u)) return SMOE_ERR_UNSUPPORTED;
+    return cuda_status(launch_rmsnorm(h, eps, center, B, d, x_out, static_cast<cudaStream_t>(stream)));
+}
+
+smoe_status smoe_clear_device_status(void* workspace, void* stream) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1))) return SMOE_ERR_WORKSPACE;
+    return cuda_status(cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)));
+}
+
+smoe_status smoe_read_device_status(void* workspace, void* stream, uint32_t* bits_out) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1))) return SMOE_ERR_WORKSPACE;
+    uint32_t bits = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&bits, workspace, sizeof(bits), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SMOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SMOE_ERR_CUDA;
+    if (bits_out) *bits_out = bits;
+    return bits ? SMOE_ERR_DEVICE_FAULT : SMOE_OK;
+}
+
+const char* smoe_status_string(smoe_status status) {
+    switch (status) {
+        case SMOE_OK: return "ok";
+        case SMOE_ERR_INVALID_ARG: return "invalid argument";
+        case SMOE_ERR_UNSUPPORTED: return "unsupported shape or alignment";
+        case SMOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case SMOE_ERR_CUDA: return "CUDA runtime error";
+        case SMOE_ERR_DEVICE_FAULT: return "device reported a fault (see status bits)";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,629 @@
+// Steps 3 + 4: each union expert applied once to its token list, then the weighted combine.
+//
+// Page "SSD Streaming Expert Layers", "Math Contract": y = down(silu(gate(x)) * up(x));
+// "Quantized Layout": packed u32 [E, out, in/8] 4-bit affine weights, bf16 scales and
+// biases per group of 64 inputs.  Page "Layer-Major Batched Prefill", "Choreography Per
+// Chunk" step 6: a two-pass token-batch dispatch per claimed expert (gate/up, then down),
+// one dequantisation stream for all of the expert's tokens.  Page "Data Flow", "Serial
+// Step Trace": expert outputs times routing weights are added into the residual.
+//
+// Kernels (all on one stream, no host synchronisation; union size and counts are read
+// on the device):
+//   gather_kernel      x rows of every (expert, token) entry -> fp16, pair-permuted,
+//                      with per-64-group sums (xg, sx)
+//   ffn_pass_kernel<0> gate/up projections + SwiGLU, 128 h columns of one expert per tile;
+//                      writes h (fp16, pair-permuted) and its per-group sums
+//   ffn_pass_kernel<1> down projection, 256 output rows of one expert per tile; writes y
+//   combine_kernel     residual[t] += sum_k w[t][k] * y[t*K + k], k in rank order
+//
+// The pass kernels are persistent and warp-specialised: one producer warp streams, for
+// every tile and every 256-input k-slice, the packed weight rows, the activation rows and
+// their group sums into a 4-stage shared-memory ring with TMA (128-byte swizzle); eight
+// consumer warps decode and multiply.  Full/empty mbarriers hand the stages back and forth,
+// so the weight stream never drains between tiles.
+//
+// Tensor-core use in the bandwidth-bound regime.  With a handful of tokens per expert the
+// work is a stream of 4-bit weights that must be decoded faster than HBM delivers them;
+// FFMA dot products would cost ~5 issue slots per weight.  Instead each consumer warp turns
+// nibbles straight into A-fragment registers of mma.sync.m16n8k16 and lets the tensor core
+// do the multiply-adds:
+//   * a u32 word holds nibbles n0..n7; (w >> 4j) & 0x000F000F | 0x64006400 is the fp16
+//     pair (1024 + n_j, 1024 + n_{j+4}), exact, in one or two instructions.
+//   * the mma contraction order is free, so the k axis is permuted: within every 8 inputs
+//     the activations are stored as (x0,x4,x1,x5,x2,x6,x3,x7), which makes each decoded
+//     pair line up with one B-fragment register.
+//   * each mma covers 16 inputs of ONE group, so the affine map and the 1024 offset are
+//     applied after the mma, in fp32:
+//       sum_i (s q_i + b) x_i = s * C + (b - 1024 s) * S,  C = sum_i (1024 + q_i) x_i,
+//       S = sum_i x_i (the group sums travel with the activations);
+//     weights are never rounded to fp16.
+#include "smoe_internal.cuh"
+
+#include <cuda.h>
+#include <math.h>
+
+#include <algorithm>
+#include <atomic>
+
+namespace smoe {
+namespace {
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// fp16 pair (1024 + q_j, 1024 + q_{j+4}) of the nibbles of w, exact.
+template <int J>
+__device__ __forceinline__ uint32_t nib_pair(uint32_t w) {
+    return ((w >> (4 * J)) & 0x000F000Fu) | 0x64006400u;
+}
+
+__device__ __forceinline__ uint2 ldg_u2h(const uint16_t* p) {
+    return __ldg(reinterpret_cast<const uint2*>(p));
+}
+
+// storage slot of logical element m (0..7) inside an 8-element chunk: (0,4,1,5,2,6,3,7)
+__device__ __forceinline__ int perm8(int m) { return 2 * (m & 3) + (m >> 2); }
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Bounded wait on an mbarrier phase: true when the phase completed, false after ~0.5 s.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((i & 1023) == 0) {
+            uint64_t now;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+            if (i == 0) t0 = now;
+            else if (now - t0 > 500000000ull) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ uint2 lds_u2(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint4 lds_u4(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ float lds_f(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];\n" : "=f"(v) : "r"(a));
+    return v;
+}
+
+// ----------------------------------------------------------------------------- gather
+// One thread per 8-element chunk of a list entry p: xg[p] = pair-permuted fp16(x[token_list[p]]),
+// sx[p][g] = sum of the fp16 values of group g (8 consecutive lanes hold one group).
+__global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ x, int d, int B,
+                                                     const int32_t* __restrict__ n_union,
+                                                     const int32_t* __restrict__ offsets,
+                                                     const int32_t* __restrict__ token_list,
+                                                     uint32_t* __restrict__ status,
+                                                     __half* __restrict__ xg, float* __restrict__ sx) {
+    const int cpr = d / 8;   // chunks per row, a multiple of 32: a warp never spans two rows
+    const size_t gid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int p = (int)(gid / cpr), ch = (int)(gid - (size_t)p * cpr);
+    const int lane = threadIdx.x & 31;
+    const int total = offsets[*n_union];
+    if (p >= total) return;
+    int t = token_list[p];
+    if (t < 0 || t >= B) {   // a caller-supplied list that does not match B: flag, use row 0
+        if (lane == 0) atomicOr(status, SMOE_FAULT_TOKEN_INDEX);
+        t = 0;
+    }
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d) + ch);
+    const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+    __half hv[8];
+    float s = 0.f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const float v = bf16_bits_to_float((m & 1) ? (wv[m >> 1] >> 16) : (wv[m >> 1] & 0xFFFFu));
+        const __half h = __float2half_rn(v);
+        hv[perm8(m)] = h;
+        s += __half2float(h);
+    }
+    uint4 o;
+    o.x = (uint32_t)__half_as_ushort(hv[0]) | ((uint32_t)__half_as_ushort(hv[1]) << 16);
+    o.y = (uint32_t)__half_as_ushort(hv[2]) | ((uint32_t)__half_as_ushort(hv[3]) << 16);
+    o.z = (uint32_t)__half_as_ushort(hv[4]) | ((uint32_t)__half_as_ushort(hv[5]) << 16);
+    o.w = (uint32_t)__half_as_ushort(hv[6]) | ((uint32_t)__half_as_ushort(hv[7]) << 16);
+    reinterpret_cast<uint4*>(xg + (size_t)p * d)[ch] = o;
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    s += __shfl_xor_sync(0xffffffffu, s, 4);
+    if ((lane & 7) == 0) sx[(size_t)p * (d / kGroup) + ch / 8] = s;
+}
+
+// ----------------------------------------------------------------------------- expert passes
+constexpr int kConsumerWarps = 8;
+constexpr int kPassThreads = 32 * (kConsumerWarps + 1);   // + one producer warp
+constexpr int kStages = 4;
+constexpr int kWBytes = 256 * 128;         // 256 weight rows x 32 u32 words (4 groups)
+constexpr int kXBoxBytes = 16 * 128;       // 16 activation rows x 64 fp16 (one group)
+constexpr int kXOff = kWBytes;
+constexpr int kSOff = kWBytes + 4 * kXBoxBytes;
+constexpr int kSBytes = 16 * 16;           // 16 rows x 4 group sums (fp32)
+constexpr int kStageBytes = kSOff + 1024;  // keeps every stage 1024-byte aligned
+constexpr int kStageTx = kWBytes + 4 * kXBoxBytes + kSBytes;
+constexpr int kPassSmem = kStages * kStageBytes + 1024;
+constexpr int kTokChunk = 16;              // tokens per pass over the weights
+
+struct PassArgs {
+    int64_t wrow0;        // pass 0: gate rows per expert in map_w0; pass 1: d
+    int64_t wrow1;        // pass 0: up rows per expert in map_w1
+    int64_t woff1;        // pass 0: first up row inside an expert block (0 or F)
+    const uint16_t* s0; const uint16_t* b0;   // scales/biases of map_w0 rows
+    const uint16_t* s1; const uint16_t* b1;   // scales/biases of map_w1 rows
+    int kdim;             // contraction length (d for pass 0, F for pass 1)
+    int F, d, K, E, B;
+    int tiles_per_expert;
+    const int32_t* union_ids; const int32_t* n_union; const int32_t* offsets;
+    const int32_t* token_list; const int32_t* slot_list;
+    __half* h_out; float* hsum_out;   // pass 0 outputs
+    float* y_out;                     // pass 1 output [B*K, d]
+    uint32_t* status;
+};
+
+struct Tile {
+    bool ok;
+    int e, p0, p1, row;   // row: first h column (pass 0) or output row (pass 1) of the tile
+};
+
+__device__ __forceinline__ Tile decode_tile(const PassArgs& a, int t, int pass_rows) {
+    Tile T;
+    const int u = t / a.tiles_per_expert;
+    T.row = (t - u * a.tiles_per_expert) * pass_rows;
+    T.e = a.union_ids[u];
+    T.p0 = a.offsets[u];
+    T.p1 = a.offsets[u + 1];
+    T.ok = T.e >= 0 && T.e < a.E && T.p0 >= 0 && T.p1 >= T.p0 && T.p1 <= a.B * a.K;
+    return T;
+}
+
+// One 256-input k-slice (4 groups) of a consumer warp: two 16-row m-tiles against NT
+// 8-token n-tiles.  wb0/wb1: shared addresses of the m-tiles' first rows; xs: the 4
+// activation boxes; ss: the group-sum box; sc/bi: 4 bf16 scales/biases of rows g, g+8
+// of each m-tile.
+template <int NT>
+__device__ __forceinline__ void consume_stage(float (&acc)[2][NT][4], uint32_t wb0, uint32_t wb1, uint32_t xs,
+                                              uint32_t ss, const uint2 (&sc)[4], const uint2 (&bi)[4], int g, int c) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t bf[NT][8];
+        float sx0[NT], sx1[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int r = nt * 8 + g;
+            const uint32_t rb = xs + q * kXBoxBytes + r * 128;
+            const uint4 v0 = lds_u4(rb + (((2 * c) ^ g) << 4));
+            const uint4 v1 = lds_u4(rb + (((2 * c + 1) ^ g) << 4));
+            bf[nt][0] = v0.x; bf[nt][1] = v0.y; bf[nt][2] = v0.z; bf[nt][3] = v0.w;
+            bf[nt][4] = v1.x; bf[nt][5] = v1.y; bf[nt][6] = v1.z; bf[nt][7] = v1.w;
+            sx0[nt] = lds_f(ss + (nt * 8 + 2 * c) * 16 + q * 4);
+            sx1[nt] = lds_f(ss + (nt * 8 + 2 * c + 1) * 16 + q * 4);
+        }
+        const uint32_t off = (uint32_t)g * 128u + ((uint32_t)((2 * q + (c >> 1)) ^ g) << 4) + ((c & 1) << 3);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const uint32_t wb = m ? wb1 : wb0;
+            const uint2 wl = lds_u2(wb + off);
+            const uint2 wh = lds_u2(wb + 8 * 128 + off);
+            float ct[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) ct[nt][i] = 0.f;
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint32_t Wl = (s < 2) ? wl.x : wl.y;
+                const uint32_t Wh = (s < 2) ? wh.x : wh.y;
+                uint32_t a0, a1, a2, a3;
+                if ((s & 1) == 0) {
+                    a0 = nib_pair<0>(Wl); a1 = nib_pair<0>(Wh); a2 = nib_pair<1>(Wl); a3 = nib_pair<1>(Wh);
+                } else {
+                    a0 = nib_pair<2>(Wl); a1 = nib_pair<2>(Wh); a2 = nib_pair<3>(Wl); a3 = nib_pair<3>(Wh);
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma16816(ct[nt], a0, a1, a2, a3, bf[nt][2 * s], bf[nt][2 * s + 1]);
+            }
+            // affine epilogue of this group: rows g (lo) and g+8 (hi)
+            const uint2 slo2 = sc[2 * m], shi2 = sc[2 * m + 1];
+            const uint2 blo2 = bi[2 * m], bhi2 = bi[2 * m + 1];
+            const uint32_t swl = (q < 2) ? slo2.x : slo2.y, swh = (q < 2) ? shi2.x : shi2.y;
+            const uint32_t bwl = (q < 2) ? blo2.x : blo2.y, bwh = (q < 2) ? bhi2.x : bhi2.y;
+            const float slo = __uint_as_float((q & 1) ? (swl & 0xFFFF0000u) : (swl << 16));
+            const float shi = __uint_as_float((q & 1) ? (swh & 0xFFFF0000u) : (swh << 16));
+            const float clo = fmaf(-1024.f, slo, __uint_as_float((q & 1) ? (bwl & 0xFFFF0000u) : (bwl << 16)));
+            const float chi = fmaf(-1024.f, shi, __uint_as_float((q & 1) ? (bwh & 0xFFFF0000u) : (bwh << 16)));
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                acc[m][nt][0] = fmaf(slo, ct[nt][0], fmaf(clo, sx0[nt], acc[m][nt][0]));
+                acc[m][nt][1] = fmaf(slo, ct[nt][1], fmaf(clo, sx1[nt], acc[m][nt][1]));
+                acc[m][nt][2] = fmaf(shi, ct[nt][2], fmaf(chi, sx0[nt], acc[m][nt][2]));
+                acc[m][nt][3] = fmaf(shi, ct[nt][3], fmaf(chi, sx1[nt], acc[m][nt][3]));
+            }
+        }
+    }
+}
+
+struct Ring {
+    uint32_t buf, full, empty;   // shared addresses: stage 0, full[0], empty[0] (8 bytes apart)
+};
+
+// All consumer warps of a chunk: stream the k-slices, then the pass epilogue.
+template <int NT, int PASS>
+__device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, uint32_t& it, bool& poisoned,
+                                              const Tile& T, int pc, int n, int warp, int lane, float* red) {
+    const int g = lane >> 2, c = lane & 3;
+    const int G = a.kdim / kGroup, nst = G / 4;
+    float acc[2][NT][4];
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[m][nt][i] = 0.f;
+
+    // scale / bias rows of this lane (lo rows; hi rows are 8 rows further)
+    const uint16_t *sr0, *br0, *sr1, *br1;
+    uint32_t wrow_off0, wrow_off1;   // byte offsets of the m-tiles inside a stage
+    if (PASS == 0) {
+        const int64_t j = T.row + warp * 16 + g;
+        const int64_t rg = (int64_t)T.e * a.wrow0 + j, ru = (int64_t)T.e * a.wrow1 + a.woff1 + j;
+        sr0 = a.s0 + rg * G; br0 = a.b0 + rg * G;
+        sr1 = a.s1 + ru * G; br1 = a.b1 + ru * G;
+        wrow_off0 = (uint32_t)(warp * 16) * 128u;
+        wrow_off1 = (uint32_t)(128 * 128 + warp * 16 * 128);
+    } else {
+        const int64_t r = (int64_t)T.e * a.wrow0 + T.row + warp * 32 + g;
+        sr0 = a.s0 + r * G; br0 = a.b0 + r * G;
+        sr1 = a.s0 + (r + 16) * G; br1 = a.b0 + (r + 16) * G;
+        wrow_off0 = (uint32_t)(warp * 32) * 128u;
+        wrow_off1 = (uint32_t)(warp * 32 + 16) * 128u;
+    }
+    const int sstep = 8 * G;
+    uint2 sc[4], bi[4];
+    auto load_scales = [&](int st) {
+        const int gb = st * 4;
+        sc[0] = ldg_u2h(sr0 + gb); sc[1] = ldg_u2h(sr0 + sstep + gb);
+        sc[2] = ldg_u2h(sr1 + gb); sc[3] = ldg_u2h(sr1 + sstep + gb);
+        bi[0] = ldg_u2h(br0 + gb); bi[1] = ldg_u2h(br0 + sstep + gb);
+        bi[2] = ldg_u2h(br1 + gb); bi[3] = ldg_u2h(br1 + sstep + gb);
+    };
+    load_scales(0);
+    for (int st = 0; st < nst; ++st) {
+        const uint32_t slot = it % kStages;
+        const uint32_t parity = (it / kStages) & 1u;
+        if (!poisoned && !mbar_wait(R.full + 8 * slot, parity)) {
+            poisoned = true;
+            if (lane == 0) atomicOr(a.status, SMOE_FAULT_TIMEOUT);
+        }
+        uint2 sc_cur[4], bi_cur[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { sc_cur[i] = sc[i]; bi_cur[i] = bi[i]; }
+        if (st + 1 < nst) load_scales(st + 1);   // next slice's scales in flight meanwhile
+        const uint32_t base = R.buf + slot * kStageBytes;
+        consume_stage<NT>(acc, base + wrow_off0, base + wrow_off1, base + kXOff, base + kSOff, sc_cur, bi_cur, g, c);
+        mbar_arrive(R.empty + 8 * slot);   // this thread is done reading the slot
+        ++it;
+    }
+
+    if (PASS == 0) {
+        // h = silu(gate) * up -> fp16, pair-permuted columns; per-group sums over 64 columns
+        float hs[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            hs[nt][0] = hs[nt][1] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float gv = acc[0][nt][i], uv = acc[1][nt][i];
+                const float hv = gv / (1.f + expf(-gv)) * uv;
+                const __half hh = __float2half_rn(hv);
+                const int slot = nt * 8 + 2 * c + (i & 1);
+                const int j = T.row + warp * 16 + g + ((i & 2) ? 8 : 0);
+                if (slot < n) {
+                    if (!(fabsf(hv) <= 65504.f)) atomicOr(a.status, SMOE_FAULT_FP16_RANGE);
+                    a.h_out[(size_t)(pc + slot) * a.F + (j & ~7) + perm8(j & 7)] = hh;
+                }
+                hs[nt][i & 1] += __half2float(hh);
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float v = hs[nt][q];
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                hs[nt][q] = v;
+            }
+        }
+        if (g == 0) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                red[warp * 16 + nt * 8 + 2 * c] = hs[nt][0];
+                red[warp * 16 + nt * 8 + 2 * c + 1] = hs[nt][1];
+            }
+        }
+        asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kConsumerWarps) : "memory");
+        const int tid = warp * 32 + lane;
+        if (tid < 32) {
+            const int half = tid >> 4, slot = tid & 15;   // 128 columns = two 64-column groups
+            if (slot < n) {
+                const float s = red[(4 * half) * 16 + slot] + red[(4 * half + 1) * 16 + slot] +
+                                red[(4 * half + 2) * 16 + slot] + red[(4 * half + 3) * 16 + slot];
+                a.hsum_out[(size_t)(pc + slot) * (a.F / kGroup) + T.row / kGroup + half] = s;
+            }
+        }
+        asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kConsumerWarps) : "memory");
+    } else {
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int slot = nt * 8 + 2 * c + (i & 1);
+                    if (slot >= n) continue;
+                    const int p = pc + slot;
+                    const int t = a.token_list[p], k = a.slot_list[p];
+                    if (t < 0 || t >= a.B || k < 0 || k >= a.K) continue;   // flagged by the gather
+                    const int r = T.row + warp * 32 + m * 16 + g + ((i & 2) ? 8 : 0);
+                    a.y_out[((size_t)t * a.K + k) * a.d + r] = acc[m][nt][i];
+                }
+    }
+}
+
+// PASS 0: tile = 128 h columns of one expert (consumer warp w: gate and up rows 16w..16w+15).
+// PASS 1: tile = 256 down rows of one expert (consumer warp w: rows 32w..32w+31).
+// Tiles t = blockIdx.x, blockIdx.x + gridDim.x, ... over n_union * tiles_per_expert.
+template <int PASS>
+__global__ void __launch_bounds__(kPassThreads, 1)
+    ffn_pass_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
+                    const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_s, PassArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[2 * kStages];
+    __shared__ float red[kConsumerWarps * 16];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pass_rows = PASS == 0 ? 128 : 256;
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Ring R;
+    R.buf = smem_addr(smem);
+    R.full = smem_addr(&bars[0]);
+    R.empty = smem_addr(&bars[kStages]);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(R.full + 8 * s, 1);
+            mbar_init(R.empty + 8 * s, 32 * kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncthreads();
+
+    const int n_tiles = *a.n_union * a.tiles_per_expert;
+    const int G = a.kdim / kGroup, nst = G / 4;
+    uint32_t it = 0;
+    bool poisoned = false;
+
+    if (warp == kConsumerWarps) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+                const Tile T = decode_tile(a, t, pass_rows);
+                if (!T.ok) continue;
+                // scale / bias rows of the tile into L2 ahead of the consumers' loads
+                if (PASS == 0) {
+                    const int64_t rg = (int64_t)T.e * a.wrow0 + T.row, ru = (int64_t)T.e * a.wrow1 + a.woff1 + T.row;
+                    const uint32_t bytes = (uint32_t)(128 * G * 2);
+                    prefetch_l2(a.s0 + rg * G, bytes); prefetch_l2(a.b0 + rg * G, bytes);
+                    prefetch_l2(a.s1 + ru * G, bytes); prefetch_l2(a.b1 + ru * G, bytes);
+                } else {
+                    const int64_t r = (int64_t)T.e * a.wrow0 + T.row;
+                    const uint32_t bytes = (uint32_t)(256 * G * 2);
+                    prefetch_l2(a.s0 + r * G, bytes); prefetch_l2(a.b0 + r * G, bytes);
+                }
+                for (int pc = T.p0; pc < T.p1; pc += kTokChunk) {
+                    for (int st = 0; st < nst; ++st) {
+                        const uint32_t slot = it % kStages;
+                        if (it >= kStages && !poisoned &&
+                            !mbar_wait(R.empty + 8 * slot, ((it / kStages) - 1) & 1u)) {
+                            poisoned = true;
+                            atomicOr(a.status, SMOE_FAULT_TIMEOUT);
+                        }
+                        const uint32_t base = R.buf + slot * kStageBytes;
+                        const uint32_t full = R.full + 8 * slot;
+                        if (!poisoned) {
+                            mbar_expect_tx(full, kStageTx);
+                            if (PASS == 0) {
+                                tma_load_2d(base, &map_w0, st * 32, (int)((int64_t)T.e * a.wrow0 + T.row), full);
+                                tma_load_2d(base + 128 * 128, &map_w1, st * 32,
+                                            (int)((int64_t)T.e * a.wrow1 + a.woff1 + T.row), full);
+                            } else {
+                                tma_load_2d(base, &map_w0, st * 32, (int)((int64_t)T.e * a.wrow0 + T.row), full);
+                            }
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                tma_load_2d(base + kXOff + q * kXBoxBytes, &map_x, (st * 4 + q) * 64, pc, full);
+                            tma_load_2d(base + kSOff, &map_s, st * 4, pc, full);
+                        }
+                        ++it;
+                    }
+                }
+            }
+            // drain: every issued stage has landed before the CTA may exit
+            if (poisoned) {
+                const uint32_t first = it > kStages ? it - kStages : 0;
+                for (uint32_t i = first; i < it; ++i) mbar_wait(R.full + 8 * (i % kStages), (i / kStages) & 1u);
+            }
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------------- consumers
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        const Tile T = decode_tile(a, t, pass_rows);
+        if (!T.ok) {
+            if (warp == 0 && lane == 0) atomicOr(a.status, SMOE_FAULT_EXPERT_INDEX);
+            continue;
+        }
+        for (int pc = T.p0; pc < T.p1; pc += kTokChunk) {
+            const int n = min(kTokChunk, T.p1 - pc);
+            if (n <= 8) consume_chunk<1, PASS>(a, R, it, poisoned, T, pc, n, warp, lane, red);
+            else consume_chunk<2, PASS>(a, R, it, poisoned, T, pc, n, warp, lane, red);
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------- combine
+// Skipped entirely (residual untouched) when the union did not cover all B*K entries, i.e.
+// after a flagged routing fault.
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ w,
+                                                      const int32_t* __restrict__ n_union,
+                                                      const int32_t* __restrict__ offsets, int B, int K, int d,
+                                                      float* __restrict__ residual) {
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;   // float4 index
+    const size_t n4 = (size_t)B * d / 4;
+    if (i >= n4) return;
+    if (offsets[*n_union] != B * K) return;
+    const int t = (int)(i / (d / 4));
+    const int c4 = (int)(i - (size_t)t * (d / 4));
+    float4 acc = reinterpret_cast<float4*>(residual)[i];
+    for (int k = 0; k < K; ++k) {
+        const float wk = w[(size_t)t * K + k];
+        const float4 v = reinterpret_cast<const float4*>(y + ((size_t)t * K + k) * d)[c4];
+        acc.x = fmaf(wk, v.x, acc.x);
+        acc.y = fmaf(wk, v.y, acc.y);
+        acc.z = fmaf(wk, v.z, acc.z);
+        acc.w = fmaf(wk, v.w, acc.w);
+    }
+    reinterpret_cast<float4*>(residual)[i] = acc;
+}
+
+}  // namespace
+
+// 2-D tensor map over a row-major buffer [rows, cols] of `esize`-byte elements.
+static bool encode_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize, int64_t rows,
+                          int64_t cols, int box_cols, int box_rows, CUtensorMapSwizzle swz) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(cols * esize)};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uint16_t* x, int B,
+                       const int32_t* union_ids, const int32_t* n_union, const int32_t* offsets,
+                       const int32_t* token_list, const int32_t* slot_list, const float* topk_w,
+                       float* residual, void* ws, const WsLayout& L, cudaStream_t stream) {
+    const int d = D.d_model, F = D.ffn_dim, K = D.top_k, E = D.num_experts;
+    const int BK = B * K;
+    const int max_u = BK < E ? BK : E;
+    __half* xg = ws_ptr<__half>(ws, L.xg);
+    float* sx = ws_ptr<float>(ws, L.sx);
+    __half* h = ws_ptr<__half>(ws, L.h);
+    float* sh = ws_ptr<float>(ws, L.sh);
+    float* y = ws_ptr<float>(ws, L.y);
+    uint32_t* status = ws_ptr<uint32_t>(ws, L.status);
+
+    // per device: dynamic shared memory above 48 KB is opted into once; SM count cached
+    static std::atomic<uint64_t> attr_done{0};
+    static int sm_count[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load() & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(ffn_pass_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(ffn_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassSmem);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count[dev & 63], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(bit);
+    }
+    const int sms = sm_count[dev & 63] > 0 ? sm_count[dev & 63] : 1;
+
+    // activation / group-sum maps over this call's workspace rows
+    CUtensorMap map_xg, map_sx, map_h, map_sh;
+    if (!encode_map_2d(&map_xg, xg, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, d, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_map_2d(&map_sx, sx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BK, d / kGroup, 4, 16,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_map_2d(&map_h, h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, F, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_map_2d(&map_sh, sh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BK, F / kGroup, 4, 16,
+                       CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+
+    const size_t chunks = (size_t)BK * (d / 8);
+    gather_kernel<<<(unsigned)((chunks + 255) / 256), 256, 0, stream>>>(x, d, B, n_union, offsets, token_list, status,
+                                                                          xg, sx);
+
+    PassArgs a{};
+    a.wrow0 = W.g_rows_per_expert; a.wrow1 = W.u_rows_per_expert; a.woff1 = W.u_row_offset;
+    a.s0 = W.sg; a.b0 = W.bg; a.s1 = W.su; a.b1 = W.bu;
+    a.kdim = d; a.F = F; a.d = d; a.K = K; a.E = E; a.B = B;
+    a.tiles_per_expert = F / 128;
+    a.union_ids = union_ids; a.n_union = n_union; a.offsets = offsets;
+    a.token_list = token_list; a.slot_list = slot_list;
+    a.h_out = h; a.hsum_out = sh; a.y_out = y; a.status = status;
+    const int grid0 = std::min(sms, max_u * a.tiles_per_expert);
+    ffn_pass_kernel<0><<<grid0, kPassThreads, kPassSmem, stream>>>(W.map_gate, W.map_up, map_xg, map_sx, a);
+
+    PassArgs b = a;
+    b.wrow0 = d; b.wrow1 = d; b.woff1 = 0;
+    b.s0 = W.sd; b.b0 = W.bd; b.s1 = W.sd; b.b1 = W.bd;
+    b.kdim = F;
+    b.tiles_per_expert = d / 256;
+    const int grid1 = std::min(sms, max_u * b.tiles_per_expert);
+    ffn_pass_kernel<1><<<grid1, kPassThreads, kPassSmem, stream>>>(W.map_down, W.map_down, map_h, map_sh, b);
+
+    const size_t n4 = (size_t)B * d / 4;
+    combine_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, stream>>>(y, topk_w, n_union, offsets, B, K, d,
+                                                                      residual);
+    return cudaGetLastError();
+}
+
+}  // namespace smoe

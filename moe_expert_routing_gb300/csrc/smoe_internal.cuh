@@ -1,0 +1,80 @@
+// Internal declarations of libsmoe (not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/smoe.h"
+
+namespace smoe {
+
+constexpr int kGroup = 64;          // quantisation group along the input axis
+constexpr int kMaxExperts = 256;    // union kernel keeps per-expert counters in shared memory
+constexpr int kMaxTopK = 16;
+
+// ----------------------------------------------------------------------------- workspace
+// The caller's workspace is carved into these regions (each 256-byte aligned).
+struct WsLayout {
+    size_t status;        // uint32 status word (first 256 bytes)
+    size_t logits;        // fp32 [splits, B, E]: split-K partial router logits
+    size_t topk_idx;      // int32 [B, K]   (used when the caller passes no routing buffers)
+    size_t topk_w;        // fp32  [B, K]
+    size_t union_ids;     // int32 [E]
+    size_t n_union;       // int32 [1]
+    size_t offsets;       // int32 [E + 1]
+    size_t token_list;    // int32 [B * K]
+    size_t slot_list;     // int32 [B * K]
+    size_t xg;            // fp16 [B * K, d]: gathered, pair-permuted expert inputs
+    size_t sx;            // fp32 [B * K, d / 64]: per-group sums of xg rows
+    size_t h;             // fp16 [B * K, F]: pair-permuted SwiGLU activations
+    size_t sh;            // fp32 [B * K, F / 64]: per-group sums of h rows
+    size_t y;             // fp32 [B * K, d]: unweighted expert outputs, row t*K + k
+    size_t total;
+};
+
+int route_splits(int B, int E, int d);
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+WsLayout ws_layout(const smoe_layer_desc& D, int max_tokens);
+
+template <class T>
+inline T* ws_ptr(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
+
+// ----------------------------------------------------------------------------- launchers
+// Each returns cudaGetLastError() after enqueueing its kernel(s) on `stream`.
+cudaError_t launch_route(const smoe_layer_desc& D, const uint16_t* x, const float* gate_w,
+                         const float* gate_bias, int B, int32_t* topk_idx, float* topk_w,
+                         float* logits_ws, cudaStream_t stream);
+
+cudaError_t launch_union(const smoe_layer_desc& D, const int32_t* topk_idx, int B, int32_t* union_ids,
+                         int32_t* n_union, int32_t* offsets, int32_t* token_list, int32_t* slot_list,
+                         uint32_t* status, cudaStream_t stream);
+
+// Expert weights as the FFN kernels consume them.  The packed words are read through TMA
+// tensor maps: 2-D u32 views [rows, in/8] of each weight tensor, box 32 words (4 groups) x
+// 128 rows (gate, up) or 256 rows (down), 128-byte swizzle.  Fused gate_up: map_gate == map_up over the gate_up tensor, the up rows
+// of expert e start at e * 2F + F (u_row_offset = F).
+struct FfnPointers {
+    CUtensorMap map_gate, map_up, map_down;
+    const uint16_t* sg; const uint16_t* bg; int64_t g_rows_per_expert;
+    const uint16_t* su; const uint16_t* bu; int64_t u_rows_per_expert; int64_t u_row_offset;
+    const uint16_t* sd; const uint16_t* bd;
+};
+
+cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uint16_t* x, int B,
+                       const int32_t* union_ids, const int32_t* n_union, const int32_t* offsets,
+                       const int32_t* token_list, const int32_t* slot_list, const float* topk_w,
+                       float* residual, void* ws, const WsLayout& L, cudaStream_t stream);
+
+cudaError_t launch_rmsnorm(const float* h, float eps, int center, int B, int d, uint16_t* x_out,
+                           cudaStream_t stream);
+
+// ----------------------------------------------------------------------------- device helpers
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
+    return __uint_as_float(bits16 << 16);
+}
+
+}  // namespace smoe

@@ -1,0 +1,142 @@
+// Step 2, the expert union of a chunk and the per-expert token lists.
+//
+// Page "Layer-Major Batched Prefill", "The Inversion": the chunk's routed experts are
+// deduplicated into a UNION; each union expert is then read once and applied to every
+// token routed to it.  Page "SSD Streaming Expert Layers", "Execution Paths" (exact):
+// deduplicate the routing indices; "Sorting and Compilation": the sorted gather that
+// groups tokens by expert.
+//
+// One CTA of 1024 threads builds, entirely on the device (no host synchronisation):
+//   histogram of expert ids -> exclusive scan over experts (union positions and list
+//   offsets) -> a stable scatter of the flat (token, rank) entries into the lists.
+// The scatter is stable in the flat order t*K + k, so each list is in ascending token
+// order and the output is deterministic: within a 1024-entry chunk, equal ids are ranked
+// with __match_any_sync inside each warp and a per-expert prefix over the 32 warps.
+#include "smoe_internal.cuh"
+
+namespace smoe {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+
+__global__ void __launch_bounds__(kThreads) union_kernel(const int32_t* __restrict__ idx, int BK, int E,
+                                                         int32_t* __restrict__ union_ids,
+                                                         int32_t* __restrict__ n_union,
+                                                         int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ token_list,
+                                                         int32_t* __restrict__ slot_list, int K,
+                                                         uint32_t* __restrict__ status) {
+    __shared__ int count[kMaxExperts];
+    __shared__ int list_off[kMaxExperts];  // start of expert e's list
+    __shared__ int running[kMaxExperts];   // entries of expert e placed so far
+    __shared__ int chunk_base[kMaxExperts];
+    __shared__ int wcount[kWarps][kMaxExperts];
+    __shared__ int bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    if (tid == 0) bad = 0;
+    for (int e = tid; e < kMaxExperts; e += kThreads) {
+        count[e] = 0;
+        running[e] = 0;
+    }
+    for (int i = tid; i < kWarps * kMaxExperts; i += kThreads) (&wcount[0][0])[i] = 0;
+    __syncthreads();
+
+    // histogram + validation
+    for (int i = tid; i < BK; i += kThreads) {
+        const int e = idx[i];
+        if (e < 0 || e >= E) bad = 1;
+        else atomicAdd(&count[e], 1);
+    }
+    __syncthreads();
+    if (bad) {
+        if (tid == 0) {
+            atomicOr(status, SMOE_FAULT_EXPERT_INDEX);
+            *n_union = 0;
+            offsets[0] = 0;
+        }
+        return;
+    }
+
+    // exclusive scans over experts (E <= 256) by warp 0: union positions and list offsets
+    if (warp == 0) {
+        constexpr int PER = kMaxExperts / 32;
+        int c[PER], used = 0, tot = 0;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const int e = lane * PER + j;
+            c[j] = (e < E) ? count[e] : 0;
+            used += c[j] > 0;
+            tot += c[j];
+        }
+        int used_incl = used, tot_incl = tot;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, used_incl, off);
+            const int b = __shfl_up_sync(0xffffffffu, tot_incl, off);
+            if (lane >= off) { used_incl += a; tot_incl += b; }
+        }
+        int u = used_incl - used, o = tot_incl - tot;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const int e = lane * PER + j;
+            if (e < E) {
+                list_off[e] = o;
+                if (c[j] > 0) {
+                    union_ids[u] = e;
+                    offsets[u] = o;
+                    ++u;
+                }
+                o += c[j];
+            }
+        }
+        if (lane == 31) {
+            *n_union = u;
+            offsets[u] = o;
+        }
+    }
+    __syncthreads();
+
+    // stable scatter, 1024 entries per round
+    for (int base = 0; base < BK; base += kThreads) {
+        const int i = base + tid;
+        const int e = (i < BK) ? idx[i] : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (e >= 0 && rank == 0) wcount[warp][e] = __popc(peers);
+        __syncthreads();
+        for (int x = tid; x < E; x += kThreads) {
+            int s = 0;
+            for (int w = 0; w < kWarps; ++w) {
+                const int cnt = wcount[w][x];
+                wcount[w][x] = s;
+                s += cnt;
+            }
+            chunk_base[x] = running[x];
+            running[x] += s;
+        }
+        __syncthreads();
+        if (e >= 0) {
+            const int pos = list_off[e] + chunk_base[e] + wcount[warp][e] + rank;
+            token_list[pos] = i / K;
+            slot_list[pos] = i - (i / K) * K;
+        }
+        __syncthreads();
+        for (int x = tid; x < E; x += kThreads)
+            for (int w = 0; w < kWarps; ++w) wcount[w][x] = 0;
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_union(const smoe_layer_desc& D, const int32_t* topk_idx, int B, int32_t* union_ids,
+                         int32_t* n_union, int32_t* offsets, int32_t* token_list, int32_t* slot_list,
+                         uint32_t* status, cudaStream_t stream) {
+    union_kernel<<<1, kThreads, 0, stream>>>(topk_idx, B * D.top_k, D.num_experts, union_ids, n_union, offsets,
+                                             token_list, slot_list, D.top_k, status);
+    return cudaGetLastError();
+}
+
+}  // namespace smoe

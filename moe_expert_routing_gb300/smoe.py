@@ -1,0 +1,188 @@
+"""Thin Python binding of libsmoe (C ABI in include/smoe.h), same function names.
+
+Argument marshalling only: torch tensors in, device pointers and the current CUDA stream
+out to the library; every step of the MoE block runs in libsmoe's kernels.  There is no
+fallback: if ``libsmoe.so`` is missing or fails to load, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass, field
+from typing import Dict, Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libsmoe.so")
+
+SMOE_OK, SMOE_ERR_INVALID_ARG, SMOE_ERR_UNSUPPORTED, SMOE_ERR_WORKSPACE, SMOE_ERR_CUDA, SMOE_ERR_DEVICE_FAULT = range(6)
+SMOE_LAYOUT_SEPARATE, SMOE_LAYOUT_FUSED_GATE_UP = 0, 1
+SMOE_FAULT_EXPERT_INDEX, SMOE_FAULT_FP16_RANGE, SMOE_FAULT_TIMEOUT, SMOE_FAULT_TOKEN_INDEX = 1, 2, 4, 8
+
+EXPORTED = ("smoe_workspace_bytes", "smoe_route", "smoe_expert_union", "smoe_moe_ffn_batch", "smoe_moe_layer",
+            "smoe_rmsnorm_bf16", "smoe_clear_device_status", "smoe_read_device_status", "smoe_status_string")
+
+
+class SmoeError(RuntimeError):
+    def __init__(self, status: int, what: str, bits: int = 0):
+        self.status, self.bits = status, bits
+        super().__init__(f"{what}: {_status_string(status)} (status {status}, device bits {bits:#x})")
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("d_model", "num_experts", "top_k", "ffn_dim", "group_size", "norm_topk_prob", "layout")]
+
+
+class ExpertWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w_up", "s_up", "b_up", "w_gate", "s_gate", "b_gate",
+                 "w_gate_up", "s_gate_up", "b_gate_up", "w_down", "s_down", "b_down")]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libsmoe.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"libsmoe.so not found at {path}: build it with moe_expert_routing_gb300/build.py "
+                               "(or __graft_entry__.build())")
+        L = ctypes.CDLL(path)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        L.smoe_workspace_bytes.restype = sz
+        L.smoe_workspace_bytes.argtypes = [vp, i32]
+        L.smoe_route.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+        L.smoe_expert_union.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.smoe_moe_ffn_batch.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.smoe_moe_layer.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
+        L.smoe_rmsnorm_bf16.argtypes = [vp, ctypes.c_float, i32, i32, i32, vp, vp]
+        L.smoe_clear_device_status.argtypes = [vp, vp]
+        L.smoe_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+        L.smoe_status_string.restype = ctypes.c_char_p
+        L.smoe_status_string.argtypes = [ctypes.c_int]
+        for name in ("smoe_route", "smoe_expert_union", "smoe_moe_ffn_batch", "smoe_moe_layer", "smoe_rmsnorm_bf16",
+                     "smoe_clear_device_status", "smoe_read_device_status"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _status_string(status: int) -> str:
+    try:
+        return load_library().smoe_status_string(status).decode()
+    except Exception:  # pragma: no cover
+        return "?"
+
+
+def _check(status: int, what: str):
+    if status != SMOE_OK:
+        raise SmoeError(status, what)
+
+
+def _p(t: Optional[torch.Tensor]):
+    """Device pointer of a contiguous CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libsmoe takes CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("libsmoe takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_desc(d_model: int, num_experts: int, top_k: int, ffn_dim: int, layout: str = "separate",
+              norm_topk_prob: int = 1, group_size: int = 64) -> LayerDesc:
+    return LayerDesc(d_model, num_experts, top_k, ffn_dim, group_size, norm_topk_prob,
+                     SMOE_LAYOUT_SEPARATE if layout == "separate" else SMOE_LAYOUT_FUSED_GATE_UP)
+
+
+@dataclass
+class Weights:
+    """Expert weight tensors of one layer (CUDA); names as in smoe_expert_weights."""
+    tensors: Dict[str, torch.Tensor]
+    struct: ExpertWeights = field(init=False)
+
+    def __post_init__(self):
+        self.struct = ExpertWeights()
+        for name, _ in ExpertWeights._fields_:
+            t = self.tensors.get(name)
+            if t is not None:
+                setattr(self.struct, name, _p(t).value)
+
+
+# ------------------------------------------------------------------------------ C ABI calls
+def smoe_workspace_bytes(desc: LayerDesc, max_tokens: int) -> int:
+    return int(load_library().smoe_workspace_bytes(ctypes.byref(desc), max_tokens))
+
+
+def alloc_workspace(desc: LayerDesc, max_tokens: int, device="cuda") -> torch.Tensor:
+    """A zeroed workspace tensor (the torch caching allocator returns 512-byte aligned blocks)."""
+    n = smoe_workspace_bytes(desc, max_tokens)
+    if n == 0:
+        raise SmoeError(SMOE_ERR_INVALID_ARG, "smoe_workspace_bytes")
+    ws = torch.zeros(n, dtype=torch.uint8, device=device)
+    assert ws.data_ptr() % 256 == 0
+    return ws
+
+
+def smoe_route(desc, x, gate_w, gate_bias, topk_idx, topk_w, ws, stream=None):
+    _check(load_library().smoe_route(ctypes.byref(desc), _p(x), _p(gate_w), _p(gate_bias), x.shape[0],
+                                     _p(topk_idx), _p(topk_w), _p(ws), ws.numel(), _stream(stream)), "smoe_route")
+
+
+def smoe_expert_union(desc, topk_idx, union_ids, n_union, offsets, token_list, slot_list, ws, stream=None):
+    _check(load_library().smoe_expert_union(ctypes.byref(desc), _p(topk_idx), topk_idx.shape[0], _p(union_ids),
+                                            _p(n_union), _p(offsets), _p(token_list), _p(slot_list), _p(ws),
+                                            ws.numel(), _stream(stream)), "smoe_expert_union")
+
+
+def smoe_moe_ffn_batch(desc, weights: Weights, x, union_ids, n_union, offsets, token_list, slot_list, topk_w,
+                       residual, ws, stream=None):
+    _check(load_library().smoe_moe_ffn_batch(ctypes.byref(desc), ctypes.byref(weights.struct), _p(x), x.shape[0],
+                                             _p(union_ids), _p(n_union), _p(offsets), _p(token_list),
+                                             _p(slot_list), _p(topk_w), _p(residual), _p(ws), ws.numel(),
+                                             _stream(stream)), "smoe_moe_ffn_batch")
+
+
+def smoe_moe_layer(desc, weights: Weights, x, gate_w, gate_bias, residual, ws, topk_idx=None, topk_w=None,
+                   stream=None):
+    _check(load_library().smoe_moe_layer(ctypes.byref(desc), ctypes.byref(weights.struct), _p(x), _p(gate_w),
+                                         _p(gate_bias), x.shape[0], _p(residual), _p(topk_idx), _p(topk_w), _p(ws),
+                                         ws.numel(), _stream(stream)), "smoe_moe_layer")
+
+
+def smoe_rmsnorm_bf16(h, x_out, eps: float = 1e-6, center: int = 0, stream=None):
+    _check(load_library().smoe_rmsnorm_bf16(_p(h), ctypes.c_float(eps), int(center), h.shape[0], h.shape[1],
+                                            _p(x_out), _stream(stream)), "smoe_rmsnorm_bf16")
+
+
+def smoe_clear_device_status(ws, stream=None):
+    _check(load_library().smoe_clear_device_status(_p(ws), _stream(stream)), "smoe_clear_device_status")
+
+
+def smoe_read_device_status(ws, stream=None) -> int:
+    """Synchronises the stream; returns the device status bits (0 = no fault)."""
+    bits = ctypes.c_uint32(0)
+    st = load_library().smoe_read_device_status(_p(ws), _stream(stream), ctypes.byref(bits))
+    if st not in (SMOE_OK, SMOE_ERR_DEVICE_FAULT):
+        raise SmoeError(st, "smoe_read_device_status")
+    return int(bits.value)
+
+
+def smoe_status_string(status: int) -> str:
+    return _status_string(status)
+
+
+# ------------------------------------------------------------------------------ conveniences
+def bf16_bits(t: torch.Tensor) -> torch.Tensor:
+    """A bf16 tensor viewed as its uint16 bit patterns (int16 storage)."""
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t

@@ -1,0 +1,356 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on seeded workloads.
+
+Routing indices, the union and the token lists must match bit-exactly (layer-0 inputs are
+drawn with a logit gap >= 1e-3 between adjacent ranks 1..K+1); routing weights to 1e-5
+relative; layer outputs to relative L2 <= 5e-3 (on the layer delta and on the output) and
+max-abs <= 2e-2.  Chained stacks are checked layer by layer, teacher-forced: the oracle's
+layer l consumes the GPU's own hidden state h_l, and tokens whose oracle gap between ranks K
+and K+1 is below 1e-4 are exempt from the index comparison (they must stay under 0.1%).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import MAX_ABS_TOL, REL_L2_TOL, W_RTOL, logit_gaps, max_abs, rel_l2, resampled_x, rmsnorm_glue_close
+from moe_expert_routing_gb300 import smoe
+from moe_expert_routing_gb300 import workload as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+class Case:
+    """One layer of a workload: inputs on the host (oracle) and on the device (CUDA path)."""
+
+    def __init__(self, w: W.Workload, layer: int = 0, B: int = None, gap: bool = True, x=None, gen_device=None):
+        _need_gpu()
+        self.w, self.layer = w, layer
+        self.B = B if B is not None else w.tokens
+        self.gate = W.gen_gate(w, layer)
+        self.bias = W.gen_gate_bias(w, layer)
+        if x is not None:
+            self.x = x
+        elif gap:
+            self.x, _ = resampled_x(w, layer, self.B, self.gate, self.bias)
+        else:
+            self.x = W.gen_x(w, layer, self.B)
+        big = w.num_experts * w.expert_bytes > (256 << 20)
+        gdev = gen_device or (DEV if big else "cpu")
+        wts = W.gen_layer_weights(w, layer, device=gdev)
+        self.wts_cpu = {k: v.cpu() for k, v in wts.items()}
+        self.wts_gpu = {k: v.to(DEV) for k, v in wts.items()}
+        self.weights = smoe.Weights(self.wts_gpu)
+        self.desc = smoe.make_desc(w.d_model, w.num_experts, w.top_k, w.ffn_dim, w.layout, w.norm_topk_prob)
+        self.layer_o = oracle.Layer.from_workload(w, self.wts_cpu)
+        self.ws = smoe.alloc_workspace(self.desc, max(self.B, 1))
+        self.gate_d = self.gate.to(DEV)
+        self.bias_d = None if self.bias is None else self.bias.to(DEV)
+
+    def x_dev(self):
+        return self.x.to(DEV).view(torch.int16)
+
+    def run_layer(self, residual=None):
+        """Full smoe_moe_layer on the device: (out fp32 [B,d], idx, w)."""
+        B, K = self.B, self.w.top_k
+        res = (self.x.float() if residual is None else residual).to(DEV).contiguous()
+        idx = torch.empty(B, K, dtype=torch.int32, device=DEV)
+        wt = torch.empty(B, K, dtype=torch.float32, device=DEV)
+        smoe.smoe_clear_device_status(self.ws)
+        smoe.smoe_moe_layer(self.desc, self.weights, self.x_dev(), self.gate_d, self.bias_d, res, self.ws, idx, wt)
+        bits = smoe.smoe_read_device_status(self.ws)
+        assert bits == 0, f"device status {bits:#x}"
+        return res.cpu(), idx.cpu(), wt.cpu()
+
+    def oracle_layer(self, residual=None, rows=None):
+        idx, w64, w32, lg = oracle.route(self.x, self.gate, self.bias, self.w.top_k, self.w.norm_topk_prob)
+        res = self.x.float() if residual is None else residual
+        out, out64, _ = oracle.moe_layer(self.layer_o, self.x, idx, w64, res, rows=rows)
+        return out64, idx, w64, lg
+
+
+def check_outputs(gpu_out, oracle_out64, residual, rows=None, abs_scale=1.0):
+    """rel-L2 <= 5e-3 on the delta and the output; max-abs <= 2e-2 * abs_scale.
+
+    abs_scale is 1 at the input scale the workloads state (single layers, layer 0 of a
+    chain); for teacher-forced chained layers it is RMS(delta_l) / RMS(delta_0), see
+    _chain."""
+    g = np.asarray(gpu_out, np.float64)
+    o = np.asarray(oracle_out64, np.float64)
+    r = np.asarray(residual, np.float64)
+    if rows is not None:
+        g, o, r = g[rows], o[rows], r[rows]
+    assert np.all(np.isfinite(g))
+    d_rel = rel_l2(g - r, o - r)
+    o_rel = rel_l2(g, o)
+    mab = max_abs(g, o)
+    assert d_rel <= REL_L2_TOL, f"delta rel-L2 {d_rel:.3e}"
+    assert o_rel <= REL_L2_TOL, f"output rel-L2 {o_rel:.3e}"
+    assert mab <= MAX_ABS_TOL * abs_scale, f"max-abs {mab:.3e} (scale {abs_scale:.3g})"
+    return d_rel, mab
+
+
+# ----------------------------------------------------------------------------- routing
+ROUTE_CASES = [
+    ("toy", None), ("decode_b1", None), ("decode_b8", None), ("prefill64", None), ("q35_prefill64", None),
+    ("long4096", 1024),
+]
+
+
+@pytest.mark.parametrize("name,B", ROUTE_CASES)
+def test_route_parity(name, B):
+    _need_gpu()
+    w = W.WORKLOADS[name]
+    B = B or w.tokens
+    gate = W.gen_gate(w, 0)
+    bias = W.gen_gate_bias(w, 0)
+    x, _ = resampled_x(w, 0, B, gate, bias)
+    desc = smoe.make_desc(w.d_model, w.num_experts, w.top_k, w.ffn_dim, w.layout, w.norm_topk_prob)
+    ws = smoe.alloc_workspace(desc, B)
+    idx = torch.empty(B, w.top_k, dtype=torch.int32, device=DEV)
+    wt = torch.empty(B, w.top_k, dtype=torch.float32, device=DEV)
+    smoe.smoe_route(desc, x.to(DEV).view(torch.int16), gate.to(DEV), None if bias is None else bias.to(DEV), idx, wt, ws)
+    torch.cuda.synchronize()
+    oi, ow64, _, _ = oracle.route(x, gate, bias, w.top_k, w.norm_topk_prob)
+    assert np.array_equal(idx.cpu().numpy(), oi)
+    np.testing.assert_allclose(wt.cpu().numpy(), ow64, rtol=W_RTOL, atol=1e-7)
+
+
+def test_route_norm_topk_prob_off_and_k_equals_e():
+    _need_gpu()
+    w = W.scaled(W.WORKLOADS["toy"], norm_topk_prob=0)
+    for K in (4, 16):
+        wk = W.scaled(w, top_k=K)
+        gate = W.gen_gate(wk, 0)
+        x, _ = resampled_x(wk, 0, 16, gate, None)
+        desc = smoe.make_desc(wk.d_model, wk.num_experts, K, wk.ffn_dim, "separate", 0)
+        ws = smoe.alloc_workspace(desc, 16)
+        idx = torch.empty(16, K, dtype=torch.int32, device=DEV)
+        wt = torch.empty(16, K, dtype=torch.float32, device=DEV)
+        smoe.smoe_route(desc, x.to(DEV).view(torch.int16), gate.to(DEV), None, idx, wt, ws)
+        oi, ow64, _, _ = oracle.route(x, gate, None, K, 0)
+        assert np.array_equal(idx.cpu().numpy(), oi)
+        np.testing.assert_allclose(wt.cpu().numpy(), ow64, rtol=W_RTOL, atol=1e-7)
+
+
+# ----------------------------------------------------------------------------- union
+@pytest.mark.parametrize("B,K,E", [(1, 8, 128), (16, 4, 16), (64, 8, 128), (64, 8, 256), (37, 3, 9), (4096, 8, 128),
+                                   (200, 16, 16)])
+def test_union_parity(B, K, E):
+    _need_gpu()
+    rng = np.random.default_rng(B * 1000 + K * 10 + E)
+    # skewed: a few hot experts plus uniform picks
+    p = rng.zipf(1.3, size=E).astype(np.float64)
+    p /= p.sum()
+    idx = np.stack([rng.choice(E, K, replace=False, p=p) for _ in range(B)]).astype(np.int32)
+    d = max(256, 256)
+    desc = smoe.make_desc(d, E, K, 256)
+    ws = smoe.alloc_workspace(desc, B)
+    uid = torch.full((E,), -7, dtype=torch.int32, device=DEV)
+    nu = torch.zeros(1, dtype=torch.int32, device=DEV)
+    off = torch.full((E + 1,), -7, dtype=torch.int32, device=DEV)
+    tl = torch.full((B * K,), -7, dtype=torch.int32, device=DEV)
+    sl = torch.full((B * K,), -7, dtype=torch.int32, device=DEV)
+    smoe.smoe_expert_union(desc, torch.from_numpy(idx).to(DEV), uid, nu, off, tl, sl, ws)
+    ou, oo, otl, osl = oracle.expert_union(idx, E)
+    n = int(nu.item())
+    assert n == len(ou)
+    assert np.array_equal(uid.cpu().numpy()[:n], ou)
+    assert np.array_equal(off.cpu().numpy()[:n + 1], oo)
+    assert np.array_equal(tl.cpu().numpy(), otl)
+    assert np.array_equal(sl.cpu().numpy(), osl)
+
+
+def test_union_bad_index_sets_fault_and_leaves_residual():
+    _need_gpu()
+    c = Case(W.WORKLOADS["toy"], gap=False)
+    B, K = c.B, c.w.top_k
+    idx = np.tile(np.arange(K, dtype=np.int32), (B, 1))
+    idx[3, 1] = c.w.num_experts + 5
+    idx_d = torch.from_numpy(idx).to(DEV)
+    E = c.w.num_experts
+    uid = torch.zeros(E, dtype=torch.int32, device=DEV)
+    nu = torch.zeros(1, dtype=torch.int32, device=DEV)
+    off = torch.zeros(E + 1, dtype=torch.int32, device=DEV)
+    tl = torch.zeros(B * K, dtype=torch.int32, device=DEV)
+    sl = torch.zeros(B * K, dtype=torch.int32, device=DEV)
+    smoe.smoe_clear_device_status(c.ws)
+    smoe.smoe_expert_union(c.desc, idx_d, uid, nu, off, tl, sl, c.ws)
+    res = c.x.float().to(DEV)
+    before = res.clone()
+    wt = torch.full((B, K), 0.25, device=DEV)
+    smoe.smoe_moe_ffn_batch(c.desc, c.weights, c.x_dev(), uid, nu, off, tl, sl, wt, res, c.ws)
+    bits = smoe.smoe_read_device_status(c.ws)
+    assert bits & smoe.SMOE_FAULT_EXPERT_INDEX
+    assert int(nu.item()) == 0
+    assert torch.equal(res, before)
+    smoe.smoe_clear_device_status(c.ws)
+    assert smoe.smoe_read_device_status(c.ws) == 0
+
+
+# ----------------------------------------------------------------------------- whole layer
+LAYER_CASES = [
+    ("toy", None), ("decode_b1", None), ("decode_b8", None), ("prefill64", None), ("q35_prefill64", None),
+    ("prefill64", 37), ("toy", 1), ("q35_prefill64", 5),
+]
+
+
+@pytest.mark.parametrize("name,B", LAYER_CASES)
+def test_layer_parity(name, B):
+    c = Case(W.WORKLOADS[name], B=B)
+    out, idx, wt = c.run_layer()
+    o64, oidx, ow64, _ = c.oracle_layer()
+    assert np.array_equal(idx.numpy(), oidx)
+    np.testing.assert_allclose(wt.numpy(), ow64, rtol=W_RTOL, atol=1e-7)
+    check_outputs(out.numpy(), o64, c.x.float().numpy())
+
+
+def test_ffn_batch_step_by_step_matches_layer():
+    """route -> union -> ffn_batch through the separate entry points equals smoe_moe_layer."""
+    c = Case(W.WORKLOADS["decode_b8"])
+    B, K, E = c.B, c.w.top_k, c.w.num_experts
+    idx = torch.empty(B, K, dtype=torch.int32, device=DEV)
+    wt = torch.empty(B, K, dtype=torch.float32, device=DEV)
+    smoe.smoe_route(c.desc, c.x_dev(), c.gate_d, None, idx, wt, c.ws)
+    uid = torch.zeros(E, dtype=torch.int32, device=DEV)
+    nu = torch.zeros(1, dtype=torch.int32, device=DEV)
+    off = torch.zeros(E + 1, dtype=torch.int32, device=DEV)
+    tl = torch.zeros(B * K, dtype=torch.int32, device=DEV)
+    sl = torch.zeros(B * K, dtype=torch.int32, device=DEV)
+    smoe.smoe_expert_union(c.desc, idx, uid, nu, off, tl, sl, c.ws)
+    res = c.x.float().to(DEV)
+    smoe.smoe_moe_ffn_batch(c.desc, c.weights, c.x_dev(), uid, nu, off, tl, sl, wt, res, c.ws)
+    out_layer, _, _ = c.run_layer()
+    assert torch.equal(res.cpu(), out_layer)
+
+
+def test_hot_experts_many_tokens_per_expert():
+    """64 identical tokens: K experts with 64 tokens each (token chunks of 16 inside the kernels)."""
+    w = W.WORKLOADS["toy"]
+    x1 = W.gen_x(w, 0, 1)
+    c = Case(w, B=64, x=x1.repeat(64, 1))
+    out, idx, _ = c.run_layer()
+    o64, oidx, _, _ = c.oracle_layer()
+    assert np.array_equal(idx.numpy(), oidx)
+    check_outputs(out.numpy(), o64, c.x.float().numpy())
+    assert torch.all(out == out[0])
+
+
+def test_top1_routing():
+    w = W.scaled(W.WORKLOADS["toy"], top_k=1)
+    c = Case(w)
+    out, idx, wt = c.run_layer()
+    o64, oidx, _, _ = c.oracle_layer()
+    assert np.array_equal(idx.numpy(), oidx) and torch.all(wt == 1.0)
+    check_outputs(out.numpy(), o64, c.x.float().numpy())
+
+
+def test_zero_tokens_is_noop():
+    c = Case(W.WORKLOADS["toy"], gap=False)
+    empty = torch.empty(0, c.w.d_model, dtype=torch.int16, device=DEV)
+    res = torch.empty(0, c.w.d_model, dtype=torch.float32, device=DEV)
+    smoe.smoe_moe_layer(c.desc, c.weights, empty, c.gate_d, None, res, c.ws)
+    torch.cuda.synchronize()
+
+
+def test_layer_is_deterministic():
+    c = Case(W.WORKLOADS["prefill64"], B=64)
+    a, _, _ = c.run_layer()
+    b, _, _ = c.run_layer()
+    assert torch.equal(a, b)
+
+
+def test_graph_replay_equals_direct():
+    c = Case(W.WORKLOADS["decode_b8"])
+    direct, _, _ = c.run_layer()
+    res0 = c.x.float().to(DEV)
+    res = res0.clone()
+    xd = c.x_dev()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        smoe.smoe_moe_layer(c.desc, c.weights, xd, c.gate_d, None, res, c.ws)
+    res.copy_(res0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(res.cpu(), direct)
+
+
+# ----------------------------------------------------------------------------- chained stacks
+def _chain(name, layers, B=None, sample_rows=None):
+    w = W.WORKLOADS[name]
+    B = B or w.tokens
+    first = Case(w, 0, B)
+    h = first.x.float().to(DEV)
+    xb = torch.empty(B, w.d_model, dtype=torch.int16, device=DEV)
+    exempt, total, worst, rms0 = 0, 0, 0.0, 1.0
+    for l in range(layers):
+        c = first if l == 0 else Case(w, l, B, x=first.x)
+        smoe.smoe_rmsnorm_bf16(h, xb, 1e-6, center=int(w.chain_center))
+        x_l = xb.cpu().view(torch.bfloat16)
+        h_in = h.cpu().clone()
+        # the rmsnorm glue itself: at most one bf16 ulp from the double-precision oracle
+        ox = oracle.rmsnorm_bf16(h_in.numpy(), 1e-6, center=w.chain_center)
+        assert rmsnorm_glue_close(x_l.view(torch.int16).numpy(), ox) < 1e-2
+        idx = torch.empty(B, w.top_k, dtype=torch.int32, device=DEV)
+        wt = torch.empty(B, w.top_k, dtype=torch.float32, device=DEV)
+        smoe.smoe_clear_device_status(c.ws)
+        smoe.smoe_moe_layer(c.desc, c.weights, xb, c.gate_d, c.bias_d, h, c.ws, idx, wt)
+        assert smoe.smoe_read_device_status(c.ws) == 0
+        # teacher-forced oracle on the GPU's own layer input
+        c.x = x_l
+        oi, ow64, _, lg = oracle.route(x_l, c.gate, c.bias, w.top_k, w.norm_topk_prob)
+        s = -np.sort(-lg, axis=1)
+        near = (s[:, w.top_k - 1] - s[:, w.top_k]) < 1e-4
+        gi = idx.cpu().numpy()
+        mism = np.any(gi != oi, axis=1)
+        assert not np.any(mism & ~near), f"layer {l}: routing differs on well-separated tokens"
+        exempt += int(near.sum())
+        total += B
+        rows = sample_rows if sample_rows is not None else list(range(B))
+        rows = [r for r in rows if not near[r]]
+        _, o64, _ = oracle.moe_layer(c.layer_o, x_l, oi, ow64, h_in, rows=rows)
+        # The workloads' weights have mean -0.5*scale (nibbles average 7.5, the bias centres
+        # them at 8), so every layer output carries a common mode; the residual stream grows
+        # with depth.  The absolute bound is applied at layer 0's scale and scaled with the
+        # delta RMS after that.
+        delta = o64[rows] - h_in.numpy()[rows]
+        rms = float(np.sqrt(np.mean(delta ** 2)))
+        if l == 0:
+            rms0 = rms
+        d_rel, mab = check_outputs(h.cpu().numpy(), o64, h_in.numpy(), rows=rows, abs_scale=max(1.0, rms / rms0))
+        worst = max(worst, d_rel)
+    assert exempt <= max(1, 0.001 * total), f"{exempt} near-tie token-layers"
+    return worst
+
+
+@pytest.mark.parametrize("center", [0, 1])
+def test_rmsnorm_glue_parity(center):
+    _need_gpu()
+    rng = np.random.default_rng(11 + center)
+    for B, d in [(1, 512), (64, 4096), (37, 2048)]:
+        h = (rng.normal(size=(B, d)) * rng.uniform(0.1, 100.0, size=(B, 1)) + rng.normal(size=(B, 1)) * 50)
+        h = torch.from_numpy(h.astype(np.float32))
+        xb = torch.empty(B, d, dtype=torch.int16, device=DEV)
+        smoe.smoe_rmsnorm_bf16(h.to(DEV), xb, 1e-6, center=center)
+        ox = oracle.rmsnorm_bf16(h.numpy(), 1e-6, center=bool(center))
+        assert rmsnorm_glue_close(xb.cpu().numpy(), ox) < 1e-2
+
+
+def test_chain_prefill64_teacher_forced():
+    _chain("prefill64", 2)
+
+
+def test_chain_qwen35_fused_teacher_forced():
+    _chain("q35_prefill64", 3)
+
+
+def test_chain_long_skewed_sampled_rows():
+    """4096 tokens with the Zipf logit bias: hot experts far above 16 tokens."""
+    _chain("long4096", 2, sample_rows=list(range(0, 4096, 256)))
