@@ -165,6 +165,21 @@ SMOE_API smoe_status smoe_moe_layer(const smoe_layer_desc* desc, const smoe_expe
 SMOE_API smoe_status smoe_rmsnorm_bf16(const float* h, float eps, int32_t center, int32_t B, int32_t d,
                                        uint16_t* x_out, void* stream);
 
+/* Step 1 without a workspace, for callers that cannot allocate device memory (a plugin
+ * inside a host application that owns the device-memory budget, or a latency-critical loop
+ * that cannot risk the device-wide synchronisation of a cudaMalloc).  The pages have no
+ * counterpart: it is an addition of this library.  Arguments and results are those of
+ * smoe_route; the split-K scratch is a fixed 1 MiB device array inside the library (held by
+ * every GPU that loads it until the process exits), so a call needs
+ * splits * B * num_experts <= 262144 floats (B <= 128 at 128 experts) and returns
+ * SMOE_ERR_UNSUPPORTED beyond that, without launching.  The first call on a device looks up
+ * the array's address (cudaGetSymbolAddress) with that device current: make it before any
+ * stream capture.  All calls share the array: calls that overlap on the GPU race and must be
+ * ordered by the caller.  Allocates nothing. */
+SMOE_API smoe_status smoe_route_noalloc(const smoe_layer_desc* desc, const uint16_t* x, const float* gate_w,
+                                        const float* gate_bias, int32_t B, int32_t* topk_idx, float* topk_w,
+                                        void* stream);
+
 /* Zero the device status word (asynchronous). */
 SMOE_API smoe_status smoe_clear_device_status(void* workspace, void* stream);
 

@@ -1,0 +1,83 @@
+// smoe_route_noalloc: the routing step with its scratch in a fixed device array instead of a
+// caller-provided workspace.
+//
+// Some callers cannot call cudaMalloc.  A plugin running inside a host application that owns
+// the whole device-memory budget (an inference server with a preallocated arena, a game or
+// visualisation engine) may be forbidden to allocate; other callers cannot afford the implicit
+// device-wide synchronisation a cudaMalloc may cause in the middle of a latency-critical loop.
+// For them this entry point needs nothing but its inputs and outputs: the split-K partial
+// router logits live in g_route_scratch below, a file-scope device array of
+// kNoallocScratchFloats floats (1 MiB) that every GPU which loads the library holds until the
+// process exits.
+//
+// Set-up: the first call on a device (with that device current) looks up the array's device
+// address with cudaGetSymbolAddress and caches it; make that first call before any stream
+// capture.  In host code the name g_route_scratch is only a host-side stand-in for the
+// symbol, never a usable device address, which is why the looked-up address is passed to
+// the kernels.
+//
+// Sharing: every call on a device uses the same array and leaves the last call's partial
+// logits in it.  Nothing has to start at zero (each call overwrites every partial it reads),
+// but calls whose work overlaps on the GPU (different streams, no ordering) race on the array
+// and must be serialised by the caller.
+#include "smoe_internal.cuh"
+
+#include <mutex>
+
+namespace smoe {
+namespace {
+
+constexpr size_t kNoallocScratchFloats = 262144;   // 1 MiB: splits * B * E partial logits
+
+static __device__ __align__(256) float g_route_scratch[kNoallocScratchFloats];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+float* g_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Device address of g_route_scratch on the current device (looked up once per device).
+cudaError_t scratch_for_current_device(float** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_route_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace smoe
+
+using namespace smoe;
+
+extern "C" SMOE_API smoe_status smoe_route_noalloc(const smoe_layer_desc* desc, const uint16_t* x,
+                                                   const float* gate_w, const float* gate_bias, int32_t B,
+                                                   int32_t* topk_idx, float* topk_w, void* stream) {
+    if (!desc) return SMOE_ERR_INVALID_ARG;
+    if (desc->d_model <= 0 || desc->num_experts <= 0 || desc->top_k <= 0 || desc->top_k > desc->num_experts ||
+        desc->ffn_dim <= 0 || desc->group_size <= 0 || (desc->norm_topk_prob != 0 && desc->norm_topk_prob != 1) ||
+        (desc->layout != SMOE_LAYOUT_SEPARATE && desc->layout != SMOE_LAYOUT_FUSED_GATE_UP))
+        return SMOE_ERR_INVALID_ARG;
+    if (smoe_workspace_bytes(desc, 1) == 0) return SMOE_ERR_UNSUPPORTED;   // shape the kernels do not take
+    if (B < 0) return SMOE_ERR_INVALID_ARG;
+    if (B == 0) return SMOE_OK;
+    if (!x || !gate_w || !topk_idx || !topk_w) return SMOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(gate_w) & 15u))
+        return SMOE_ERR_UNSUPPORTED;
+    // the partial logits of this call must fit the fixed array
+    const size_t need = (size_t)route_splits(B, desc->num_experts, desc->d_model) * (size_t)B * desc->num_experts;
+    if (need > kNoallocScratchFloats) return SMOE_ERR_UNSUPPORTED;
+    float* scratch = nullptr;
+    if (scratch_for_current_device(&scratch) != cudaSuccess) return SMOE_ERR_CUDA;
+    return launch_route(*desc, x, gate_w, gate_bias, B, topk_idx, topk_w, scratch,
+                        static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SMOE_OK
+               : SMOE_ERR_CUDA;
+}

@@ -21,7 +21,8 @@ SMOE_LAYOUT_SEPARATE, SMOE_LAYOUT_FUSED_GATE_UP = 0, 1
 SMOE_FAULT_EXPERT_INDEX, SMOE_FAULT_FP16_RANGE, SMOE_FAULT_TIMEOUT, SMOE_FAULT_TOKEN_INDEX = 1, 2, 4, 8
 
 EXPORTED = ("smoe_workspace_bytes", "smoe_route", "smoe_expert_union", "smoe_moe_ffn_batch", "smoe_moe_layer",
-            "smoe_rmsnorm_bf16", "smoe_clear_device_status", "smoe_read_device_status", "smoe_status_string")
+            "smoe_rmsnorm_bf16", "smoe_clear_device_status", "smoe_read_device_status", "smoe_status_string",
+            "smoe_route_noalloc")
 
 
 class SmoeError(RuntimeError):
@@ -60,6 +61,8 @@ def load_library(path: str = LIB_PATH):
         L.smoe_moe_ffn_batch.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.smoe_moe_layer.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
         L.smoe_rmsnorm_bf16.argtypes = [vp, ctypes.c_float, i32, i32, i32, vp, vp]
+        L.smoe_route_noalloc.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp]
+        L.smoe_route_noalloc.restype = ctypes.c_int
         L.smoe_clear_device_status.argtypes = [vp, vp]
         L.smoe_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         L.smoe_status_string.restype = ctypes.c_char_p
@@ -137,6 +140,12 @@ def alloc_workspace(desc: LayerDesc, max_tokens: int, device="cuda") -> torch.Te
 def smoe_route(desc, x, gate_w, gate_bias, topk_idx, topk_w, ws, stream=None):
     _check(load_library().smoe_route(ctypes.byref(desc), _p(x), _p(gate_w), _p(gate_bias), x.shape[0],
                                      _p(topk_idx), _p(topk_w), _p(ws), ws.numel(), _stream(stream)), "smoe_route")
+
+
+def smoe_route_noalloc(desc, x, gate_w, gate_bias, topk_idx, topk_w, stream=None):
+    """smoe_route without a workspace (fixed 1 MiB scratch inside the library; see smoe.h)."""
+    _check(load_library().smoe_route_noalloc(ctypes.byref(desc), _p(x), _p(gate_w), _p(gate_bias), x.shape[0],
+                                             _p(topk_idx), _p(topk_w), _stream(stream)), "smoe_route_noalloc")
 
 
 def smoe_expert_union(desc, topk_idx, union_ids, n_union, offsets, token_list, slot_list, ws, stream=None):
