@@ -128,7 +128,7 @@ WsLayout ws_layout(const smoe_layer_desc& D, int max_tokens) {
     L.slot_list = take(BK * 4);
     L.xg = take(BK * d * 2);
     L.sx = take(BK * (d / kGroup) * 4);
-    L.h = take(BK * F * 2);
+    L.h = take(BK * 2 * F * 2);
     L.sh = take(BK * (F / kGroup) * 4);
     L.y = take(BK * d * 4);
     L.total = o;

@@ -27,16 +27,22 @@
 // FFMA dot products would cost ~5 issue slots per weight.  Instead each consumer warp turns
 // nibbles straight into A-fragment registers of mma.sync.m16n8k16 and lets the tensor core
 // do the multiply-adds:
-//   * a u32 word holds nibbles n0..n7; (w >> 4j) & 0x000F000F | 0x64006400 is the fp16
-//     pair (1024 + n_j, 1024 + n_{j+4}), exact, in one or two instructions.
+//   * a u32 word holds nibbles n0..n7.  w & 0x000F000F is the fp16 pair (n0, n4) * 2^-24
+//     (fp16 subnormals, exact); w & 0x00F000F0 is (n1, n5) * 16 * 2^-24; the same masks on
+//     w >> 8 give n2/n6 and n3/n7: five integer ops per eight weights and no offset to take
+//     back out.  The activations at odd positions within every 8 inputs are stored divided
+//     by 16 (exact), so 16 q x/16 = q x.  (Measured on GB300: mma.sync multiplies subnormal
+//     fp16 operands exactly and accumulates them to ~3e-6 of the result.)
 //   * the mma contraction order is free, so the k axis is permuted: within every 8 inputs
 //     the activations are stored as (x0,x4,x1,x5,x2,x6,x3,x7), which makes each decoded
 //     pair line up with one B-fragment register.
-//   * each mma covers 16 inputs of ONE group, so the affine map and the 1024 offset are
-//     applied after the mma, in fp32:
-//       sum_i (s q_i + b) x_i = s * C + (b - 1024 s) * S,  C = sum_i (1024 + q_i) x_i,
-//       S = sum_i x_i (the group sums travel with the activations);
-//     weights are never rounded to fp16.
+//   * each mma covers 16 inputs of ONE group, so the affine map is applied after the mma,
+//     in fp32:  sum_i (s q_i + b) x_i = (s * 2^24) * C + b * S,  C = mma result,
+//     S = sum of the group's activations; weights are never rounded.  The bias part,
+//     sum over groups of b[row][g] * S[token][g], is a small product of its own: it runs on
+//     the tensor cores once per token chunk (b as fp16, S as an fp16 hi + lo pair).
+//   * the down projection's input h = silu(g) * up is carried as two fp16 terms, hi + lo
+//     (lo = the rounding remainder), and both are multiplied: h keeps ~22 bits.
 #include "smoe_internal.cuh"
 
 #include <cuda.h>
@@ -57,11 +63,11 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// fp16 pair (1024 + q_j, 1024 + q_{j+4}) of the nibbles of w, exact.
-template <int J>
-__device__ __forceinline__ uint32_t nib_pair(uint32_t w) {
-    return ((w >> (4 * J)) & 0x000F000Fu) | 0x64006400u;
-}
+// Exact fp16 pairs of the nibbles of a word w (w8 = w >> 8), as subnormals (units of 2^-24):
+//   even(w) = (n0, n4),  odd(w) = 16 (n1, n5),  even(w8) = (n2, n6),  odd(w8) = 16 (n3, n7).
+__device__ __forceinline__ uint32_t nib_even(uint32_t w) { return w & 0x000F000Fu; }
+__device__ __forceinline__ uint32_t nib_odd(uint32_t w) { return w & 0x00F000F0u; }
+
 
 __device__ __forceinline__ uint2 ldg_u2h(const uint16_t* p) {
     return __ldg(reinterpret_cast<const uint2*>(p));
@@ -114,6 +120,9 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+
+
+
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
 }
@@ -130,15 +139,11 @@ __device__ __forceinline__ uint4 lds_u4(uint32_t a) {
     return v;
 }
 
-__device__ __forceinline__ float lds_f(uint32_t a) {
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];\n" : "=f"(v) : "r"(a));
-    return v;
-}
 
 // ----------------------------------------------------------------------------- gather
-// One thread per 8-element chunk of a list entry p: xg[p] = pair-permuted fp16(x[token_list[p]]),
-// sx[p][g] = sum of the fp16 values of group g (8 consecutive lanes hold one group).
+// One thread per 8-element chunk of a list entry p: xg[p] = pair-permuted fp16(x[token_list[p]])
+// with the odd elements of every 8 divided by 16; sx[p][g] = sum of the values the stored
+// halves stand for in group g (8 consecutive lanes hold a group).
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ x, int d, int B,
                                                      const int32_t* __restrict__ n_union,
                                                      const int32_t* __restrict__ offsets,
@@ -159,13 +164,13 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
     const uint4 raw = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d) + ch);
     const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
     __half hv[8];
-    float s = 0.f;
+    float sa = 0.f;
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
         const float v = bf16_bits_to_float((m & 1) ? (wv[m >> 1] >> 16) : (wv[m >> 1] & 0xFFFFu));
-        const __half h = __float2half_rn(v);
+        const __half h = __float2half_rn((m & 1) ? v * 0.0625f : v);
         hv[perm8(m)] = h;
-        s += __half2float(h);
+        sa += (m & 1) ? __half2float(h) * 16.f : __half2float(h);
     }
     uint4 o;
     o.x = (uint32_t)__half_as_ushort(hv[0]) | ((uint32_t)__half_as_ushort(hv[1]) << 16);
@@ -173,23 +178,20 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
     o.z = (uint32_t)__half_as_ushort(hv[4]) | ((uint32_t)__half_as_ushort(hv[5]) << 16);
     o.w = (uint32_t)__half_as_ushort(hv[6]) | ((uint32_t)__half_as_ushort(hv[7]) << 16);
     reinterpret_cast<uint4*>(xg + (size_t)p * d)[ch] = o;
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    s += __shfl_xor_sync(0xffffffffu, s, 2);
-    s += __shfl_xor_sync(0xffffffffu, s, 4);
-    if ((lane & 7) == 0) sx[(size_t)p * (d / kGroup) + ch / 8] = s;
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) sa += __shfl_xor_sync(0xffffffffu, sa, off);
+    if ((lane & 7) == 0) sx[(size_t)p * (d / kGroup) + ch / 8] = sa;
 }
 
 // ----------------------------------------------------------------------------- expert passes
 constexpr int kConsumerWarps = 8;
 constexpr int kPassThreads = 32 * (kConsumerWarps + 1);   // + one producer warp
-constexpr int kStages = 4;
+constexpr int kStages = 3;   // 3 x 49 KB: leaves ~80 KB of L1 for the scale rows
 constexpr int kWBytes = 256 * 128;         // 256 weight rows x 32 u32 words (4 groups)
 constexpr int kXBoxBytes = 16 * 128;       // 16 activation rows x 64 fp16 (one group)
-constexpr int kXOff = kWBytes;
-constexpr int kSOff = kWBytes + 4 * kXBoxBytes;
-constexpr int kSBytes = 16 * 16;           // 16 rows x 4 group sums (fp32)
-constexpr int kStageBytes = kSOff + 1024;  // keeps every stage 1024-byte aligned
-constexpr int kStageTx = kWBytes + 4 * kXBoxBytes + kSBytes;
+constexpr int kXOff = kWBytes;             // 4 boxes (x, pass 0) or 8 boxes (h hi then lo, pass 1)
+constexpr int kStageBytes = kWBytes + 8 * kXBoxBytes;   // 48 KB, a 1024-byte multiple
+__host__ __device__ constexpr int stage_tx(int pass) { return kWBytes + (pass ? 8 : 4) * kXBoxBytes; }
 constexpr int kPassSmem = kStages * kStageBytes + 1024;
 constexpr int kTokChunk = 16;              // tokens per pass over the weights
 
@@ -199,6 +201,7 @@ struct PassArgs {
     int64_t woff1;        // pass 0: first up row inside an expert block (0 or F)
     const uint16_t* s0; const uint16_t* b0;   // scales/biases of map_w0 rows
     const uint16_t* s1; const uint16_t* b1;   // scales/biases of map_w1 rows
+    const float* bsum;    // per-group sums of the activation rows [B*K, kdim/64] (sx or sh)
     int kdim;             // contraction length (d for pass 0, F for pass 1)
     int F, d, K, E, B;
     int tiles_per_expert;
@@ -226,26 +229,27 @@ __device__ __forceinline__ Tile decode_tile(const PassArgs& a, int t, int pass_r
 }
 
 // One 256-input k-slice (4 groups) of a consumer warp: two 16-row m-tiles against NT
-// 8-token n-tiles.  wb0/wb1: shared addresses of the m-tiles' first rows; xs: the 4
-// activation boxes; ss: the group-sum box; sc/bi: 4 bf16 scales/biases of rows g, g+8
-// of each m-tile.
-template <int NT>
+// 8-token n-tiles.  wb0/wb1: shared addresses of the m-tiles' first rows; xs: the activation
+// boxes (4, or with LO 4 hi + 4 lo); sc: 4 bf16 scales of rows g, g+8 of each m-tile.
+// acc += (scale * 2^24) * C per group; the bias part is added once per chunk (bias_term).
+template <int NT, bool LO>
 __device__ __forceinline__ void consume_stage(float (&acc)[2][NT][4], uint32_t wb0, uint32_t wb1, uint32_t xs,
-                                              uint32_t ss, const uint2 (&sc)[4], const uint2 (&bi)[4], int g, int c) {
+                                              const uint2 (&sc)[4], int g, int c) {
+    constexpr int NB = LO ? 2 : 1;   // activation terms per input
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        uint32_t bf[NT][8];
-        float sx0[NT], sx1[NT];
+        uint32_t bf[NT][NB][8];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int r = nt * 8 + g;
-            const uint32_t rb = xs + q * kXBoxBytes + r * 128;
-            const uint4 v0 = lds_u4(rb + (((2 * c) ^ g) << 4));
-            const uint4 v1 = lds_u4(rb + (((2 * c + 1) ^ g) << 4));
-            bf[nt][0] = v0.x; bf[nt][1] = v0.y; bf[nt][2] = v0.z; bf[nt][3] = v0.w;
-            bf[nt][4] = v1.x; bf[nt][5] = v1.y; bf[nt][6] = v1.z; bf[nt][7] = v1.w;
-            sx0[nt] = lds_f(ss + (nt * 8 + 2 * c) * 16 + q * 4);
-            sx1[nt] = lds_f(ss + (nt * 8 + 2 * c + 1) * 16 + q * 4);
+#pragma unroll
+            for (int hl = 0; hl < NB; ++hl) {
+                const uint32_t rb = xs + (hl * 4 + q) * kXBoxBytes + r * 128;
+                const uint4 v0 = lds_u4(rb + (((2 * c) ^ g) << 4));
+                const uint4 v1 = lds_u4(rb + (((2 * c + 1) ^ g) << 4));
+                bf[nt][hl][0] = v0.x; bf[nt][hl][1] = v0.y; bf[nt][hl][2] = v0.z; bf[nt][hl][3] = v0.w;
+                bf[nt][hl][4] = v1.x; bf[nt][hl][5] = v1.y; bf[nt][hl][6] = v1.z; bf[nt][hl][7] = v1.w;
+            }
         }
         const uint32_t off = (uint32_t)g * 128u + ((uint32_t)((2 * q + (c >> 1)) ^ g) << 4) + ((c & 1) << 3);
 #pragma unroll
@@ -259,33 +263,76 @@ __device__ __forceinline__ void consume_stage(float (&acc)[2][NT][4], uint32_t w
 #pragma unroll
                 for (int i = 0; i < 4; ++i) ct[nt][i] = 0.f;
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint32_t Wl = (s < 2) ? wl.x : wl.y;
-                const uint32_t Wh = (s < 2) ? wh.x : wh.y;
-                uint32_t a0, a1, a2, a3;
-                if ((s & 1) == 0) {
-                    a0 = nib_pair<0>(Wl); a1 = nib_pair<0>(Wh); a2 = nib_pair<1>(Wl); a3 = nib_pair<1>(Wh);
-                } else {
-                    a0 = nib_pair<2>(Wl); a1 = nib_pair<2>(Wh); a2 = nib_pair<3>(Wl); a3 = nib_pair<3>(Wh);
-                }
+            for (int h = 0; h < 2; ++h) {   // word 2c (h = 0) and word 2c+1 (h = 1) of the group
+                const uint32_t Wl = h ? wl.y : wl.x, Wh = h ? wh.y : wh.x;
+                const uint32_t Wl8 = __umulhi(Wl, 0x01000000u), Wh8 = __umulhi(Wh, 0x01000000u);   // >> 8 on the FMA pipe
+                const uint32_t e0 = nib_even(Wl), e1 = nib_even(Wh), o0 = nib_odd(Wl), o1 = nib_odd(Wh);
+                const uint32_t f0 = nib_even(Wl8), f1 = nib_even(Wh8), p0 = nib_odd(Wl8), p1 = nib_odd(Wh8);
+                // step 2h: pairs of n0/n4 and n1/n5; step 2h+1: pairs of n2/n6 and n3/n7
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma16816(ct[nt], a0, a1, a2, a3, bf[nt][2 * s], bf[nt][2 * s + 1]);
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int hl = 0; hl < NB; ++hl) {
+                        mma16816(ct[nt], e0, e1, o0, o1, bf[nt][hl][4 * h], bf[nt][hl][4 * h + 1]);
+                        mma16816(ct[nt], f0, f1, p0, p1, bf[nt][hl][4 * h + 2], bf[nt][hl][4 * h + 3]);
+                    }
             }
-            // affine epilogue of this group: rows g (lo) and g+8 (hi)
+            // scale of this group: rows g (lo) and g+8 (hi); C is in units of 2^-24
             const uint2 slo2 = sc[2 * m], shi2 = sc[2 * m + 1];
-            const uint2 blo2 = bi[2 * m], bhi2 = bi[2 * m + 1];
             const uint32_t swl = (q < 2) ? slo2.x : slo2.y, swh = (q < 2) ? shi2.x : shi2.y;
-            const uint32_t bwl = (q < 2) ? blo2.x : blo2.y, bwh = (q < 2) ? bhi2.x : bhi2.y;
-            const float slo = __uint_as_float((q & 1) ? (swl & 0xFFFF0000u) : (swl << 16));
-            const float shi = __uint_as_float((q & 1) ? (swh & 0xFFFF0000u) : (swh << 16));
-            const float clo = fmaf(-1024.f, slo, __uint_as_float((q & 1) ? (bwl & 0xFFFF0000u) : (bwl << 16)));
-            const float chi = fmaf(-1024.f, shi, __uint_as_float((q & 1) ? (bwh & 0xFFFF0000u) : (bwh << 16)));
+            const float slo = __uint_as_float((q & 1) ? (swl & 0xFFFF0000u) : (swl * 65536u)) * 16777216.f;
+            const float shi = __uint_as_float((q & 1) ? (swh & 0xFFFF0000u) : (swh * 65536u)) * 16777216.f;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                acc[m][nt][0] = fmaf(slo, ct[nt][0], fmaf(clo, sx0[nt], acc[m][nt][0]));
-                acc[m][nt][1] = fmaf(slo, ct[nt][1], fmaf(clo, sx1[nt], acc[m][nt][1]));
-                acc[m][nt][2] = fmaf(shi, ct[nt][2], fmaf(chi, sx0[nt], acc[m][nt][2]));
-                acc[m][nt][3] = fmaf(shi, ct[nt][3], fmaf(chi, sx1[nt], acc[m][nt][3]));
+                acc[m][nt][0] = fmaf(slo, ct[nt][0], acc[m][nt][0]);
+                acc[m][nt][1] = fmaf(slo, ct[nt][1], acc[m][nt][1]);
+                acc[m][nt][2] = fmaf(shi, ct[nt][2], acc[m][nt][2]);
+                acc[m][nt][3] = fmaf(shi, ct[nt][3], acc[m][nt][3]);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// bf16 pair (two consecutive biases) -> fp16 pair
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t v) {
+    return h2_bits(__floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u)));
+}
+
+// acc += sum over groups of b[row][g] * S[token][g] for the warp's rows (lo row pointers br[m],
+// hi rows 8 rows further) and the chunk's tokens; 16 groups per mma, S split into fp16 hi + lo.
+template <int NT>
+__device__ __forceinline__ void bias_term(float (&acc)[2][NT][4], const uint16_t* const (&br)[2], int sstep,
+                                          const float* bsum, int G, int pc, int n, int g, int c) {
+    for (int k0 = 0; k0 < G; k0 += 16) {
+        const bool in0 = k0 + 2 * c < G, in1 = k0 + 2 * c + 8 < G;   // G is a multiple of 4
+        uint32_t shi[NT][2], slo[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int slot = nt * 8 + g;
+            const float* srow = bsum + (size_t)(pc + (slot < n ? slot : 0)) * G + k0 + 2 * c;
+            const float2 v0 = in0 ? *reinterpret_cast<const float2*>(srow) : make_float2(0.f, 0.f);
+            const float2 v1 = in1 ? *reinterpret_cast<const float2*>(srow + 8) : make_float2(0.f, 0.f);
+            const __half2 h0 = __float22half2_rn(v0), h1 = __float22half2_rn(v1);
+            const float2 r0 = __half22float2(h0), r1 = __half22float2(h1);
+            shi[nt][0] = h2_bits(h0);
+            shi[nt][1] = h2_bits(h1);
+            slo[nt][0] = h2_bits(__floats2half2_rn(v0.x - r0.x, v0.y - r0.y));
+            slo[nt][1] = h2_bits(__floats2half2_rn(v1.x - r1.x, v1.y - r1.y));
+        }
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const uint16_t* lo = br[m] + k0 + 2 * c;
+            const uint16_t* hi = lo + sstep;
+            const uint32_t a0 = in0 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(lo)) : 0u;
+            const uint32_t a1 = in0 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(hi)) : 0u;
+            const uint32_t a2 = in1 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(lo + 8)) : 0u;
+            const uint32_t a3 = in1 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(hi + 8)) : 0u;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                mma16816(acc[m][nt], a0, a1, a2, a3, shi[nt][0], shi[nt][1]);
+                mma16816(acc[m][nt], a0, a1, a2, a3, slo[nt][0], slo[nt][1]);
             }
         }
     }
@@ -300,7 +347,7 @@ template <int NT, int PASS>
 __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, uint32_t& it, bool& poisoned,
                                               const Tile& T, int pc, int n, int warp, int lane, float* red) {
     const int g = lane >> 2, c = lane & 3;
-    const int G = a.kdim / kGroup, nst = G / 4;
+    const int nst = a.kdim / kGroup / 4;
     float acc[2][NT][4];
 #pragma unroll
     for (int m = 0; m < 2; ++m)
@@ -309,16 +356,18 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[m][nt][i] = 0.f;
 
-    // scale / bias rows of this lane (lo rows; hi rows are 8 rows further)
+    // scale / bias rows of this lane (lo rows; hi rows are 8 rows further) and the byte
+    // offsets of the m-tiles' first rows inside a stage
+    const int G = a.kdim / kGroup;
     const uint16_t *sr0, *br0, *sr1, *br1;
-    uint32_t wrow_off0, wrow_off1;   // byte offsets of the m-tiles inside a stage
+    uint32_t wrow_off0, wrow_off1;
     if (PASS == 0) {
         const int64_t j = T.row + warp * 16 + g;
         const int64_t rg = (int64_t)T.e * a.wrow0 + j, ru = (int64_t)T.e * a.wrow1 + a.woff1 + j;
         sr0 = a.s0 + rg * G; br0 = a.b0 + rg * G;
         sr1 = a.s1 + ru * G; br1 = a.b1 + ru * G;
-        wrow_off0 = (uint32_t)(warp * 16) * 128u;
-        wrow_off1 = (uint32_t)(128 * 128 + warp * 16 * 128);
+        wrow_off0 = (uint32_t)(warp * 16) * 128u;             // gate box rows 16w..
+        wrow_off1 = (uint32_t)(128 * 128 + warp * 16 * 128);  // up box rows 16w..
     } else {
         const int64_t r = (int64_t)T.e * a.wrow0 + T.row + warp * 32 + g;
         sr0 = a.s0 + r * G; br0 = a.b0 + r * G;
@@ -327,13 +376,11 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
         wrow_off1 = (uint32_t)(warp * 32 + 16) * 128u;
     }
     const int sstep = 8 * G;
-    uint2 sc[4], bi[4];
+    uint2 sc[4];   // the next stage's scales, loaded one stage ahead
     auto load_scales = [&](int st) {
         const int gb = st * 4;
         sc[0] = ldg_u2h(sr0 + gb); sc[1] = ldg_u2h(sr0 + sstep + gb);
         sc[2] = ldg_u2h(sr1 + gb); sc[3] = ldg_u2h(sr1 + sstep + gb);
-        bi[0] = ldg_u2h(br0 + gb); bi[1] = ldg_u2h(br0 + sstep + gb);
-        bi[2] = ldg_u2h(br1 + gb); bi[3] = ldg_u2h(br1 + sstep + gb);
     };
     load_scales(0);
     for (int st = 0; st < nst; ++st) {
@@ -343,19 +390,25 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
             poisoned = true;
             if (lane == 0) atomicOr(a.status, SMOE_FAULT_TIMEOUT);
         }
-        uint2 sc_cur[4], bi_cur[4];
+        uint2 sc_cur[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) { sc_cur[i] = sc[i]; bi_cur[i] = bi[i]; }
-        if (st + 1 < nst) load_scales(st + 1);   // next slice's scales in flight meanwhile
+        for (int i = 0; i < 4; ++i) sc_cur[i] = sc[i];
+        if (st + 1 < nst) load_scales(st + 1);
         const uint32_t base = R.buf + slot * kStageBytes;
-        consume_stage<NT>(acc, base + wrow_off0, base + wrow_off1, base + kXOff, base + kSOff, sc_cur, bi_cur, g, c);
+        consume_stage<NT, PASS == 1>(acc, base + wrow_off0, base + wrow_off1, base + kXOff, sc_cur, g, c);
         mbar_arrive(R.empty + 8 * slot);   // this thread is done reading the slot
         ++it;
     }
+    {
+        const uint16_t* const br[2] = {br0, br1};
+        bias_term<NT>(acc, br, sstep, a.bsum, G, pc, n, g, c);
+    }
 
     if (PASS == 0) {
-        // h = silu(gate) * up -> fp16, pair-permuted columns; per-group sums over 64 columns
-        float hs[NT][2];
+        // h = silu(gate) * up as two fp16 terms hi + lo, pair-permuted columns [0, F) and
+        // [F, 2F), odd columns of every 8 divided by 16; per 64-column group the sum of the
+        // values the stored halves stand for
+        float hs[NT][2];   // [nt][token 2c / 2c+1]
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             hs[nt][0] = hs[nt][1] = 0.f;
@@ -363,14 +416,21 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
             for (int i = 0; i < 4; ++i) {
                 const float gv = acc[0][nt][i], uv = acc[1][nt][i];
                 const float hv = gv / (1.f + expf(-gv)) * uv;
-                const __half hh = __float2half_rn(hv);
                 const int slot = nt * 8 + 2 * c + (i & 1);
                 const int j = T.row + warp * 16 + g + ((i & 2) ? 8 : 0);
+                const bool odd = j & 1;   // same parity as g
+                const float hsv = odd ? hv * 0.0625f : hv;
+                const __half hh = __float2half_rn(hsv);
+                const __half hl = __float2half_rn(hsv - __half2float(hh));
                 if (slot < n) {
                     if (!(fabsf(hv) <= 65504.f)) atomicOr(a.status, SMOE_FAULT_FP16_RANGE);
-                    a.h_out[(size_t)(pc + slot) * a.F + (j & ~7) + perm8(j & 7)] = hh;
+                    __half* row = a.h_out + (size_t)(pc + slot) * (2 * a.F);
+                    const int col = (j & ~7) + perm8(j & 7);
+                    row[col] = hh;
+                    row[a.F + col] = hl;
                 }
-                hs[nt][i & 1] += __half2float(hh);
+                const float stood = __half2float(hh) + __half2float(hl);
+                hs[nt][i & 1] += odd ? stood * 16.f : stood;
             }
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
@@ -423,7 +483,7 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
 template <int PASS>
 __global__ void __launch_bounds__(kPassThreads, 1)
     ffn_pass_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
-                    const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_s, PassArgs a) {
+                    const __grid_constant__ CUtensorMap map_x, PassArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[2 * kStages];
     __shared__ float red[kConsumerWarps * 16];
@@ -449,7 +509,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
     bool poisoned = false;
 
     if (warp == kConsumerWarps) {
-        // ---------------------------------------------------------------- producer
+        // ---------------------------------------------------------------- producer (one thread)
         if (lane == 0) {
             for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
                 const Tile T = decode_tile(a, t, pass_rows);
@@ -476,7 +536,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
                         const uint32_t base = R.buf + slot * kStageBytes;
                         const uint32_t full = R.full + 8 * slot;
                         if (!poisoned) {
-                            mbar_expect_tx(full, kStageTx);
+                            mbar_expect_tx(full, stage_tx(PASS));
                             if (PASS == 0) {
                                 tma_load_2d(base, &map_w0, st * 32, (int)((int64_t)T.e * a.wrow0 + T.row), full);
                                 tma_load_2d(base + 128 * 128, &map_w1, st * 32,
@@ -487,7 +547,12 @@ __global__ void __launch_bounds__(kPassThreads, 1)
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
                                 tma_load_2d(base + kXOff + q * kXBoxBytes, &map_x, (st * 4 + q) * 64, pc, full);
-                            tma_load_2d(base + kSOff, &map_s, st * 4, pc, full);
+                            if (PASS == 1) {   // lo terms of h: columns F.. of the same rows
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    tma_load_2d(base + kXOff + (4 + q) * kXBoxBytes, &map_x,
+                                                a.F + (st * 4 + q) * 64, pc, full);
+                            }
                         }
                         ++it;
                     }
@@ -588,13 +653,10 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     const int sms = sm_count[dev & 63] > 0 ? sm_count[dev & 63] : 1;
 
     // activation / group-sum maps over this call's workspace rows
-    CUtensorMap map_xg, map_sx, map_h, map_sh;
+    CUtensorMap map_xg, map_h;
     if (!encode_map_2d(&map_xg, xg, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, d, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_map_2d(&map_sx, sx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BK, d / kGroup, 4, 16,
-                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_map_2d(&map_h, h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, F, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_map_2d(&map_sh, sh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BK, F / kGroup, 4, 16,
-                       CU_TENSOR_MAP_SWIZZLE_NONE))
+        !encode_map_2d(&map_h, h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, 2 * F, 64, 16,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
 
     const size_t chunks = (size_t)BK * (d / 8);
@@ -604,21 +666,21 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     PassArgs a{};
     a.wrow0 = W.g_rows_per_expert; a.wrow1 = W.u_rows_per_expert; a.woff1 = W.u_row_offset;
     a.s0 = W.sg; a.b0 = W.bg; a.s1 = W.su; a.b1 = W.bu;
-    a.kdim = d; a.F = F; a.d = d; a.K = K; a.E = E; a.B = B;
+    a.bsum = sx; a.kdim = d; a.F = F; a.d = d; a.K = K; a.E = E; a.B = B;
     a.tiles_per_expert = F / 128;
     a.union_ids = union_ids; a.n_union = n_union; a.offsets = offsets;
     a.token_list = token_list; a.slot_list = slot_list;
     a.h_out = h; a.hsum_out = sh; a.y_out = y; a.status = status;
     const int grid0 = std::min(sms, max_u * a.tiles_per_expert);
-    ffn_pass_kernel<0><<<grid0, kPassThreads, kPassSmem, stream>>>(W.map_gate, W.map_up, map_xg, map_sx, a);
+    ffn_pass_kernel<0><<<grid0, kPassThreads, kPassSmem, stream>>>(W.map_gate, W.map_up, map_xg, a);
 
     PassArgs b = a;
     b.wrow0 = d; b.wrow1 = d; b.woff1 = 0;
     b.s0 = W.sd; b.b0 = W.bd; b.s1 = W.sd; b.b1 = W.bd;
-    b.kdim = F;
+    b.bsum = sh; b.kdim = F;
     b.tiles_per_expert = d / 256;
     const int grid1 = std::min(sms, max_u * b.tiles_per_expert);
-    ffn_pass_kernel<1><<<grid1, kPassThreads, kPassSmem, stream>>>(W.map_down, W.map_down, map_h, map_sh, b);
+    ffn_pass_kernel<1><<<grid1, kPassThreads, kPassSmem, stream>>>(W.map_down, W.map_down, map_h, b);
 
     const size_t n4 = (size_t)B * d / 4;
     combine_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, stream>>>(y, topk_w, n_union, offsets, B, K, d,

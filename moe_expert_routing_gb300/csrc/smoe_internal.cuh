@@ -28,10 +28,10 @@ struct WsLayout {
     size_t offsets;       // int32 [E + 1]
     size_t token_list;    // int32 [B * K]
     size_t slot_list;     // int32 [B * K]
-    size_t xg;            // fp16 [B * K, d]: gathered, pair-permuted expert inputs
-    size_t sx;            // fp32 [B * K, d / 64]: per-group sums of xg rows
-    size_t h;             // fp16 [B * K, F]: pair-permuted SwiGLU activations
-    size_t sh;            // fp32 [B * K, F / 64]: per-group sums of h rows
+    size_t xg;            // fp16 [B * K, d]: gathered, pair-permuted expert inputs (odd inputs / 16)
+    size_t sx;            // fp32 [B * K, d / 64]: per-group sums of the inputs
+    size_t h;             // fp16 [B * K, 2F]: SwiGLU activations as hi | lo terms, pair-permuted
+    size_t sh;            // fp32 [B * K, F / 64]: per-group sums of the activations
     size_t y;             // fp32 [B * K, d]: unweighted expert outputs, row t*K + k
     size_t total;
 };

@@ -4,8 +4,10 @@ Routing indices, the union and the token lists must match bit-exactly (layer-0 i
 drawn with a logit gap >= 1e-3 between adjacent ranks 1..K+1); routing weights to 1e-5
 relative; layer outputs to relative L2 <= 5e-3 (on the layer delta and on the output) and
 max-abs <= 2e-2.  Chained stacks are checked layer by layer, teacher-forced: the oracle's
-layer l consumes the GPU's own hidden state h_l, and tokens whose oracle gap between ranks K
-and K+1 is below 1e-4 are exempt from the index comparison (they must stay under 0.1%).
+layer l consumes the GPU's own hidden state h_l.  Tokens whose oracle gap between ranks K and
+K+1 is below 1e-4 are exempt from the index comparison (they must stay under 0.1%); for the
+others the expert set must match exactly and two ranks may only appear swapped where their
+oracle logits tie within 1e-4.
 """
 import numpy as np
 import pytest
@@ -309,8 +311,12 @@ def _chain(name, layers, B=None, sample_rows=None):
         s = -np.sort(-lg, axis=1)
         near = (s[:, w.top_k - 1] - s[:, w.top_k]) < 1e-4
         gi = idx.cpu().numpy()
-        mism = np.any(gi != oi, axis=1)
-        assert not np.any(mism & ~near), f"layer {l}: routing differs on well-separated tokens"
+        for t in np.nonzero(np.any(gi != oi, axis=1) & ~near)[0]:
+            # same expert set; ranks may only swap where the oracle logits tie within 1e-4
+            assert set(gi[t].tolist()) == set(oi[t].tolist()), f"layer {l} token {t}: expert set differs"
+            diff = gi[t] != oi[t]
+            assert np.all(np.abs(lg[t, gi[t][diff]] - lg[t, oi[t][diff]]) < 1e-4), \
+                f"layer {l} token {t}: rank order differs on separated logits"
         exempt += int(near.sum())
         total += B
         rows = sample_rows if sample_rows is not None else list(range(B))
