@@ -39,15 +39,16 @@ smoe_status check_ws(const smoe_layer_desc& D, int B, void* ws, size_t ws_bytes,
 
 // 2-D u32 view [rows, in/8] of a packed weight tensor; box 32 words (4 groups) x box_rows,
 // 128-byte swizzle.
-bool encode_weight_map(CUtensorMap* map, const uint32_t* words, int64_t rows, int64_t in, int box_rows) {
+bool encode_weight_map(CUtensorMap* map, const uint32_t* words, int64_t rows, int64_t in, int box_rows,
+                       int box_words = 32, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)(in / 8), (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(in / 2)};
-    cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {(cuuint32_t)box_words, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(words), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -75,13 +76,19 @@ smoe_status check_weights(const smoe_layer_desc& D, const smoe_expert_weights* W
         P->sg = W->s_gate_up; P->bg = W->b_gate_up; P->g_rows_per_expert = 2 * F;
         P->su = W->s_gate_up; P->bu = W->b_gate_up; P->u_rows_per_expert = 2 * F; P->u_row_offset = F;
     }
+    const CUtensorMapSwizzle none = CU_TENSOR_MAP_SWIZZLE_NONE;
     if (!encode_weight_map(&P->map_down, W->w_down, E * d, F, 256)) return SMOE_ERR_CUDA;
+    if (!encode_weight_map(&P->pm_down, W->w_down, E * d, F, 256, 8, none)) return SMOE_ERR_CUDA;
     if (sep) {
         if (!encode_weight_map(&P->map_gate, W->w_gate, E * F, d, 128)) return SMOE_ERR_CUDA;
         if (!encode_weight_map(&P->map_up, W->w_up, E * F, d, 128)) return SMOE_ERR_CUDA;
+        if (!encode_weight_map(&P->pm_gate, W->w_gate, E * F, d, 128, 8, none)) return SMOE_ERR_CUDA;
+        if (!encode_weight_map(&P->pm_up, W->w_up, E * F, d, 128, 8, none)) return SMOE_ERR_CUDA;
     } else {
         if (!encode_weight_map(&P->map_gate, W->w_gate_up, E * 2 * F, d, 128)) return SMOE_ERR_CUDA;
+        if (!encode_weight_map(&P->pm_gate, W->w_gate_up, E * 2 * F, d, 128, 8, none)) return SMOE_ERR_CUDA;
         P->map_up = P->map_gate;
+        P->pm_up = P->pm_gate;
     }
     return SMOE_OK;
 }
@@ -130,6 +137,8 @@ WsLayout ws_layout(const smoe_layer_desc& D, int max_tokens) {
     L.sx = take(BK * (d / kGroup) * 4);
     L.h = take(BK * 2 * F * 2);
     L.sh = take(BK * (F / kGroup) * 4);
+    L.s16x = take(2 * BK * (d / kGroup) * 2);
+    L.s16h = take(2 * BK * (F / kGroup) * 2);
     L.y = take(BK * d * 4);
     L.total = o;
     return L;

@@ -143,13 +143,15 @@ __device__ __forceinline__ uint4 lds_u4(uint32_t a) {
 // ----------------------------------------------------------------------------- gather
 // One thread per 8-element chunk of a list entry p: xg[p] = pair-permuted fp16(x[token_list[p]])
 // with the odd elements of every 8 divided by 16; sx[p][g] = sum of the values the stored
-// halves stand for in group g (8 consecutive lanes hold a group).
+// halves stand for in group g (8 consecutive lanes hold a group), also as fp16 hi and lo
+// planes s16[0|1][p][g].
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ x, int d, int B,
                                                      const int32_t* __restrict__ n_union,
                                                      const int32_t* __restrict__ offsets,
                                                      const int32_t* __restrict__ token_list,
                                                      uint32_t* __restrict__ status,
-                                                     __half* __restrict__ xg, float* __restrict__ sx) {
+                                                     __half* __restrict__ xg, float* __restrict__ sx,
+                                                     __half* __restrict__ s16, int BK) {
     const int cpr = d / 8;   // chunks per row, a multiple of 32: a warp never spans two rows
     const size_t gid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int p = (int)(gid / cpr), ch = (int)(gid - (size_t)p * cpr);
@@ -180,7 +182,13 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
     reinterpret_cast<uint4*>(xg + (size_t)p * d)[ch] = o;
 #pragma unroll
     for (int off = 1; off < 8; off <<= 1) sa += __shfl_xor_sync(0xffffffffu, sa, off);
-    if ((lane & 7) == 0) sx[(size_t)p * (d / kGroup) + ch / 8] = sa;
+    if ((lane & 7) == 0) {
+        const size_t i = (size_t)p * (d / kGroup) + ch / 8;
+        sx[i] = sa;
+        const __half hh = __float2half_rn(sa);   // hi and lo planes for the tensor-core path
+        s16[i] = hh;
+        s16[(size_t)BK * (d / kGroup) + i] = __float2half_rn(sa - __half2float(hh));
+    }
 }
 
 // ----------------------------------------------------------------------------- expert passes
@@ -205,6 +213,7 @@ struct PassArgs {
     int kdim;             // contraction length (d for pass 0, F for pass 1)
     int F, d, K, E, B;
     int tiles_per_expert;
+    int tc_min;           // experts with at least this many entries belong to the tensor-core path (0: none)
     const int32_t* union_ids; const int32_t* n_union; const int32_t* offsets;
     const int32_t* token_list; const int32_t* slot_list;
     __half* h_out; float* hsum_out;   // pass 0 outputs
@@ -213,7 +222,8 @@ struct PassArgs {
 };
 
 struct Tile {
-    bool ok;
+    bool ok;              // indices valid
+    bool mine;            // handled by this kernel (not by the tensor-core path)
     int e, p0, p1, row;   // row: first h column (pass 0) or output row (pass 1) of the tile
 };
 
@@ -225,6 +235,7 @@ __device__ __forceinline__ Tile decode_tile(const PassArgs& a, int t, int pass_r
     T.p0 = a.offsets[u];
     T.p1 = a.offsets[u + 1];
     T.ok = T.e >= 0 && T.e < a.E && T.p0 >= 0 && T.p1 >= T.p0 && T.p1 <= a.B * a.K;
+    T.mine = a.tc_min <= 0 || T.p1 - T.p0 < a.tc_min;
     return T;
 }
 
@@ -513,7 +524,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
         if (lane == 0) {
             for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
                 const Tile T = decode_tile(a, t, pass_rows);
-                if (!T.ok) continue;
+                if (!T.ok || !T.mine) continue;
                 // scale / bias rows of the tile into L2 ahead of the consumers' loads
                 if (PASS == 0) {
                     const int64_t rg = (int64_t)T.e * a.wrow0 + T.row, ru = (int64_t)T.e * a.wrow1 + a.woff1 + T.row;
@@ -574,6 +585,7 @@ __global__ void __launch_bounds__(kPassThreads, 1)
             if (warp == 0 && lane == 0) atomicOr(a.status, SMOE_FAULT_EXPERT_INDEX);
             continue;
         }
+        if (!T.mine) continue;
         for (int pc = T.p0; pc < T.p1; pc += kTokChunk) {
             const int n = min(kTokChunk, T.p1 - pc);
             if (n <= 8) consume_chunk<1, PASS>(a, R, it, poisoned, T, pc, n, warp, lane, red);
@@ -661,18 +673,33 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
 
     const size_t chunks = (size_t)BK * (d / 8);
     gather_kernel<<<(unsigned)((chunks + 255) / 256), 256, 0, stream>>>(x, d, B, n_union, offsets, token_list, status,
-                                                                          xg, sx);
+                                                                          xg, sx, ws_ptr<__half>(ws, L.s16x), BK);
+
+    // experts with many tokens go to the tcgen05 path; with fewer than 256 tokens in the chunk
+    // an expert rarely reaches the threshold, so the extra launches are skipped
+    const int tc_min = (tc_path_supported(D) && B >= 256) ? kTcMinTokens : 0;
+    FfnTcWeights TW{};
+    TW.pm_gate = W.pm_gate; TW.pm_up = W.pm_up; TW.pm_down = W.pm_down;
+    TW.sg = W.sg; TW.bg = W.bg; TW.g_rows = W.g_rows_per_expert;
+    TW.su = W.su; TW.bu = W.bu; TW.u_rows = W.u_rows_per_expert; TW.u_off = W.u_row_offset;
+    TW.sd = W.sd; TW.bd = W.bd;
 
     PassArgs a{};
     a.wrow0 = W.g_rows_per_expert; a.wrow1 = W.u_rows_per_expert; a.woff1 = W.u_row_offset;
     a.s0 = W.sg; a.b0 = W.bg; a.s1 = W.su; a.b1 = W.bu;
     a.bsum = sx; a.kdim = d; a.F = F; a.d = d; a.K = K; a.E = E; a.B = B;
     a.tiles_per_expert = F / 128;
+    a.tc_min = tc_min;
     a.union_ids = union_ids; a.n_union = n_union; a.offsets = offsets;
     a.token_list = token_list; a.slot_list = slot_list;
     a.h_out = h; a.hsum_out = sh; a.y_out = y; a.status = status;
     const int grid0 = std::min(sms, max_u * a.tiles_per_expert);
     ffn_pass_kernel<0><<<grid0, kPassThreads, kPassSmem, stream>>>(W.map_gate, W.map_up, map_xg, a);
+    if (tc_min > 0) {
+        cudaError_t e = launch_ffn_tc(D, TW, B, 0, union_ids, n_union, offsets, token_list, slot_list, ws, L, tc_min,
+                                      sms, stream);
+        if (e != cudaSuccess) return e;
+    }
 
     PassArgs b = a;
     b.wrow0 = d; b.wrow1 = d; b.woff1 = 0;
@@ -681,6 +708,11 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     b.tiles_per_expert = d / 256;
     const int grid1 = std::min(sms, max_u * b.tiles_per_expert);
     ffn_pass_kernel<1><<<grid1, kPassThreads, kPassSmem, stream>>>(W.map_down, W.map_down, map_h, b);
+    if (tc_min > 0) {
+        cudaError_t e = launch_ffn_tc(D, TW, B, 1, union_ids, n_union, offsets, token_list, slot_list, ws, L, tc_min,
+                                      sms, stream);
+        if (e != cudaSuccess) return e;
+    }
 
     const size_t n4 = (size_t)B * d / 4;
     combine_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, stream>>>(y, topk_w, n_union, offsets, B, K, d,

@@ -1,0 +1,648 @@
+// Expert FFN for experts with many tokens: tcgen05 (5th-generation tensor core) GEMM tiles.
+//
+// Same math as ffn.cu (page "SSD Streaming Expert Layers", "Math Contract" and "Quantized
+// Layout"), for union experts whose token list is long enough (long prompts with hot
+// experts) that the contraction is a real dense GEMM: per expert, D[rows, tokens] =
+// W[rows, k] X[k, tokens], W dequantised from 4-bit affine groups of 64.
+//
+// Exact fp16 weights.  w = s q + b = s (q - 8) + (b + 8 s).  s is bf16 (8-bit significand)
+// and q - 8 a 4-bit signed integer, so s (q - 8) has at most 11 significant bits and is
+// exactly an fp16 number; the rest, eps = b + 8 s, depends only on (row, group).  Hence
+//   sum_i w_i x_i = sum_i [s (q_i - 8)]_fp16 x_i  +  sum_g eps_g S_g,   S_g = sum_{i in g} x_i,
+// the first term one long fp16 contraction with fp32 accumulation in tensor memory, the
+// second a small [rows x groups] x [groups x tokens] product that runs as one extra k-stage
+// (eps as fp16, S as an fp16 hi + lo pair).
+//
+// Tile per CTA: 256 weight rows (two UMMA M=128 accumulators) x 128 tokens; k in stages of
+// one 64-input group.  Warp roles (one CTA per SM, persistent over the work items):
+//   warp 0      producer: TMA of the packed weight rows and the activation rows (B operand)
+//   warp 1      TMEM owner; lane 0 issues tcgen05.mma and tcgen05.commit
+//   warps 2-5   dequantisers: packed nibbles -> fp16 s (q - 8) in the SW128 K-major layout
+//   warps 6-9   epilogue: tcgen05.ld of the accumulators -> SwiGLU (pass 0) or y (pass 1)
+// Accumulators are double-buffered in TMEM (2 x 256 columns) so one tile's epilogue
+// overlaps the next tile's MMAs.  Every mbarrier wait is bounded.
+//
+// Activation layouts are those of ffn.cu (pair-permuted k within every 8 inputs, odd
+// inputs stored divided by 16); the dequantisers write the weights in the same k order and
+// multiply the odd ones by 16, which the fp16 format absorbs exactly.
+#include "smoe_internal.cuh"
+
+#include <cuda.h>
+#include <math.h>
+
+#include <algorithm>
+#include <atomic>
+
+namespace smoe {
+namespace {
+
+constexpr int TC_N = 128;                    // tokens per tile (UMMA N)
+constexpr int TC_STAGES = 3;
+constexpr int TC_A_BYTES = 256 * 128;        // 256 rows x 64 fp16, SW128 K-major
+constexpr int TC_P_BYTES = 256 * 32;         // 256 rows x 8 packed words
+constexpr int TC_B_BYTES = TC_N * 128;       // 128 token rows x 64 fp16, SW128 K-major
+constexpr int TC_OFF_P = TC_A_BYTES;
+constexpr int TC_OFF_B0 = TC_A_BYTES + TC_P_BYTES;
+constexpr int TC_OFF_B1 = TC_OFF_B0 + TC_B_BYTES;
+constexpr int TC_STAGE = TC_OFF_B1 + TC_B_BYTES;   // 72 KB, a 1024-byte multiple
+constexpr int TC_SMEM = TC_STAGES * TC_STAGE + 1024;
+constexpr int TC_THREADS = 320;
+constexpr uint32_t TC_TMEM_COLS = 512;
+
+// ----------------------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+// Bounded wait (~0.5 s): true when the phase with this parity completed.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((i & 1023) == 0) {
+            uint64_t now;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+            if (i == 0) t0 = now;
+            else if (now - t0 > 500000000ull) return false;
+        }
+    }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 B
+// apart; start address advanced by 32 B per 16-element k step inside the swizzle atom.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+    uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;            // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: next 8-row group
+    d |= (uint64_t)1 << 46;            // descriptor version
+    d |= (uint64_t)2 << 61;            // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B, fp32 D, both K-major, M = 128, N = TC_N.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(TC_N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// storage slot of logical element m (0..7) inside an 8-element chunk: (0,4,1,5,2,6,3,7)
+__device__ __forceinline__ int perm8(int m) { return 2 * (m & 3) + (m >> 2); }
+
+// One packed word (8 nibbles of a row) -> 8 fp16 weights s (q - 8) in storage order, odd
+// elements times 16 (exact): (n0, n4), 16 (n1, n5), (n2, n6), 16 (n3, n7).
+__device__ __forceinline__ uint4 dequant_word(uint32_t w, __half2 s2) {
+    const __half2 o1 = u2h(0x64086408u);   // 1032 = 1024 + 8
+    const __half2 o2 = u2h(0x64806480u);   // 1152 = 1024 + 16 * 8
+    const uint32_t w8 = w >> 8;
+    uint4 r;
+    r.x = h2u(__hmul2(__hsub2(u2h((w & 0x000F000Fu) | 0x64006400u), o1), s2));
+    r.y = h2u(__hmul2(__hsub2(u2h((w & 0x00F000F0u) | 0x64006400u), o2), s2));
+    r.z = h2u(__hmul2(__hsub2(u2h((w8 & 0x000F000Fu) | 0x64006400u), o1), s2));
+    r.w = h2u(__hmul2(__hsub2(u2h((w8 & 0x00F000F0u) | 0x64006400u), o2), s2));
+    return r;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+struct TcArgs {
+    int64_t wrow0, wrow1, woff1;      // rows per expert (map_w0 / map_w1), first up row inside an expert
+    const uint16_t* s0; const uint16_t* b0;   // scales / biases of map_w0 rows
+    const uint16_t* s1; const uint16_t* b1;   // scales / biases of map_w1 rows (pass 0 up)
+    int kdim, F, d, K, E, B;
+    int m_tiles;                      // 256-row tiles per expert
+    int tc_min;                       // experts with at least this many entries take this path
+    const int32_t* union_ids; const int32_t* n_union; const int32_t* offsets;
+    const int32_t* token_list; const int32_t* slot_list;
+    __half* h_out;                    // pass 0: [B*K, 2F] hi | lo
+    float* y_out;                     // pass 1: [B*K, d]
+    uint32_t* status;
+};
+
+struct Item {
+    int e, p0, n, mt, nt;             // expert, first list entry, entries, row tile, token tile
+};
+
+// Work items: for every union expert with n >= tc_min, m_tiles x ceil(n / TC_N) tiles.  The
+// per-expert prefix (up to 256 experts) is built by warp 0 in shared memory.
+__device__ int build_items(const TcArgs& a, int* pref) {
+    __shared__ int total;
+    if (threadIdx.x < 32) {
+        const int nu = *a.n_union;
+        int run = 0;
+        for (int base = 0; base < nu; base += 32) {
+            const int u = base + threadIdx.x;
+            int cnt = 0;
+            if (u < nu) {
+                const int n = a.offsets[u + 1] - a.offsets[u];
+                if (n >= a.tc_min) cnt = a.m_tiles * ((n + TC_N - 1) / TC_N);
+            }
+            int incl = cnt;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, off);
+                if ((int)threadIdx.x >= off) incl += v;
+            }
+            if (u < nu) pref[u] = run + incl - cnt;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (threadIdx.x == 0) {
+            total = run;
+            pref[nu] = run;
+        }
+    }
+    __syncthreads();
+    return total;
+}
+
+__device__ __forceinline__ Item decode_item(const TcArgs& a, const int* pref, int t) {
+    const int nu = *a.n_union;
+    int lo = 0, hi = nu;   // largest u with pref[u] <= t
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pref[mid] <= t) lo = mid;
+        else hi = mid;
+    }
+    // skip experts with no items (pref[u] == pref[u+1])
+    while (lo + 1 < nu && pref[lo + 1] <= t) ++lo;
+    Item it;
+    it.e = a.union_ids[lo];
+    it.p0 = a.offsets[lo];
+    it.n = a.offsets[lo + 1] - it.p0;
+    const int r = t - pref[lo];
+    it.nt = r / a.m_tiles;
+    it.mt = r - it.nt * a.m_tiles;
+    return it;
+}
+
+template <int PASS>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    ffn_tc_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
+                  const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_shi,
+                  const __grid_constant__ CUtensorMap map_slo, TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full[TC_STAGES], deq[TC_STAGES], empty[TC_STAGES];
+    __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int pref[kMaxExperts + 1];
+    __shared__ int tok_sh[2][TC_N], slot_sh[2][TC_N];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int G = a.kdim / kGroup;
+    const int n_main = G;                        // one stage per group
+    const int n_corr = (G + 63) / 64;            // eps x S stages
+    const int n_st = n_main + n_corr;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TC_STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&deq[s]), 128);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&acc_full[b]), 1);
+            mbar_init(smem_u32(&acc_empty[b]), 128);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                         smem_u32(&tmem_base_sh)),
+                     "r"(TC_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+    const int n_items = build_items(a, pref);
+    bool poisoned = false;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int t = blockIdx.x; t < n_items; t += gridDim.x) {
+                const Item I = decode_item(a, pref, t);
+                const int row0 = I.mt * 256;   // pass 0: h columns [row0/2, row0/2 + 128); pass 1: down rows
+                const int tok0 = I.p0 + I.nt * TC_N;
+                for (int st = 0; st < n_st; ++st, ++it) {
+                    const uint32_t s = it % TC_STAGES;
+                    if (it >= TC_STAGES && !poisoned &&
+                        !mbar_wait(smem_u32(&empty[s]), ((it / TC_STAGES) - 1) & 1u)) {
+                        poisoned = true;
+                        atomicOr(a.status, SMOE_FAULT_TIMEOUT);
+                    }
+                    if (poisoned) continue;
+                    const uint32_t stg = sbase + s * TC_STAGE;
+                    const uint32_t bar = smem_u32(&full[s]);
+                    if (st < n_main) {
+                        const uint32_t bytes = TC_P_BYTES + (PASS == 1 ? 2 : 1) * TC_B_BYTES;
+                        mbar_expect_tx(bar, bytes);
+                        if (PASS == 0) {
+                            const int j0 = row0 / 2;   // 128 h columns: gate rows and up rows
+                            tma_load_2d(stg + TC_OFF_P, &map_w0, st * 8, (int)(I.e * a.wrow0 + j0), bar);
+                            tma_load_2d(stg + TC_OFF_P + 128 * 32, &map_w1, st * 8, (int)(I.e * a.wrow1 + a.woff1 + j0),
+                                        bar);
+                            tma_load_2d(stg + TC_OFF_B0, &map_b, st * 64, tok0, bar);
+                        } else {
+                            tma_load_2d(stg + TC_OFF_P, &map_w0, st * 8, (int)(I.e * a.wrow0 + row0), bar);
+                            tma_load_2d(stg + TC_OFF_B0, &map_b, st * 64, tok0, bar);            // h hi
+                            tma_load_2d(stg + TC_OFF_B1, &map_b, a.F + st * 64, tok0, bar);      // h lo
+                        }
+                    } else {
+                        const int c = st - n_main;
+                        mbar_expect_tx(bar, 2 * TC_B_BYTES);
+                        tma_load_2d(stg + TC_OFF_B0, &map_shi, c * 64, tok0, bar);
+                        tma_load_2d(stg + TC_OFF_B1, &map_slo, c * 64, tok0, bar);
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, tile = 0;
+            for (int t = blockIdx.x; t < n_items; t += gridDim.x, ++tile) {
+                const uint32_t buf = tile & 1u;
+                if (tile >= 2 && !poisoned && !mbar_wait(smem_u32(&acc_empty[buf]), ((tile >> 1) - 1) & 1u)) {
+                    poisoned = true;
+                    atomicOr(a.status, SMOE_FAULT_TIMEOUT);
+                }
+                tc_fence_after();
+                for (int st = 0; st < n_st; ++st, ++it) {
+                    const uint32_t s = it % TC_STAGES;
+                    if (!poisoned && !mbar_wait(smem_u32(&deq[s]), (it / TC_STAGES) & 1u)) {
+                        poisoned = true;
+                        atomicOr(a.status, SMOE_FAULT_TIMEOUT);
+                    }
+                    if (!poisoned && !mbar_wait(smem_u32(&full[s]), (it / TC_STAGES) & 1u)) {
+                        poisoned = true;
+                        atomicOr(a.status, SMOE_FAULT_TIMEOUT);
+                    }
+                    if (poisoned) continue;
+                    tc_fence_after();
+                    const uint32_t stg = sbase + s * TC_STAGE;
+                    const int nb = (PASS == 1 || st >= n_main) ? 2 : 1;
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        const uint32_t d_tmem = tmem + buf * 256 + m * TC_N;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = sw128_desc(stg + m * 16384 + kk * 32);
+                            for (int b = 0; b < nb; ++b) {
+                                const uint64_t bd = sw128_desc(stg + TC_OFF_B0 + b * TC_B_BYTES + kk * 32);
+                                umma_f16(d_tmem, ad, bd, (st > 0 || kk > 0 || b > 0) ? 1u : 0u);
+                            }
+                        }
+                    }
+                    umma_commit(smem_u32(&empty[s]));    // frees the stage when these MMAs finish
+                }
+                if (!poisoned) umma_commit(smem_u32(&acc_full[buf]));   // accumulators of this tile ready
+            }
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------------------ dequantisers
+        const int t = threadIdx.x - 64;   // 0..127: A rows t (m-tile 0) and t + 128 (m-tile 1)
+        uint32_t it = 0;
+        for (int ti = blockIdx.x; ti < n_items; ti += gridDim.x) {
+            const Item I = decode_item(a, pref, ti);
+            const int row0 = I.mt * 256;
+            // source rows of A rows t and t + 128
+            int64_t src[2];
+            const uint16_t* sp[2];
+            const uint16_t* bp[2];
+            uint32_t prow[2];   // packed row inside the stage's packed tile
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const int r = t + 128 * m;
+                if (PASS == 0) {
+                    const int i = (r >> 7) * 64 + ((r & 127) >> 1);   // h column offset inside the tile
+                    const bool up = r & 1;
+                    src[m] = up ? (int64_t)I.e * a.wrow1 + a.woff1 + row0 / 2 + i : (int64_t)I.e * a.wrow0 + row0 / 2 + i;
+                    sp[m] = up ? a.s1 : a.s0;
+                    bp[m] = up ? a.b1 : a.b0;
+                    prow[m] = (up ? 128 : 0) + i;
+                } else {
+                    src[m] = (int64_t)I.e * a.wrow0 + row0 + r;
+                    sp[m] = a.s0;
+                    bp[m] = a.b0;
+                    prow[m] = r;
+                }
+            }
+            uint4 scl[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};   // 8 bf16 scales of each row
+            for (int st = 0; st < n_st; ++st, ++it) {
+                const uint32_t s = it % TC_STAGES;
+                if (st < n_main && (st & 7) == 0) {
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) scl[m] = __ldg(reinterpret_cast<const uint4*>(sp[m] + src[m] * G + st));
+                }
+                if (!poisoned && !mbar_wait(smem_u32(&full[s]), (it / TC_STAGES) & 1u)) {
+                    poisoned = true;
+                    atomicOr(a.status, SMOE_FAULT_TIMEOUT);
+                }
+                const uint32_t stg = sbase + s * TC_STAGE;
+                if (!poisoned) {
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        const int r = t + 128 * m;
+                        const uint32_t arow = stg + (uint32_t)r * 128u;
+                        if (st < n_main) {
+                            const uint32_t sw = (&scl[m].x)[(st & 7) >> 1];
+                            const float sf = __uint_as_float((st & 1) ? (sw & 0xFFFF0000u) : (sw << 16));
+                            const __half2 s2 = __float2half2_rn(sf);   // exact: bf16 -> fp16
+                            const uint32_t pk = stg + TC_OFF_P + prow[m] * 32u;
+                            const uint4 w0 = lds128(pk), w1 = lds128(pk + 16);
+                            const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                sts128(arow + ((uint32_t)(c ^ (r & 7)) << 4), dequant_word(wv[c], s2));
+                        } else {
+                            // eps = b + 8 s for groups 64c .. 64c + 63 (zero beyond G)
+                            const int g0 = (st - n_main) * 64;
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                uint32_t hv[4];
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    float e2[2];
+#pragma unroll
+                                    for (int h = 0; h < 2; ++h) {
+                                        const int g = g0 + c * 8 + q * 2 + h;
+                                        float ev = 0.f;
+                                        if (g < G) {
+                                            const float sv = __uint_as_float((uint32_t)__ldg(sp[m] + src[m] * G + g) << 16);
+                                            const float bv = __uint_as_float((uint32_t)__ldg(bp[m] + src[m] * G + g) << 16);
+                                            ev = fmaf(8.f, sv, bv);
+                                        }
+                                        e2[h] = ev;
+                                    }
+                                    hv[q] = h2u(__floats2half2_rn(e2[0], e2[1]));
+                                }
+                                sts128(arow + ((uint32_t)(c ^ (r & 7)) << 4), make_uint4(hv[0], hv[1], hv[2], hv[3]));
+                            }
+                        }
+                    }
+                    fence_proxy_async();   // generic-proxy writes -> visible to the tensor core
+                }
+                mbar_arrive(smem_u32(&deq[s]));
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------ epilogue
+        const int q = warp & 3;                  // TMEM lane quarter of this warp
+        const int et = threadIdx.x - 192;        // 0..127
+        const int lr = q * 32 + lane;            // accumulator row (TMEM lane) of this thread
+        uint32_t tile = 0;
+        for (int t = blockIdx.x; t < n_items; t += gridDim.x, ++tile) {
+            const Item I = decode_item(a, pref, t);
+            const uint32_t buf = tile & 1u;
+            const int row0 = I.mt * 256;
+            const int tok0 = I.p0 + I.nt * TC_N;
+            const int ntok = min(TC_N, I.n - I.nt * TC_N);
+            // token / slot of the tile's entries (pass 1 output rows)
+            if (PASS == 1) {
+                for (int j = et; j < TC_N; j += 128) {
+                    tok_sh[buf][j] = j < ntok ? a.token_list[tok0 + j] : 0;
+                    slot_sh[buf][j] = j < ntok ? a.slot_list[tok0 + j] : 0;
+                }
+                asm volatile("bar.sync 2, 128;\n" ::: "memory");
+            }
+            if (!poisoned && !mbar_wait(smem_u32(&acc_full[buf]), (tile >> 1) & 1u)) {
+                poisoned = true;
+                atomicOr(a.status, SMOE_FAULT_TIMEOUT);
+            }
+            tc_fence_after();
+            if (!poisoned) {
+#pragma unroll 1
+                for (int m = 0; m < 2; ++m) {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < TC_N; c0 += 32) {
+                        float v[32];
+                        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * 256 + m * TC_N + c0, v);
+                        if (c0 >= ntok) continue;
+                        if (PASS == 0) {
+                            // lanes 2i (gate) and 2i+1 (up) of h column i; the even lane takes
+                            // tokens 0..15 of the chunk, the odd lane tokens 16..31
+                            const bool odd_lane = lane & 1;
+                            const int j = row0 / 2 + m * 64 + (lr >> 1);   // h column
+                            const bool odd_col = j & 1;
+                            const int col = (j & ~7) + perm8(j & 7);
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) {
+                                const float mine = v[odd_lane ? k : 16 + k];         // value the partner needs
+                                const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+                                const float g = odd_lane ? other : v[k];
+                                const float u = odd_lane ? v[16 + k] : other;
+                                const int tk = c0 + (odd_lane ? 16 + k : k);
+                                if (tk < ntok) {
+                                    const float hv = g / (1.f + expf(-g)) * u;
+                                    if (!(fabsf(hv) <= 65504.f)) atomicOr(a.status, SMOE_FAULT_FP16_RANGE);
+                                    const float hs = odd_col ? hv * 0.0625f : hv;
+                                    const __half hh = __float2half_rn(hs);
+                                    const __half hl = __float2half_rn(hs - __half2float(hh));
+                                    __half* rowp = a.h_out + (size_t)(tok0 + tk) * (2 * a.F);
+                                    rowp[col] = hh;
+                                    rowp[a.F + col] = hl;
+                                }
+                            }
+                        } else {
+                            const int r = row0 + m * 128 + lr;   // output row
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) {
+                                const int tk = c0 + k;
+                                if (tk < ntok) {
+                                    const int tok = tok_sh[buf][tk], sl = slot_sh[buf][tk];
+                                    if (tok >= 0 && tok < a.B && sl >= 0 && sl < a.K)
+                                        a.y_out[((size_t)tok * a.K + sl) * a.d + r] = v[k];
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&acc_empty[buf]));
+        }
+    }
+
+    // all roles done; the accumulators are no longer read: release the tensor memory
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(TC_TMEM_COLS)
+                     : "memory");
+}
+
+// Group sums of the SwiGLU activations (actual values: hi + lo, odd columns times 16) of
+// every list entry, as fp16 hi and lo planes [B*K, F/64]: the S operand of pass 1's eps stage.
+__global__ void __launch_bounds__(256) hsum_kernel(const __half* __restrict__ h, int F,
+                                                   const int32_t* __restrict__ n_union,
+                                                   const int32_t* __restrict__ offsets, __half* __restrict__ shi,
+                                                   __half* __restrict__ slo) {
+    const int G = F / kGroup;
+    const size_t w = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;   // one warp per (entry, group)
+    const int lane = threadIdx.x & 31;
+    const int total = offsets[*n_union];
+    const int p = (int)(w / G), g = (int)(w - (size_t)p * G);
+    if (p >= total) return;
+    const __half* row = h + (size_t)p * (2 * F) + g * 64;
+    const int c0 = 2 * lane;   // two consecutive stored columns per lane
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int c = c0 + k;
+        const float v = __half2float(row[c]) + __half2float(row[F + c]);
+        s += (c & 2) ? v * 16.f : v;   // storage slots 2, 3, 6, 7 hold the odd columns (stored / 16)
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) {
+        const __half hh = __float2half_rn(s);
+        shi[(size_t)p * G + g] = hh;
+        slo[(size_t)p * G + g] = __float2half_rn(s - __half2float(hh));
+    }
+}
+
+bool encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize, int64_t rows, int64_t cols,
+                int box_cols, int box_rows, CUtensorMapSwizzle swz) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(cols * esize)};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool tc_path_supported(const smoe_layer_desc& D) {
+    return D.d_model % 512 == 0 && D.ffn_dim % 512 == 0 && D.d_model / kGroup <= 64 * 4 && D.ffn_dim / kGroup <= 64 * 4;
+}
+
+cudaError_t launch_ffn_tc(const smoe_layer_desc& D, const FfnTcWeights& W, int B, int pass,
+                          const int32_t* union_ids, const int32_t* n_union, const int32_t* offsets,
+                          const int32_t* token_list, const int32_t* slot_list, void* ws, const WsLayout& L,
+                          int tc_min, int sms, cudaStream_t stream) {
+    const int d = D.d_model, F = D.ffn_dim, K = D.top_k, E = D.num_experts;
+    const int BK = B * K;
+    static std::atomic<uint64_t> attr_done{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load() & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(ffn_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(ffn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(bit);
+    }
+    __half* xg = ws_ptr<__half>(ws, L.xg);
+    __half* h = ws_ptr<__half>(ws, L.h);
+    __half* sxh = ws_ptr<__half>(ws, L.s16x);
+    __half* shh = ws_ptr<__half>(ws, L.s16h);
+    const int Gx = d / kGroup, Gh = F / kGroup;
+
+    TcArgs a{};
+    a.kdim = pass == 0 ? d : F;
+    a.F = F; a.d = d; a.K = K; a.E = E; a.B = B;
+    a.tc_min = tc_min;
+    a.union_ids = union_ids; a.n_union = n_union; a.offsets = offsets;
+    a.token_list = token_list; a.slot_list = slot_list;
+    a.h_out = h; a.y_out = ws_ptr<float>(ws, L.y);
+    a.status = ws_ptr<uint32_t>(ws, L.status);
+    CUtensorMap mb, mshi, mslo;
+    if (pass == 0) {
+        a.wrow0 = W.g_rows; a.wrow1 = W.u_rows; a.woff1 = W.u_off;
+        a.s0 = W.sg; a.b0 = W.bg; a.s1 = W.su; a.b1 = W.bu;
+        a.m_tiles = F / 128;
+        if (!encode_map(&mb, xg, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, d, 64, TC_N, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_map(&mshi, sxh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gx, 64, TC_N, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_map(&mslo, sxh + (size_t)BK * Gx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gx, 64, TC_N,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+        const int grid = std::max(1, std::min(sms, E * (F / 128) * ((BK + TC_N - 1) / TC_N)));
+        ffn_tc_kernel<0><<<grid, TC_THREADS, TC_SMEM, stream>>>(W.pm_gate, W.pm_up, mb, mshi, mslo, a);
+    } else {
+        const size_t nw = (size_t)BK * Gh;
+        hsum_kernel<<<(unsigned)((nw * 32 + 255) / 256), 256, 0, stream>>>(h, F, n_union, offsets, shh, shh + nw);
+        a.wrow0 = d; a.wrow1 = d; a.woff1 = 0;
+        a.s0 = W.sd; a.b0 = W.bd; a.s1 = W.sd; a.b1 = W.bd;
+        a.m_tiles = d / 256;
+        if (!encode_map(&mb, h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, 2 * F, 64, TC_N, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_map(&mshi, shh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gh, 64, TC_N, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_map(&mslo, shh + nw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gh, 64, TC_N,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+        const int grid = std::max(1, std::min(sms, E * (d / 256) * ((BK + TC_N - 1) / TC_N)));
+        ffn_tc_kernel<1><<<grid, TC_THREADS, TC_SMEM, stream>>>(W.pm_down, W.pm_down, mb, mshi, mslo, a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace smoe

@@ -32,6 +32,8 @@ struct WsLayout {
     size_t sx;            // fp32 [B * K, d / 64]: per-group sums of the inputs
     size_t h;             // fp16 [B * K, 2F]: SwiGLU activations as hi | lo terms, pair-permuted
     size_t sh;            // fp32 [B * K, F / 64]: per-group sums of the activations
+    size_t s16x;          // fp16 [2][B * K, d / 64]: input group sums as hi and lo planes
+    size_t s16h;          // fp16 [2][B * K, F / 64]: activation group sums as hi and lo planes
     size_t y;             // fp32 [B * K, d]: unweighted expert outputs, row t*K + k
     size_t total;
 };
@@ -59,10 +61,28 @@ cudaError_t launch_union(const smoe_layer_desc& D, const int32_t* topk_idx, int 
 // of expert e start at e * 2F + F (u_row_offset = F).
 struct FfnPointers {
     CUtensorMap map_gate, map_up, map_down;
+    CUtensorMap pm_gate, pm_up, pm_down;   // packed-word maps of the tensor-core path
     const uint16_t* sg; const uint16_t* bg; int64_t g_rows_per_expert;
     const uint16_t* su; const uint16_t* bu; int64_t u_rows_per_expert; int64_t u_row_offset;
     const uint16_t* sd; const uint16_t* bd;
 };
+
+// The tensor-core path reads the packed weights through maps with a 32-byte box (one
+// group of 8 words) x 128 rows (gate, up) or 256 rows (down), no swizzle.
+struct FfnTcWeights {
+    CUtensorMap pm_gate, pm_up, pm_down;
+    const uint16_t* sg; const uint16_t* bg; int64_t g_rows;
+    const uint16_t* su; const uint16_t* bu; int64_t u_rows; int64_t u_off;
+    const uint16_t* sd; const uint16_t* bd;
+};
+
+// Experts with at least this many list entries take the tcgen05 path (when the shape allows).
+constexpr int kTcMinTokens = 64;
+bool tc_path_supported(const smoe_layer_desc& D);
+cudaError_t launch_ffn_tc(const smoe_layer_desc& D, const FfnTcWeights& W, int B, int pass,
+                          const int32_t* union_ids, const int32_t* n_union, const int32_t* offsets,
+                          const int32_t* token_list, const int32_t* slot_list, void* ws, const WsLayout& L,
+                          int tc_min, int sms, cudaStream_t stream);
 
 cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uint16_t* x, int B,
                        const int32_t* union_ids, const int32_t* n_union, const int32_t* offsets,

@@ -243,6 +243,32 @@ def test_hot_experts_many_tokens_per_expert():
     assert torch.all(out == out[0])
 
 
+@pytest.mark.parametrize("layout", ["separate", "fused"])
+def test_tensor_core_path_many_tokens_per_expert(layout):
+    """512 tokens over 16 experts (top-4): every expert has ~128 entries and runs on the
+    tcgen05 path (d and ffn_dim multiples of 512, B >= 256)."""
+    w = W.scaled(W.WORKLOADS["toy"], ffn_dim=512, tokens=512, layout=layout)
+    c = Case(w)
+    out, idx, _ = c.run_layer()
+    o64, oidx, _, _ = c.oracle_layer()
+    assert np.array_equal(idx.numpy(), oidx)
+    counts = np.bincount(oidx.ravel(), minlength=w.num_experts)
+    assert counts.min() >= 64
+    check_outputs(out.numpy(), o64, c.x.float().numpy())
+
+
+def test_tensor_core_and_small_paths_mixed():
+    """Skewed routing: a few hot experts on the tcgen05 path, the rest on the mma.sync path."""
+    w = W.scaled(W.WORKLOADS["toy"], ffn_dim=512, tokens=384, num_experts=32, zipf_s=1.1)
+    c = Case(w)
+    out, idx, _ = c.run_layer()
+    o64, oidx, _, _ = c.oracle_layer()
+    assert np.array_equal(idx.numpy(), oidx)
+    counts = np.bincount(oidx.ravel(), minlength=w.num_experts)
+    assert counts.max() >= 64 and (counts[counts > 0] < 64).any()
+    check_outputs(out.numpy(), o64, c.x.float().numpy())
+
+
 def test_top1_routing():
     w = W.scaled(W.WORKLOADS["toy"], top_k=1)
     c = Case(w)
