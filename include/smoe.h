@@ -169,10 +169,11 @@ SMOE_API smoe_status smoe_rmsnorm_bf16(const float* h, float eps, int32_t center
  * inside a host application that owns the device-memory budget, or a latency-critical loop
  * that cannot risk the device-wide synchronisation of a cudaMalloc).  The pages have no
  * counterpart: it is an addition of this library.  Arguments and results are those of
- * smoe_route; the split-K scratch is a fixed 1 MiB device array inside the library (held by
- * every GPU that loads it until the process exits), so a call needs
- * splits * B * num_experts <= 262144 floats (B <= 128 at 128 experts) and returns
- * SMOE_ERR_UNSUPPORTED beyond that, without launching.  The first call on a device looks up
+ * smoe_route; the split-K scratch is a fixed 4 MiB device array inside the library (held by
+ * every GPU that loads it until the process exits).  A call needs B * num_experts <= 2^20
+ * (B <= 8192 at 128 experts) and returns SMOE_ERR_UNSUPPORTED beyond that, without launching.
+ * Up to B = 256 at 128 experts the results equal smoe_route's; beyond, fewer split-K partials
+ * fit and the logits differ from smoe_route's by fp32 summation order only.  The first call on a device looks up
  * the array's address (cudaGetSymbolAddress) with that device current: make it before any
  * stream capture.  All calls share the array: calls that overlap on the GPU race and must be
  * ordered by the caller.  Allocates nothing. */

@@ -114,9 +114,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 WsLayout ws_layout(const smoe_layer_desc& D, int max_tokens) {
     const size_t B = max_tokens > 0 ? (size_t)max_tokens : 1, E = D.num_experts, K = D.top_k;
     const size_t d = D.d_model, F = D.ffn_dim, BK = B * K;
-    // max over b <= B of splits(b) * b; splits(b) is constant between multiples of 16
+    // max over b <= B of splits(b) * b; splits(b) is constant between multiples of 8
     size_t max_split_rows = 0;
-    for (size_t b = 16; b < B + 16; b += 16) {
+    for (size_t b = 8; b < B + 8; b += 8) {
         const size_t bb = b < B ? b : B;
         const size_t v = (size_t)route_splits((int)bb, (int)E, (int)d) * bb;
         if (v > max_split_rows) max_split_rows = v;

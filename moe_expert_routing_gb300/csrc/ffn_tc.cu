@@ -14,13 +14,18 @@
 // (eps as fp16, S as an fp16 hi + lo pair).
 //
 // Tile per CTA: 256 weight rows (two UMMA M=128 accumulators) x 128 tokens; k in stages of
-// one 64-input group.  Warp roles (one CTA per SM, persistent over the work items):
+// one 64-input group.  Two shared-memory rings: a TMA ring (packed weights + activation rows;
+// 6 slots in pass 0, 3 in pass 1) deep enough to cover the copy latency, and a 2-slot ring of
+// dequantised fp16 weights.  Warp roles (one CTA per SM, persistent over the work items):
 //   warp 0      producer: TMA of the packed weight rows and the activation rows (B operand)
 //   warp 1      TMEM owner; lane 0 issues tcgen05.mma and tcgen05.commit
-//   warps 2-5   dequantisers: packed nibbles -> fp16 s (q - 8) in the SW128 K-major layout
-//   warps 6-9   epilogue: tcgen05.ld of the accumulators -> SwiGLU (pass 0) or y (pass 1)
+//   warps 2-9   dequantisers, one A row each: packed nibbles -> fp16 s (q - 8) in the SW128
+//               K-major layout
+//   warps 10-13 epilogue: tcgen05.ld of the accumulators -> SwiGLU (pass 0) or y (pass 1)
 // Accumulators are double-buffered in TMEM (2 x 256 columns) so one tile's epilogue
-// overlaps the next tile's MMAs.  Every mbarrier wait is bounded.
+// overlaps the next tile's MMAs.  Every mbarrier wait is bounded.  Pass 0's epilogue stages
+// h through shared memory for 16-byte stores and also writes the per-group sums of h that
+// pass 1's eps stage needs.
 //
 // Activation layouts are those of ffn.cu (pair-permuted k within every 8 inputs, odd
 // inputs stored divided by 16); the dequantisers write the weights in the same k order and
@@ -37,17 +42,28 @@ namespace smoe {
 namespace {
 
 constexpr int TC_N = 128;                    // tokens per tile (UMMA N)
-constexpr int TC_STAGES = 3;
-constexpr int TC_A_BYTES = 256 * 128;        // 256 rows x 64 fp16, SW128 K-major
-constexpr int TC_P_BYTES = 256 * 32;         // 256 rows x 8 packed words
-constexpr int TC_B_BYTES = TC_N * 128;       // 128 token rows x 64 fp16, SW128 K-major
-constexpr int TC_OFF_P = TC_A_BYTES;
-constexpr int TC_OFF_B0 = TC_A_BYTES + TC_P_BYTES;
-constexpr int TC_OFF_B1 = TC_OFF_B0 + TC_B_BYTES;
-constexpr int TC_STAGE = TC_OFF_B1 + TC_B_BYTES;   // 72 KB, a 1024-byte multiple
-constexpr int TC_SMEM = TC_STAGES * TC_STAGE + 1024;
-constexpr int TC_THREADS = 320;
+constexpr int TC_A_BYTES = 256 * 128;        // A slot: 256 rows x 64 fp16, SW128 K-major
+constexpr int TC_A_SLOTS = 2;
+constexpr int TC_P_BYTES = 256 * 32;         // packed weights: 256 rows x 8 words
+constexpr int TC_B_BYTES = TC_N * 128;       // one B sub-tile: 128 token rows x 64 fp16, SW128 K-major
+constexpr int TC_H_BYTES = 32 * 64 * 4;      // pass 0 epilogue staging: 32 tokens x 64 h columns fp32
+constexpr int TC_THREADS = 448;
 constexpr uint32_t TC_TMEM_COLS = 512;
+
+// Per-pass ring shapes.  Load slot: packed weights, then B sub-tile 0 (x or h hi or S hi),
+// then (pass 1) B sub-tile 1 (h lo or S lo).
+template <int PASS>
+struct TcCfg {
+    static constexpr int kLoadSlots = PASS ? 3 : 6;
+    static constexpr int kNb = PASS ? 2 : 1;                  // B sub-tiles per load slot
+    static constexpr int kSlotBytes = TC_P_BYTES + kNb * TC_B_BYTES;
+    static constexpr int kOffLoad = TC_A_SLOTS * TC_A_BYTES;
+    static constexpr int kOffStage = kOffLoad + kLoadSlots * kSlotBytes;   // epilogue staging
+    static constexpr int kSmem = kOffStage + (PASS ? 0 : TC_H_BYTES) + 1024;
+    static constexpr int kCorr = PASS ? 1 : 2;                // eps stages (pass 0: S hi, S lo)
+};
+static_assert(TcCfg<0>::kSmem <= 227 * 1024 - 4096, "pass 0 shared memory");
+static_assert(TcCfg<1>::kSmem <= 227 * 1024 - 4096, "pass 1 shared memory");
 
 // ----------------------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -134,6 +150,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// OR of v over the 128 epilogue threads (named barrier 2), so that they all take the same
+// branch around the named barriers that follow.
+__device__ __forceinline__ bool epilogue_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 2, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
@@ -174,6 +202,7 @@ struct TcArgs {
     const int32_t* union_ids; const int32_t* n_union; const int32_t* offsets;
     const int32_t* token_list; const int32_t* slot_list;
     __half* h_out;                    // pass 0: [B*K, 2F] hi | lo
+    __half* hsum_out;                 // pass 0: group sums of h, fp16 planes [2][B*K, F/64]
     float* y_out;                     // pass 1: [B*K, d]
     uint32_t* status;
 };
@@ -239,8 +268,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
                   const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_shi,
                   const __grid_constant__ CUtensorMap map_slo, TcArgs a) {
+    using C = TcCfg<PASS>;
+    constexpr int L = C::kLoadSlots;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full[TC_STAGES], deq[TC_STAGES], empty[TC_STAGES];
+    __shared__ __align__(8) uint64_t full[L], empty_l[L], deq[TC_A_SLOTS], empty_a[TC_A_SLOTS];
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int pref[kMaxExperts + 1];
@@ -249,16 +280,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const int G = a.kdim / kGroup;
-    const int n_main = G;                        // one stage per group
-    const int n_corr = (G + 63) / 64;            // eps x S stages
-    const int n_st = n_main + n_corr;
+    const int G = a.kdim / kGroup;     // <= 64
+    const int n_main = G;              // one stage per group
+    const int n_st = n_main + C::kCorr;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < TC_STAGES; ++s) {
+        for (int s = 0; s < L; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&deq[s]), 128);
-            mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&empty_l[s]), 1);
+        }
+        for (int s = 0; s < TC_A_SLOTS; ++s) {
+            mbar_init(smem_u32(&deq[s]), 256);
+            mbar_init(smem_u32(&empty_a[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&acc_full[b]), 1);
@@ -279,6 +312,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t tmem = tmem_base_sh;
     const int n_items = build_items(a, pref);
     bool poisoned = false;
+    auto fail = [&](bool ok) {
+        if (!ok && !poisoned) {
+            poisoned = true;
+            atomicOr(a.status, SMOE_FAULT_TIMEOUT);
+        }
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------------ producer
@@ -289,34 +328,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const int row0 = I.mt * 256;   // pass 0: h columns [row0/2, row0/2 + 128); pass 1: down rows
                 const int tok0 = I.p0 + I.nt * TC_N;
                 for (int st = 0; st < n_st; ++st, ++it) {
-                    const uint32_t s = it % TC_STAGES;
-                    if (it >= TC_STAGES && !poisoned &&
-                        !mbar_wait(smem_u32(&empty[s]), ((it / TC_STAGES) - 1) & 1u)) {
-                        poisoned = true;
-                        atomicOr(a.status, SMOE_FAULT_TIMEOUT);
-                    }
+                    const uint32_t s = it % L;
+                    if (it >= (uint32_t)L && !poisoned) fail(mbar_wait(smem_u32(&empty_l[s]), ((it / L) - 1) & 1u));
                     if (poisoned) continue;
-                    const uint32_t stg = sbase + s * TC_STAGE;
+                    const uint32_t slot = sbase + C::kOffLoad + s * C::kSlotBytes;
                     const uint32_t bar = smem_u32(&full[s]);
+                    const uint32_t b0 = slot + TC_P_BYTES, b1 = b0 + TC_B_BYTES;
                     if (st < n_main) {
-                        const uint32_t bytes = TC_P_BYTES + (PASS == 1 ? 2 : 1) * TC_B_BYTES;
-                        mbar_expect_tx(bar, bytes);
+                        mbar_expect_tx(bar, TC_P_BYTES + C::kNb * TC_B_BYTES);
                         if (PASS == 0) {
                             const int j0 = row0 / 2;   // 128 h columns: gate rows and up rows
-                            tma_load_2d(stg + TC_OFF_P, &map_w0, st * 8, (int)(I.e * a.wrow0 + j0), bar);
-                            tma_load_2d(stg + TC_OFF_P + 128 * 32, &map_w1, st * 8, (int)(I.e * a.wrow1 + a.woff1 + j0),
-                                        bar);
-                            tma_load_2d(stg + TC_OFF_B0, &map_b, st * 64, tok0, bar);
+                            tma_load_2d(slot, &map_w0, st * 8, (int)(I.e * a.wrow0 + j0), bar);
+                            tma_load_2d(slot + 128 * 32, &map_w1, st * 8, (int)(I.e * a.wrow1 + a.woff1 + j0), bar);
+                            tma_load_2d(b0, &map_b, st * 64, tok0, bar);
                         } else {
-                            tma_load_2d(stg + TC_OFF_P, &map_w0, st * 8, (int)(I.e * a.wrow0 + row0), bar);
-                            tma_load_2d(stg + TC_OFF_B0, &map_b, st * 64, tok0, bar);            // h hi
-                            tma_load_2d(stg + TC_OFF_B1, &map_b, a.F + st * 64, tok0, bar);      // h lo
+                            tma_load_2d(slot, &map_w0, st * 8, (int)(I.e * a.wrow0 + row0), bar);
+                            tma_load_2d(b0, &map_b, st * 64, tok0, bar);          // h hi
+                            tma_load_2d(b1, &map_b, a.F + st * 64, tok0, bar);    // h lo
                         }
+                    } else if (PASS == 0) {
+                        mbar_expect_tx(bar, TC_B_BYTES);
+                        tma_load_2d(b0, st == n_main ? &map_shi : &map_slo, 0, tok0, bar);
                     } else {
-                        const int c = st - n_main;
                         mbar_expect_tx(bar, 2 * TC_B_BYTES);
-                        tma_load_2d(stg + TC_OFF_B0, &map_shi, c * 64, tok0, bar);
-                        tma_load_2d(stg + TC_OFF_B1, &map_slo, c * 64, tok0, bar);
+                        tma_load_2d(b0, &map_shi, 0, tok0, bar);
+                        tma_load_2d(b1, &map_slo, 0, tok0, bar);
                     }
                 }
             }
@@ -327,134 +363,120 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint32_t it = 0, tile = 0;
             for (int t = blockIdx.x; t < n_items; t += gridDim.x, ++tile) {
                 const uint32_t buf = tile & 1u;
-                if (tile >= 2 && !poisoned && !mbar_wait(smem_u32(&acc_empty[buf]), ((tile >> 1) - 1) & 1u)) {
-                    poisoned = true;
-                    atomicOr(a.status, SMOE_FAULT_TIMEOUT);
-                }
+                if (tile >= 2 && !poisoned) fail(mbar_wait(smem_u32(&acc_empty[buf]), ((tile >> 1) - 1) & 1u));
                 tc_fence_after();
                 for (int st = 0; st < n_st; ++st, ++it) {
-                    const uint32_t s = it % TC_STAGES;
-                    if (!poisoned && !mbar_wait(smem_u32(&deq[s]), (it / TC_STAGES) & 1u)) {
-                        poisoned = true;
-                        atomicOr(a.status, SMOE_FAULT_TIMEOUT);
-                    }
-                    if (!poisoned && !mbar_wait(smem_u32(&full[s]), (it / TC_STAGES) & 1u)) {
-                        poisoned = true;
-                        atomicOr(a.status, SMOE_FAULT_TIMEOUT);
-                    }
+                    const uint32_t s = it % L, sa = it % TC_A_SLOTS;
+                    if (!poisoned) fail(mbar_wait(smem_u32(&deq[sa]), (it / TC_A_SLOTS) & 1u));
+                    if (!poisoned) fail(mbar_wait(smem_u32(&full[s]), (it / L) & 1u));
                     if (poisoned) continue;
                     tc_fence_after();
-                    const uint32_t stg = sbase + s * TC_STAGE;
-                    const int nb = (PASS == 1 || st >= n_main) ? 2 : 1;
+                    const uint32_t abuf = sbase + sa * TC_A_BYTES;
+                    const uint32_t bbuf = sbase + C::kOffLoad + s * C::kSlotBytes + TC_P_BYTES;
 #pragma unroll
                     for (int m = 0; m < 2; ++m) {
                         const uint32_t d_tmem = tmem + buf * 256 + m * TC_N;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = sw128_desc(stg + m * 16384 + kk * 32);
-                            for (int b = 0; b < nb; ++b) {
-                                const uint64_t bd = sw128_desc(stg + TC_OFF_B0 + b * TC_B_BYTES + kk * 32);
+                            const uint64_t ad = sw128_desc(abuf + m * 16384 + kk * 32);
+#pragma unroll
+                            for (int b = 0; b < C::kNb; ++b) {
+                                const uint64_t bd = sw128_desc(bbuf + b * TC_B_BYTES + kk * 32);
                                 umma_f16(d_tmem, ad, bd, (st > 0 || kk > 0 || b > 0) ? 1u : 0u);
                             }
                         }
                     }
-                    umma_commit(smem_u32(&empty[s]));    // frees the stage when these MMAs finish
+                    umma_commit(smem_u32(&empty_l[s]));    // load slot free once these MMAs finish
+                    umma_commit(smem_u32(&empty_a[sa]));   // and the dequantised slot
                 }
                 if (!poisoned) umma_commit(smem_u32(&acc_full[buf]));   // accumulators of this tile ready
             }
         }
-    } else if (warp < 6) {
+    } else if (warp < 10) {
         // ------------------------------------------------------------------ dequantisers
-        const int t = threadIdx.x - 64;   // 0..127: A rows t (m-tile 0) and t + 128 (m-tile 1)
+        const int r = threadIdx.x - 64;   // A row 0..255 (m-tile r >> 7)
         uint32_t it = 0;
         for (int ti = blockIdx.x; ti < n_items; ti += gridDim.x) {
             const Item I = decode_item(a, pref, ti);
             const int row0 = I.mt * 256;
-            // source rows of A rows t and t + 128
-            int64_t src[2];
-            const uint16_t* sp[2];
-            const uint16_t* bp[2];
-            uint32_t prow[2];   // packed row inside the stage's packed tile
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const int r = t + 128 * m;
-                if (PASS == 0) {
-                    const int i = (r >> 7) * 64 + ((r & 127) >> 1);   // h column offset inside the tile
-                    const bool up = r & 1;
-                    src[m] = up ? (int64_t)I.e * a.wrow1 + a.woff1 + row0 / 2 + i : (int64_t)I.e * a.wrow0 + row0 / 2 + i;
-                    sp[m] = up ? a.s1 : a.s0;
-                    bp[m] = up ? a.b1 : a.b0;
-                    prow[m] = (up ? 128 : 0) + i;
-                } else {
-                    src[m] = (int64_t)I.e * a.wrow0 + row0 + r;
-                    sp[m] = a.s0;
-                    bp[m] = a.b0;
-                    prow[m] = r;
-                }
+            // source row of A row r
+            int64_t src;
+            const uint16_t *sp, *bp;
+            uint32_t prow;   // packed row inside the load slot's packed tile
+            if (PASS == 0) {
+                const int i = (r >> 7) * 64 + ((r & 127) >> 1);   // h column offset inside the tile
+                const bool up = r & 1;
+                src = up ? (int64_t)I.e * a.wrow1 + a.woff1 + row0 / 2 + i : (int64_t)I.e * a.wrow0 + row0 / 2 + i;
+                sp = up ? a.s1 : a.s0;
+                bp = up ? a.b1 : a.b0;
+                prow = (up ? 128 : 0) + i;
+            } else {
+                src = (int64_t)I.e * a.wrow0 + row0 + r;
+                sp = a.s0;
+                bp = a.b0;
+                prow = r;
             }
-            uint4 scl[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};   // 8 bf16 scales of each row
+            const uint4* srow = reinterpret_cast<const uint4*>(sp + src * G);   // 8 bf16 per uint4
+            const uint4* brow = reinterpret_cast<const uint4*>(bp + src * G);
+            uint4 scl = __ldg(srow), scl_next = n_main > 8 ? __ldg(srow + 1) : make_uint4(0, 0, 0, 0);
+            uint4 es[8], eb[8];   // scale / bias rows for eps, loaded two stages before use
             for (int st = 0; st < n_st; ++st, ++it) {
-                const uint32_t s = it % TC_STAGES;
-                if (st < n_main && (st & 7) == 0) {
+                const uint32_t s = it % L, sa = it % TC_A_SLOTS;
+                if (st < n_main && (st & 7) == 0 && st > 0) {
+                    scl = scl_next;
+                    if (st + 8 < n_main) scl_next = __ldg(srow + (st >> 3) + 1);
+                }
+                if (st == (n_main >= 2 ? n_main - 2 : 0)) {
 #pragma unroll
-                    for (int m = 0; m < 2; ++m) scl[m] = __ldg(reinterpret_cast<const uint4*>(sp[m] + src[m] * G + st));
+                    for (int i = 0; i < 8; ++i)
+                        if (i < G / 8) {
+                            es[i] = __ldg(srow + i);
+                            eb[i] = __ldg(brow + i);
+                        }
                 }
-                if (!poisoned && !mbar_wait(smem_u32(&full[s]), (it / TC_STAGES) & 1u)) {
-                    poisoned = true;
-                    atomicOr(a.status, SMOE_FAULT_TIMEOUT);
-                }
-                const uint32_t stg = sbase + s * TC_STAGE;
+                if (!poisoned) fail(mbar_wait(smem_u32(&full[s]), (it / L) & 1u));
+                if (it >= TC_A_SLOTS && !poisoned) fail(mbar_wait(smem_u32(&empty_a[sa]), ((it / TC_A_SLOTS) - 1) & 1u));
                 if (!poisoned) {
+                    const uint32_t arow = sbase + sa * TC_A_BYTES + (uint32_t)r * 128u;
+                    if (st < n_main) {
+                        const uint32_t sw = (&scl.x)[(st & 7) >> 1];
+                        const float sf = __uint_as_float((st & 1) ? (sw & 0xFFFF0000u) : (sw << 16));
+                        const __half2 s2 = __float2half2_rn(sf);   // exact: bf16 -> fp16
+                        const uint32_t pk = sbase + C::kOffLoad + s * C::kSlotBytes + prow * 32u;
+                        const uint4 w0 = lds128(pk), w1 = lds128(pk + 16);
+                        const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-                    for (int m = 0; m < 2; ++m) {
-                        const int r = t + 128 * m;
-                        const uint32_t arow = stg + (uint32_t)r * 128u;
-                        if (st < n_main) {
-                            const uint32_t sw = (&scl[m].x)[(st & 7) >> 1];
-                            const float sf = __uint_as_float((st & 1) ? (sw & 0xFFFF0000u) : (sw << 16));
-                            const __half2 s2 = __float2half2_rn(sf);   // exact: bf16 -> fp16
-                            const uint32_t pk = stg + TC_OFF_P + prow[m] * 32u;
-                            const uint4 w0 = lds128(pk), w1 = lds128(pk + 16);
-                            const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                        for (int c = 0; c < 8; ++c) sts128(arow + ((uint32_t)(c ^ (r & 7)) << 4), dequant_word(wv[c], s2));
+                    } else {
+                        // eps = b + 8 s for the row's G groups (zero beyond G), natural group order
 #pragma unroll
-                            for (int c = 0; c < 8; ++c)
-                                sts128(arow + ((uint32_t)(c ^ (r & 7)) << 4), dequant_word(wv[c], s2));
-                        } else {
-                            // eps = b + 8 s for groups 64c .. 64c + 63 (zero beyond G)
-                            const int g0 = (st - n_main) * 64;
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) {
-                                uint32_t hv[4];
+                        for (int c = 0; c < 8; ++c) {
+                            uint32_t hv[4] = {0u, 0u, 0u, 0u};
+                            if (c < G / 8) {
+                                const uint32_t sw[4] = {es[c].x, es[c].y, es[c].z, es[c].w};
+                                const uint32_t bw[4] = {eb[c].x, eb[c].y, eb[c].z, eb[c].w};
 #pragma unroll
                                 for (int q = 0; q < 4; ++q) {
-                                    float e2[2];
-#pragma unroll
-                                    for (int h = 0; h < 2; ++h) {
-                                        const int g = g0 + c * 8 + q * 2 + h;
-                                        float ev = 0.f;
-                                        if (g < G) {
-                                            const float sv = __uint_as_float((uint32_t)__ldg(sp[m] + src[m] * G + g) << 16);
-                                            const float bv = __uint_as_float((uint32_t)__ldg(bp[m] + src[m] * G + g) << 16);
-                                            ev = fmaf(8.f, sv, bv);
-                                        }
-                                        e2[h] = ev;
-                                    }
-                                    hv[q] = h2u(__floats2half2_rn(e2[0], e2[1]));
+                                    const float e0 = fmaf(8.f, __uint_as_float(sw[q] << 16), __uint_as_float(bw[q] << 16));
+                                    const float e1 = fmaf(8.f, __uint_as_float(sw[q] & 0xFFFF0000u),
+                                                          __uint_as_float(bw[q] & 0xFFFF0000u));
+                                    hv[q] = h2u(__floats2half2_rn(e0, e1));
                                 }
-                                sts128(arow + ((uint32_t)(c ^ (r & 7)) << 4), make_uint4(hv[0], hv[1], hv[2], hv[3]));
                             }
+                            sts128(arow + ((uint32_t)(c ^ (r & 7)) << 4), make_uint4(hv[0], hv[1], hv[2], hv[3]));
                         }
                     }
                     fence_proxy_async();   // generic-proxy writes -> visible to the tensor core
                 }
-                mbar_arrive(smem_u32(&deq[s]));
+                mbar_arrive(smem_u32(&deq[sa]));
             }
         }
     } else {
         // ------------------------------------------------------------------ epilogue
         const int q = warp & 3;                  // TMEM lane quarter of this warp
-        const int et = threadIdx.x - 192;        // 0..127
+        const int et = threadIdx.x - 320;        // 0..127
         const int lr = q * 32 + lane;            // accumulator row (TMEM lane) of this thread
+        float* hsm = reinterpret_cast<float*>(smem + C::kOffStage);   // pass 0: [32 tokens][64 cols]
         uint32_t tile = 0;
         for (int t = blockIdx.x; t < n_items; t += gridDim.x, ++tile) {
             const Item I = decode_item(a, pref, t);
@@ -470,44 +492,70 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 asm volatile("bar.sync 2, 128;\n" ::: "memory");
             }
-            if (!poisoned && !mbar_wait(smem_u32(&acc_full[buf]), (tile >> 1) & 1u)) {
-                poisoned = true;
-                atomicOr(a.status, SMOE_FAULT_TIMEOUT);
-            }
+            if (!poisoned) fail(mbar_wait(smem_u32(&acc_full[buf]), (tile >> 1) & 1u));
+            poisoned = epilogue_any(poisoned);
             tc_fence_after();
             if (!poisoned) {
 #pragma unroll 1
                 for (int m = 0; m < 2; ++m) {
 #pragma unroll 1
                     for (int c0 = 0; c0 < TC_N; c0 += 32) {
+                        if (c0 >= ntok) break;
                         float v[32];
                         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * 256 + m * TC_N + c0, v);
-                        if (c0 >= ntok) continue;
                         if (PASS == 0) {
-                            // lanes 2i (gate) and 2i+1 (up) of h column i; the even lane takes
-                            // tokens 0..15 of the chunk, the odd lane tokens 16..31
+                            // lanes 2i (gate) and 2i+1 (up) of h column i of this m-tile; the even
+                            // lane takes tokens 0..15 of the chunk, the odd lane tokens 16..31
                             const bool odd_lane = lane & 1;
-                            const int j = row0 / 2 + m * 64 + (lr >> 1);   // h column
-                            const bool odd_col = j & 1;
-                            const int col = (j & ~7) + perm8(j & 7);
+                            const int hc = lr >> 1;   // 0..63
 #pragma unroll
                             for (int k = 0; k < 16; ++k) {
-                                const float mine = v[odd_lane ? k : 16 + k];         // value the partner needs
+                                const float mine = v[odd_lane ? k : 16 + k];   // value the partner needs
                                 const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
                                 const float g = odd_lane ? other : v[k];
                                 const float u = odd_lane ? v[16 + k] : other;
-                                const int tk = c0 + (odd_lane ? 16 + k : k);
-                                if (tk < ntok) {
-                                    const float hv = g / (1.f + expf(-g)) * u;
-                                    if (!(fabsf(hv) <= 65504.f)) atomicOr(a.status, SMOE_FAULT_FP16_RANGE);
-                                    const float hs = odd_col ? hv * 0.0625f : hv;
-                                    const __half hh = __float2half_rn(hs);
-                                    const __half hl = __float2half_rn(hs - __half2float(hh));
-                                    __half* rowp = a.h_out + (size_t)(tok0 + tk) * (2 * a.F);
-                                    rowp[col] = hh;
-                                    rowp[a.F + col] = hl;
+                                const int tk = (odd_lane ? 16 : 0) + k;
+                                const float hv = g / (1.f + expf(-g)) * u;
+                                if (c0 + tk < ntok && !(fabsf(hv) <= 65504.f)) atomicOr(a.status, SMOE_FAULT_FP16_RANGE);
+                                hsm[tk * 64 + hc] = hv;
+                            }
+                            asm volatile("bar.sync 2, 128;\n" ::: "memory");
+                            // 32 tokens x 64 columns: thread -> (token et >> 2, columns 16 (et & 3) .. + 16)
+                            const int tk = et >> 2, cq = et & 3;
+                            const bool valid = c0 + tk < ntok;
+                            float gs = 0.f;
+#pragma unroll
+                            for (int half = 0; half < 2; ++half) {
+                                const int cb = cq * 16 + half * 8;   // first column of this 8-chunk
+                                __half hh[8], hl[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const float hv = hsm[tk * 64 + cb + e];
+                                    const float hs = (e & 1) ? hv * 0.0625f : hv;   // odd columns / 16
+                                    const __half h1 = __float2half_rn(hs);
+                                    const __half h2 = __float2half_rn(hs - __half2float(h1));
+                                    hh[perm8(e)] = h1;
+                                    hl[perm8(e)] = h2;
+                                    const float stood = __half2float(h1) + __half2float(h2);
+                                    gs += (e & 1) ? stood * 16.f : stood;
+                                }
+                                if (valid) {
+                                    const int j = row0 / 2 + m * 64 + cb;   // first h column of the chunk
+                                    __half* rowp = a.h_out + (size_t)(tok0 + c0 + tk) * (2 * a.F) + j;
+                                    *reinterpret_cast<uint4*>(rowp) = *reinterpret_cast<const uint4*>(hh);
+                                    *reinterpret_cast<uint4*>(rowp + a.F) = *reinterpret_cast<const uint4*>(hl);
                                 }
                             }
+                            gs += __shfl_xor_sync(0xffffffffu, gs, 1);
+                            gs += __shfl_xor_sync(0xffffffffu, gs, 2);
+                            if (valid && cq == 0) {
+                                const int Gh = a.F / kGroup;
+                                const size_t i = (size_t)(tok0 + c0 + tk) * Gh + (row0 / 2 + m * 64) / kGroup;
+                                const __half sh = __float2half_rn(gs);
+                                a.hsum_out[i] = sh;
+                                a.hsum_out[(size_t)a.B * a.K * Gh + i] = __float2half_rn(gs - __half2float(sh));
+                            }
+                            asm volatile("bar.sync 2, 128;\n" ::: "memory");
                         } else {
                             const int r = row0 + m * 128 + lr;   // output row
 #pragma unroll
@@ -537,36 +585,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                      : "memory");
 }
 
-// Group sums of the SwiGLU activations (actual values: hi + lo, odd columns times 16) of
-// every list entry, as fp16 hi and lo planes [B*K, F/64]: the S operand of pass 1's eps stage.
-__global__ void __launch_bounds__(256) hsum_kernel(const __half* __restrict__ h, int F,
-                                                   const int32_t* __restrict__ n_union,
-                                                   const int32_t* __restrict__ offsets, __half* __restrict__ shi,
-                                                   __half* __restrict__ slo) {
-    const int G = F / kGroup;
-    const size_t w = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;   // one warp per (entry, group)
-    const int lane = threadIdx.x & 31;
-    const int total = offsets[*n_union];
-    const int p = (int)(w / G), g = (int)(w - (size_t)p * G);
-    if (p >= total) return;
-    const __half* row = h + (size_t)p * (2 * F) + g * 64;
-    const int c0 = 2 * lane;   // two consecutive stored columns per lane
-    float s = 0.f;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int c = c0 + k;
-        const float v = __half2float(row[c]) + __half2float(row[F + c]);
-        s += (c & 2) ? v * 16.f : v;   // storage slots 2, 3, 6, 7 hold the odd columns (stored / 16)
-    }
-#pragma unroll
-    for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) {
-        const __half hh = __float2half_rn(s);
-        shi[(size_t)p * G + g] = hh;
-        slo[(size_t)p * G + g] = __float2half_rn(s - __half2float(hh));
-    }
-}
-
 bool encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize, int64_t rows, int64_t cols,
                 int box_cols, int box_rows, CUtensorMapSwizzle swz) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
@@ -582,7 +600,8 @@ bool encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int 
 }  // namespace
 
 bool tc_path_supported(const smoe_layer_desc& D) {
-    return D.d_model % 512 == 0 && D.ffn_dim % 512 == 0 && D.d_model / kGroup <= 64 * 4 && D.ffn_dim / kGroup <= 64 * 4;
+    // one eps stage covers up to 64 groups: d_model, ffn_dim <= 4096
+    return D.d_model % 512 == 0 && D.ffn_dim % 512 == 0 && D.d_model <= 4096 && D.ffn_dim <= 4096;
 }
 
 cudaError_t launch_ffn_tc(const smoe_layer_desc& D, const FfnTcWeights& W, int B, int pass,
@@ -596,9 +615,10 @@ cudaError_t launch_ffn_tc(const smoe_layer_desc& D, const FfnTcWeights& W, int B
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_done.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(ffn_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+        cudaError_t e =
+            cudaFuncSetAttribute(ffn_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<0>::kSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(ffn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+            e = cudaFuncSetAttribute(ffn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<1>::kSmem);
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit);
     }
@@ -614,7 +634,7 @@ cudaError_t launch_ffn_tc(const smoe_layer_desc& D, const FfnTcWeights& W, int B
     a.tc_min = tc_min;
     a.union_ids = union_ids; a.n_union = n_union; a.offsets = offsets;
     a.token_list = token_list; a.slot_list = slot_list;
-    a.h_out = h; a.y_out = ws_ptr<float>(ws, L.y);
+    a.h_out = h; a.hsum_out = shh; a.y_out = ws_ptr<float>(ws, L.y);
     a.status = ws_ptr<uint32_t>(ws, L.status);
     CUtensorMap mb, mshi, mslo;
     if (pass == 0) {
@@ -627,10 +647,9 @@ cudaError_t launch_ffn_tc(const smoe_layer_desc& D, const FfnTcWeights& W, int B
                         CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         const int grid = std::max(1, std::min(sms, E * (F / 128) * ((BK + TC_N - 1) / TC_N)));
-        ffn_tc_kernel<0><<<grid, TC_THREADS, TC_SMEM, stream>>>(W.pm_gate, W.pm_up, mb, mshi, mslo, a);
+        ffn_tc_kernel<0><<<grid, TC_THREADS, TcCfg<0>::kSmem, stream>>>(W.pm_gate, W.pm_up, mb, mshi, mslo, a);
     } else {
         const size_t nw = (size_t)BK * Gh;
-        hsum_kernel<<<(unsigned)((nw * 32 + 255) / 256), 256, 0, stream>>>(h, F, n_union, offsets, shh, shh + nw);
         a.wrow0 = d; a.wrow1 = d; a.woff1 = 0;
         a.s0 = W.sd; a.b0 = W.bd; a.s1 = W.sd; a.b1 = W.bd;
         a.m_tiles = d / 256;
@@ -640,7 +659,7 @@ cudaError_t launch_ffn_tc(const smoe_layer_desc& D, const FfnTcWeights& W, int B
                         CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         const int grid = std::max(1, std::min(sms, E * (d / 256) * ((BK + TC_N - 1) / TC_N)));
-        ffn_tc_kernel<1><<<grid, TC_THREADS, TC_SMEM, stream>>>(W.pm_down, W.pm_down, mb, mshi, mslo, a);
+        ffn_tc_kernel<1><<<grid, TC_THREADS, TcCfg<1>::kSmem, stream>>>(W.pm_down, W.pm_down, mb, mshi, mslo, a);
     }
     return cudaGetLastError();
 }

@@ -7,8 +7,11 @@
 // device-wide synchronisation a cudaMalloc may cause in the middle of a latency-critical loop.
 // For them this entry point needs nothing but its inputs and outputs: the split-K partial
 // router logits live in g_route_scratch below, a file-scope device array of
-// kNoallocScratchFloats floats (1 MiB) that every GPU which loads the library holds until the
-// process exits.
+// kNoallocScratchFloats floats (4 MiB) that every GPU which loads the library holds until the
+// process exits.  A call needs B * E <= kNoallocScratchFloats.  Up to 256 tokens at 128
+// experts the call uses the same split-K partials as smoe_route and returns identical
+// results; beyond that the number of partials is capped to what fits, which changes only the
+// fp32 summation order of the logits.
 //
 // Set-up: the first call on a device (with that device current) looks up the array's device
 // address with cudaGetSymbolAddress and caches it; make that first call before any stream
@@ -22,12 +25,13 @@
 // and must be serialised by the caller.
 #include "smoe_internal.cuh"
 
+#include <algorithm>
 #include <mutex>
 
 namespace smoe {
 namespace {
 
-constexpr size_t kNoallocScratchFloats = 262144;   // 1 MiB: splits * B * E partial logits
+constexpr size_t kNoallocScratchFloats = 1u << 20;   // 4 MiB: splits * B * E partial logits
 
 static __device__ __align__(256) float g_route_scratch[kNoallocScratchFloats];
 
@@ -71,13 +75,15 @@ extern "C" SMOE_API smoe_status smoe_route_noalloc(const smoe_layer_desc* desc, 
     if (!x || !gate_w || !topk_idx || !topk_w) return SMOE_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(gate_w) & 15u))
         return SMOE_ERR_UNSUPPORTED;
-    // the partial logits of this call must fit the fixed array
-    const size_t need = (size_t)route_splits(B, desc->num_experts, desc->d_model) * (size_t)B * desc->num_experts;
-    if (need > kNoallocScratchFloats) return SMOE_ERR_UNSUPPORTED;
+    // the partial logits of this call must fit the fixed array: at least one split of B x E,
+    // and no more splits than fit
+    const size_t per_split = (size_t)B * desc->num_experts;
+    if (per_split > kNoallocScratchFloats) return SMOE_ERR_UNSUPPORTED;
+    const int cap = (int)std::min<size_t>(kNoallocScratchFloats / per_split, 1 << 20);
     float* scratch = nullptr;
     if (scratch_for_current_device(&scratch) != cudaSuccess) return SMOE_ERR_CUDA;
     return launch_route(*desc, x, gate_w, gate_bias, B, topk_idx, topk_w, scratch,
-                        static_cast<cudaStream_t>(stream)) == cudaSuccess
+                        static_cast<cudaStream_t>(stream), cap) == cudaSuccess
                ? SMOE_OK
                : SMOE_ERR_CUDA;
 }

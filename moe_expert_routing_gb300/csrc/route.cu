@@ -6,10 +6,13 @@
 // norm_topk_prob re-normalises the top-k routing weights to sum 1.
 //
 // Two kernels:
-//   gate_logits_kernel  fp32 SIMT tile GEMM, logits[s][t][e] = sum over split s of
-//                       W[e][i] * x[t][i].  Split-K over d so that even a single token
-//                       spreads the 2 MB gate read over ~100 SMs; partials are summed in a
-//                       fixed order by the top-k kernel, so results are deterministic.
+//   gate_logits_kernel  logits[s][t][e] = sum over split s of W[e][i] * x[t][i] on the tensor
+//                       cores: x is bf16 and every fp32 gate weight is split into three bf16
+//                       terms (hi + mid + lo, exact up to the last bit), so mma.sync bf16 with
+//                       fp32 accumulation gives fp32-accurate logits.  Split-K over d so that
+//                       even a single token spreads the 2 MB gate read over ~100 SMs; the
+//                       partials are summed in a fixed order by the top-k kernel, so results
+//                       are deterministic.
 //   topk_kernel         one warp per token: sums the partials (+ bias), K rounds of a
 //                       warp arg-max (ties -> lower expert id), softmax weights.
 #include "smoe_internal.cuh"
@@ -19,83 +22,90 @@
 namespace smoe {
 namespace {
 
-constexpr int BN = 64;   // experts per tile
-constexpr int BK = 32;   // k per smem stage
-constexpr int kMaxSplits = 16;
+constexpr int kMaxSplits = 32;
+constexpr int kExpertsPerCta = 128;   // 8 warps x 16 experts
 
-// BM tokens x 64 experts per CTA (BM = 16 for small batches, 64 otherwise); each of the
-// 256 threads owns BM/16 tokens x 4 experts.
-template <int BM>
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two fp32 values -> three bf16x2 terms (hi, mid, lo) with hi + mid + lo == the values
+// (the last bit of lo may round).
+__device__ __forceinline__ void split3(float2 v, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
+    const __nv_bfloat162 h = __float22bfloat162_rn(v);
+    const float2 r1 = make_float2(v.x - __low2float(h), v.y - __high2float(h));
+    const __nv_bfloat162 m = __float22bfloat162_rn(r1);
+    const float2 r2 = make_float2(r1.x - __low2float(m), r1.y - __high2float(m));
+    const __nv_bfloat162 l = __float22bfloat162_rn(r2);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    mid = *reinterpret_cast<const uint32_t*>(&m);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// CTA: 8 warps x 16 experts, 8*NT tokens, one k-split of kchunk inputs.  Warp: A = 16 gate
+// rows (three bf16 terms), B = NT 8-token tiles of x, fp32 accumulators.
+template <int NT>
 __global__ void __launch_bounds__(256) gate_logits_kernel(const uint16_t* __restrict__ x,
                                                           const float* __restrict__ W, int B, int E, int d,
                                                           int kchunk, float* __restrict__ partial) {
-    constexpr int TM = BM / 16;
-    __shared__ float As[BK][BM + 4];
-    __shared__ float Bs[BK][BN + 4];
-    const int tid = threadIdx.x;
-    const int t0 = blockIdx.x * BM, e0 = blockIdx.y * BN;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    const int e0 = blockIdx.y * kExpertsPerCta + warp * 16;
+    if (e0 >= E) return;
+    const int t0 = blockIdx.x * 8 * NT;
     const int k_begin = blockIdx.z * kchunk, k_end = k_begin + kchunk;
-    const int tx = tid & 15, ty = tid >> 4;
-    float acc[TM][4];
+    const int ea = e0 + g, eb = e0 + g + 8;
+    const float* wa = W + (size_t)(ea < E ? ea : 0) * d;
+    const float* wb = W + (size_t)(eb < E ? eb : 0) * d;
+    const uint16_t* xr[NT];
 #pragma unroll
-    for (int i = 0; i < TM; ++i)
+    for (int nt = 0; nt < NT; ++nt) {
+        const int t = t0 + nt * 8 + g;
+        xr[nt] = x + (size_t)(t < B ? t : 0) * d;
+    }
+    float acc[NT][4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-
-    for (int k0 = k_begin; k0 < k_end; k0 += BK) {
-        // x tile: BM tokens x 32 k bf16; each loading thread takes 8 consecutive k of one token
-        if (tid < BM * 4) {
-            const int r = tid >> 2, kk = (tid & 3) * 8;
-            const int t = t0 + r;
-            uint4 raw = make_uint4(0, 0, 0, 0);
-            if (t < B) raw = *reinterpret_cast<const uint4*>(x + (size_t)t * d + k0 + kk);
-            const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                As[kk + 2 * q][r] = bf16_bits_to_float(w4[q] & 0xFFFFu);
-                As[kk + 2 * q + 1][r] = bf16_bits_to_float(w4[q] >> 16);
-            }
+        for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+    for (int k = k_begin; k < k_end; k += 16) {
+        const int k0 = k + 2 * c, k1 = k0 + 8;
+        float2 va0 = __ldg(reinterpret_cast<const float2*>(wa + k0));
+        float2 vb0 = __ldg(reinterpret_cast<const float2*>(wb + k0));
+        float2 va1 = __ldg(reinterpret_cast<const float2*>(wa + k1));
+        float2 vb1 = __ldg(reinterpret_cast<const float2*>(wb + k1));
+        if (ea >= E) va0 = va1 = make_float2(0.f, 0.f);
+        if (eb >= E) vb0 = vb1 = make_float2(0.f, 0.f);
+        uint32_t a[3][4];   // [term][a0..a3]: rows g / g+8, k 2c.. / 2c+8..
+        split3(va0, a[0][0], a[1][0], a[2][0]);
+        split3(vb0, a[0][1], a[1][1], a[2][1]);
+        split3(va1, a[0][2], a[1][2], a[2][2]);
+        split3(vb1, a[0][3], a[1][3], a[2][3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const uint32_t b0 = __ldg(reinterpret_cast<const uint32_t*>(xr[nt] + k0));
+            const uint32_t b1 = __ldg(reinterpret_cast<const uint32_t*>(xr[nt] + k1));
+#pragma unroll
+            for (int term = 2; term >= 0; --term)   // small terms first
+                mma_bf16(acc[nt], a[term][0], a[term][1], a[term][2], a[term][3], b0, b1);
         }
-        {   // W tile: 64 experts x 32 k fp32; each thread 8 consecutive k of one expert
-            const int r = tid >> 2, kk = (tid & 3) * 8;
-            const int e = e0 + r;
-            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-            if (e < E) {
-                a = *reinterpret_cast<const float4*>(W + (size_t)e * d + k0 + kk);
-                b = *reinterpret_cast<const float4*>(W + (size_t)e * d + k0 + kk + 4);
-            }
-            Bs[kk + 0][r] = a.x; Bs[kk + 1][r] = a.y; Bs[kk + 2][r] = a.z; Bs[kk + 3][r] = a.w;
-            Bs[kk + 4][r] = b.x; Bs[kk + 5][r] = b.y; Bs[kk + 6][r] = b.z; Bs[kk + 7][r] = b.w;
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int kk = 0; kk < BK; ++kk) {
-            float av[TM], bv[4];
-#pragma unroll
-            for (int i = 0; i < TM; ++i) av[i] = As[kk][ty * TM + i];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx * 4 + j];
-#pragma unroll
-            for (int i = 0; i < TM; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-        }
-        __syncthreads();
     }
     float* out = partial + (size_t)blockIdx.z * B * E;
 #pragma unroll
-    for (int i = 0; i < TM; ++i) {
-        const int t = t0 + ty * TM + i;
-        if (t >= B) continue;
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = e0 + tx * 4 + j;
-            if (e < E) out[(size_t)t * E + e] = acc[i][j];
+        for (int i = 0; i < 4; ++i) {
+            const int t = t0 + nt * 8 + 2 * c + (i & 1);
+            const int e = (i & 2) ? eb : ea;
+            if (t < B && e < E) out[(size_t)t * E + e] = acc[nt][i];
         }
-    }
 }
 
-int tile_tokens(int B) { return B <= 256 ? 16 : 64; }
+int tile_tokens(int B) { return B <= 64 ? 8 : 64; }
 
 // One warp per token.  Lane l holds experts l, l+32, ... (E <= 256).
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ partial, int splits,
@@ -176,22 +186,24 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
 }  // namespace
 
 int route_splits(int B, int E, int d) {
-    const int bm = tile_tokens(B);
-    const int tiles = ((B + bm - 1) / bm) * ((E + BN - 1) / BN);
+    const int bt = tile_tokens(B);
+    const int tiles = ((B + bt - 1) / bt) * ((E + kExpertsPerCta - 1) / kExpertsPerCta);
     const int target = 2 * 152;
     int s = 1;
-    while (s < kMaxSplits && s * tiles < target && (d / (2 * s)) % BK == 0 && d / (2 * s) >= 128) s *= 2;
+    while (s < kMaxSplits && s * tiles < target && (d / (2 * s)) % 16 == 0 && d / (2 * s) >= 128) s *= 2;
     return s;
 }
 
 cudaError_t launch_route(const smoe_layer_desc& D, const uint16_t* x, const float* gate_w, const float* gate_bias,
-                         int B, int32_t* topk_idx, float* topk_w, float* logits_ws, cudaStream_t stream) {
+                         int B, int32_t* topk_idx, float* topk_w, float* logits_ws, cudaStream_t stream,
+                         int split_cap) {
     const int E = D.num_experts, d = D.d_model, K = D.top_k;
-    const int S = route_splits(B, E, d);
-    const int bm = tile_tokens(B);
-    dim3 grid((B + bm - 1) / bm, (E + BN - 1) / BN, S);
-    if (bm == 16) gate_logits_kernel<16><<<grid, 256, 0, stream>>>(x, gate_w, B, E, d, d / S, logits_ws);
-    else gate_logits_kernel<64><<<grid, 256, 0, stream>>>(x, gate_w, B, E, d, d / S, logits_ws);
+    int S = route_splits(B, E, d);
+    while (split_cap > 0 && S > split_cap) S >>= 1;
+    const int bt = tile_tokens(B);
+    dim3 grid((B + bt - 1) / bt, (E + kExpertsPerCta - 1) / kExpertsPerCta, S);
+    if (bt == 8) gate_logits_kernel<1><<<grid, 256, 0, stream>>>(x, gate_w, B, E, d, d / S, logits_ws);
+    else gate_logits_kernel<8><<<grid, 256, 0, stream>>>(x, gate_w, B, E, d, d / S, logits_ws);
     const int warps_per_block = 8;
     topk_kernel<<<(B + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0, stream>>>(
         logits_ws, S, gate_bias, B, E, K, D.norm_topk_prob, topk_idx, topk_w);

@@ -47,9 +47,10 @@ inline T* ws_ptr(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast
 
 // ----------------------------------------------------------------------------- launchers
 // Each returns cudaGetLastError() after enqueueing its kernel(s) on `stream`.
+// split_cap > 0 limits the number of split-K partials (callers with a fixed scratch size).
 cudaError_t launch_route(const smoe_layer_desc& D, const uint16_t* x, const float* gate_w,
                          const float* gate_bias, int B, int32_t* topk_idx, float* topk_w,
-                         float* logits_ws, cudaStream_t stream);
+                         float* logits_ws, cudaStream_t stream, int split_cap = 0);
 
 cudaError_t launch_union(const smoe_layer_desc& D, const int32_t* topk_idx, int B, int32_t* union_ids,
                          int32_t* n_union, int32_t* offsets, int32_t* token_list, int32_t* slot_list,
