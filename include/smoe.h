@@ -29,7 +29,8 @@
  *     kept at the start of the workspace; the kernels then skip the bad work and return,
  *     they never trap.  smoe_read_device_status reports them.
  *   - bf16 values are passed as uint16_t bit patterns.
- *   - Supported shapes: group_size 64; d_model and ffn_dim multiples of 256; 1 <= top_k
+ *   - Supported shapes: group_size 64; d_model and ffn_dim each 256 or a multiple of 512
+ *     (a row of scales or biases is 8 bytes or a multiple of 16); 1 <= top_k
  *     <= 16; top_k <= num_experts <= 256.  Weight, scale, bias, x and residual pointers
  *     16-byte aligned.  Other shapes return SMOE_ERR_UNSUPPORTED.
  */

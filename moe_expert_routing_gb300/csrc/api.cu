@@ -24,7 +24,9 @@ smoe_status check_desc(const smoe_layer_desc* D) {
     if (D->layout != SMOE_LAYOUT_SEPARATE && D->layout != SMOE_LAYOUT_FUSED_GATE_UP) return SMOE_ERR_INVALID_ARG;
     if (D->norm_topk_prob != 0 && D->norm_topk_prob != 1) return SMOE_ERR_INVALID_ARG;
     if (D->group_size != kGroup) return SMOE_ERR_UNSUPPORTED;
-    if (D->d_model % 256 || D->ffn_dim % 256) return SMOE_ERR_UNSUPPORTED;
+    // 256 or a multiple of 512: the scale rows are 8 bytes or a multiple of 16 (TMA strides)
+    if ((D->d_model % 512 && D->d_model != 256) || (D->ffn_dim % 512 && D->ffn_dim != 256))
+        return SMOE_ERR_UNSUPPORTED;
     if (D->num_experts > kMaxExperts || D->top_k > kMaxTopK) return SMOE_ERR_UNSUPPORTED;
     if ((int64_t)D->d_model * D->ffn_dim > (int64_t)1 << 30) return SMOE_ERR_UNSUPPORTED;
     return SMOE_OK;
@@ -49,6 +51,24 @@ bool encode_weight_map(CUtensorMap* map, const uint32_t* words, int64_t rows, in
     cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(words), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D bf16 view of a scale or bias tensor [rows, G] (G = in / 64 groups per row) for the
+// per-stage tables of the expert passes: box 8 groups x box_rows rows.  With G == 4 a row
+// is 8 bytes and the tensor is viewed as [rows / 2, 8] with box_rows / 2 rows, which lands
+// in shared memory as the same [box_rows][4] table.
+bool encode_group_map(CUtensorMap* map, const uint16_t* p, int64_t rows, int64_t in, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const int64_t G = in / kGroup;
+    const bool packed = G == 4;
+    cuuint64_t dims[2] = {(cuuint64_t)(packed ? 8 : G), (cuuint64_t)(packed ? rows / 2 : rows)};
+    cuuint64_t strides[1] = {(cuuint64_t)((packed ? 8 : G) * 2)};
+    cuuint32_t box[2] = {8, (cuuint32_t)(packed ? box_rows / 2 : box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -79,16 +99,26 @@ smoe_status check_weights(const smoe_layer_desc& D, const smoe_expert_weights* W
     const CUtensorMapSwizzle none = CU_TENSOR_MAP_SWIZZLE_NONE;
     if (!encode_weight_map(&P->map_down, W->w_down, E * d, F, 256)) return SMOE_ERR_CUDA;
     if (!encode_weight_map(&P->pm_down, W->w_down, E * d, F, 256, 8, none)) return SMOE_ERR_CUDA;
+    if (!encode_group_map(&P->map_sd, W->s_down, E * d, F, 256) || !encode_group_map(&P->map_bd, W->b_down, E * d, F, 256))
+        return SMOE_ERR_CUDA;
     if (sep) {
         if (!encode_weight_map(&P->map_gate, W->w_gate, E * F, d, 128)) return SMOE_ERR_CUDA;
         if (!encode_weight_map(&P->map_up, W->w_up, E * F, d, 128)) return SMOE_ERR_CUDA;
         if (!encode_weight_map(&P->pm_gate, W->w_gate, E * F, d, 128, 8, none)) return SMOE_ERR_CUDA;
         if (!encode_weight_map(&P->pm_up, W->w_up, E * F, d, 128, 8, none)) return SMOE_ERR_CUDA;
+        if (!encode_group_map(&P->map_sg, W->s_gate, E * F, d, 128) || !encode_group_map(&P->map_bg, W->b_gate, E * F, d, 128) ||
+            !encode_group_map(&P->map_su, W->s_up, E * F, d, 128) || !encode_group_map(&P->map_bu, W->b_up, E * F, d, 128))
+            return SMOE_ERR_CUDA;
     } else {
         if (!encode_weight_map(&P->map_gate, W->w_gate_up, E * 2 * F, d, 128)) return SMOE_ERR_CUDA;
         if (!encode_weight_map(&P->pm_gate, W->w_gate_up, E * 2 * F, d, 128, 8, none)) return SMOE_ERR_CUDA;
         P->map_up = P->map_gate;
         P->pm_up = P->pm_gate;
+        if (!encode_group_map(&P->map_sg, W->s_gate_up, E * 2 * F, d, 128) ||
+            !encode_group_map(&P->map_bg, W->b_gate_up, E * 2 * F, d, 128))
+            return SMOE_ERR_CUDA;
+        P->map_su = P->map_sg;
+        P->map_bu = P->map_bg;
     }
     return SMOE_OK;
 }

@@ -17,10 +17,11 @@
 //   combine_kernel     residual[t] += sum_k w[t][k] * y[t*K + k], k in rank order
 //
 // The pass kernels are persistent and warp-specialised: one producer warp streams, for
-// every tile and every 256-input k-slice, the packed weight rows, the activation rows and
-// their group sums into a 4-stage shared-memory ring with TMA (128-byte swizzle); eight
-// consumer warps decode and multiply.  Full/empty mbarriers hand the stages back and forth,
-// so the weight stream never drains between tiles.
+// every tile and every 256-input k-slice, the packed weight rows and the activation rows
+// (TMA, 128-byte swizzle), the activations' group sums and the rows' scales and biases (TMA)
+// into a shared-memory ring; eight consumer warps decode and multiply.
+// Full/empty mbarriers hand the stages back and forth, so the weight stream never drains
+// between tiles and the consumers never wait on a global load.
 //
 // Tensor-core use in the bandwidth-bound regime.  With a handful of tokens per expert the
 // work is a stream of 4-bit weights that must be decoded faster than HBM delivers them;
@@ -38,9 +39,8 @@
 //     pair line up with one B-fragment register.
 //   * each mma covers 16 inputs of ONE group, so the affine map is applied after the mma,
 //     in fp32:  sum_i (s q_i + b) x_i = (s * 2^24) * C + b * S,  C = mma result,
-//     S = sum of the group's activations; weights are never rounded.  The bias part,
-//     sum over groups of b[row][g] * S[token][g], is a small product of its own: it runs on
-//     the tensor cores once per token chunk (b as fp16, S as an fp16 hi + lo pair).
+//     S = sum of the group's activations; weights are never rounded.  Both terms are fp32
+//     FMAs per group.
 //   * the down projection's input h = silu(g) * up is carried as two fp16 terms, hi + lo
 //     (lo = the rounding remainder), and both are multiplied: h keeps ~22 bits.
 #include "smoe_internal.cuh"
@@ -68,10 +68,6 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 __device__ __forceinline__ uint32_t nib_even(uint32_t w) { return w & 0x000F000Fu; }
 __device__ __forceinline__ uint32_t nib_odd(uint32_t w) { return w & 0x00F000F0u; }
 
-
-__device__ __forceinline__ uint2 ldg_u2h(const uint16_t* p) {
-    return __ldg(reinterpret_cast<const uint2*>(p));
-}
 
 // storage slot of logical element m (0..7) inside an 8-element chunk: (0,4,1,5,2,6,3,7)
 __device__ __forceinline__ int perm8(int m) { return 2 * (m & 3) + (m >> 2); }
@@ -194,14 +190,32 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
 // ----------------------------------------------------------------------------- expert passes
 constexpr int kConsumerWarps = 8;
 constexpr int kPassThreads = 32 * (kConsumerWarps + 1);   // + one producer warp
-constexpr int kStages = 3;   // 3 x 49 KB: leaves ~80 KB of L1 for the scale rows
 constexpr int kWBytes = 256 * 128;         // 256 weight rows x 32 u32 words (4 groups)
 constexpr int kXBoxBytes = 16 * 128;       // 16 activation rows x 64 fp16 (one group)
-constexpr int kXOff = kWBytes;             // 4 boxes (x, pass 0) or 8 boxes (h hi then lo, pass 1)
-constexpr int kStageBytes = kWBytes + 8 * kXBoxBytes;   // 48 KB, a 1024-byte multiple
-__host__ __device__ constexpr int stage_tx(int pass) { return kWBytes + (pass ? 8 : 4) * kXBoxBytes; }
-constexpr int kPassSmem = kStages * kStageBytes + 1024;
 constexpr int kTokChunk = 16;              // tokens per pass over the weights
+constexpr int kSbBytes = 256 * 16;         // 256 rows x up to 8 bf16 (a table of scales or biases)
+
+// One ring stage: packed weights | activation boxes (4, or 4 hi + 4 lo) | scales | biases |
+// activation group sums fp32 [16 tokens][4 groups]; a 1024-byte multiple.  The scale and
+// bias tables hold, per weight row, the 8 groups of the 16-byte-aligned window that
+// contains the stage's 4 groups ([256][8] bf16), or with 4 groups per row ([256][4]) the
+// whole row.
+template <int PASS>
+struct PassCfg {
+    static constexpr int kStages = PASS ? 3 : 4;
+    static constexpr int kXBoxes = PASS ? 8 : 4;
+    static constexpr int kXOff = kWBytes;
+    static constexpr int kSOff = kXOff + kXBoxes * kXBoxBytes;
+    static constexpr int kBOff = kSOff + kSbBytes;
+    static constexpr int kSumOff = kBOff + kSbBytes;
+    static constexpr int kSumBytes = kTokChunk * 4 * 4;
+    static constexpr int kStageBytes = (kSumOff + kSumBytes + 1023) / 1024 * 1024;
+    static constexpr int kTx = kWBytes + kXBoxes * kXBoxBytes + kSumBytes;   // TMA bytes of a stage
+                                                                              // (without the tables)
+    static constexpr int kSmem = kStages * kStageBytes + 1024;
+};
+static_assert(PassCfg<0>::kSmem <= 227 * 1024 - 2048, "pass 0 shared memory");
+static_assert(PassCfg<1>::kSmem <= 227 * 1024 - 2048, "pass 1 shared memory");
 
 struct PassArgs {
     int64_t wrow0;        // pass 0: gate rows per expert in map_w0; pass 1: d
@@ -209,7 +223,6 @@ struct PassArgs {
     int64_t woff1;        // pass 0: first up row inside an expert block (0 or F)
     const uint16_t* s0; const uint16_t* b0;   // scales/biases of map_w0 rows
     const uint16_t* s1; const uint16_t* b1;   // scales/biases of map_w1 rows
-    const float* bsum;    // per-group sums of the activation rows [B*K, kdim/64] (sx or sh)
     int kdim;             // contraction length (d for pass 0, F for pass 1)
     int F, d, K, E, B;
     int tiles_per_expert;
@@ -241,12 +254,25 @@ __device__ __forceinline__ Tile decode_tile(const PassArgs& a, int t, int pass_r
 
 // One 256-input k-slice (4 groups) of a consumer warp: two 16-row m-tiles against NT
 // 8-token n-tiles.  wb0/wb1: shared addresses of the m-tiles' first rows; xs: the activation
-// boxes (4, or with LO 4 hi + 4 lo); sc: 4 bf16 scales of rows g, g+8 of each m-tile.
-// acc += (scale * 2^24) * C per group; the bias part is added once per chunk (bias_term).
+// boxes (4, or with LO 4 hi + 4 lo); sc/bi: the stage's bf16 scales / biases of rows g and
+// g+8 of each m-tile ([m][row], 4 groups each); sums: the stage's activation group sums.
+// Per group: acc += (scale * 2^24) * C + bias * S, C the exact mma result in units of 2^-24
+// and S the tokens' group sums.
 template <int NT, bool LO>
 __device__ __forceinline__ void consume_stage(float (&acc)[2][NT][4], uint32_t wb0, uint32_t wb1, uint32_t xs,
-                                              const uint2 (&sc)[4], int g, int c) {
+                                              const uint2 (&sc)[2][2], const uint2 (&bi)[2][2], uint32_t sums,
+                                              int g, int c) {
     constexpr int NB = LO ? 2 : 1;   // activation terms per input
+    float4 S[NT][2];                 // group sums of tokens 2c and 2c+1 of each n-tile, 4 groups
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const uint4 v0 = lds_u4(sums + (uint32_t)(nt * 8 + 2 * c) * 16u);
+        const uint4 v1 = lds_u4(sums + (uint32_t)(nt * 8 + 2 * c + 1) * 16u);
+        S[nt][0] = make_float4(__uint_as_float(v0.x), __uint_as_float(v0.y), __uint_as_float(v0.z),
+                               __uint_as_float(v0.w));
+        S[nt][1] = make_float4(__uint_as_float(v1.x), __uint_as_float(v1.y), __uint_as_float(v1.z),
+                               __uint_as_float(v1.w));
+    }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         uint32_t bf[NT][NB][8];
@@ -288,62 +314,21 @@ __device__ __forceinline__ void consume_stage(float (&acc)[2][NT][4], uint32_t w
                         mma16816(ct[nt], f0, f1, p0, p1, bf[nt][hl][4 * h + 2], bf[nt][hl][4 * h + 3]);
                     }
             }
-            // scale of this group: rows g (lo) and g+8 (hi); C is in units of 2^-24
-            const uint2 slo2 = sc[2 * m], shi2 = sc[2 * m + 1];
-            const uint32_t swl = (q < 2) ? slo2.x : slo2.y, swh = (q < 2) ? shi2.x : shi2.y;
+            // scale and bias of this group: rows g (lo) and g+8 (hi); C is in units of 2^-24
+            const uint32_t swl = (q < 2) ? sc[m][0].x : sc[m][0].y, swh = (q < 2) ? sc[m][1].x : sc[m][1].y;
+            const uint32_t bwl = (q < 2) ? bi[m][0].x : bi[m][0].y, bwh = (q < 2) ? bi[m][1].x : bi[m][1].y;
             const float slo = __uint_as_float((q & 1) ? (swl & 0xFFFF0000u) : (swl * 65536u)) * 16777216.f;
             const float shi = __uint_as_float((q & 1) ? (swh & 0xFFFF0000u) : (swh * 65536u)) * 16777216.f;
+            const float blo = __uint_as_float((q & 1) ? (bwl & 0xFFFF0000u) : (bwl * 65536u));
+            const float bhi = __uint_as_float((q & 1) ? (bwh & 0xFFFF0000u) : (bwh * 65536u));
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                acc[m][nt][0] = fmaf(slo, ct[nt][0], acc[m][nt][0]);
-                acc[m][nt][1] = fmaf(slo, ct[nt][1], acc[m][nt][1]);
-                acc[m][nt][2] = fmaf(shi, ct[nt][2], acc[m][nt][2]);
-                acc[m][nt][3] = fmaf(shi, ct[nt][3], acc[m][nt][3]);
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
-
-// bf16 pair (two consecutive biases) -> fp16 pair
-__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t v) {
-    return h2_bits(__floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u)));
-}
-
-// acc += sum over groups of b[row][g] * S[token][g] for the warp's rows (lo row pointers br[m],
-// hi rows 8 rows further) and the chunk's tokens; 16 groups per mma, S split into fp16 hi + lo.
-template <int NT>
-__device__ __forceinline__ void bias_term(float (&acc)[2][NT][4], const uint16_t* const (&br)[2], int sstep,
-                                          const float* bsum, int G, int pc, int n, int g, int c) {
-    for (int k0 = 0; k0 < G; k0 += 16) {
-        const bool in0 = k0 + 2 * c < G, in1 = k0 + 2 * c + 8 < G;   // G is a multiple of 4
-        uint32_t shi[NT][2], slo[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int slot = nt * 8 + g;
-            const float* srow = bsum + (size_t)(pc + (slot < n ? slot : 0)) * G + k0 + 2 * c;
-            const float2 v0 = in0 ? *reinterpret_cast<const float2*>(srow) : make_float2(0.f, 0.f);
-            const float2 v1 = in1 ? *reinterpret_cast<const float2*>(srow + 8) : make_float2(0.f, 0.f);
-            const __half2 h0 = __float22half2_rn(v0), h1 = __float22half2_rn(v1);
-            const float2 r0 = __half22float2(h0), r1 = __half22float2(h1);
-            shi[nt][0] = h2_bits(h0);
-            shi[nt][1] = h2_bits(h1);
-            slo[nt][0] = h2_bits(__floats2half2_rn(v0.x - r0.x, v0.y - r0.y));
-            slo[nt][1] = h2_bits(__floats2half2_rn(v1.x - r1.x, v1.y - r1.y));
-        }
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            const uint16_t* lo = br[m] + k0 + 2 * c;
-            const uint16_t* hi = lo + sstep;
-            const uint32_t a0 = in0 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(lo)) : 0u;
-            const uint32_t a1 = in0 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(hi)) : 0u;
-            const uint32_t a2 = in1 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(lo + 8)) : 0u;
-            const uint32_t a3 = in1 ? bf2_to_h2(*reinterpret_cast<const uint32_t*>(hi + 8)) : 0u;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                mma16816(acc[m][nt], a0, a1, a2, a3, shi[nt][0], shi[nt][1]);
-                mma16816(acc[m][nt], a0, a1, a2, a3, slo[nt][0], slo[nt][1]);
+                const float s0 = q == 0 ? S[nt][0].x : q == 1 ? S[nt][0].y : q == 2 ? S[nt][0].z : S[nt][0].w;
+                const float s1 = q == 0 ? S[nt][1].x : q == 1 ? S[nt][1].y : q == 2 ? S[nt][1].z : S[nt][1].w;
+                acc[m][nt][0] = fmaf(slo, ct[nt][0], fmaf(blo, s0, acc[m][nt][0]));
+                acc[m][nt][1] = fmaf(slo, ct[nt][1], fmaf(blo, s1, acc[m][nt][1]));
+                acc[m][nt][2] = fmaf(shi, ct[nt][2], fmaf(bhi, s0, acc[m][nt][2]));
+                acc[m][nt][3] = fmaf(shi, ct[nt][3], fmaf(bhi, s1, acc[m][nt][3]));
             }
         }
     }
@@ -357,6 +342,7 @@ struct Ring {
 template <int NT, int PASS>
 __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, uint32_t& it, bool& poisoned,
                                               const Tile& T, int pc, int n, int warp, int lane, float* red) {
+    using C = PassCfg<PASS>;
     const int g = lane >> 2, c = lane & 3;
     const int nst = a.kdim / kGroup / 4;
     float acc[2][NT][4];
@@ -367,52 +353,44 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[m][nt][i] = 0.f;
 
-    // scale / bias rows of this lane (lo rows; hi rows are 8 rows further) and the byte
-    // offsets of the m-tiles' first rows inside a stage
-    const int G = a.kdim / kGroup;
-    const uint16_t *sr0, *br0, *sr1, *br1;
+    // the m-tiles' first rows inside a stage (weight box and scale / bias tables)
     uint32_t wrow_off0, wrow_off1;
+    int lrow0, lrow1;
     if (PASS == 0) {
-        const int64_t j = T.row + warp * 16 + g;
-        const int64_t rg = (int64_t)T.e * a.wrow0 + j, ru = (int64_t)T.e * a.wrow1 + a.woff1 + j;
-        sr0 = a.s0 + rg * G; br0 = a.b0 + rg * G;
-        sr1 = a.s1 + ru * G; br1 = a.b1 + ru * G;
-        wrow_off0 = (uint32_t)(warp * 16) * 128u;             // gate box rows 16w..
-        wrow_off1 = (uint32_t)(128 * 128 + warp * 16 * 128);  // up box rows 16w..
+        lrow0 = warp * 16;          // gate rows 16w.. of the tile
+        lrow1 = 128 + warp * 16;    // up rows
     } else {
-        const int64_t r = (int64_t)T.e * a.wrow0 + T.row + warp * 32 + g;
-        sr0 = a.s0 + r * G; br0 = a.b0 + r * G;
-        sr1 = a.s0 + (r + 16) * G; br1 = a.b0 + (r + 16) * G;
-        wrow_off0 = (uint32_t)(warp * 32) * 128u;
-        wrow_off1 = (uint32_t)(warp * 32 + 16) * 128u;
+        lrow0 = warp * 32;
+        lrow1 = warp * 32 + 16;
     }
-    const int sstep = 8 * G;
-    uint2 sc[4];   // the next stage's scales, loaded one stage ahead
-    auto load_scales = [&](int st) {
-        const int gb = st * 4;
-        sc[0] = ldg_u2h(sr0 + gb); sc[1] = ldg_u2h(sr0 + sstep + gb);
-        sc[2] = ldg_u2h(sr1 + gb); sc[3] = ldg_u2h(sr1 + sstep + gb);
-    };
-    load_scales(0);
+    wrow_off0 = (uint32_t)lrow0 * 128u;
+    wrow_off1 = (uint32_t)lrow1 * 128u;
+    const bool packed = a.kdim / kGroup == 4;   // tables [256][4]: the whole row
+    const uint32_t rs = packed ? 8u : 16u;
+    auto tab_off = [&](int st) { return packed ? 0u : (uint32_t)(st & 1) * 8u; };
     for (int st = 0; st < nst; ++st) {
-        const uint32_t slot = it % kStages;
-        const uint32_t parity = (it / kStages) & 1u;
+        const uint32_t slot = it % C::kStages;
+        const uint32_t parity = (it / C::kStages) & 1u;
         if (!poisoned && !mbar_wait(R.full + 8 * slot, parity)) {
             poisoned = true;
             if (lane == 0) atomicOr(a.status, SMOE_FAULT_TIMEOUT);
         }
-        uint2 sc_cur[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) sc_cur[i] = sc[i];
-        if (st + 1 < nst) load_scales(st + 1);
-        const uint32_t base = R.buf + slot * kStageBytes;
-        consume_stage<NT, PASS == 1>(acc, base + wrow_off0, base + wrow_off1, base + kXOff, sc_cur, g, c);
+        const uint32_t base = R.buf + slot * C::kStageBytes;
+        // this stage's 4 groups in the tables: row stride rs, at byte tab_off inside a row
+        const uint32_t ts = base + C::kSOff + tab_off(st), tb = base + C::kBOff + tab_off(st);
+        uint2 sc[2][2], bi[2][2];
+        sc[0][0] = lds_u2(ts + (uint32_t)(lrow0 + g) * rs);
+        sc[0][1] = lds_u2(ts + (uint32_t)(lrow0 + g + 8) * rs);
+        sc[1][0] = lds_u2(ts + (uint32_t)(lrow1 + g) * rs);
+        sc[1][1] = lds_u2(ts + (uint32_t)(lrow1 + g + 8) * rs);
+        bi[0][0] = lds_u2(tb + (uint32_t)(lrow0 + g) * rs);
+        bi[0][1] = lds_u2(tb + (uint32_t)(lrow0 + g + 8) * rs);
+        bi[1][0] = lds_u2(tb + (uint32_t)(lrow1 + g) * rs);
+        bi[1][1] = lds_u2(tb + (uint32_t)(lrow1 + g + 8) * rs);
+        consume_stage<NT, PASS == 1>(acc, base + wrow_off0, base + wrow_off1, base + C::kXOff, sc, bi,
+                                     base + C::kSumOff, g, c);
         mbar_arrive(R.empty + 8 * slot);   // this thread is done reading the slot
         ++it;
-    }
-    {
-        const uint16_t* const br[2] = {br0, br1};
-        bias_term<NT>(acc, br, sstep, a.bsum, G, pc, n, g, c);
     }
 
     if (PASS == 0) {
@@ -491,12 +469,19 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
 // PASS 0: tile = 128 h columns of one expert (consumer warp w: gate and up rows 16w..16w+15).
 // PASS 1: tile = 256 down rows of one expert (consumer warp w: rows 32w..32w+31).
 // Tiles t = blockIdx.x, blockIdx.x + gridDim.x, ... over n_union * tiles_per_expert.
+// Producer warp (lane 0): the TMA copies of a stage (weights, activations, group sums, and
+// the scale and bias tables: map_sc0 / map_bi0 rows of map_w0, map_sc1 / map_bi1 rows of
+// map_w1).
 template <int PASS>
 __global__ void __launch_bounds__(kPassThreads, 1)
     ffn_pass_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
-                    const __grid_constant__ CUtensorMap map_x, PassArgs a) {
+                    const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_s,
+                    const __grid_constant__ CUtensorMap map_sc0, const __grid_constant__ CUtensorMap map_sc1,
+                    const __grid_constant__ CUtensorMap map_bi0, const __grid_constant__ CUtensorMap map_bi1,
+                    PassArgs a) {
+    using C = PassCfg<PASS>;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[2 * kStages];
+    __shared__ __align__(8) uint64_t bars[2 * C::kStages];
     __shared__ float red[kConsumerWarps * 16];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int pass_rows = PASS == 0 ? 128 : 256;
@@ -504,10 +489,10 @@ __global__ void __launch_bounds__(kPassThreads, 1)
     Ring R;
     R.buf = smem_addr(smem);
     R.full = smem_addr(&bars[0]);
-    R.empty = smem_addr(&bars[kStages]);
+    R.empty = smem_addr(&bars[C::kStages]);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(R.full + 8 * s, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(R.full + 8 * s, 1);   // TMA arrive + one cp.async arrive per producer lane
             mbar_init(R.empty + 8 * s, 32 * kConsumerWarps);
         }
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -522,48 +507,55 @@ __global__ void __launch_bounds__(kPassThreads, 1)
     if (warp == kConsumerWarps) {
         // ---------------------------------------------------------------- producer (one thread)
         if (lane == 0) {
+            const bool packed = G == 4;
+            const uint32_t rs = packed ? 8u : 16u;
+            const uint32_t tx = C::kTx + 2u * 256u * rs;
             for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
                 const Tile T = decode_tile(a, t, pass_rows);
                 if (!T.ok || !T.mine) continue;
-                // scale / bias rows of the tile into L2 ahead of the consumers' loads
-                if (PASS == 0) {
-                    const int64_t rg = (int64_t)T.e * a.wrow0 + T.row, ru = (int64_t)T.e * a.wrow1 + a.woff1 + T.row;
-                    const uint32_t bytes = (uint32_t)(128 * G * 2);
-                    prefetch_l2(a.s0 + rg * G, bytes); prefetch_l2(a.b0 + rg * G, bytes);
-                    prefetch_l2(a.s1 + ru * G, bytes); prefetch_l2(a.b1 + ru * G, bytes);
-                } else {
-                    const int64_t r = (int64_t)T.e * a.wrow0 + T.row;
-                    const uint32_t bytes = (uint32_t)(256 * G * 2);
-                    prefetch_l2(a.s0 + r * G, bytes); prefetch_l2(a.b0 + r * G, bytes);
-                }
+                // first rows of the tile in map_w0 and (pass 0) map_w1
+                const int64_t r0 = (int64_t)T.e * a.wrow0 + T.row;
+                const int64_t r1 = PASS == 0 ? (int64_t)T.e * a.wrow1 + a.woff1 + T.row : r0;
+                // the tile's scale / bias rows into L2 ahead of the table copies
+                const uint32_t bytes = (uint32_t)(pass_rows * G * 2);
+                prefetch_l2(a.s0 + r0 * G, bytes); prefetch_l2(a.b0 + r0 * G, bytes);
+                if (PASS == 0) { prefetch_l2(a.s1 + r1 * G, bytes); prefetch_l2(a.b1 + r1 * G, bytes); }
+                const int ty0 = (int)(packed ? r0 / 2 : r0), ty1 = (int)(packed ? r1 / 2 : r1);
                 for (int pc = T.p0; pc < T.p1; pc += kTokChunk) {
                     for (int st = 0; st < nst; ++st) {
-                        const uint32_t slot = it % kStages;
-                        if (it >= kStages && !poisoned &&
-                            !mbar_wait(R.empty + 8 * slot, ((it / kStages) - 1) & 1u)) {
+                        const uint32_t slot = it % C::kStages;
+                        if (it >= C::kStages && !poisoned &&
+                            !mbar_wait(R.empty + 8 * slot, ((it / C::kStages) - 1) & 1u)) {
                             poisoned = true;
                             atomicOr(a.status, SMOE_FAULT_TIMEOUT);
                         }
-                        const uint32_t base = R.buf + slot * kStageBytes;
+                        const uint32_t base = R.buf + slot * C::kStageBytes;
                         const uint32_t full = R.full + 8 * slot;
                         if (!poisoned) {
-                            mbar_expect_tx(full, stage_tx(PASS));
+                            mbar_expect_tx(full, tx);
+                            const int tx0 = packed ? 0 : (st * 4) & ~7;   // 16-byte window of the stage's groups
                             if (PASS == 0) {
-                                tma_load_2d(base, &map_w0, st * 32, (int)((int64_t)T.e * a.wrow0 + T.row), full);
-                                tma_load_2d(base + 128 * 128, &map_w1, st * 32,
-                                            (int)((int64_t)T.e * a.wrow1 + a.woff1 + T.row), full);
+                                tma_load_2d(base, &map_w0, st * 32, (int)r0, full);
+                                tma_load_2d(base + 128 * 128, &map_w1, st * 32, (int)r1, full);
+                                tma_load_2d(base + C::kSOff, &map_sc0, tx0, ty0, full);
+                                tma_load_2d(base + C::kSOff + 128 * rs, &map_sc1, tx0, ty1, full);
+                                tma_load_2d(base + C::kBOff, &map_bi0, tx0, ty0, full);
+                                tma_load_2d(base + C::kBOff + 128 * rs, &map_bi1, tx0, ty1, full);
                             } else {
-                                tma_load_2d(base, &map_w0, st * 32, (int)((int64_t)T.e * a.wrow0 + T.row), full);
+                                tma_load_2d(base, &map_w0, st * 32, (int)r0, full);
+                                tma_load_2d(base + C::kSOff, &map_sc0, tx0, ty0, full);
+                                tma_load_2d(base + C::kBOff, &map_bi0, tx0, ty0, full);
                             }
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
-                                tma_load_2d(base + kXOff + q * kXBoxBytes, &map_x, (st * 4 + q) * 64, pc, full);
+                                tma_load_2d(base + C::kXOff + q * kXBoxBytes, &map_x, (st * 4 + q) * 64, pc, full);
                             if (PASS == 1) {   // lo terms of h: columns F.. of the same rows
 #pragma unroll
                                 for (int q = 0; q < 4; ++q)
-                                    tma_load_2d(base + kXOff + (4 + q) * kXBoxBytes, &map_x,
+                                    tma_load_2d(base + C::kXOff + (4 + q) * kXBoxBytes, &map_x,
                                                 a.F + (st * 4 + q) * 64, pc, full);
                             }
+                            tma_load_2d(base + C::kSumOff, &map_s, st * 4, pc, full);
                         }
                         ++it;
                     }
@@ -571,8 +563,8 @@ __global__ void __launch_bounds__(kPassThreads, 1)
             }
             // drain: every issued stage has landed before the CTA may exit
             if (poisoned) {
-                const uint32_t first = it > kStages ? it - kStages : 0;
-                for (uint32_t i = first; i < it; ++i) mbar_wait(R.full + 8 * (i % kStages), (i / kStages) & 1u);
+                const uint32_t first = it > C::kStages ? it - C::kStages : 0;
+                for (uint32_t i = first; i < it; ++i) mbar_wait(R.full + 8 * (i % C::kStages), (i / C::kStages) & 1u);
             }
         }
         return;
@@ -655,9 +647,10 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_done.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(ffn_pass_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassSmem);
+        cudaError_t e =
+            cudaFuncSetAttribute(ffn_pass_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, PassCfg<0>::kSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(ffn_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassSmem);
+            e = cudaFuncSetAttribute(ffn_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, PassCfg<1>::kSmem);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count[dev & 63], cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit);
@@ -665,10 +658,14 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     const int sms = sm_count[dev & 63] > 0 ? sm_count[dev & 63] : 1;
 
     // activation / group-sum maps over this call's workspace rows
-    CUtensorMap map_xg, map_h;
+    CUtensorMap map_xg, map_h, map_sx, map_sh;
     if (!encode_map_2d(&map_xg, xg, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, d, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_map_2d(&map_h, h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, 2 * F, 64, 16,
-                       CU_TENSOR_MAP_SWIZZLE_128B))
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_map_2d(&map_sx, sx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BK, d / kGroup, 4, kTokChunk,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_map_2d(&map_sh, sh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BK, F / kGroup, 4, kTokChunk,
+                       CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
 
     const size_t chunks = (size_t)BK * (d / 8);
@@ -687,14 +684,15 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     PassArgs a{};
     a.wrow0 = W.g_rows_per_expert; a.wrow1 = W.u_rows_per_expert; a.woff1 = W.u_row_offset;
     a.s0 = W.sg; a.b0 = W.bg; a.s1 = W.su; a.b1 = W.bu;
-    a.bsum = sx; a.kdim = d; a.F = F; a.d = d; a.K = K; a.E = E; a.B = B;
+    a.kdim = d; a.F = F; a.d = d; a.K = K; a.E = E; a.B = B;
     a.tiles_per_expert = F / 128;
     a.tc_min = tc_min;
     a.union_ids = union_ids; a.n_union = n_union; a.offsets = offsets;
     a.token_list = token_list; a.slot_list = slot_list;
     a.h_out = h; a.hsum_out = sh; a.y_out = y; a.status = status;
     const int grid0 = std::min(sms, max_u * a.tiles_per_expert);
-    ffn_pass_kernel<0><<<grid0, kPassThreads, kPassSmem, stream>>>(W.map_gate, W.map_up, map_xg, a);
+    ffn_pass_kernel<0><<<grid0, kPassThreads, PassCfg<0>::kSmem, stream>>>(W.map_gate, W.map_up, map_xg, map_sx,
+                                                                            W.map_sg, W.map_su, W.map_bg, W.map_bu, a);
     if (tc_min > 0) {
         cudaError_t e = launch_ffn_tc(D, TW, B, 0, union_ids, n_union, offsets, token_list, slot_list, ws, L, tc_min,
                                       sms, stream);
@@ -704,10 +702,11 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     PassArgs b = a;
     b.wrow0 = d; b.wrow1 = d; b.woff1 = 0;
     b.s0 = W.sd; b.b0 = W.bd; b.s1 = W.sd; b.b1 = W.bd;
-    b.bsum = sh; b.kdim = F;
+    b.kdim = F;
     b.tiles_per_expert = d / 256;
     const int grid1 = std::min(sms, max_u * b.tiles_per_expert);
-    ffn_pass_kernel<1><<<grid1, kPassThreads, kPassSmem, stream>>>(W.map_down, W.map_down, map_h, b);
+    ffn_pass_kernel<1><<<grid1, kPassThreads, PassCfg<1>::kSmem, stream>>>(W.map_down, W.map_down, map_h, map_sh,
+                                                                            W.map_sd, W.map_sd, W.map_bd, W.map_bd, b);
     if (tc_min > 0) {
         cudaError_t e = launch_ffn_tc(D, TW, B, 1, union_ids, n_union, offsets, token_list, slot_list, ws, L, tc_min,
                                       sms, stream);

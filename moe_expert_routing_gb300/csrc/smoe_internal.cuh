@@ -63,6 +63,9 @@ cudaError_t launch_union(const smoe_layer_desc& D, const int32_t* topk_idx, int 
 struct FfnPointers {
     CUtensorMap map_gate, map_up, map_down;
     CUtensorMap pm_gate, pm_up, pm_down;   // packed-word maps of the tensor-core path
+    // scale / bias tables of the expert passes: bf16 [rows, in/64], box 8 groups x 128 rows
+    // (gate, up) or 256 rows (down); see encode_group_map
+    CUtensorMap map_sg, map_bg, map_su, map_bu, map_sd, map_bd;
     const uint16_t* sg; const uint16_t* bg; int64_t g_rows_per_expert;
     const uint16_t* su; const uint16_t* bu; int64_t u_rows_per_expert; int64_t u_row_offset;
     const uint16_t* sd; const uint16_t* bd;

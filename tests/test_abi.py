@@ -59,6 +59,10 @@ def test_workspace_size_monotone_and_invalid(lib):
     assert smoe.smoe_workspace_bytes(_desc(group_size=32), 8) == 0
     assert smoe.smoe_workspace_bytes(_desc(top_k=200), 8) == 0
     assert smoe.smoe_workspace_bytes(_desc(d_model=4000), 8) == 0
+    # scale rows must be 8 bytes (256 inputs) or a multiple of 16 bytes (512 inputs)
+    assert smoe.smoe_workspace_bytes(_desc(d_model=768), 8) == 0
+    assert smoe.smoe_workspace_bytes(_desc(ffn_dim=1280), 8) == 0
+    assert smoe.smoe_workspace_bytes(_desc(d_model=256, ffn_dim=256), 8) > 0
     assert smoe.smoe_workspace_bytes(_desc(num_experts=512), 8) == 0
 
 
