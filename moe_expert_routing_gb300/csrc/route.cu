@@ -13,8 +13,9 @@
 //                       even a single token spreads the 2 MB gate read over ~100 SMs; the
 //                       partials are summed in a fixed order by the top-k kernel, so results
 //                       are deterministic.
-//   topk_kernel         one warp per token: sums the partials (+ bias), K rounds of a
-//                       warp arg-max (ties -> lower expert id), softmax weights.
+//   topk_kernel         one CTA per token: sums the partials (+ bias) with one thread per
+//                       expert, then K rounds of a warp arg-max (ties -> lower expert id),
+//                       softmax weights.
 #include "smoe_internal.cuh"
 
 #include <math.h>
@@ -48,8 +49,10 @@ __device__ __forceinline__ void split3(float2 v, uint32_t& hi, uint32_t& mid, ui
 }
 
 // CTA: 8 warps x 16 experts, 8*NT tokens, one k-split of kchunk inputs.  Warp: A = 16 gate
-// rows (three bf16 terms), B = NT 8-token tiles of x, fp32 accumulators.
-template <int NT>
+// rows (three bf16 terms), B = NT 8-token tiles of x, fp32 accumulators.  The loads of KB
+// k-steps are issued together before their products, so a warp has KB steps of its weight
+// and activation reads in flight (kchunk is a multiple of 16 * KB).
+template <int NT, int KB>
 __global__ void __launch_bounds__(256) gate_logits_kernel(const uint16_t* __restrict__ x,
                                                           const float* __restrict__ W, int B, int E, int d,
                                                           int kchunk, float* __restrict__ partial) {
@@ -72,26 +75,36 @@ __global__ void __launch_bounds__(256) gate_logits_kernel(const uint16_t* __rest
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
-    for (int k = k_begin; k < k_end; k += 16) {
-        const int k0 = k + 2 * c, k1 = k0 + 8;
-        float2 va0 = __ldg(reinterpret_cast<const float2*>(wa + k0));
-        float2 vb0 = __ldg(reinterpret_cast<const float2*>(wb + k0));
-        float2 va1 = __ldg(reinterpret_cast<const float2*>(wa + k1));
-        float2 vb1 = __ldg(reinterpret_cast<const float2*>(wb + k1));
-        if (ea >= E) va0 = va1 = make_float2(0.f, 0.f);
-        if (eb >= E) vb0 = vb1 = make_float2(0.f, 0.f);
-        uint32_t a[3][4];   // [term][a0..a3]: rows g / g+8, k 2c.. / 2c+8..
-        split3(va0, a[0][0], a[1][0], a[2][0]);
-        split3(vb0, a[0][1], a[1][1], a[2][1]);
-        split3(va1, a[0][2], a[1][2], a[2][2]);
-        split3(vb1, a[0][3], a[1][3], a[2][3]);
+    for (int kb = k_begin; kb < k_end; kb += 16 * KB) {
+        float2 wv[KB][4];
+        uint32_t xv[KB][NT][2];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const uint32_t b0 = __ldg(reinterpret_cast<const uint32_t*>(xr[nt] + k0));
-            const uint32_t b1 = __ldg(reinterpret_cast<const uint32_t*>(xr[nt] + k1));
+        for (int j = 0; j < KB; ++j) {
+            const int k0 = kb + 16 * j + 2 * c, k1 = k0 + 8;
+            wv[j][0] = __ldg(reinterpret_cast<const float2*>(wa + k0));
+            wv[j][1] = __ldg(reinterpret_cast<const float2*>(wb + k0));
+            wv[j][2] = __ldg(reinterpret_cast<const float2*>(wa + k1));
+            wv[j][3] = __ldg(reinterpret_cast<const float2*>(wb + k1));
 #pragma unroll
-            for (int term = 2; term >= 0; --term)   // small terms first
-                mma_bf16(acc[nt], a[term][0], a[term][1], a[term][2], a[term][3], b0, b1);
+            for (int nt = 0; nt < NT; ++nt) {
+                xv[j][nt][0] = __ldg(reinterpret_cast<const uint32_t*>(xr[nt] + k0));
+                xv[j][nt][1] = __ldg(reinterpret_cast<const uint32_t*>(xr[nt] + k1));
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < KB; ++j) {
+            if (ea >= E) wv[j][0] = wv[j][2] = make_float2(0.f, 0.f);
+            if (eb >= E) wv[j][1] = wv[j][3] = make_float2(0.f, 0.f);
+            uint32_t a[3][4];   // [term][a0..a3]: rows g / g+8, k 2c.. / 2c+8..
+            split3(wv[j][0], a[0][0], a[1][0], a[2][0]);
+            split3(wv[j][1], a[0][1], a[1][1], a[2][1]);
+            split3(wv[j][2], a[0][2], a[1][2], a[2][2]);
+            split3(wv[j][3], a[0][3], a[1][3], a[2][3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int term = 2; term >= 0; --term)   // small terms first
+                    mma_bf16(acc[nt], a[term][0], a[term][1], a[term][2], a[term][3], xv[j][nt][0], xv[j][nt][1]);
         }
     }
     float* out = partial + (size_t)blockIdx.z * B * E;
@@ -107,28 +120,39 @@ __global__ void __launch_bounds__(256) gate_logits_kernel(const uint16_t* __rest
 
 int tile_tokens(int B) { return B <= 64 ? 8 : 64; }
 
-// One warp per token.  Lane l holds experts l, l+32, ... (E <= 256).
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ partial, int splits,
-                                                   const float* __restrict__ bias, int B, int E, int K, int norm,
-                                                   int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (warp >= B) return;
-    const int t = warp;
+// One CTA per token.  Thread e sums expert e's split-K partials in split order (all loads
+// issued before the sum) and adds the bias; warp 0 then takes K rounds of a warp arg-max
+// (lane l holds experts l, l+32, ...; ties -> lower expert id) and the softmax weights.
+__global__ void __launch_bounds__(kMaxExperts) topk_kernel(const float* __restrict__ partial, int splits,
+                                                           const float* __restrict__ bias, int B, int E, int K,
+                                                           int norm, int32_t* __restrict__ idx_out,
+                                                           float* __restrict__ w_out) {
+    __shared__ float logit[kMaxExperts];
+    const int t = blockIdx.x;
+    const int e = threadIdx.x;
+    if (e < E) {
+        float p[kMaxSplits];
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplits; ++sp)
+            if (sp < splits) p[sp] = __ldg(partial + ((size_t)sp * B + t) * E + e);
+        float s = 0.f;
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplits; ++sp)
+            if (sp < splits) s += p[sp];
+        if (bias) s += bias[e];
+        logit[e] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x >= 32) return;
+    const int lane = threadIdx.x;
     constexpr int PER = kMaxExperts / 32;
     float v[PER];
     bool live[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
-        const int e = lane + 32 * i;
-        live[i] = e < E;
-        float s = 0.f;
-        if (live[i]) {
-#pragma unroll 4
-            for (int sp = 0; sp < splits; ++sp) s += __ldg(partial + ((size_t)sp * B + t) * E + e);
-            if (bias) s += bias[e];
-        }
-        v[i] = s;
+        const int ex = lane + 32 * i;
+        live[i] = ex < E;
+        v[i] = live[i] ? logit[ex] : 0.f;
     }
     // max logit over all experts
     float mx = -INFINITY;
@@ -153,8 +177,8 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
         int bi = 0x7fffffff;
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            const int e = lane + 32 * i;
-            if (live[i] && (v[i] > bv || (v[i] == bv && e < bi))) { bv = v[i]; bi = e; }
+            const int ex = lane + 32 * i;
+            if (live[i] && (v[i] > bv || (v[i] == bv && ex < bi))) { bv = v[i]; bi = ex; }
         }
 #pragma unroll
         for (int off = 16; off; off >>= 1) {
@@ -190,7 +214,8 @@ int route_splits(int B, int E, int d) {
     const int tiles = ((B + bt - 1) / bt) * ((E + kExpertsPerCta - 1) / kExpertsPerCta);
     const int target = 2 * 152;
     int s = 1;
-    while (s < kMaxSplits && s * tiles < target && (d / (2 * s)) % 16 == 0 && d / (2 * s) >= 128) s *= 2;
+    // a split keeps at least 128 inputs and a multiple of 128 (8 k-steps of 16 per load batch)
+    while (s < kMaxSplits && s * tiles < target && (d / (2 * s)) % 128 == 0) s *= 2;
     return s;
 }
 
@@ -202,11 +227,11 @@ cudaError_t launch_route(const smoe_layer_desc& D, const uint16_t* x, const floa
     while (split_cap > 0 && S > split_cap) S >>= 1;
     const int bt = tile_tokens(B);
     dim3 grid((B + bt - 1) / bt, (E + kExpertsPerCta - 1) / kExpertsPerCta, S);
-    if (bt == 8) gate_logits_kernel<1><<<grid, 256, 0, stream>>>(x, gate_w, B, E, d, d / S, logits_ws);
-    else gate_logits_kernel<8><<<grid, 256, 0, stream>>>(x, gate_w, B, E, d, d / S, logits_ws);
-    const int warps_per_block = 8;
-    topk_kernel<<<(B + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0, stream>>>(
-        logits_ws, S, gate_bias, B, E, K, D.norm_topk_prob, topk_idx, topk_w);
+    const int kchunk = d / S;   // a multiple of 128 (route_splits)
+    if (bt == 8) gate_logits_kernel<1, 8><<<grid, 256, 0, stream>>>(x, gate_w, B, E, d, kchunk, logits_ws);
+    else gate_logits_kernel<8, 2><<<grid, 256, 0, stream>>>(x, gate_w, B, E, d, kchunk, logits_ws);
+    const int threads = (E + 31) / 32 * 32;
+    topk_kernel<<<B, threads, 0, stream>>>(logits_ws, S, gate_bias, B, E, K, D.norm_topk_prob, topk_idx, topk_w);
     return cudaGetLastError();
 }
 
