@@ -170,6 +170,7 @@ WsLayout ws_layout(const smoe_layer_desc& D, int max_tokens) {
     L.s16x = take(2 * BK * (d / kGroup) * 2);
     L.s16h = take(2 * BK * (F / kGroup) * 2);
     L.y = take(BK * d * 4);
+    L.ticket = take((E + 2) * 4);
     L.total = o;
     return L;
 }

@@ -11,9 +11,11 @@
 // on the device):
 //   gather_kernel      x rows of every (expert, token) entry -> fp16, pair-permuted,
 //                      with per-64-group sums (xg, sx)
-//   ffn_pass_kernel<0> gate/up projections + SwiGLU, 128 h columns of one expert per tile;
-//                      writes h (fp16, pair-permuted) and its per-group sums
-//   ffn_pass_kernel<1> down projection, 256 output rows of one expert per tile; writes y
+//   ffn_expert_kernel  the experts with few tokens, persistent, from a device-side work
+//                      queue: gate/up projections + SwiGLU, 128 h columns of one expert per
+//                      tile, writing h (fp16, pair-permuted) and its per-group sums; the down
+//                      projection, 256 output rows of one expert per tile, writing y.  One
+//                      launch per pass, or both passes in one launch for long prompts
 //   combine_kernel     residual[t] += sum_k w[t][k] * y[t*K + k], k in rank order
 //
 // The pass kernels are persistent and warp-specialised: one producer warp streams, for
@@ -147,7 +149,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
                                                      const int32_t* __restrict__ token_list,
                                                      uint32_t* __restrict__ status,
                                                      __half* __restrict__ xg, float* __restrict__ sx,
-                                                     __half* __restrict__ s16, int BK) {
+                                                     __half* __restrict__ s16, int BK, int32_t* __restrict__ ticket,
+                                                     int n_ticket) {
+    if (blockIdx.x == 0)   // work queue of the expert passes that follow
+        for (int i = threadIdx.x; i < n_ticket; i += blockDim.x) ticket[i] = 0;
     const int cpr = d / 8;   // chunks per row, a multiple of 32: a warp never spans two rows
     const size_t gid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int p = (int)(gid / cpr), ch = (int)(gid - (size_t)p * cpr);
@@ -189,7 +194,12 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
 
 // ----------------------------------------------------------------------------- expert passes
 constexpr int kConsumerWarps = 8;
-constexpr int kPassThreads = 32 * (kConsumerWarps + 1);   // + one producer warp
+constexpr int kMailbox = 4;                                // finished gate/up tiles awaiting publication
+
+// Which passes a launch of the expert-pass kernel runs.
+constexpr int kGateUp = 1, kDown = 2, kBoth = 3;
+// consumer warps + a producer warp (+ a publisher warp when both passes share a launch)
+constexpr int pass_threads(int mode) { return 32 * (kConsumerWarps + 1 + (mode == kBoth)); }
 constexpr int kWBytes = 256 * 128;         // 256 weight rows x 32 u32 words (4 groups)
 constexpr int kXBoxBytes = 16 * 128;       // 16 activation rows x 64 fp16 (one group)
 constexpr int kTokChunk = 16;              // tokens per pass over the weights
@@ -199,23 +209,23 @@ constexpr int kSbBytes = 256 * 16;         // 256 rows x up to 8 bf16 (a table o
 // activation group sums fp32 [16 tokens][4 groups]; a 1024-byte multiple.  The scale and
 // bias tables hold, per weight row, the 8 groups of the 16-byte-aligned window that
 // contains the stage's 4 groups ([256][8] bf16), or with 4 groups per row ([256][4]) the
-// whole row.
-template <int PASS>
-struct PassCfg {
-    static constexpr int kStages = PASS ? 3 : 4;
-    static constexpr int kXBoxes = PASS ? 8 : 4;
+// whole row.  A gate/up-only launch has room for 4 of its smaller stages; launches that run
+// down tiles use 3 stages sized for them.
+template <int MODE>
+struct StageCfg {
+    static constexpr int kCount = MODE == kGateUp ? 4 : 3;
     static constexpr int kXOff = kWBytes;
-    static constexpr int kSOff = kXOff + kXBoxes * kXBoxBytes;
+    static constexpr int kSOff = kXOff + (MODE == kGateUp ? 4 : 8) * kXBoxBytes;
     static constexpr int kBOff = kSOff + kSbBytes;
     static constexpr int kSumOff = kBOff + kSbBytes;
     static constexpr int kSumBytes = kTokChunk * 4 * 4;
-    static constexpr int kStageBytes = (kSumOff + kSumBytes + 1023) / 1024 * 1024;
-    static constexpr int kTx = kWBytes + kXBoxes * kXBoxBytes + kSumBytes;   // TMA bytes of a stage
-                                                                              // (without the tables)
-    static constexpr int kSmem = kStages * kStageBytes + 1024;
+    static constexpr int kBytes = (kSumOff + kSumBytes + 1023) / 1024 * 1024;
+    static constexpr int kSmem = kCount * kBytes + 1024;
+    // TMA bytes of a pass's stage, without the scale / bias tables
+    static constexpr int tx(int pass) { return kWBytes + (pass ? 8 : 4) * kXBoxBytes + kSumBytes; }
 };
-static_assert(PassCfg<0>::kSmem <= 227 * 1024 - 2048, "pass 0 shared memory");
-static_assert(PassCfg<1>::kSmem <= 227 * 1024 - 2048, "pass 1 shared memory");
+static_assert(StageCfg<kGateUp>::kSmem <= 227 * 1024 - 3072, "gate/up pass shared memory");
+static_assert(StageCfg<kBoth>::kSmem <= 227 * 1024 - 3072, "expert pass shared memory");
 
 struct PassArgs {
     int64_t wrow0;        // pass 0: gate rows per expert in map_w0; pass 1: d
@@ -239,18 +249,6 @@ struct Tile {
     bool mine;            // handled by this kernel (not by the tensor-core path)
     int e, p0, p1, row;   // row: first h column (pass 0) or output row (pass 1) of the tile
 };
-
-__device__ __forceinline__ Tile decode_tile(const PassArgs& a, int t, int pass_rows) {
-    Tile T;
-    const int u = t / a.tiles_per_expert;
-    T.row = (t - u * a.tiles_per_expert) * pass_rows;
-    T.e = a.union_ids[u];
-    T.p0 = a.offsets[u];
-    T.p1 = a.offsets[u + 1];
-    T.ok = T.e >= 0 && T.e < a.E && T.p0 >= 0 && T.p1 >= T.p0 && T.p1 <= a.B * a.K;
-    T.mine = a.tc_min <= 0 || T.p1 - T.p0 < a.tc_min;
-    return T;
-}
 
 // One 256-input k-slice (4 groups) of a consumer warp: two 16-row m-tiles against NT
 // 8-token n-tiles.  wb0/wb1: shared addresses of the m-tiles' first rows; xs: the activation
@@ -339,10 +337,34 @@ struct Ring {
 };
 
 // All consumer warps of a chunk: stream the k-slices, then the pass epilogue.
-template <int NT, int PASS>
+// Finished gate/up tiles go to the publisher warp through a small mailbox ring: slot k % 4
+// holds the union slot of the k-th finished tile (-1: no more), full/empty mbarriers.
+struct Mailbox {
+    int* uu;                // [kMailbox]
+    uint32_t full, empty;   // shared addresses of full[0], empty[0] (8 bytes apart)
+    uint32_t k;             // posts so far (consumer thread 0)
+};
+
+// Consumer thread 0: hand the k-th entry to the publisher (bounded wait for a free slot).
+__device__ __forceinline__ bool mailbox_post(Mailbox& M, int uu) {
+    const uint32_t slot = M.k % kMailbox;
+    if (M.k >= kMailbox && !mbar_wait(M.empty + 8 * slot, ((M.k / kMailbox) - 1) & 1u)) return false;
+    M.uu[slot] = uu;
+    mbar_arrive(M.full + 8 * slot);   // release: the consumers' stores before it (named barrier)
+    ++M.k;
+    return true;
+}
+
+// Pass 0, the tile's last chunk (done_uu >= 0): after the named barrier that ends the
+// epilogue, every consumer thread's h and group-sum stores happen before consumer thread 0
+// posts the tile to the publisher, which makes them visible device-wide and counts the tile
+// for the expert's down tiles.  Publishing from a warp of its own keeps the fence's wait for
+// outstanding stores off the consumers.
+template <int NT, int PASS, int MODE>
 __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, uint32_t& it, bool& poisoned,
-                                              const Tile& T, int pc, int n, int warp, int lane, float* red) {
-    using C = PassCfg<PASS>;
+                                              const Tile& T, int pc, int n, int warp, int lane, float* red,
+                                              int done_uu, Mailbox& M) {
+    using C = StageCfg<MODE>;
     const int g = lane >> 2, c = lane & 3;
     const int nst = a.kdim / kGroup / 4;
     float acc[2][NT][4];
@@ -365,17 +387,31 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
     }
     wrow_off0 = (uint32_t)lrow0 * 128u;
     wrow_off1 = (uint32_t)lrow1 * 128u;
+    // pass 1: token and slot of this thread's output columns, loaded before the k loop
+    int tok[NT][2], slt[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int slot = nt * 8 + 2 * c + j;
+            tok[nt][j] = -1;
+            slt[nt][j] = 0;
+            if (PASS == 1 && slot < n) {
+                tok[nt][j] = a.token_list[pc + slot];
+                slt[nt][j] = a.slot_list[pc + slot];
+            }
+        }
     const bool packed = a.kdim / kGroup == 4;   // tables [256][4]: the whole row
     const uint32_t rs = packed ? 8u : 16u;
     auto tab_off = [&](int st) { return packed ? 0u : (uint32_t)(st & 1) * 8u; };
     for (int st = 0; st < nst; ++st) {
-        const uint32_t slot = it % C::kStages;
-        const uint32_t parity = (it / C::kStages) & 1u;
+        const uint32_t slot = it % C::kCount;
+        const uint32_t parity = (it / C::kCount) & 1u;
         if (!poisoned && !mbar_wait(R.full + 8 * slot, parity)) {
             poisoned = true;
             if (lane == 0) atomicOr(a.status, SMOE_FAULT_TIMEOUT);
         }
-        const uint32_t base = R.buf + slot * C::kStageBytes;
+        const uint32_t base = R.buf + slot * C::kBytes;
         // this stage's 4 groups in the tables: row stride rs, at byte tab_off inside a row
         const uint32_t ts = base + C::kSOff + tab_off(st), tb = base + C::kBOff + tab_off(st);
         uint2 sc[2][2], bi[2][2];
@@ -448,6 +484,9 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
             }
         }
         asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kConsumerWarps) : "memory");
+        // every consumer thread's h / sum stores happen before this point (named barrier);
+        // the fence makes them visible device-wide before the count
+        if (done_uu >= 0 && tid == 0 && !mailbox_post(M, done_uu)) atomicOr(a.status, SMOE_FAULT_TIMEOUT);
     } else {
 #pragma unroll
         for (int m = 0; m < 2; ++m)
@@ -455,10 +494,7 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int slot = nt * 8 + 2 * c + (i & 1);
-                    if (slot >= n) continue;
-                    const int p = pc + slot;
-                    const int t = a.token_list[p], k = a.slot_list[p];
+                    const int t = tok[nt][i & 1], k = slt[nt][i & 1];   // t < 0: slot past the chunk
                     if (t < 0 || t >= a.B || k < 0 || k >= a.K) continue;   // flagged by the gather
                     const int r = T.row + warp * 32 + m * 16 + g + ((i & 2) ? 8 : 0);
                     a.y_out[((size_t)t * a.K + k) * a.d + r] = acc[m][nt][i];
@@ -466,124 +502,307 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
     }
 }
 
-// PASS 0: tile = 128 h columns of one expert (consumer warp w: gate and up rows 16w..16w+15).
-// PASS 1: tile = 256 down rows of one expert (consumer warp w: rows 32w..32w+31).
-// Tiles t = blockIdx.x, blockIdx.x + gridDim.x, ... over n_union * tiles_per_expert.
-// Producer warp (lane 0): the TMA copies of a stage (weights, activations, group sums, and
-// the scale and bias tables: map_sc0 / map_bi0 rows of map_w0, map_sc1 / map_bi1 rows of
-// map_w1).
-template <int PASS>
-__global__ void __launch_bounds__(kPassThreads, 1)
-    ffn_pass_kernel(const __grid_constant__ CUtensorMap map_w0, const __grid_constant__ CUtensorMap map_w1,
-                    const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_s,
-                    const __grid_constant__ CUtensorMap map_sc0, const __grid_constant__ CUtensorMap map_sc1,
-                    const __grid_constant__ CUtensorMap map_bi0, const __grid_constant__ CUtensorMap map_bi1,
-                    PassArgs a) {
-    using C = PassCfg<PASS>;
+// The expert passes as persistent kernels with a device-side work queue.  Work items, in this
+// order: the gate/up tiles (128 h columns of one union expert: consumer warp w takes gate and
+// up rows 16w..16w+15), then the down tiles (256 output rows of one union expert: consumer
+// warp w takes rows 32w..32w+31), expert-major.  A launch runs the gate/up items, the down
+// items, or both (MODE).  The producer thread takes the next item with an atomic ticket, so
+// CTAs that draw long items (experts with many tokens) do not hold up the rest.  With both
+// passes in one launch, items are claimed in order and every item a CTA waits for has been
+// claimed by a running CTA: a down tile waits (bounded) until all gate/up tiles of its expert
+// have been published, which lets the down tiles of finished experts fill the SMs while the
+// last gate/up tiles run, with no grid-wide barrier.  The item of every ring stage travels
+// with it in shared memory; an item < 0 tells the consumers to stop.
+struct FusedArgs {
+    PassArgs p[2];
+    int32_t* ticket;      // [0]: next item of a gate/up or both-pass launch; [1]: next item of a
+                          // down launch; [2 + u]: published gate/up tiles of union expert u
+};
+
+// OR of v over the consumer threads (named barrier 1).
+__device__ __forceinline__ bool consumers_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(32 * kConsumerWarps)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bounded wait (~0.5 s) until *p >= target.
+__device__ __forceinline__ bool wait_count(const int32_t* p, int target) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (ld_acquire(p) >= target) return true;
+        uint64_t now;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+        if (i == 0) t0 = now;
+        else if (now - t0 > 500000000ull) return false;
+        __nanosleep(256);
+    }
+}
+
+__device__ __forceinline__ int ld_relaxed(const int32_t* p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// A claimed work item and the global values it needs, loaded as soon as the item is known
+// and used one item later (so the producer does not wait on their latency).
+struct Claim {
+    int item, pass, j, uu;   // item, its pass, index inside the pass, union slot of the expert
+    int e, p0, p1;           // expert id and its token-list range
+    int done;                // pass 1: finished gate/up tiles of the expert when loaded
+};
+
+__device__ __forceinline__ Claim claim_item(const FusedArgs& f, int item, int n0, int n_items) {
+    Claim c{};
+    c.item = item;
+    if (item >= n_items) return c;
+    c.pass = item >= n0;
+    c.j = c.pass ? item - n0 : item;
+    c.uu = c.j / (c.pass ? f.p[1].tiles_per_expert : f.p[0].tiles_per_expert);
+    c.e = f.p[0].union_ids[c.uu];
+    c.p0 = f.p[0].offsets[c.uu];
+    c.p1 = f.p[0].offsets[c.uu + 1];
+    if (c.pass) c.done = ld_relaxed(f.ticket + 2 + c.uu);
+    return c;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(pass_threads(MODE), 1)
+    ffn_expert_kernel(const __grid_constant__ CUtensorMap map_gate, const __grid_constant__ CUtensorMap map_up,
+                     const __grid_constant__ CUtensorMap map_down, const __grid_constant__ CUtensorMap map_xg,
+                     const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_sx,
+                     const __grid_constant__ CUtensorMap map_sh, const __grid_constant__ CUtensorMap map_sg,
+                     const __grid_constant__ CUtensorMap map_su, const __grid_constant__ CUtensorMap map_bg,
+                     const __grid_constant__ CUtensorMap map_bu, const __grid_constant__ CUtensorMap map_sd,
+                     const __grid_constant__ CUtensorMap map_bd, FusedArgs f) {
+    using C = StageCfg<MODE>;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[2 * C::kStages];
+    __shared__ __align__(8) uint64_t bars[2 * C::kCount];
+    // per stage: item (< 0: stop), chunk start, and the decoded tile (expert, list range, row)
+    __shared__ int slot_meta[C::kCount][6];
     __shared__ float red[kConsumerWarps * 16];
+    __shared__ __align__(8) uint64_t mbars[2 * kMailbox];
+    __shared__ int mail[kMailbox];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int pass_rows = PASS == 0 ? 128 : 256;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Ring R;
     R.buf = smem_addr(smem);
     R.full = smem_addr(&bars[0]);
-    R.empty = smem_addr(&bars[C::kStages]);
+    R.empty = smem_addr(&bars[C::kCount]);
+    Mailbox M;
+    M.uu = mail;
+    M.full = smem_addr(&mbars[0]);
+    M.empty = smem_addr(&mbars[kMailbox]);
+    M.k = 0;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(R.full + 8 * s, 1);   // TMA arrive + one cp.async arrive per producer lane
+        for (int s = 0; s < C::kCount; ++s) {
+            mbar_init(R.full + 8 * s, 1);
             mbar_init(R.empty + 8 * s, 32 * kConsumerWarps);
+        }
+        for (int s = 0; s < kMailbox; ++s) {
+            mbar_init(M.full + 8 * s, 1);
+            mbar_init(M.empty + 8 * s, 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     __syncthreads();
 
-    const int n_tiles = *a.n_union * a.tiles_per_expert;
-    const int G = a.kdim / kGroup, nst = G / 4;
+    const int nu = *f.p[0].n_union;
+    const int t0 = f.p[0].tiles_per_expert, n0 = nu * t0;
+    const int first_item = MODE == kDown ? n0 : 0;
+    const int n_items = MODE == kGateUp ? n0 : n0 + nu * f.p[1].tiles_per_expert;
+    int32_t* queue = f.ticket + (MODE == kDown ? 1 : 0);
     uint32_t it = 0;
     bool poisoned = false;
+
+    if (MODE == kBoth && warp == kConsumerWarps + 1) {
+        // ---------------------------------------------------------------- publisher (one thread)
+        if (lane == 0) {
+            for (uint32_t k = 0;; ++k) {
+                const uint32_t slot = k % kMailbox;
+                if (!mbar_wait(M.full + 8 * slot, (k / kMailbox) & 1u)) {
+                    atomicOr(f.p[0].status, SMOE_FAULT_TIMEOUT);
+                    break;
+                }
+                const int uu = *reinterpret_cast<volatile int*>(&mail[slot]);
+                if (uu < 0) break;
+                __threadfence();                 // the tile's h / sums before the count
+                atomicAdd(f.ticket + 2 + uu, 1);
+                mbar_arrive(M.empty + 8 * slot);
+            }
+        }
+        return;
+    }
 
     if (warp == kConsumerWarps) {
         // ---------------------------------------------------------------- producer (one thread)
         if (lane == 0) {
-            const bool packed = G == 4;
-            const uint32_t rs = packed ? 8u : 16u;
-            const uint32_t tx = C::kTx + 2u * 256u * rs;
-            for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-                const Tile T = decode_tile(a, t, pass_rows);
-                if (!T.ok || !T.mine) continue;
-                // first rows of the tile in map_w0 and (pass 0) map_w1
-                const int64_t r0 = (int64_t)T.e * a.wrow0 + T.row;
-                const int64_t r1 = PASS == 0 ? (int64_t)T.e * a.wrow1 + a.woff1 + T.row : r0;
-                // the tile's scale / bias rows into L2 ahead of the table copies
-                const uint32_t bytes = (uint32_t)(pass_rows * G * 2);
-                prefetch_l2(a.s0 + r0 * G, bytes); prefetch_l2(a.b0 + r0 * G, bytes);
-                if (PASS == 0) { prefetch_l2(a.s1 + r1 * G, bytes); prefetch_l2(a.b1 + r1 * G, bytes); }
-                const int ty0 = (int)(packed ? r0 / 2 : r0), ty1 = (int)(packed ? r1 / 2 : r1);
-                for (int pc = T.p0; pc < T.p1; pc += kTokChunk) {
-                    for (int st = 0; st < nst; ++st) {
-                        const uint32_t slot = it % C::kStages;
-                        if (it >= C::kStages && !poisoned &&
-                            !mbar_wait(R.empty + 8 * slot, ((it / C::kStages) - 1) & 1u)) {
+            // tickets run two items ahead and the globals of an item are loaded one item ahead,
+            // so no latency of the queue sits between the stages of consecutive items
+            // one-pass launches: static round-robin (uniform items, no queue latency); both
+            // passes: the ordered queue that makes the cross-CTA waits safe
+            int sk = 0;
+            auto take = [&]() { return MODE == kBoth ? atomicAdd(queue, 1) : (int)(blockIdx.x + gridDim.x * sk++); };
+            Claim cur = claim_item(f, first_item + take(), n0, n_items);
+            int next_item = first_item + take();
+            for (;;) {
+                const int item = cur.item;
+                if (item >= n_items || poisoned) break;
+                const int after_next = first_item + take();
+                const Claim nxt = claim_item(f, next_item, n0, n_items);
+                const PassArgs& a = cur.pass ? f.p[1] : f.p[0];
+                Tile T;
+                T.e = cur.e;
+                T.p0 = cur.p0;
+                T.p1 = cur.p1;
+                T.row = (cur.j - cur.uu * a.tiles_per_expert) * (cur.pass ? 256 : 128);
+                T.ok = T.e >= 0 && T.e < a.E && T.p0 >= 0 && T.p1 >= T.p0 && T.p1 <= a.B * a.K;
+                T.mine = a.tc_min <= 0 || T.p1 - T.p0 < a.tc_min;
+                if (!T.ok) atomicOr(a.status, SMOE_FAULT_EXPERT_INDEX);
+                if (T.ok && T.mine) {
+                    if (MODE == kBoth && cur.pass == 1) {
+                        // every gate/up tile of this expert has published h and its group sums
+                        // (an acquire load, not a fence: a fence would also wait for this
+                        // thread's copies in flight)
+                        if (!(cur.done >= t0 && ld_acquire(f.ticket + 2 + cur.uu) >= t0) &&
+                            !wait_count(f.ticket + 2 + cur.uu, t0)) {
                             poisoned = true;
                             atomicOr(a.status, SMOE_FAULT_TIMEOUT);
+                            break;
                         }
-                        const uint32_t base = R.buf + slot * C::kStageBytes;
-                        const uint32_t full = R.full + 8 * slot;
-                        if (!poisoned) {
+                        asm volatile("fence.proxy.async.global;\n" ::: "memory");   // h is read by TMA
+                    }
+                    const int G = a.kdim / kGroup, nst = G / 4;
+                    const bool packed = G == 4;
+                    const uint32_t rs = packed ? 8u : 16u;
+                    const uint32_t tx = (uint32_t)C::tx(cur.pass) + 2u * 256u * rs;
+                    // first rows of the tile in the weight maps
+                    const int64_t r0 = (int64_t)T.e * a.wrow0 + T.row;
+                    const int64_t r1 = cur.pass == 0 ? (int64_t)T.e * a.wrow1 + a.woff1 + T.row : r0;
+                    // the tile's scale / bias rows into L2 ahead of the table copies
+                    const uint32_t bytes = (uint32_t)((cur.pass ? 256 : 128) * G * 2);
+                    prefetch_l2(a.s0 + r0 * G, bytes); prefetch_l2(a.b0 + r0 * G, bytes);
+                    if (cur.pass == 0) { prefetch_l2(a.s1 + r1 * G, bytes); prefetch_l2(a.b1 + r1 * G, bytes); }
+                    const int ty0 = (int)(packed ? r0 / 2 : r0), ty1 = (int)(packed ? r1 / 2 : r1);
+                    for (int pc = T.p0; pc < T.p1 && !poisoned; pc += kTokChunk) {
+                        for (int st = 0; st < nst; ++st) {
+                            const uint32_t slot = it % C::kCount;
+                            if (it >= C::kCount && !mbar_wait(R.empty + 8 * slot, ((it / C::kCount) - 1) & 1u)) {
+                                poisoned = true;
+                                atomicOr(a.status, SMOE_FAULT_TIMEOUT);
+                                break;
+                            }
+                            const uint32_t base = R.buf + slot * C::kBytes;
+                            const uint32_t full = R.full + 8 * slot;
+                            slot_meta[slot][0] = item;
+                            slot_meta[slot][1] = pc;
+                            slot_meta[slot][2] = T.e;
+                            slot_meta[slot][3] = T.p0;
+                            slot_meta[slot][4] = T.p1;
+                            slot_meta[slot][5] = T.row;
                             mbar_expect_tx(full, tx);
                             const int tx0 = packed ? 0 : (st * 4) & ~7;   // 16-byte window of the stage's groups
-                            if (PASS == 0) {
-                                tma_load_2d(base, &map_w0, st * 32, (int)r0, full);
-                                tma_load_2d(base + 128 * 128, &map_w1, st * 32, (int)r1, full);
-                                tma_load_2d(base + C::kSOff, &map_sc0, tx0, ty0, full);
-                                tma_load_2d(base + C::kSOff + 128 * rs, &map_sc1, tx0, ty1, full);
-                                tma_load_2d(base + C::kBOff, &map_bi0, tx0, ty0, full);
-                                tma_load_2d(base + C::kBOff + 128 * rs, &map_bi1, tx0, ty1, full);
-                            } else {
-                                tma_load_2d(base, &map_w0, st * 32, (int)r0, full);
-                                tma_load_2d(base + C::kSOff, &map_sc0, tx0, ty0, full);
-                                tma_load_2d(base + C::kBOff, &map_bi0, tx0, ty0, full);
-                            }
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                tma_load_2d(base + C::kXOff + q * kXBoxBytes, &map_x, (st * 4 + q) * 64, pc, full);
-                            if (PASS == 1) {   // lo terms of h: columns F.. of the same rows
+                            if (MODE == kGateUp || (MODE == kBoth && cur.pass == 0)) {
+                                tma_load_2d(base, &map_gate, st * 32, (int)r0, full);
+                                tma_load_2d(base + 128 * 128, &map_up, st * 32, (int)r1, full);
+                                tma_load_2d(base + C::kSOff, &map_sg, tx0, ty0, full);
+                                tma_load_2d(base + C::kSOff + 128 * rs, &map_su, tx0, ty1, full);
+                                tma_load_2d(base + C::kBOff, &map_bg, tx0, ty0, full);
+                                tma_load_2d(base + C::kBOff + 128 * rs, &map_bu, tx0, ty1, full);
 #pragma unroll
                                 for (int q = 0; q < 4; ++q)
-                                    tma_load_2d(base + C::kXOff + (4 + q) * kXBoxBytes, &map_x,
+                                    tma_load_2d(base + C::kXOff + q * kXBoxBytes, &map_xg, (st * 4 + q) * 64, pc,
+                                                full);
+                                tma_load_2d(base + C::kSumOff, &map_sx, st * 4, pc, full);
+                            } else if (MODE != kGateUp) {
+                                tma_load_2d(base, &map_down, st * 32, (int)r0, full);
+                                tma_load_2d(base + C::kSOff, &map_sd, tx0, ty0, full);
+                                tma_load_2d(base + C::kBOff, &map_bd, tx0, ty0, full);
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {   // h hi, then its lo terms (columns F..)
+                                    tma_load_2d(base + C::kXOff + q * kXBoxBytes, &map_h, (st * 4 + q) * 64, pc, full);
+                                    tma_load_2d(base + C::kXOff + (4 + q) * kXBoxBytes, &map_h,
                                                 a.F + (st * 4 + q) * 64, pc, full);
+                                }
+                                tma_load_2d(base + C::kSumOff, &map_sh, st * 4, pc, full);
                             }
-                            tma_load_2d(base + C::kSumOff, &map_s, st * 4, pc, full);
+                            ++it;
                         }
-                        ++it;
                     }
+                }
+                cur = nxt;
+                next_item = after_next;
+            }
+            if (!poisoned) {
+                // end of work: a stage with item -1 and no copies
+                const uint32_t slot = it % C::kCount;
+                if (it >= C::kCount && !mbar_wait(R.empty + 8 * slot, ((it / C::kCount) - 1) & 1u)) {
+                    poisoned = true;
+                    atomicOr(f.p[0].status, SMOE_FAULT_TIMEOUT);
+                } else {
+                    slot_meta[slot][0] = -1;
+                    mbar_arrive(R.full + 8 * slot);
                 }
             }
             // drain: every issued stage has landed before the CTA may exit
             if (poisoned) {
-                const uint32_t first = it > C::kStages ? it - C::kStages : 0;
-                for (uint32_t i = first; i < it; ++i) mbar_wait(R.full + 8 * (i % C::kStages), (i / C::kStages) & 1u);
+                const uint32_t first = it > C::kCount ? it - C::kCount : 0;
+                for (uint32_t i = first; i < it; ++i) mbar_wait(R.full + 8 * (i % C::kCount), (i / C::kCount) & 1u);
             }
         }
         return;
     }
 
     // -------------------------------------------------------------------- consumers
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-        const Tile T = decode_tile(a, t, pass_rows);
-        if (!T.ok) {
-            if (warp == 0 && lane == 0) atomicOr(a.status, SMOE_FAULT_EXPERT_INDEX);
-            continue;
+    for (;;) {
+        const uint32_t slot = it % C::kCount;
+        // all consumer threads take the same decision, so that they run the same chunks and
+        // meet at the same named barriers
+        if (consumers_any(!mbar_wait(R.full + 8 * slot, (it / C::kCount) & 1u))) {
+            if (threadIdx.x == 0) atomicOr(f.p[0].status, SMOE_FAULT_TIMEOUT);
+            break;
         }
-        if (!T.mine) continue;
-        for (int pc = T.p0; pc < T.p1; pc += kTokChunk) {
-            const int n = min(kTokChunk, T.p1 - pc);
-            if (n <= 8) consume_chunk<1, PASS>(a, R, it, poisoned, T, pc, n, warp, lane, red);
-            else consume_chunk<2, PASS>(a, R, it, poisoned, T, pc, n, warp, lane, red);
+        const volatile int* meta = slot_meta[slot];
+        const int item = meta[0];
+        if (item < 0) break;
+        const int pc = meta[1];
+        Tile T;
+        T.ok = T.mine = true;
+        T.e = meta[2];
+        T.p0 = meta[3];
+        T.p1 = meta[4];
+        T.row = meta[5];
+        const int n = min(kTokChunk, T.p1 - pc);
+        const bool gate_up = MODE == kGateUp || (MODE == kBoth && item < n0);
+        if constexpr (MODE != kDown) {
+            if (gate_up) {
+                // both passes in this launch: publish the tile after its last chunk
+                const int done_uu = MODE == kBoth && pc + kTokChunk >= T.p1 ? item / t0 : -1;
+                if (n <= 8) consume_chunk<1, 0, MODE>(f.p[0], R, it, poisoned, T, pc, n, warp, lane, red, done_uu, M);
+                else consume_chunk<2, 0, MODE>(f.p[0], R, it, poisoned, T, pc, n, warp, lane, red, done_uu, M);
+            }
         }
+        if constexpr (MODE != kGateUp) {
+            if (!gate_up) {
+                if (n <= 8) consume_chunk<1, 1, MODE>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
+                else consume_chunk<2, 1, MODE>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
+            }
+        }
+        if (poisoned) break;
     }
+    // no more tiles to publish
+    if (MODE == kBoth && threadIdx.x == 0 && !mailbox_post(M, -1)) atomicOr(f.p[0].status, SMOE_FAULT_TIMEOUT);
 }
 
 // ----------------------------------------------------------------------------- combine
@@ -647,10 +866,14 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_done.load() & bit)) {
-        cudaError_t e =
-            cudaFuncSetAttribute(ffn_pass_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, PassCfg<0>::kSmem);
+        cudaError_t e = cudaFuncSetAttribute(ffn_expert_kernel<kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             StageCfg<kGateUp>::kSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(ffn_pass_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, PassCfg<1>::kSmem);
+            e = cudaFuncSetAttribute(ffn_expert_kernel<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     StageCfg<kDown>::kSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(ffn_expert_kernel<kBoth>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     StageCfg<kBoth>::kSmem);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count[dev & 63], cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit);
@@ -669,8 +892,10 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
         return cudaErrorInvalidValue;
 
     const size_t chunks = (size_t)BK * (d / 8);
+    int32_t* ticket = ws_ptr<int32_t>(ws, L.ticket);
     gather_kernel<<<(unsigned)((chunks + 255) / 256), 256, 0, stream>>>(x, d, B, n_union, offsets, token_list, status,
-                                                                          xg, sx, ws_ptr<__half>(ws, L.s16x), BK);
+                                                                          xg, sx, ws_ptr<__half>(ws, L.s16x), BK,
+                                                                          ticket, E + 2);
 
     // experts with many tokens go to the tcgen05 path; with fewer than 256 tokens in the chunk
     // an expert rarely reaches the threshold, so the extra launches are skipped
@@ -690,27 +915,36 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     a.union_ids = union_ids; a.n_union = n_union; a.offsets = offsets;
     a.token_list = token_list; a.slot_list = slot_list;
     a.h_out = h; a.hsum_out = sh; a.y_out = y; a.status = status;
-    const int grid0 = std::min(sms, max_u * a.tiles_per_expert);
-    ffn_pass_kernel<0><<<grid0, kPassThreads, PassCfg<0>::kSmem, stream>>>(W.map_gate, W.map_up, map_xg, map_sx,
-                                                                            W.map_sg, W.map_su, W.map_bg, W.map_bu, a);
-    if (tc_min > 0) {
-        cudaError_t e = launch_ffn_tc(D, TW, B, 0, union_ids, n_union, offsets, token_list, slot_list, ws, L, tc_min,
-                                      sms, stream);
-        if (e != cudaSuccess) return e;
-    }
-
     PassArgs b = a;
     b.wrow0 = d; b.wrow1 = d; b.woff1 = 0;
     b.s0 = W.sd; b.b0 = W.bd; b.s1 = W.sd; b.b1 = W.bd;
     b.kdim = F;
     b.tiles_per_expert = d / 256;
-    const int grid1 = std::min(sms, max_u * b.tiles_per_expert);
-    ffn_pass_kernel<1><<<grid1, kPassThreads, PassCfg<1>::kSmem, stream>>>(W.map_down, W.map_down, map_h, map_sh,
-                                                                            W.map_sd, W.map_sd, W.map_bd, W.map_bd, b);
+    FusedArgs fa{};
+    fa.p[0] = a;
+    fa.p[1] = b;
+    fa.ticket = ticket;
+    const int t0 = a.tiles_per_expert, t1 = b.tiles_per_expert;
     if (tc_min > 0) {
-        cudaError_t e = launch_ffn_tc(D, TW, B, 1, union_ids, n_union, offsets, token_list, slot_list, ws, L, tc_min,
-                                      sms, stream);
-        if (e != cudaSuccess) return e;
+        // long prompts: experts with a few tokens each run both passes from one queue
+        const int grid = std::min(sms, max_u * (t0 + t1));
+        ffn_expert_kernel<kBoth><<<grid, pass_threads(kBoth), StageCfg<kBoth>::kSmem, stream>>>(
+            W.map_gate, W.map_up, W.map_down, map_xg, map_h, map_sx, map_sh, W.map_sg, W.map_su, W.map_bg, W.map_bu,
+            W.map_sd, W.map_bd, fa);
+    } else {
+        ffn_expert_kernel<kGateUp><<<std::min(sms, max_u * t0), pass_threads(kGateUp), StageCfg<kGateUp>::kSmem,
+                                    stream>>>(W.map_gate, W.map_up, W.map_down, map_xg, map_h, map_sx, map_sh,
+                                              W.map_sg, W.map_su, W.map_bg, W.map_bu, W.map_sd, W.map_bd, fa);
+        ffn_expert_kernel<kDown><<<std::min(sms, max_u * t1), pass_threads(kDown), StageCfg<kDown>::kSmem,
+                                  stream>>>(W.map_gate, W.map_up, W.map_down, map_xg, map_h, map_sx, map_sh,
+                                            W.map_sg, W.map_su, W.map_bg, W.map_bu, W.map_sd, W.map_bd, fa);
+    }
+    if (tc_min > 0) {
+        for (int pass = 0; pass < 2; ++pass) {
+            cudaError_t e = launch_ffn_tc(D, TW, B, pass, union_ids, n_union, offsets, token_list, slot_list, ws, L,
+                                          tc_min, sms, stream);
+            if (e != cudaSuccess) return e;
+        }
     }
 
     const size_t n4 = (size_t)B * d / 4;

@@ -35,6 +35,7 @@ struct WsLayout {
     size_t s16x;          // fp16 [2][B * K, d / 64]: input group sums as hi and lo planes
     size_t s16h;          // fp16 [2][B * K, F / 64]: activation group sums as hi and lo planes
     size_t y;             // fp32 [B * K, d]: unweighted expert outputs, row t*K + k
+    size_t ticket;        // int32 [2 + E]: work queues of the expert passes and per-expert counts
     size_t total;
 };
 
