@@ -46,7 +46,8 @@ constexpr int TC_A_BYTES = 256 * 128;        // A slot: 256 rows x 64 fp16, SW12
 constexpr int TC_A_SLOTS = 2;
 constexpr int TC_P_BYTES = 256 * 32;         // packed weights: 256 rows x 8 words
 constexpr int TC_B_BYTES = TC_N * 128;       // one B sub-tile: 128 token rows x 64 fp16, SW128 K-major
-constexpr int TC_H_BYTES = 32 * 64 * 4;      // pass 0 epilogue staging: 32 tokens x 64 h columns fp32
+constexpr int TC_H_STRIDE = 33;             // pass 0 epilogue staging: 64 h columns x 32 tokens fp32,
+constexpr int TC_H_BYTES = 64 * TC_H_STRIDE * 4;   // column-major, padded (conflict-free both ways)
 constexpr int TC_THREADS = 448;
 constexpr uint32_t TC_TMEM_COLS = 512;
 
@@ -276,6 +277,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     __shared__ uint32_t tmem_base_sh;
     __shared__ int pref[kMaxExperts + 1];
     __shared__ int tok_sh[2][TC_N], slot_sh[2][TC_N];
+    __shared__ float gsum_sh[4][32];   // pass 0 epilogue: partial group sums [column quarter][token]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -442,8 +444,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         const uint32_t sw = (&scl.x)[(st & 7) >> 1];
                         const float sf = __uint_as_float((st & 1) ? (sw & 0xFFFF0000u) : (sw << 16));
                         const __half2 s2 = __float2half2_rn(sf);   // exact: bf16 -> fp16
+                        // packed rows land with a 32-byte swizzle: the 16-byte halves of row p
+                        // swap when bit 2 of p is set (conflict-free 16-byte reads)
                         const uint32_t pk = sbase + C::kOffLoad + s * C::kSlotBytes + prow * 32u;
-                        const uint4 w0 = lds128(pk), w1 = lds128(pk + 16);
+                        const uint32_t swz = ((prow >> 2) & 1u) << 4;
+                        const uint4 w0 = lds128(pk + swz), w1 = lds128(pk + (16u ^ swz));
                         const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
                         for (int c = 0; c < 8; ++c) sts128(arow + ((uint32_t)(c ^ (r & 7)) << 4), dequant_word(wv[c], s2));
@@ -476,7 +481,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int q = warp & 3;                  // TMEM lane quarter of this warp
         const int et = threadIdx.x - 320;        // 0..127
         const int lr = q * 32 + lane;            // accumulator row (TMEM lane) of this thread
-        float* hsm = reinterpret_cast<float*>(smem + C::kOffStage);   // pass 0: [32 tokens][64 cols]
+        float* hsm = reinterpret_cast<float*>(smem + C::kOffStage);   // pass 0: [64 cols][33]
         uint32_t tile = 0;
         for (int t = blockIdx.x; t < n_items; t += gridDim.x, ++tile) {
             const Item I = decode_item(a, pref, t);
@@ -517,11 +522,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                 const int tk = (odd_lane ? 16 : 0) + k;
                                 const float hv = g / (1.f + expf(-g)) * u;
                                 if (c0 + tk < ntok && !(fabsf(hv) <= 65504.f)) atomicOr(a.status, SMOE_FAULT_FP16_RANGE);
-                                hsm[tk * 64 + hc] = hv;
+                                hsm[hc * TC_H_STRIDE + tk] = hv;
                             }
                             asm volatile("bar.sync 2, 128;\n" ::: "memory");
-                            // 32 tokens x 64 columns: thread -> (token et >> 2, columns 16 (et & 3) .. + 16)
-                            const int tk = et >> 2, cq = et & 3;
+                            // 32 tokens x 64 columns: thread -> (token et & 31, columns 16 (et >> 5) .. + 16)
+                            const int tk = et & 31, cq = et >> 5;
                             const bool valid = c0 + tk < ntok;
                             float gs = 0.f;
 #pragma unroll
@@ -530,7 +535,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                 __half hh[8], hl[8];
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) {
-                                    const float hv = hsm[tk * 64 + cb + e];
+                                    const float hv = hsm[(cb + e) * TC_H_STRIDE + tk];
                                     const float hs = (e & 1) ? hv * 0.0625f : hv;   // odd columns / 16
                                     const __half h1 = __float2half_rn(hs);
                                     const __half h2 = __float2half_rn(hs - __half2float(h1));
@@ -546,16 +551,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                     *reinterpret_cast<uint4*>(rowp + a.F) = *reinterpret_cast<const uint4*>(hl);
                                 }
                             }
-                            gs += __shfl_xor_sync(0xffffffffu, gs, 1);
-                            gs += __shfl_xor_sync(0xffffffffu, gs, 2);
-                            if (valid && cq == 0) {
+                            gsum_sh[cq][tk] = gs;   // the group's 4 column quarters, summed by warp 0
+                            asm volatile("bar.sync 2, 128;\n" ::: "memory");
+                            if (cq == 0 && valid) {
+                                const float g4 = gsum_sh[0][tk] + gsum_sh[1][tk] + gsum_sh[2][tk] + gsum_sh[3][tk];
                                 const int Gh = a.F / kGroup;
                                 const size_t i = (size_t)(tok0 + c0 + tk) * Gh + (row0 / 2 + m * 64) / kGroup;
-                                const __half sh = __float2half_rn(gs);
+                                const __half sh = __float2half_rn(g4);
                                 a.hsum_out[i] = sh;
-                                a.hsum_out[(size_t)a.B * a.K * Gh + i] = __float2half_rn(gs - __half2float(sh));
+                                a.hsum_out[(size_t)a.B * a.K * Gh + i] = __float2half_rn(g4 - __half2float(sh));
                             }
-                            asm volatile("bar.sync 2, 128;\n" ::: "memory");
                         } else {
                             const int r = row0 + m * 128 + lr;   // output row
 #pragma unroll

@@ -73,7 +73,7 @@ struct FfnPointers {
 };
 
 // The tensor-core path reads the packed weights through maps with a 32-byte box (one
-// group of 8 words) x 128 rows (gate, up) or 256 rows (down), no swizzle.
+// group of 8 words) x 128 rows (gate, up) or 256 rows (down), 32-byte swizzle.
 struct FfnTcWeights {
     CUtensorMap pm_gate, pm_up, pm_down;
     const uint16_t* sg; const uint16_t* bg; int64_t g_rows;
