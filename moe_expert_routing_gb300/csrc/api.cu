@@ -41,16 +41,15 @@ smoe_status check_ws(const smoe_layer_desc& D, int B, void* ws, size_t ws_bytes,
 
 // 2-D u32 view [rows, in/8] of a packed weight tensor; box 32 words (4 groups) x box_rows,
 // 128-byte swizzle.
-bool encode_weight_map(CUtensorMap* map, const uint32_t* words, int64_t rows, int64_t in, int box_rows,
-                       int box_words = 32, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+bool encode_weight_map(CUtensorMap* map, const uint32_t* words, int64_t rows, int64_t in, int box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)(in / 8), (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(in / 2)};
-    cuuint32_t box[2] = {(cuuint32_t)box_words, (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(words), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -96,26 +95,18 @@ smoe_status check_weights(const smoe_layer_desc& D, const smoe_expert_weights* W
         P->sg = W->s_gate_up; P->bg = W->b_gate_up; P->g_rows_per_expert = 2 * F;
         P->su = W->s_gate_up; P->bu = W->b_gate_up; P->u_rows_per_expert = 2 * F; P->u_row_offset = F;
     }
-    // packed-word maps of the tensor-core path: one group (8 words, 32 bytes) per row, with the
-    // 32-byte swizzle (the two 16-byte halves of a row swap on every other 4-row block)
-    const CUtensorMapSwizzle sw32 = CU_TENSOR_MAP_SWIZZLE_32B;
     if (!encode_weight_map(&P->map_down, W->w_down, E * d, F, 256)) return SMOE_ERR_CUDA;
-    if (!encode_weight_map(&P->pm_down, W->w_down, E * d, F, 256, 8, sw32)) return SMOE_ERR_CUDA;
     if (!encode_group_map(&P->map_sd, W->s_down, E * d, F, 256) || !encode_group_map(&P->map_bd, W->b_down, E * d, F, 256))
         return SMOE_ERR_CUDA;
     if (sep) {
         if (!encode_weight_map(&P->map_gate, W->w_gate, E * F, d, 128)) return SMOE_ERR_CUDA;
         if (!encode_weight_map(&P->map_up, W->w_up, E * F, d, 128)) return SMOE_ERR_CUDA;
-        if (!encode_weight_map(&P->pm_gate, W->w_gate, E * F, d, 128, 8, sw32)) return SMOE_ERR_CUDA;
-        if (!encode_weight_map(&P->pm_up, W->w_up, E * F, d, 128, 8, sw32)) return SMOE_ERR_CUDA;
         if (!encode_group_map(&P->map_sg, W->s_gate, E * F, d, 128) || !encode_group_map(&P->map_bg, W->b_gate, E * F, d, 128) ||
             !encode_group_map(&P->map_su, W->s_up, E * F, d, 128) || !encode_group_map(&P->map_bu, W->b_up, E * F, d, 128))
             return SMOE_ERR_CUDA;
     } else {
         if (!encode_weight_map(&P->map_gate, W->w_gate_up, E * 2 * F, d, 128)) return SMOE_ERR_CUDA;
-        if (!encode_weight_map(&P->pm_gate, W->w_gate_up, E * 2 * F, d, 128, 8, sw32)) return SMOE_ERR_CUDA;
         P->map_up = P->map_gate;
-        P->pm_up = P->pm_gate;
         if (!encode_group_map(&P->map_sg, W->s_gate_up, E * 2 * F, d, 128) ||
             !encode_group_map(&P->map_bg, W->b_gate_up, E * 2 * F, d, 128))
             return SMOE_ERR_CUDA;

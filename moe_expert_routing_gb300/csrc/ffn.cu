@@ -425,7 +425,8 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
         bi[1][1] = lds_u2(tb + (uint32_t)(lrow1 + g + 8) * rs);
         consume_stage<NT, PASS == 1>(acc, base + wrow_off0, base + wrow_off1, base + C::kXOff, sc, bi,
                                      base + C::kSumOff, g, c);
-        mbar_arrive(R.empty + 8 * slot);   // this thread is done reading the slot
+        __syncwarp();   // the warp's reads of the slot, then one arrival for the warp
+        if (lane == 0) mbar_arrive(R.empty + 8 * slot);
         ++it;
     }
 
@@ -608,7 +609,7 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kCount; ++s) {
             mbar_init(R.full + 8 * s, 1);
-            mbar_init(R.empty + 8 * s, 32 * kConsumerWarps);
+            mbar_init(R.empty + 8 * s, kConsumerWarps);   // one arrival per consumer warp
         }
         for (int s = 0; s < kMailbox; ++s) {
             mbar_init(M.full + 8 * s, 1);
@@ -901,7 +902,7 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     // an expert rarely reaches the threshold, so the extra launches are skipped
     const int tc_min = (tc_path_supported(D) && B >= 256) ? kTcMinTokens : 0;
     FfnTcWeights TW{};
-    TW.pm_gate = W.pm_gate; TW.pm_up = W.pm_up; TW.pm_down = W.pm_down;
+    TW.map_gate = W.map_gate; TW.map_up = W.map_up; TW.map_down = W.map_down;
     TW.sg = W.sg; TW.bg = W.bg; TW.g_rows = W.g_rows_per_expert;
     TW.su = W.su; TW.bu = W.bu; TW.u_rows = W.u_rows_per_expert; TW.u_off = W.u_row_offset;
     TW.sd = W.sd; TW.bd = W.bd;

@@ -14,14 +14,14 @@
 // (eps as fp16, S as an fp16 hi + lo pair).
 //
 // Tile per CTA: 256 weight rows (two UMMA M=128 accumulators) x 128 tokens; k in stages of
-// one 64-input group.  Two shared-memory rings: a TMA ring (packed weights + activation rows;
-// 6 slots in pass 0, 3 in pass 1) deep enough to cover the copy latency, and a 2-slot ring of
-// dequantised fp16 weights.  Warp roles (one CTA per SM, persistent over the work items):
-//   warp 0      producer: TMA of the packed weight rows and the activation rows (B operand)
+// one 64-input group.  Three shared-memory rings (see TcCfg): packed weights, activation rows
+// and dequantised fp16 weights.  Warp roles (one CTA per SM, persistent over the work items):
+//   warp 0      producer of the packed weight rows (TMA)
 //   warp 1      TMEM owner; lane 0 issues tcgen05.mma and tcgen05.commit
 //   warps 2-9   dequantisers, one A row each: packed nibbles -> fp16 s (q - 8) in the SW128
 //               K-major layout
 //   warps 10-13 epilogue: tcgen05.ld of the accumulators -> SwiGLU (pass 0) or y (pass 1)
+//   warp 14     producer of the activation rows (B operand, TMA)
 // Accumulators are double-buffered in TMEM (2 x 256 columns) so one tile's epilogue
 // overlaps the next tile's MMAs.  Every mbarrier wait is bounded.  Pass 0's epilogue stages
 // h through shared memory for 16-byte stores and also writes the per-group sums of h that
@@ -43,28 +43,33 @@ namespace {
 
 constexpr int TC_N = 128;                    // tokens per tile (UMMA N)
 constexpr int TC_A_BYTES = 256 * 128;        // A slot: 256 rows x 64 fp16, SW128 K-major
-constexpr int TC_A_SLOTS = 2;
-constexpr int TC_P_BYTES = 256 * 32;         // packed weights: 256 rows x 8 words
+constexpr int TC_P_BYTES = 256 * 128;        // packed slot: 256 rows x 32 words (4 stages), SW128
 constexpr int TC_B_BYTES = TC_N * 128;       // one B sub-tile: 128 token rows x 64 fp16, SW128 K-major
 constexpr int TC_H_STRIDE = 33;             // pass 0 epilogue staging: 64 h columns x 32 tokens fp32,
 constexpr int TC_H_BYTES = 64 * TC_H_STRIDE * 4;   // column-major, padded (conflict-free both ways)
-constexpr int TC_THREADS = 448;
+constexpr int TC_THREADS = 480;
 constexpr uint32_t TC_TMEM_COLS = 512;
 
-// Per-pass ring shapes.  Load slot: packed weights, then B sub-tile 0 (x or h hi or S hi),
-// then (pass 1) B sub-tile 1 (h lo or S lo).
+// Per-pass ring shapes.  Three rings: dequantised A slots (kA), B slots (kB: x, or h hi + lo,
+// or the group sums of the eps stages; kNb sub-tiles each) and packed-weight slots (kP, each
+// 4 stages of 128-byte rows: a quarter of the copy rows that one 32-byte group per row
+// takes).  Packed slots are freed by the dequantisers once they have consumed them, so the
+// packed stream runs ahead of the MMAs; B slots are freed by the MMAs.
 template <int PASS>
 struct TcCfg {
-    static constexpr int kLoadSlots = PASS ? 3 : 6;
-    static constexpr int kNb = PASS ? 2 : 1;                  // B sub-tiles per load slot
-    static constexpr int kSlotBytes = TC_P_BYTES + kNb * TC_B_BYTES;
-    static constexpr int kOffLoad = TC_A_SLOTS * TC_A_BYTES;
-    static constexpr int kOffStage = kOffLoad + kLoadSlots * kSlotBytes;   // epilogue staging
+    static constexpr int kA = PASS ? 2 : 3;
+    static constexpr int kB = PASS ? 2 : 3;
+    static constexpr int kP = 2;
+    static constexpr int kNb = PASS ? 2 : 1;
+    static constexpr int kBSlot = kNb * TC_B_BYTES;
+    static constexpr int kOffB = kA * TC_A_BYTES;
+    static constexpr int kOffP = kOffB + kB * kBSlot;
+    static constexpr int kOffStage = kOffP + kP * TC_P_BYTES;   // epilogue staging
     static constexpr int kSmem = kOffStage + (PASS ? 0 : TC_H_BYTES) + 1024;
     static constexpr int kCorr = PASS ? 1 : 2;                // eps stages (pass 0: S hi, S lo)
 };
-static_assert(TcCfg<0>::kSmem <= 227 * 1024 - 4096, "pass 0 shared memory");
-static_assert(TcCfg<1>::kSmem <= 227 * 1024 - 4096, "pass 1 shared memory");
+static_assert(TcCfg<0>::kSmem <= 227 * 1024 - 4608, "pass 0 shared memory");
+static_assert(TcCfg<1>::kSmem <= 227 * 1024 - 4608, "pass 1 shared memory");
 
 // ----------------------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -270,9 +275,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                   const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_shi,
                   const __grid_constant__ CUtensorMap map_slo, TcArgs a) {
     using C = TcCfg<PASS>;
-    constexpr int L = C::kLoadSlots;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full[L], empty_l[L], deq[TC_A_SLOTS], empty_a[TC_A_SLOTS];
+    __shared__ __align__(8) uint64_t full_p[C::kP], empty_p[C::kP], full_b[C::kB], empty_b[C::kB];
+    __shared__ __align__(8) uint64_t deq[C::kA], empty_a[C::kA];
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int pref[kMaxExperts + 1];
@@ -287,17 +292,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int n_st = n_main + C::kCorr;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < L; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty_l[s]), 1);
+        for (int s = 0; s < C::kP; ++s) {
+            mbar_init(smem_u32(&full_p[s]), 1);
+            mbar_init(smem_u32(&empty_p[s]), 8);     // every dequantiser warp has read the slot
         }
-        for (int s = 0; s < TC_A_SLOTS; ++s) {
-            mbar_init(smem_u32(&deq[s]), 256);
+        for (int s = 0; s < C::kB; ++s) {
+            mbar_init(smem_u32(&full_b[s]), 1);
+            mbar_init(smem_u32(&empty_b[s]), 1);     // tcgen05.commit of the stage's MMAs
+        }
+        for (int s = 0; s < C::kA; ++s) {
+            mbar_init(smem_u32(&deq[s]), 8);         // one arrival per dequantiser warp
             mbar_init(smem_u32(&empty_a[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&acc_full[b]), 1);
-            mbar_init(smem_u32(&acc_empty[b]), 128);
+            mbar_init(smem_u32(&acc_empty[b]), 4);   // one arrival per epilogue warp
         }
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
@@ -322,37 +331,49 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     };
 
     if (warp == 0) {
-        // ------------------------------------------------------------------ producer
+        // ------------------------------------------------------------------ packed-weight producer
         if (lane == 0) {
-            uint32_t it = 0;
-            for (int t = blockIdx.x; t < n_items; t += gridDim.x) {
+            uint32_t ip = 0;
+            for (int t = blockIdx.x; t < n_items && !poisoned; t += gridDim.x) {
                 const Item I = decode_item(a, pref, t);
                 const int row0 = I.mt * 256;   // pass 0: h columns [row0/2, row0/2 + 128); pass 1: down rows
+                for (int st = 0; st < n_main; st += 4, ++ip) {   // one slot per 4 groups
+                    const uint32_t s = ip % C::kP;
+                    if (ip >= (uint32_t)C::kP) fail(mbar_wait(smem_u32(&empty_p[s]), ((ip / C::kP) - 1) & 1u));
+                    if (poisoned) break;
+                    const uint32_t slot = sbase + C::kOffP + s * TC_P_BYTES;
+                    const uint32_t bar = smem_u32(&full_p[s]);
+                    mbar_expect_tx(bar, TC_P_BYTES);
+                    if (PASS == 0) {
+                        const int j0 = row0 / 2;   // 128 h columns: gate rows and up rows
+                        tma_load_2d(slot, &map_w0, st * 8, (int)(I.e * a.wrow0 + j0), bar);
+                        tma_load_2d(slot + 128 * 128, &map_w1, st * 8, (int)(I.e * a.wrow1 + a.woff1 + j0), bar);
+                    } else {
+                        tma_load_2d(slot, &map_w0, st * 8, (int)(I.e * a.wrow0 + row0), bar);
+                    }
+                }
+            }
+        }
+    } else if (warp == 14) {
+        // ------------------------------------------------------------------ activation producer
+        if (lane == 0) {
+            uint32_t ib = 0;
+            for (int t = blockIdx.x; t < n_items && !poisoned; t += gridDim.x) {
+                const Item I = decode_item(a, pref, t);
                 const int tok0 = I.p0 + I.nt * TC_N;
-                for (int st = 0; st < n_st; ++st, ++it) {
-                    const uint32_t s = it % L;
-                    if (it >= (uint32_t)L && !poisoned) fail(mbar_wait(smem_u32(&empty_l[s]), ((it / L) - 1) & 1u));
-                    if (poisoned) continue;
-                    const uint32_t slot = sbase + C::kOffLoad + s * C::kSlotBytes;
-                    const uint32_t bar = smem_u32(&full[s]);
-                    const uint32_t b0 = slot + TC_P_BYTES, b1 = b0 + TC_B_BYTES;
+                for (int st = 0; st < n_st; ++st, ++ib) {
+                    const uint32_t s = ib % C::kB;
+                    if (ib >= (uint32_t)C::kB) fail(mbar_wait(smem_u32(&empty_b[s]), ((ib / C::kB) - 1) & 1u));
+                    if (poisoned) break;
+                    const uint32_t b0 = sbase + C::kOffB + s * C::kBSlot, b1 = b0 + TC_B_BYTES;
+                    const uint32_t bar = smem_u32(&full_b[s]);
+                    mbar_expect_tx(bar, (uint32_t)C::kBSlot);
                     if (st < n_main) {
-                        mbar_expect_tx(bar, TC_P_BYTES + C::kNb * TC_B_BYTES);
-                        if (PASS == 0) {
-                            const int j0 = row0 / 2;   // 128 h columns: gate rows and up rows
-                            tma_load_2d(slot, &map_w0, st * 8, (int)(I.e * a.wrow0 + j0), bar);
-                            tma_load_2d(slot + 128 * 32, &map_w1, st * 8, (int)(I.e * a.wrow1 + a.woff1 + j0), bar);
-                            tma_load_2d(b0, &map_b, st * 64, tok0, bar);
-                        } else {
-                            tma_load_2d(slot, &map_w0, st * 8, (int)(I.e * a.wrow0 + row0), bar);
-                            tma_load_2d(b0, &map_b, st * 64, tok0, bar);          // h hi
-                            tma_load_2d(b1, &map_b, a.F + st * 64, tok0, bar);    // h lo
-                        }
+                        tma_load_2d(b0, &map_b, st * 64, tok0, bar);                    // x, or h hi
+                        if (PASS == 1) tma_load_2d(b1, &map_b, a.F + st * 64, tok0, bar);  // h lo
                     } else if (PASS == 0) {
-                        mbar_expect_tx(bar, TC_B_BYTES);
                         tma_load_2d(b0, st == n_main ? &map_shi : &map_slo, 0, tok0, bar);
                     } else {
-                        mbar_expect_tx(bar, 2 * TC_B_BYTES);
                         tma_load_2d(b0, &map_shi, 0, tok0, bar);
                         tma_load_2d(b1, &map_slo, 0, tok0, bar);
                     }
@@ -368,13 +389,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (tile >= 2 && !poisoned) fail(mbar_wait(smem_u32(&acc_empty[buf]), ((tile >> 1) - 1) & 1u));
                 tc_fence_after();
                 for (int st = 0; st < n_st; ++st, ++it) {
-                    const uint32_t s = it % L, sa = it % TC_A_SLOTS;
-                    if (!poisoned) fail(mbar_wait(smem_u32(&deq[sa]), (it / TC_A_SLOTS) & 1u));
-                    if (!poisoned) fail(mbar_wait(smem_u32(&full[s]), (it / L) & 1u));
+                    const uint32_t s = it % C::kB, sa = it % C::kA;
+                    if (!poisoned) fail(mbar_wait(smem_u32(&deq[sa]), (it / C::kA) & 1u));
+                    if (!poisoned) fail(mbar_wait(smem_u32(&full_b[s]), (it / C::kB) & 1u));
                     if (poisoned) continue;
                     tc_fence_after();
                     const uint32_t abuf = sbase + sa * TC_A_BYTES;
-                    const uint32_t bbuf = sbase + C::kOffLoad + s * C::kSlotBytes + TC_P_BYTES;
+                    const uint32_t bbuf = sbase + C::kOffB + s * C::kBSlot;
 #pragma unroll
                     for (int m = 0; m < 2; ++m) {
                         const uint32_t d_tmem = tmem + buf * 256 + m * TC_N;
@@ -388,7 +409,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             }
                         }
                     }
-                    umma_commit(smem_u32(&empty_l[s]));    // load slot free once these MMAs finish
+                    umma_commit(smem_u32(&empty_b[s]));    // B slot free once these MMAs finish
                     umma_commit(smem_u32(&empty_a[sa]));   // and the dequantised slot
                 }
                 if (!poisoned) umma_commit(smem_u32(&acc_full[buf]));   // accumulators of this tile ready
@@ -397,7 +418,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else if (warp < 10) {
         // ------------------------------------------------------------------ dequantisers
         const int r = threadIdx.x - 64;   // A row 0..255 (m-tile r >> 7)
-        uint32_t it = 0;
+        uint32_t it = 0, ip = 0;   // stages (A ring), packed slots (4 main stages each)
         for (int ti = blockIdx.x; ti < n_items; ti += gridDim.x) {
             const Item I = decode_item(a, pref, ti);
             const int row0 = I.mt * 256;
@@ -423,7 +444,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint4 scl = __ldg(srow), scl_next = n_main > 8 ? __ldg(srow + 1) : make_uint4(0, 0, 0, 0);
             uint4 es[8], eb[8];   // scale / bias rows for eps, loaded two stages before use
             for (int st = 0; st < n_st; ++st, ++it) {
-                const uint32_t s = it % L, sa = it % TC_A_SLOTS;
+                const uint32_t sa = it % C::kA;
                 if (st < n_main && (st & 7) == 0 && st > 0) {
                     scl = scl_next;
                     if (st + 8 < n_main) scl_next = __ldg(srow + (st >> 3) + 1);
@@ -436,19 +457,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             eb[i] = __ldg(brow + i);
                         }
                 }
-                if (!poisoned) fail(mbar_wait(smem_u32(&full[s]), (it / L) & 1u));
-                if (it >= TC_A_SLOTS && !poisoned) fail(mbar_wait(smem_u32(&empty_a[sa]), ((it / TC_A_SLOTS) - 1) & 1u));
+                // main stage: this row's 8 packed words, read before the A slot is waited for;
+                // the packed slot is handed back once the words have been consumed (a release
+                // right after the loads would not wait for their data)
+                uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
+                const uint32_t sp_ = ip % C::kP;
+                if (st < n_main) {
+                    if ((st & 3) == 0 && !poisoned) fail(mbar_wait(smem_u32(&full_p[sp_]), (ip / C::kP) & 1u));
+                    if (!poisoned) {
+                        // packed rows of 128 bytes (4 groups) with the 128-byte swizzle: the
+                        // group's two 16-byte chunks 2q, 2q+1 sit at chunk (c ^ (row & 7))
+                        const uint32_t pk = sbase + C::kOffP + sp_ * TC_P_BYTES + prow * 128u;
+                        const uint32_t q2 = (uint32_t)(st & 3) * 2u, x7 = prow & 7u;
+                        w0 = lds128(pk + ((q2 ^ x7) << 4));
+                        w1 = lds128(pk + (((q2 + 1u) ^ x7) << 4));
+                    }
+                }
+                if (it >= (uint32_t)C::kA && !poisoned) fail(mbar_wait(smem_u32(&empty_a[sa]), ((it / C::kA) - 1) & 1u));
                 if (!poisoned) {
                     const uint32_t arow = sbase + sa * TC_A_BYTES + (uint32_t)r * 128u;
                     if (st < n_main) {
                         const uint32_t sw = (&scl.x)[(st & 7) >> 1];
                         const float sf = __uint_as_float((st & 1) ? (sw & 0xFFFF0000u) : (sw << 16));
                         const __half2 s2 = __float2half2_rn(sf);   // exact: bf16 -> fp16
-                        // packed rows land with a 32-byte swizzle: the 16-byte halves of row p
-                        // swap when bit 2 of p is set (conflict-free 16-byte reads)
-                        const uint32_t pk = sbase + C::kOffLoad + s * C::kSlotBytes + prow * 32u;
-                        const uint32_t swz = ((prow >> 2) & 1u) << 4;
-                        const uint4 w0 = lds128(pk + swz), w1 = lds128(pk + (16u ^ swz));
                         const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
                         for (int c = 0; c < 8; ++c) sts128(arow + ((uint32_t)(c ^ (r & 7)) << 4), dequant_word(wv[c], s2));
@@ -473,7 +504,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                     fence_proxy_async();   // generic-proxy writes -> visible to the tensor core
                 }
-                mbar_arrive(smem_u32(&deq[sa]));
+                // one arrival per warp: __syncwarp orders the lanes' reads and writes (and their
+                // proxy fences) before lane 0's release
+                __syncwarp();
+                if (st < n_main && ((st & 3) == 3 || st == n_main - 1)) {   // the slot's last group consumed
+                    if (lane == 0) mbar_arrive(smem_u32(&empty_p[sp_]));
+                    ++ip;
+                }
+                if (lane == 0) mbar_arrive(smem_u32(&deq[sa]));
             }
         }
     } else {
@@ -577,7 +615,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(smem_u32(&acc_empty[buf]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[buf]));
         }
     }
 
@@ -652,7 +691,7 @@ cudaError_t launch_ffn_tc(const smoe_layer_desc& D, const FfnTcWeights& W, int B
                         CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         const int grid = std::max(1, std::min(sms, E * (F / 128) * ((BK + TC_N - 1) / TC_N)));
-        ffn_tc_kernel<0><<<grid, TC_THREADS, TcCfg<0>::kSmem, stream>>>(W.pm_gate, W.pm_up, mb, mshi, mslo, a);
+        ffn_tc_kernel<0><<<grid, TC_THREADS, TcCfg<0>::kSmem, stream>>>(W.map_gate, W.map_up, mb, mshi, mslo, a);
     } else {
         const size_t nw = (size_t)BK * Gh;
         a.wrow0 = d; a.wrow1 = d; a.woff1 = 0;
@@ -664,7 +703,7 @@ cudaError_t launch_ffn_tc(const smoe_layer_desc& D, const FfnTcWeights& W, int B
                         CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         const int grid = std::max(1, std::min(sms, E * (d / 256) * ((BK + TC_N - 1) / TC_N)));
-        ffn_tc_kernel<1><<<grid, TC_THREADS, TcCfg<1>::kSmem, stream>>>(W.pm_down, W.pm_down, mb, mshi, mslo, a);
+        ffn_tc_kernel<1><<<grid, TC_THREADS, TcCfg<1>::kSmem, stream>>>(W.map_down, W.map_down, mb, mshi, mslo, a);
     }
     return cudaGetLastError();
 }

@@ -63,7 +63,6 @@ cudaError_t launch_union(const smoe_layer_desc& D, const int32_t* topk_idx, int 
 // of expert e start at e * 2F + F (u_row_offset = F).
 struct FfnPointers {
     CUtensorMap map_gate, map_up, map_down;
-    CUtensorMap pm_gate, pm_up, pm_down;   // packed-word maps of the tensor-core path
     // scale / bias tables of the expert passes: bf16 [rows, in/64], box 8 groups x 128 rows
     // (gate, up) or 256 rows (down); see encode_group_map
     CUtensorMap map_sg, map_bg, map_su, map_bu, map_sd, map_bd;
@@ -72,10 +71,9 @@ struct FfnPointers {
     const uint16_t* sd; const uint16_t* bd;
 };
 
-// The tensor-core path reads the packed weights through maps with a 32-byte box (one
-// group of 8 words) x 128 rows (gate, up) or 256 rows (down), 32-byte swizzle.
+// The tensor-core path reads the packed weights through the same maps as the other passes.
 struct FfnTcWeights {
-    CUtensorMap pm_gate, pm_up, pm_down;
+    CUtensorMap map_gate, map_up, map_down;
     const uint16_t* sg; const uint16_t* bg; int64_t g_rows;
     const uint16_t* su; const uint16_t* bu; int64_t u_rows; int64_t u_off;
     const uint16_t* sd; const uint16_t* bd;
