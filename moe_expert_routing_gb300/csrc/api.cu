@@ -96,17 +96,22 @@ smoe_status check_weights(const smoe_layer_desc& D, const smoe_expert_weights* W
         P->su = W->s_gate_up; P->bu = W->b_gate_up; P->u_rows_per_expert = 2 * F; P->u_row_offset = F;
     }
     if (!encode_weight_map(&P->map_down, W->w_down, E * d, F, 256)) return SMOE_ERR_CUDA;
+    if (!encode_weight_map(&P->tc_down, W->w_down, E * d, F, 128)) return SMOE_ERR_CUDA;
     if (!encode_group_map(&P->map_sd, W->s_down, E * d, F, 256) || !encode_group_map(&P->map_bd, W->b_down, E * d, F, 256))
         return SMOE_ERR_CUDA;
     if (sep) {
         if (!encode_weight_map(&P->map_gate, W->w_gate, E * F, d, 128)) return SMOE_ERR_CUDA;
         if (!encode_weight_map(&P->map_up, W->w_up, E * F, d, 128)) return SMOE_ERR_CUDA;
+        if (!encode_weight_map(&P->tc_gate, W->w_gate, E * F, d, 64)) return SMOE_ERR_CUDA;
+        if (!encode_weight_map(&P->tc_up, W->w_up, E * F, d, 64)) return SMOE_ERR_CUDA;
         if (!encode_group_map(&P->map_sg, W->s_gate, E * F, d, 128) || !encode_group_map(&P->map_bg, W->b_gate, E * F, d, 128) ||
             !encode_group_map(&P->map_su, W->s_up, E * F, d, 128) || !encode_group_map(&P->map_bu, W->b_up, E * F, d, 128))
             return SMOE_ERR_CUDA;
     } else {
         if (!encode_weight_map(&P->map_gate, W->w_gate_up, E * 2 * F, d, 128)) return SMOE_ERR_CUDA;
+        if (!encode_weight_map(&P->tc_gate, W->w_gate_up, E * 2 * F, d, 64)) return SMOE_ERR_CUDA;
         P->map_up = P->map_gate;
+        P->tc_up = P->tc_gate;
         if (!encode_group_map(&P->map_sg, W->s_gate_up, E * 2 * F, d, 128) ||
             !encode_group_map(&P->map_bg, W->b_gate_up, E * 2 * F, d, 128))
             return SMOE_ERR_CUDA;

@@ -902,7 +902,7 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     // an expert rarely reaches the threshold, so the extra launches are skipped
     const int tc_min = (tc_path_supported(D) && B >= 256) ? kTcMinTokens : 0;
     FfnTcWeights TW{};
-    TW.map_gate = W.map_gate; TW.map_up = W.map_up; TW.map_down = W.map_down;
+    TW.map_gate = W.tc_gate; TW.map_up = W.tc_up; TW.map_down = W.tc_down;
     TW.sg = W.sg; TW.bg = W.bg; TW.g_rows = W.g_rows_per_expert;
     TW.su = W.su; TW.bu = W.bu; TW.u_rows = W.u_rows_per_expert; TW.u_off = W.u_row_offset;
     TW.sd = W.sd; TW.bd = W.bd;

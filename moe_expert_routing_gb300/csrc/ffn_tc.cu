@@ -41,25 +41,29 @@
 namespace smoe {
 namespace {
 
-constexpr int TC_N = 128;                    // tokens per tile (UMMA N)
-constexpr int TC_A_BYTES = 256 * 128;        // A slot: 256 rows x 64 fp16, SW128 K-major
-constexpr int TC_P_BYTES = 256 * 128;        // packed slot: 256 rows x 32 words (4 stages), SW128
-constexpr int TC_B_BYTES = TC_N * 128;       // one B sub-tile: 128 token rows x 64 fp16, SW128 K-major
+constexpr int TC_M = 128;                    // weight rows per tile (UMMA M, one TMEM lane each)
+constexpr int TC_N = 256;                    // tokens per tile (UMMA N; 128 for an expert's last short tile)
+constexpr int TC_A_BYTES = TC_M * 128;       // A slot: 128 rows x 64 fp16, SW128 K-major
+constexpr int TC_P_BYTES = TC_M * 128;       // packed slot: 128 rows x 32 words (4 stages), SW128
+constexpr int TC_BOX_BYTES = 128 * 128;      // one activation box: 128 token rows x 64 fp16, SW128 K-major
+constexpr int TC_B_BYTES = 2 * TC_BOX_BYTES; // one B sub-tile: 256 token rows
 constexpr int TC_H_STRIDE = 33;             // pass 0 epilogue staging: 64 h columns x 32 tokens fp32,
 constexpr int TC_H_BYTES = 64 * TC_H_STRIDE * 4;   // column-major, padded (conflict-free both ways)
 constexpr int TC_THREADS = 480;
-constexpr uint32_t TC_TMEM_COLS = 512;
+constexpr uint32_t TC_TMEM_COLS = 512;       // two accumulator buffers of TC_N columns
 
 // Per-pass ring shapes.  Three rings: dequantised A slots (kA), B slots (kB: x, or h hi + lo,
 // or the group sums of the eps stages; kNb sub-tiles each) and packed-weight slots (kP, each
-// 4 stages of 128-byte rows: a quarter of the copy rows that one 32-byte group per row
-// takes).  Packed slots are freed by the dequantisers once they have consumed them, so the
-// packed stream runs ahead of the MMAs; B slots are freed by the MMAs.
+// 4 stages of 128-byte rows).  Packed slots are freed by the dequantisers once they have
+// consumed them, so the packed stream runs ahead of the MMAs; B slots are freed by the MMAs.
+// The tile shape (128 rows x 256 tokens) reads each B row for 128 weight rows and each A row
+// for 256 tokens per MMA, which keeps the shared-memory traffic per MAC low enough for the
+// tensor core (shared-memory bandwidth, not the MMA rate, limits narrower tiles).
 template <int PASS>
 struct TcCfg {
-    static constexpr int kA = PASS ? 2 : 3;
+    static constexpr int kA = PASS ? 3 : 4;
     static constexpr int kB = PASS ? 2 : 3;
-    static constexpr int kP = 2;
+    static constexpr int kP = PASS ? 2 : 3;
     static constexpr int kNb = PASS ? 2 : 1;
     static constexpr int kBSlot = kNb * TC_B_BYTES;
     static constexpr int kOffB = kA * TC_A_BYTES;
@@ -68,8 +72,8 @@ struct TcCfg {
     static constexpr int kSmem = kOffStage + (PASS ? 0 : TC_H_BYTES) + 1024;
     static constexpr int kCorr = PASS ? 1 : 2;                // eps stages (pass 0: S hi, S lo)
 };
-static_assert(TcCfg<0>::kSmem <= 227 * 1024 - 4608, "pass 0 shared memory");
-static_assert(TcCfg<1>::kSmem <= 227 * 1024 - 4608, "pass 1 shared memory");
+static_assert(TcCfg<0>::kSmem <= 227 * 1024 - 7168, "pass 0 shared memory");
+static_assert(TcCfg<1>::kSmem <= 227 * 1024 - 7168, "pass 1 shared memory");
 
 // ----------------------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -125,14 +129,16 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: fp16 A and B, fp32 D, both K-major, M = 128, N = TC_N.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(TC_N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+// Instruction descriptor, kind::f16: fp16 A and B, fp32 D, both K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_f16(int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TC_M >> 4) << 24);
+}
 
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -203,7 +209,7 @@ struct TcArgs {
     const uint16_t* s0; const uint16_t* b0;   // scales / biases of map_w0 rows
     const uint16_t* s1; const uint16_t* b1;   // scales / biases of map_w1 rows (pass 0 up)
     int kdim, F, d, K, E, B;
-    int m_tiles;                      // 256-row tiles per expert
+    int m_tiles;                      // 128-row tiles per expert (pass 0: 64 h columns, gate and up rows)
     int tc_min;                       // experts with at least this many entries take this path
     const int32_t* union_ids; const int32_t* n_union; const int32_t* offsets;
     const int32_t* token_list; const int32_t* slot_list;
@@ -287,14 +293,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const int G = a.kdim / kGroup;     // <= 64
+    const int G = a.kdim / kGroup;     // <= 64, a multiple of 8
     const int n_main = G;              // one stage per group
     const int n_st = n_main + C::kCorr;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kP; ++s) {
             mbar_init(smem_u32(&full_p[s]), 1);
-            mbar_init(smem_u32(&empty_p[s]), 8);     // every dequantiser warp has read the slot
+            mbar_init(smem_u32(&empty_p[s]), 8);     // every dequantiser warp has consumed the slot
         }
         for (int s = 0; s < C::kB; ++s) {
             mbar_init(smem_u32(&full_b[s]), 1);
@@ -336,7 +342,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint32_t ip = 0;
             for (int t = blockIdx.x; t < n_items && !poisoned; t += gridDim.x) {
                 const Item I = decode_item(a, pref, t);
-                const int row0 = I.mt * 256;   // pass 0: h columns [row0/2, row0/2 + 128); pass 1: down rows
                 for (int st = 0; st < n_main; st += 4, ++ip) {   // one slot per 4 groups
                     const uint32_t s = ip % C::kP;
                     if (ip >= (uint32_t)C::kP) fail(mbar_wait(smem_u32(&empty_p[s]), ((ip / C::kP) - 1) & 1u));
@@ -345,11 +350,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const uint32_t bar = smem_u32(&full_p[s]);
                     mbar_expect_tx(bar, TC_P_BYTES);
                     if (PASS == 0) {
-                        const int j0 = row0 / 2;   // 128 h columns: gate rows and up rows
+                        const int j0 = I.mt * 64;   // 64 h columns: gate rows, then up rows
                         tma_load_2d(slot, &map_w0, st * 8, (int)(I.e * a.wrow0 + j0), bar);
-                        tma_load_2d(slot + 128 * 128, &map_w1, st * 8, (int)(I.e * a.wrow1 + a.woff1 + j0), bar);
+                        tma_load_2d(slot + 64 * 128, &map_w1, st * 8, (int)(I.e * a.wrow1 + a.woff1 + j0), bar);
                     } else {
-                        tma_load_2d(slot, &map_w0, st * 8, (int)(I.e * a.wrow0 + row0), bar);
+                        tma_load_2d(slot, &map_w0, st * 8, (int)(I.e * a.wrow0 + I.mt * TC_M), bar);
                     }
                 }
             }
@@ -361,21 +366,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             for (int t = blockIdx.x; t < n_items && !poisoned; t += gridDim.x) {
                 const Item I = decode_item(a, pref, t);
                 const int tok0 = I.p0 + I.nt * TC_N;
+                const int boxes = I.n - I.nt * TC_N > 128 ? 2 : 1;   // 128-token boxes of this tile
                 for (int st = 0; st < n_st; ++st, ++ib) {
                     const uint32_t s = ib % C::kB;
                     if (ib >= (uint32_t)C::kB) fail(mbar_wait(smem_u32(&empty_b[s]), ((ib / C::kB) - 1) & 1u));
                     if (poisoned) break;
-                    const uint32_t b0 = sbase + C::kOffB + s * C::kBSlot, b1 = b0 + TC_B_BYTES;
                     const uint32_t bar = smem_u32(&full_b[s]);
-                    mbar_expect_tx(bar, (uint32_t)C::kBSlot);
-                    if (st < n_main) {
-                        tma_load_2d(b0, &map_b, st * 64, tok0, bar);                    // x, or h hi
-                        if (PASS == 1) tma_load_2d(b1, &map_b, a.F + st * 64, tok0, bar);  // h lo
-                    } else if (PASS == 0) {
-                        tma_load_2d(b0, st == n_main ? &map_shi : &map_slo, 0, tok0, bar);
-                    } else {
-                        tma_load_2d(b0, &map_shi, 0, tok0, bar);
-                        tma_load_2d(b1, &map_slo, 0, tok0, bar);
+                    mbar_expect_tx(bar, (uint32_t)(C::kNb * boxes * TC_BOX_BYTES));
+#pragma unroll
+                    for (int sub = 0; sub < C::kNb; ++sub) {
+                        const uint32_t dst = sbase + C::kOffB + s * C::kBSlot + sub * TC_B_BYTES;
+                        for (int bx = 0; bx < boxes; ++bx) {
+                            const int y = tok0 + bx * 128;
+                            const uint32_t d = dst + bx * TC_BOX_BYTES;
+                            if (st < n_main)   // x, or h hi (sub 0) and h lo (sub 1)
+                                tma_load_2d(d, &map_b, (sub ? a.F : 0) + st * 64, y, bar);
+                            else if (PASS == 0)   // eps stages: S hi, then S lo
+                                tma_load_2d(d, st == n_main ? &map_shi : &map_slo, 0, y, bar);
+                            else
+                                tma_load_2d(d, sub ? &map_slo : &map_shi, 0, y, bar);
+                        }
                     }
                 }
             }
@@ -385,6 +395,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (lane == 0) {
             uint32_t it = 0, tile = 0;
             for (int t = blockIdx.x; t < n_items; t += gridDim.x, ++tile) {
+                const Item I = decode_item(a, pref, t);
+                const uint32_t idesc = idesc_f16(I.n - I.nt * TC_N > 128 ? TC_N : 128);
                 const uint32_t buf = tile & 1u;
                 if (tile >= 2 && !poisoned) fail(mbar_wait(smem_u32(&acc_empty[buf]), ((tile >> 1) - 1) & 1u));
                 tc_fence_after();
@@ -396,17 +408,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     tc_fence_after();
                     const uint32_t abuf = sbase + sa * TC_A_BYTES;
                     const uint32_t bbuf = sbase + C::kOffB + s * C::kBSlot;
+                    const uint32_t d_tmem = tmem + buf * TC_N;
 #pragma unroll
-                    for (int m = 0; m < 2; ++m) {
-                        const uint32_t d_tmem = tmem + buf * 256 + m * TC_N;
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = sw128_desc(abuf + kk * 32);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = sw128_desc(abuf + m * 16384 + kk * 32);
-#pragma unroll
-                            for (int b = 0; b < C::kNb; ++b) {
-                                const uint64_t bd = sw128_desc(bbuf + b * TC_B_BYTES + kk * 32);
-                                umma_f16(d_tmem, ad, bd, (st > 0 || kk > 0 || b > 0) ? 1u : 0u);
-                            }
+                        for (int b = 0; b < C::kNb; ++b) {
+                            const uint64_t bd = sw128_desc(bbuf + b * TC_B_BYTES + kk * 32);
+                            umma_f16(d_tmem, ad, bd, idesc, (st > 0 || kk > 0 || b > 0) ? 1u : 0u);
                         }
                     }
                     umma_commit(smem_u32(&empty_b[s]));    // B slot free once these MMAs finish
@@ -417,24 +426,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
     } else if (warp < 10) {
         // ------------------------------------------------------------------ dequantisers
-        const int r = threadIdx.x - 64;   // A row 0..255 (m-tile r >> 7)
+        // 256 threads for 128 A rows: thread -> row r, half hf of the row's 8 packed words
+        const int r = (threadIdx.x - 64) & (TC_M - 1);
+        const int hf = (threadIdx.x - 64) >> 7;
         uint32_t it = 0, ip = 0;   // stages (A ring), packed slots (4 main stages each)
         for (int ti = blockIdx.x; ti < n_items; ti += gridDim.x) {
             const Item I = decode_item(a, pref, ti);
-            const int row0 = I.mt * 256;
             // source row of A row r
             int64_t src;
             const uint16_t *sp, *bp;
-            uint32_t prow;   // packed row inside the load slot's packed tile
+            uint32_t prow;   // packed row inside the packed slot
             if (PASS == 0) {
-                const int i = (r >> 7) * 64 + ((r & 127) >> 1);   // h column offset inside the tile
+                const int i = r >> 1;   // h column offset inside the tile; odd A rows are up rows
                 const bool up = r & 1;
-                src = up ? (int64_t)I.e * a.wrow1 + a.woff1 + row0 / 2 + i : (int64_t)I.e * a.wrow0 + row0 / 2 + i;
+                src = up ? (int64_t)I.e * a.wrow1 + a.woff1 + I.mt * 64 + i : (int64_t)I.e * a.wrow0 + I.mt * 64 + i;
                 sp = up ? a.s1 : a.s0;
                 bp = up ? a.b1 : a.b0;
-                prow = (up ? 128 : 0) + i;
+                prow = (up ? 64 : 0) + i;
             } else {
-                src = (int64_t)I.e * a.wrow0 + row0 + r;
+                src = (int64_t)I.e * a.wrow0 + I.mt * TC_M + r;
                 sp = a.s0;
                 bp = a.b0;
                 prow = r;
@@ -442,35 +452,32 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint4* srow = reinterpret_cast<const uint4*>(sp + src * G);   // 8 bf16 per uint4
             const uint4* brow = reinterpret_cast<const uint4*>(bp + src * G);
             uint4 scl = __ldg(srow), scl_next = n_main > 8 ? __ldg(srow + 1) : make_uint4(0, 0, 0, 0);
-            uint4 es[8], eb[8];   // scale / bias rows for eps, loaded two stages before use
+            uint4 es[4], eb[4];   // this half's scale / bias chunks for eps, loaded two stages early
             for (int st = 0; st < n_st; ++st, ++it) {
                 const uint32_t sa = it % C::kA;
                 if (st < n_main && (st & 7) == 0 && st > 0) {
                     scl = scl_next;
                     if (st + 8 < n_main) scl_next = __ldg(srow + (st >> 3) + 1);
                 }
-                if (st == (n_main >= 2 ? n_main - 2 : 0)) {
+                if (st == n_main - 2) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (i < G / 8) {
-                            es[i] = __ldg(srow + i);
-                            eb[i] = __ldg(brow + i);
+                    for (int i = 0; i < 4; ++i)
+                        if (4 * hf + i < G / 8) {
+                            es[i] = __ldg(srow + 4 * hf + i);
+                            eb[i] = __ldg(brow + 4 * hf + i);
                         }
                 }
-                // main stage: this row's 8 packed words, read before the A slot is waited for;
-                // the packed slot is handed back once the words have been consumed (a release
-                // right after the loads would not wait for their data)
-                uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
+                // main stage: this half-row's 4 packed words, read before the A slot is waited
+                // for; the packed slot is handed back once the words have been consumed
+                uint4 w = make_uint4(0, 0, 0, 0);
                 const uint32_t sp_ = ip % C::kP;
                 if (st < n_main) {
                     if ((st & 3) == 0 && !poisoned) fail(mbar_wait(smem_u32(&full_p[sp_]), (ip / C::kP) & 1u));
                     if (!poisoned) {
-                        // packed rows of 128 bytes (4 groups) with the 128-byte swizzle: the
-                        // group's two 16-byte chunks 2q, 2q+1 sit at chunk (c ^ (row & 7))
+                        // packed rows of 128 bytes (4 groups) with the 128-byte swizzle: chunk
+                        // 2q + hf of the row (group q = st % 4) sits at chunk ((2q + hf) ^ (row & 7))
                         const uint32_t pk = sbase + C::kOffP + sp_ * TC_P_BYTES + prow * 128u;
-                        const uint32_t q2 = (uint32_t)(st & 3) * 2u, x7 = prow & 7u;
-                        w0 = lds128(pk + ((q2 ^ x7) << 4));
-                        w1 = lds128(pk + (((q2 + 1u) ^ x7) << 4));
+                        w = lds128(pk + ((((uint32_t)(st & 3) * 2u + hf) ^ (prow & 7u)) << 4));
                     }
                 }
                 if (it >= (uint32_t)C::kA && !poisoned) fail(mbar_wait(smem_u32(&empty_a[sa]), ((it / C::kA) - 1) & 1u));
@@ -480,15 +487,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         const uint32_t sw = (&scl.x)[(st & 7) >> 1];
                         const float sf = __uint_as_float((st & 1) ? (sw & 0xFFFF0000u) : (sw << 16));
                         const __half2 s2 = __float2half2_rn(sf);   // exact: bf16 -> fp16
-                        const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) sts128(arow + ((uint32_t)(c ^ (r & 7)) << 4), dequant_word(wv[c], s2));
+                        for (int c = 0; c < 4; ++c) {
+                            const uint32_t ch = 4u * hf + c;   // word ch -> A chunk ch (8 inputs)
+                            sts128(arow + ((ch ^ (uint32_t)(r & 7)) << 4), dequant_word(wv[c], s2));
+                        }
                     } else {
-                        // eps = b + 8 s for the row's G groups (zero beyond G), natural group order
+                        // eps = b + 8 s for the row's G groups (zero beyond G), natural group order;
+                        // this half writes chunks 4 hf .. 4 hf + 3 (groups 32 hf ..)
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
+                        for (int c = 0; c < 4; ++c) {
                             uint32_t hv[4] = {0u, 0u, 0u, 0u};
-                            if (c < G / 8) {
+                            if (4 * hf + c < G / 8) {
                                 const uint32_t sw[4] = {es[c].x, es[c].y, es[c].z, es[c].w};
                                 const uint32_t bw[4] = {eb[c].x, eb[c].y, eb[c].z, eb[c].w};
 #pragma unroll
@@ -499,7 +510,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                     hv[q] = h2u(__floats2half2_rn(e0, e1));
                                 }
                             }
-                            sts128(arow + ((uint32_t)(c ^ (r & 7)) << 4), make_uint4(hv[0], hv[1], hv[2], hv[3]));
+                            const uint32_t ch = 4u * hf + c;
+                            sts128(arow + ((ch ^ (uint32_t)(r & 7)) << 4), make_uint4(hv[0], hv[1], hv[2], hv[3]));
                         }
                     }
                     fence_proxy_async();   // generic-proxy writes -> visible to the tensor core
@@ -507,7 +519,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // one arrival per warp: __syncwarp orders the lanes' reads and writes (and their
                 // proxy fences) before lane 0's release
                 __syncwarp();
-                if (st < n_main && ((st & 3) == 3 || st == n_main - 1)) {   // the slot's last group consumed
+                if (st < n_main && (st & 3) == 3) {   // the slot's last group consumed
                     if (lane == 0) mbar_arrive(smem_u32(&empty_p[sp_]));
                     ++ip;
                 }
@@ -524,7 +536,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int t = blockIdx.x; t < n_items; t += gridDim.x, ++tile) {
             const Item I = decode_item(a, pref, t);
             const uint32_t buf = tile & 1u;
-            const int row0 = I.mt * 256;
             const int tok0 = I.p0 + I.nt * TC_N;
             const int ntok = min(TC_N, I.n - I.nt * TC_N);
             // token / slot of the tile's entries (pass 1 output rows)
@@ -540,75 +551,72 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tc_fence_after();
             if (!poisoned) {
 #pragma unroll 1
-                for (int m = 0; m < 2; ++m) {
-#pragma unroll 1
-                    for (int c0 = 0; c0 < TC_N; c0 += 32) {
-                        if (c0 >= ntok) break;
-                        float v[32];
-                        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * 256 + m * TC_N + c0, v);
-                        if (PASS == 0) {
-                            // lanes 2i (gate) and 2i+1 (up) of h column i of this m-tile; the even
-                            // lane takes tokens 0..15 of the chunk, the odd lane tokens 16..31
-                            const bool odd_lane = lane & 1;
-                            const int hc = lr >> 1;   // 0..63
+                for (int c0 = 0; c0 < TC_N; c0 += 32) {
+                    if (c0 >= ntok) break;
+                    float v[32];
+                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * TC_N + c0, v);
+                    if (PASS == 0) {
+                        // lanes 2i (gate) and 2i+1 (up) of h column i; the even lane takes tokens
+                        // 0..15 of the chunk, the odd lane tokens 16..31
+                        const bool odd_lane = lane & 1;
+                        const int hc = lr >> 1;   // 0..63
 #pragma unroll
-                            for (int k = 0; k < 16; ++k) {
-                                const float mine = v[odd_lane ? k : 16 + k];   // value the partner needs
-                                const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-                                const float g = odd_lane ? other : v[k];
-                                const float u = odd_lane ? v[16 + k] : other;
-                                const int tk = (odd_lane ? 16 : 0) + k;
-                                const float hv = g / (1.f + expf(-g)) * u;
-                                if (c0 + tk < ntok && !(fabsf(hv) <= 65504.f)) atomicOr(a.status, SMOE_FAULT_FP16_RANGE);
-                                hsm[hc * TC_H_STRIDE + tk] = hv;
+                        for (int k = 0; k < 16; ++k) {
+                            const float mine = v[odd_lane ? k : 16 + k];   // value the partner needs
+                            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+                            const float g = odd_lane ? other : v[k];
+                            const float u = odd_lane ? v[16 + k] : other;
+                            const int tk = (odd_lane ? 16 : 0) + k;
+                            const float hv = g / (1.f + expf(-g)) * u;
+                            if (c0 + tk < ntok && !(fabsf(hv) <= 65504.f)) atomicOr(a.status, SMOE_FAULT_FP16_RANGE);
+                            hsm[hc * TC_H_STRIDE + tk] = hv;
+                        }
+                        asm volatile("bar.sync 2, 128;\n" ::: "memory");
+                        // 32 tokens x 64 columns: thread -> (token et & 31, columns 16 (et >> 5) .. + 16)
+                        const int tk = et & 31, cq = et >> 5;
+                        const bool valid = c0 + tk < ntok;
+                        float gs = 0.f;
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            const int cb = cq * 16 + half * 8;   // first column of this 8-chunk
+                            __half hh[8], hl[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float hv = hsm[(cb + e) * TC_H_STRIDE + tk];
+                                const float hs = (e & 1) ? hv * 0.0625f : hv;   // odd columns / 16
+                                const __half h1 = __float2half_rn(hs);
+                                const __half h2 = __float2half_rn(hs - __half2float(h1));
+                                hh[perm8(e)] = h1;
+                                hl[perm8(e)] = h2;
+                                const float stood = __half2float(h1) + __half2float(h2);
+                                gs += (e & 1) ? stood * 16.f : stood;
                             }
-                            asm volatile("bar.sync 2, 128;\n" ::: "memory");
-                            // 32 tokens x 64 columns: thread -> (token et & 31, columns 16 (et >> 5) .. + 16)
-                            const int tk = et & 31, cq = et >> 5;
-                            const bool valid = c0 + tk < ntok;
-                            float gs = 0.f;
-#pragma unroll
-                            for (int half = 0; half < 2; ++half) {
-                                const int cb = cq * 16 + half * 8;   // first column of this 8-chunk
-                                __half hh[8], hl[8];
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) {
-                                    const float hv = hsm[(cb + e) * TC_H_STRIDE + tk];
-                                    const float hs = (e & 1) ? hv * 0.0625f : hv;   // odd columns / 16
-                                    const __half h1 = __float2half_rn(hs);
-                                    const __half h2 = __float2half_rn(hs - __half2float(h1));
-                                    hh[perm8(e)] = h1;
-                                    hl[perm8(e)] = h2;
-                                    const float stood = __half2float(h1) + __half2float(h2);
-                                    gs += (e & 1) ? stood * 16.f : stood;
-                                }
-                                if (valid) {
-                                    const int j = row0 / 2 + m * 64 + cb;   // first h column of the chunk
-                                    __half* rowp = a.h_out + (size_t)(tok0 + c0 + tk) * (2 * a.F) + j;
-                                    *reinterpret_cast<uint4*>(rowp) = *reinterpret_cast<const uint4*>(hh);
-                                    *reinterpret_cast<uint4*>(rowp + a.F) = *reinterpret_cast<const uint4*>(hl);
-                                }
+                            if (valid) {
+                                const int j = I.mt * 64 + cb;   // first h column of the chunk
+                                __half* rowp = a.h_out + (size_t)(tok0 + c0 + tk) * (2 * a.F) + j;
+                                *reinterpret_cast<uint4*>(rowp) = *reinterpret_cast<const uint4*>(hh);
+                                *reinterpret_cast<uint4*>(rowp + a.F) = *reinterpret_cast<const uint4*>(hl);
                             }
-                            gsum_sh[cq][tk] = gs;   // the group's 4 column quarters, summed by warp 0
-                            asm volatile("bar.sync 2, 128;\n" ::: "memory");
-                            if (cq == 0 && valid) {
-                                const float g4 = gsum_sh[0][tk] + gsum_sh[1][tk] + gsum_sh[2][tk] + gsum_sh[3][tk];
-                                const int Gh = a.F / kGroup;
-                                const size_t i = (size_t)(tok0 + c0 + tk) * Gh + (row0 / 2 + m * 64) / kGroup;
-                                const __half sh = __float2half_rn(g4);
-                                a.hsum_out[i] = sh;
-                                a.hsum_out[(size_t)a.B * a.K * Gh + i] = __float2half_rn(g4 - __half2float(sh));
-                            }
-                        } else {
-                            const int r = row0 + m * 128 + lr;   // output row
+                        }
+                        gsum_sh[cq][tk] = gs;   // the group's 4 column quarters, summed by warp 0
+                        asm volatile("bar.sync 2, 128;\n" ::: "memory");
+                        if (cq == 0 && valid) {
+                            const float g4 = gsum_sh[0][tk] + gsum_sh[1][tk] + gsum_sh[2][tk] + gsum_sh[3][tk];
+                            const int Gh = a.F / kGroup;
+                            const size_t i = (size_t)(tok0 + c0 + tk) * Gh + I.mt;   // 64 columns = group mt
+                            const __half sh = __float2half_rn(g4);
+                            a.hsum_out[i] = sh;
+                            a.hsum_out[(size_t)a.B * a.K * Gh + i] = __float2half_rn(g4 - __half2float(sh));
+                        }
+                    } else {
+                        const int r = I.mt * TC_M + lr;   // output row
 #pragma unroll
-                            for (int k = 0; k < 32; ++k) {
-                                const int tk = c0 + k;
-                                if (tk < ntok) {
-                                    const int tok = tok_sh[buf][tk], sl = slot_sh[buf][tk];
-                                    if (tok >= 0 && tok < a.B && sl >= 0 && sl < a.K)
-                                        a.y_out[((size_t)tok * a.K + sl) * a.d + r] = v[k];
-                                }
+                        for (int k = 0; k < 32; ++k) {
+                            const int tk = c0 + k;
+                            if (tk < ntok) {
+                                const int tok = tok_sh[buf][tk], sl = slot_sh[buf][tk];
+                                if (tok >= 0 && tok < a.B && sl >= 0 && sl < a.K)
+                                    a.y_out[((size_t)tok * a.K + sl) * a.d + r] = v[k];
                             }
                         }
                     }
@@ -684,25 +692,25 @@ cudaError_t launch_ffn_tc(const smoe_layer_desc& D, const FfnTcWeights& W, int B
     if (pass == 0) {
         a.wrow0 = W.g_rows; a.wrow1 = W.u_rows; a.woff1 = W.u_off;
         a.s0 = W.sg; a.b0 = W.bg; a.s1 = W.su; a.b1 = W.bu;
-        a.m_tiles = F / 128;
-        if (!encode_map(&mb, xg, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, d, 64, TC_N, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_map(&mshi, sxh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gx, 64, TC_N, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_map(&mslo, sxh + (size_t)BK * Gx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gx, 64, TC_N,
+        a.m_tiles = F / 64;
+        if (!encode_map(&mb, xg, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, d, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_map(&mshi, sxh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gx, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_map(&mslo, sxh + (size_t)BK * Gx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gx, 64, 128,
                         CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
-        const int grid = std::max(1, std::min(sms, E * (F / 128) * ((BK + TC_N - 1) / TC_N)));
+        const int grid = std::max(1, std::min(sms, E * a.m_tiles * ((BK + TC_N - 1) / TC_N)));
         ffn_tc_kernel<0><<<grid, TC_THREADS, TcCfg<0>::kSmem, stream>>>(W.map_gate, W.map_up, mb, mshi, mslo, a);
     } else {
         const size_t nw = (size_t)BK * Gh;
         a.wrow0 = d; a.wrow1 = d; a.woff1 = 0;
         a.s0 = W.sd; a.b0 = W.bd; a.s1 = W.sd; a.b1 = W.bd;
-        a.m_tiles = d / 256;
-        if (!encode_map(&mb, h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, 2 * F, 64, TC_N, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_map(&mshi, shh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gh, 64, TC_N, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_map(&mslo, shh + nw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gh, 64, TC_N,
+        a.m_tiles = d / TC_M;
+        if (!encode_map(&mb, h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, 2 * F, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_map(&mshi, shh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gh, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_map(&mslo, shh + nw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gh, 64, 128,
                         CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
-        const int grid = std::max(1, std::min(sms, E * (d / 256) * ((BK + TC_N - 1) / TC_N)));
+        const int grid = std::max(1, std::min(sms, E * a.m_tiles * ((BK + TC_N - 1) / TC_N)));
         ffn_tc_kernel<1><<<grid, TC_THREADS, TcCfg<1>::kSmem, stream>>>(W.map_down, W.map_down, mb, mshi, mslo, a);
     }
     return cudaGetLastError();

@@ -63,6 +63,7 @@ cudaError_t launch_union(const smoe_layer_desc& D, const int32_t* topk_idx, int 
 // of expert e start at e * 2F + F (u_row_offset = F).
 struct FfnPointers {
     CUtensorMap map_gate, map_up, map_down;
+    CUtensorMap tc_gate, tc_up, tc_down;   // the same views, boxes of 64 (gate, up) / 128 (down) rows
     // scale / bias tables of the expert passes: bf16 [rows, in/64], box 8 groups x 128 rows
     // (gate, up) or 256 rows (down); see encode_group_map
     CUtensorMap map_sg, map_bg, map_su, map_bu, map_sd, map_bd;
@@ -71,7 +72,8 @@ struct FfnPointers {
     const uint16_t* sd; const uint16_t* bd;
 };
 
-// The tensor-core path reads the packed weights through the same maps as the other passes.
+// The tensor-core path reads the packed weights through maps with 128-byte rows (4 groups)
+// and boxes of 64 rows (gate, up) or 128 rows (down).
 struct FfnTcWeights {
     CUtensorMap map_gate, map_up, map_down;
     const uint16_t* sg; const uint16_t* bg; int64_t g_rows;
