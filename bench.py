@@ -94,13 +94,16 @@ class Clocks:
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(smax), "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _traffic_from_profile(kernel_src: str):
-    """DRAM bytes per FFN-step launch recorded in the committed ncu summary, if the kernel
-    source is unchanged since the capture (sha256 of csrc/ffn.cu must match)."""
+def _traffic_from_profile(kernel_src: str, workload: str):
+    """DRAM bytes per FFN-step launch recorded in the committed ncu summary of this workload,
+    if the kernel source is unchanged since the capture (sha256 of csrc/ffn.cu must match)."""
     path = os.path.join(ROOT, "profiles", "expert_ffn_prefill64.md")
     try:
         text = open(path).read()
     except OSError:
+        return None
+    m_wl = re.search(r"workload:\s*(\S+)", text)
+    if not m_wl or m_wl.group(1) != workload:
         return None
     m_sha = re.search(r"ffn\.cu sha256:\s*([0-9a-f]{64})", text)
     m_b = re.search(r"dram bytes per smoe_moe_ffn_batch launch:\s*([0-9]+)", text)
@@ -333,7 +336,7 @@ def run_gpu(args, w, world, rank, local):
         cpu = {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"layer 0, first {n} of {B} tokens ({n} token-layers), layer-major fp64 oracle, "
                          f"{dt:.1f} s"}
-    traffic = _traffic_from_profile(os.path.join(ROOT, "moe_expert_routing_gb300", "csrc", "ffn.cu"))
+    traffic = _traffic_from_profile(os.path.join(ROOT, "moe_expert_routing_gb300", "csrc", "ffn.cu"), w.name)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
