@@ -768,9 +768,11 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
     // -------------------------------------------------------------------- consumers
     for (;;) {
         const uint32_t slot = it % C::kCount;
-        // all consumer threads take the same decision, so that they run the same chunks and
-        // meet at the same named barriers
-        if (consumers_any(!mbar_wait(R.full + 8 * slot, (it / C::kCount) & 1u))) {
+        // launches with gate/up tiles: all consumer threads take the same decision, so that
+        // they run the same chunks and meet at the same named barriers; a down-only launch has
+        // none, and each warp decides for itself (no cross-warp sync per chunk)
+        const bool late = !mbar_wait(R.full + 8 * slot, (it / C::kCount) & 1u);
+        if (MODE == kDown ? __any_sync(0xffffffffu, late) : consumers_any(late)) {
             if (threadIdx.x == 0) atomicOr(f.p[0].status, SMOE_FAULT_TIMEOUT);
             break;
         }
