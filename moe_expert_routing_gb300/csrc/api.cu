@@ -169,6 +169,7 @@ WsLayout ws_layout(const smoe_layer_desc& D, int max_tokens) {
     L.s16h = take(2 * BK * (F / kGroup) * 2);
     L.y = take(BK * d * 4);
     L.ticket = take((E + 2) * 4);
+    L.uscratch = take((1 + (size_t)union_chunks((int)BK) * E) * 4);
     L.total = o;
     return L;
 }
@@ -209,7 +210,8 @@ smoe_status smoe_expert_union(const smoe_layer_desc* desc, const int32_t* topk_i
     WsLayout L;
     if ((st = check_ws(*desc, B, workspace, workspace_bytes, &L)) != SMOE_OK) return st;
     return cuda_status(launch_union(*desc, topk_idx, B, union_ids, n_union, offsets, token_list, slot_list,
-                                    ws_ptr<uint32_t>(workspace, L.status), static_cast<cudaStream_t>(stream)));
+                                    ws_ptr<uint32_t>(workspace, L.status), ws_ptr<int32_t>(workspace, L.uscratch),
+                                    static_cast<cudaStream_t>(stream)));
 }
 
 smoe_status smoe_moe_ffn_batch(const smoe_layer_desc* desc, const smoe_expert_weights* weights, const uint16_t* x,
@@ -254,7 +256,8 @@ smoe_status smoe_moe_layer(const smoe_layer_desc* desc, const smoe_expert_weight
     int32_t* sl = ws_ptr<int32_t>(workspace, L.slot_list);
     cudaError_t e = launch_route(*desc, x, gate_w, gate_bias, B, idx, w, ws_ptr<float>(workspace, L.logits), s);
     if (e == cudaSuccess)
-        e = launch_union(*desc, idx, B, uid, nu, off, tl, sl, ws_ptr<uint32_t>(workspace, L.status), s);
+        e = launch_union(*desc, idx, B, uid, nu, off, tl, sl, ws_ptr<uint32_t>(workspace, L.status),
+                         ws_ptr<int32_t>(workspace, L.uscratch), s);
     if (e == cudaSuccess) e = launch_ffn(*desc, P, x, B, uid, nu, off, tl, sl, w, residual, workspace, L, s);
     return cuda_status(e);
 }

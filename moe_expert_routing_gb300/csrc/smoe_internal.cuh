@@ -36,6 +36,7 @@ struct WsLayout {
     size_t s16h;          // fp16 [2][B * K, F / 64]: activation group sums as hi and lo planes
     size_t y;             // fp32 [B * K, d]: unweighted expert outputs, row t*K + k
     size_t ticket;        // int32 [2 + E]: work queues of the expert passes and per-expert counts
+    size_t uscratch;      // int32 [1 + chunks * E]: the union's per-chunk counts (B * K > 1024)
     size_t total;
 };
 
@@ -53,9 +54,12 @@ cudaError_t launch_route(const smoe_layer_desc& D, const uint16_t* x, const floa
                          const float* gate_bias, int B, int32_t* topk_idx, float* topk_w,
                          float* logits_ws, cudaStream_t stream, int split_cap = 0);
 
+// scratch: int32 [1 + union_chunks(B*K) * E] for batches of more than 1024 entries (may be
+// NULL for smaller ones)
+int union_chunks(int BK);
 cudaError_t launch_union(const smoe_layer_desc& D, const int32_t* topk_idx, int B, int32_t* union_ids,
                          int32_t* n_union, int32_t* offsets, int32_t* token_list, int32_t* slot_list,
-                         uint32_t* status, cudaStream_t stream);
+                         uint32_t* status, int32_t* scratch, cudaStream_t stream);
 
 // Expert weights as the FFN kernels consume them.  The packed words are read through TMA
 // tensor maps: 2-D u32 views [rows, in/8] of each weight tensor, box 32 words (4 groups) x
