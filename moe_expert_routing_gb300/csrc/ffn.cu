@@ -139,10 +139,13 @@ __device__ __forceinline__ uint4 lds_u4(uint32_t a) {
 
 
 // ----------------------------------------------------------------------------- gather
-// One thread per 8-element chunk of a list entry p: xg[p] = pair-permuted fp16(x[token_list[p]])
-// with the odd elements of every 8 divided by 16; sx[p][g] = sum of the values the stored
-// halves stand for in group g (8 consecutive lanes hold a group), also as fp16 hi and lo
-// planes s16[0|1][p][g].
+// One warp per segment of 32 x U 8-element chunks of a list entry p: xg[p] = pair-permuted
+// fp16(x[token_list[p]]) with the odd elements of every 8 divided by 16; sx[p][g] = sum of the
+// values the stored halves stand for in group g (8 consecutive lanes hold a group's chunks),
+// also as fp16 hi and lo planes s16[0|1][p][g].  The warp issues all U of its loads before
+// converting, so the kernel streams instead of waiting on one dependent load chain per 16
+// bytes; small batches use U = 1 (more warps), large ones U = 16 (fewer index loads).
+template <int U>
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ x, int d, int B,
                                                      const int32_t* __restrict__ n_union,
                                                      const int32_t* __restrict__ offsets,
@@ -153,42 +156,60 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
                                                      int n_ticket) {
     if (blockIdx.x == 0)   // work queue of the expert passes that follow
         for (int i = threadIdx.x; i < n_ticket; i += blockDim.x) ticket[i] = 0;
-    const int cpr = d / 8;   // chunks per row, a multiple of 32: a warp never spans two rows
-    const size_t gid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int p = (int)(gid / cpr), ch = (int)(gid - (size_t)p * cpr);
     const int lane = threadIdx.x & 31;
     const int total = offsets[*n_union];
-    if (p >= total) return;
-    int t = token_list[p];
-    if (t < 0 || t >= B) {   // a caller-supplied list that does not match B: flag, use row 0
-        if (lane == 0) atomicOr(status, SMOE_FAULT_TOKEN_INDEX);
-        t = 0;
-    }
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d) + ch);
-    const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-    __half hv[8];
-    float sa = 0.f;
+    const int cpr = d / 8;   // 8-element chunks per row, a multiple of 32
+    const int G = d / kGroup;
+    const int segs = (cpr + 32 * U - 1) / (32 * U);   // warps per row
+    for (int wg = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; wg < total * segs;
+         wg += (gridDim.x * blockDim.x) >> 5) {
+        const int p = wg / segs, seg = wg - p * segs;
+        int t = token_list[p];
+        if (t < 0 || t >= B) {   // a caller-supplied list that does not match B: flag, use row 0
+            if (lane == 0) atomicOr(status, SMOE_FAULT_TOKEN_INDEX);
+            t = 0;
+        }
+        const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+        uint4* orow = reinterpret_cast<uint4*>(xg + (size_t)p * d);
+        {
+            const int base = seg * 32 * U;
+            uint4 raw[U];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        const float v = bf16_bits_to_float((m & 1) ? (wv[m >> 1] >> 16) : (wv[m >> 1] & 0xFFFFu));
-        const __half h = __float2half_rn((m & 1) ? v * 0.0625f : v);
-        hv[perm8(m)] = h;
-        sa += (m & 1) ? __half2float(h) * 16.f : __half2float(h);
-    }
-    uint4 o;
-    o.x = (uint32_t)__half_as_ushort(hv[0]) | ((uint32_t)__half_as_ushort(hv[1]) << 16);
-    o.y = (uint32_t)__half_as_ushort(hv[2]) | ((uint32_t)__half_as_ushort(hv[3]) << 16);
-    o.z = (uint32_t)__half_as_ushort(hv[4]) | ((uint32_t)__half_as_ushort(hv[5]) << 16);
-    o.w = (uint32_t)__half_as_ushort(hv[6]) | ((uint32_t)__half_as_ushort(hv[7]) << 16);
-    reinterpret_cast<uint4*>(xg + (size_t)p * d)[ch] = o;
+            for (int u = 0; u < U; ++u) {
+                const int ch = base + u * 32 + lane;
+                raw[u] = ch < cpr ? __ldg(xr + ch) : make_uint4(0, 0, 0, 0);
+            }
 #pragma unroll
-    for (int off = 1; off < 8; off <<= 1) sa += __shfl_xor_sync(0xffffffffu, sa, off);
-    if ((lane & 7) == 0) {
-        const size_t i = (size_t)p * (d / kGroup) + ch / 8;
-        sx[i] = sa;
-        const __half hh = __float2half_rn(sa);   // hi and lo planes for the tensor-core path
-        s16[i] = hh;
-        s16[(size_t)BK * (d / kGroup) + i] = __float2half_rn(sa - __half2float(hh));
+            for (int u = 0; u < U; ++u) {
+                const int ch = base + u * 32 + lane;   // warp-uniform validity: cpr % 32 == 0
+                if (ch >= cpr) break;
+                const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+                __half hv[8];
+                float sa = 0.f;
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const float v = bf16_bits_to_float((m & 1) ? (wv[m >> 1] >> 16) : (wv[m >> 1] & 0xFFFFu));
+                    const __half h = __float2half_rn((m & 1) ? v * 0.0625f : v);
+                    hv[perm8(m)] = h;
+                    sa += (m & 1) ? __half2float(h) * 16.f : __half2float(h);
+                }
+                uint4 o;
+                o.x = (uint32_t)__half_as_ushort(hv[0]) | ((uint32_t)__half_as_ushort(hv[1]) << 16);
+                o.y = (uint32_t)__half_as_ushort(hv[2]) | ((uint32_t)__half_as_ushort(hv[3]) << 16);
+                o.z = (uint32_t)__half_as_ushort(hv[4]) | ((uint32_t)__half_as_ushort(hv[5]) << 16);
+                o.w = (uint32_t)__half_as_ushort(hv[6]) | ((uint32_t)__half_as_ushort(hv[7]) << 16);
+                orow[ch] = o;
+#pragma unroll
+                for (int off = 1; off < 8; off <<= 1) sa += __shfl_xor_sync(0xffffffffu, sa, off);
+                if ((lane & 7) == 0) {
+                    const size_t i = (size_t)p * G + ch / 8;
+                    sx[i] = sa;
+                    const __half hh = __float2half_rn(sa);   // hi and lo planes for the tensor-core path
+                    s16[i] = hh;
+                    s16[(size_t)BK * G + i] = __float2half_rn(sa - __half2float(hh));
+                }
+            }
+        }
     }
 }
 
@@ -894,9 +915,13 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
                        CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
 
-    const size_t chunks = (size_t)BK * (d / 8);
     int32_t* ticket = ws_ptr<int32_t>(ws, L.ticket);
-    gather_kernel<<<(unsigned)((chunks + 255) / 256), 256, 0, stream>>>(x, d, B, n_union, offsets, token_list, status,
+    // warps: one per 256 elements of a row for small batches, one per 4096 for large ones
+    const bool big = BK > 4096;
+    const int segs = (d / 8 + 32 * (big ? 16 : 1) - 1) / (32 * (big ? 16 : 1));
+    const int gather_blocks = std::max(1, std::min((BK * segs + 7) / 8, sms * 16));
+    (big ? gather_kernel<16> : gather_kernel<1>)<<<gather_blocks, 256, 0, stream>>>(x, d, B, n_union, offsets,
+                                                                                     token_list, status,
                                                                           xg, sx, ws_ptr<__half>(ws, L.s16x), BK,
                                                                           ticket, E + 2);
 

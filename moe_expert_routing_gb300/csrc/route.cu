@@ -118,6 +118,91 @@ __global__ void __launch_bounds__(256) gate_logits_kernel(const uint16_t* __rest
         }
 }
 
+// Large batches: the same tile with the CTA's 64 token rows staged in shared memory piece by
+// piece (256 inputs at a time, cp.async), so the 8 warps read each activation once from
+// global memory instead of once per warp.  Rows padded by 16 bytes: the 8 rows a fragment
+// load touches fall in different banks.
+constexpr int kPiece = 256;
+constexpr int kPieceStride = kPiece + 8;   // bf16 elements per staged row
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+
+template <int NT, int KB>
+__global__ void __launch_bounds__(256) gate_logits_staged_kernel(const uint16_t* __restrict__ x,
+                                                                 const float* __restrict__ W, int B, int E, int d,
+                                                                 int kchunk, float* __restrict__ partial) {
+    extern __shared__ __align__(16) uint16_t xs[];   // [8 NT rows][kPieceStride]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    const int e0 = blockIdx.y * kExpertsPerCta + warp * 16;
+    const int t0 = blockIdx.x * 8 * NT;
+    const int k_begin = blockIdx.z * kchunk, k_end = k_begin + kchunk;
+    const int ea = e0 + g, eb = e0 + g + 8;
+    const float* wa = W + (size_t)(ea < E ? ea : 0) * d;
+    const float* wb = W + (size_t)(eb < E ? eb : 0) * d;
+    const uint32_t xs_base = static_cast<uint32_t>(__cvta_generic_to_shared(xs));
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+    for (int kp = k_begin; kp < k_end; kp += kPiece) {
+        // stage rows t0.., inputs kp..kp+255: 32 chunks of 16 bytes per row
+        for (int i = threadIdx.x; i < 8 * NT * 32; i += 256) {
+            const int row = i >> 5, ch = i & 31;
+            const int t = t0 + row < B ? t0 + row : 0;
+            cp_async16(xs_base + (uint32_t)(row * kPieceStride + ch * 8) * 2u, x + (size_t)t * d + kp + ch * 8);
+        }
+        asm volatile("cp.async.wait_all;\n" ::: "memory");
+        __syncthreads();
+        if (e0 < E) {
+            for (int kb = 0; kb < kPiece; kb += 16 * KB) {
+                float2 wv[KB][4];
+#pragma unroll
+                for (int j = 0; j < KB; ++j) {
+                    const int k0 = kp + kb + 16 * j + 2 * c, k1 = k0 + 8;
+                    wv[j][0] = __ldg(reinterpret_cast<const float2*>(wa + k0));
+                    wv[j][1] = __ldg(reinterpret_cast<const float2*>(wb + k0));
+                    wv[j][2] = __ldg(reinterpret_cast<const float2*>(wa + k1));
+                    wv[j][3] = __ldg(reinterpret_cast<const float2*>(wb + k1));
+                }
+#pragma unroll
+                for (int j = 0; j < KB; ++j) {
+                    if (ea >= E) wv[j][0] = wv[j][2] = make_float2(0.f, 0.f);
+                    if (eb >= E) wv[j][1] = wv[j][3] = make_float2(0.f, 0.f);
+                    uint32_t a[3][4];   // [term][a0..a3]: rows g / g+8, k 2c.. / 2c+8..
+                    split3(wv[j][0], a[0][0], a[1][0], a[2][0]);
+                    split3(wv[j][1], a[0][1], a[1][1], a[2][1]);
+                    split3(wv[j][2], a[0][2], a[1][2], a[2][2]);
+                    split3(wv[j][3], a[0][3], a[1][3], a[2][3]);
+                    const int kk = kb + 16 * j + 2 * c;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const uint16_t* xr = xs + (nt * 8 + g) * kPieceStride + kk;
+                        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(xr);
+                        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(xr + 8);
+#pragma unroll
+                        for (int term = 2; term >= 0; --term)   // small terms first
+                            mma_bf16(acc[nt], a[term][0], a[term][1], a[term][2], a[term][3], b0, b1);
+                    }
+                }
+            }
+        }
+        __syncthreads();   // the piece is consumed before the next one is staged
+    }
+    if (e0 >= E) return;
+    float* out = partial + (size_t)blockIdx.z * B * E;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = t0 + nt * 8 + 2 * c + (i & 1);
+            const int e = (i & 2) ? eb : ea;
+            if (t < B && e < E) out[(size_t)t * E + e] = acc[nt][i];
+        }
+}
+
 int tile_tokens(int B) { return B <= 64 ? 8 : 64; }
 
 // One CTA per token.  Thread e sums expert e's split-K partials in split order (all loads
@@ -214,8 +299,10 @@ int route_splits(int B, int E, int d) {
     const int tiles = ((B + bt - 1) / bt) * ((E + kExpertsPerCta - 1) / kExpertsPerCta);
     const int target = 2 * 152;
     int s = 1;
-    // a split keeps at least 128 inputs and a multiple of 128 (8 k-steps of 16 per load batch)
-    while (s < kMaxSplits && s * tiles < target && (d / (2 * s)) % 128 == 0) s *= 2;
+    // a split keeps a multiple of 128 inputs (8 k-steps of 16 per load batch) and, for the
+    // staged large-batch kernel, of 256 (one staged piece)
+    const int quantum = bt == 64 ? 256 : 128;
+    while (s < kMaxSplits && s * tiles < target && (d / (2 * s)) % quantum == 0) s *= 2;
     return s;
 }
 
@@ -228,8 +315,12 @@ cudaError_t launch_route(const smoe_layer_desc& D, const uint16_t* x, const floa
     const int bt = tile_tokens(B);
     dim3 grid((B + bt - 1) / bt, (E + kExpertsPerCta - 1) / kExpertsPerCta, S);
     const int kchunk = d / S;   // a multiple of 128 (route_splits)
-    if (bt == 8) gate_logits_kernel<1, 8><<<grid, 256, 0, stream>>>(x, gate_w, B, E, d, kchunk, logits_ws);
-    else gate_logits_kernel<8, 2><<<grid, 256, 0, stream>>>(x, gate_w, B, E, d, kchunk, logits_ws);
+    if (bt == 8) {
+        gate_logits_kernel<1, 8><<<grid, 256, 0, stream>>>(x, gate_w, B, E, d, kchunk, logits_ws);
+    } else {
+        const int smem = 64 * kPieceStride * 2;   // 33 KB: below the default dynamic limit
+        gate_logits_staged_kernel<8, 4><<<grid, 256, smem, stream>>>(x, gate_w, B, E, d, kchunk, logits_ws);
+    }
     const int threads = (E + 31) / 32 * 32;
     topk_kernel<<<B, threads, 0, stream>>>(logits_ws, S, gate_bias, B, E, K, D.norm_topk_prob, topk_idx, topk_w);
     return cudaGetLastError();
