@@ -13,17 +13,20 @@
 // second a small [rows x groups] x [groups x tokens] product that runs as one extra k-stage
 // (eps as fp16, S as an fp16 hi + lo pair).
 //
-// Tile per CTA: 256 weight rows (two UMMA M=128 accumulators) x 128 tokens; k in stages of
-// one 64-input group.  Three shared-memory rings (see TcCfg): packed weights, activation rows
-// and dequantised fp16 weights.  Warp roles (one CTA per SM, persistent over the work items):
+// Tile per CTA: 128 weight rows (UMMA M = 128) x 192 tokens (UMMA N); k in stages of one
+// 64-input group.  The dequantised weights (the A operand) go from registers straight into
+// tensor memory and the MMAs read them there, so shared memory carries only the packed
+// weights and the activations (the B operand): two shared-memory rings (see TcCfg).
+// Tensor memory (512 columns): two accumulator buffers of 192 columns (one tile's epilogue
+// overlaps the next tile's MMAs) and a ring of 4 A stages of 32 columns (128 rows x 64 fp16).
+// Warp roles (one CTA per SM, persistent over the work items):
 //   warp 0      producer of the packed weight rows (TMA)
 //   warp 1      TMEM owner; lane 0 issues tcgen05.mma and tcgen05.commit
-//   warps 2-9   dequantisers, one A row each: packed nibbles -> fp16 s (q - 8) in the SW128
-//               K-major layout
+//   warps 2-9   dequantisers, one A row per thread and half of its group: packed nibbles ->
+//               fp16 s (q - 8) -> tcgen05.st into the row's TMEM lane
 //   warps 10-13 epilogue: tcgen05.ld of the accumulators -> SwiGLU (pass 0) or y (pass 1)
 //   warp 14     producer of the activation rows (B operand, TMA)
-// Accumulators are double-buffered in TMEM (2 x 256 columns) so one tile's epilogue
-// overlaps the next tile's MMAs.  Every mbarrier wait is bounded.  Pass 0's epilogue stages
+// Every mbarrier wait is bounded.  Pass 0's epilogue stages
 // h through shared memory for 16-byte stores and also writes the per-group sums of h that
 // pass 1's eps stage needs.
 //
@@ -42,31 +45,32 @@ namespace smoe {
 namespace {
 
 constexpr int TC_M = 128;                    // weight rows per tile (UMMA M, one TMEM lane each)
-constexpr int TC_N = 256;                    // tokens per tile (UMMA N; 128 for an expert's last short tile)
-constexpr int TC_A_BYTES = TC_M * 128;       // A slot: 128 rows x 64 fp16, SW128 K-major
+constexpr int TC_N = 192;                    // tokens per tile (UMMA N; 64 / 128 for an expert's last short tile)
+constexpr int TC_BOX_ROWS = 64;              // token rows per activation box
 constexpr int TC_P_BYTES = TC_M * 128;       // packed slot: 128 rows x 32 words (4 stages), SW128
-constexpr int TC_BOX_BYTES = 128 * 128;      // one activation box: 128 token rows x 64 fp16, SW128 K-major
-constexpr int TC_B_BYTES = 2 * TC_BOX_BYTES; // one B sub-tile: 256 token rows
+constexpr int TC_BOX_BYTES = TC_BOX_ROWS * 128;   // one activation box: 64 token rows x 64 fp16, SW128 K-major
+constexpr int TC_B_BYTES = (TC_N / TC_BOX_ROWS) * TC_BOX_BYTES;   // one B sub-tile: 192 token rows
 constexpr int TC_H_STRIDE = 33;             // pass 0 epilogue staging: 64 h columns x 32 tokens fp32,
 constexpr int TC_H_BYTES = 64 * TC_H_STRIDE * 4;   // column-major, padded (conflict-free both ways)
 constexpr int TC_THREADS = 480;
-constexpr uint32_t TC_TMEM_COLS = 512;       // two accumulator buffers of TC_N columns
+constexpr uint32_t TC_TMEM_COLS = 512;       // 2 accumulator buffers of TC_N columns + the A ring
+constexpr int TC_KA = 4;                     // A stages in tensor memory
+constexpr uint32_t TC_A_COL = 2 * TC_N;      // first TMEM column of the A ring (32 columns per stage)
+static_assert(TC_A_COL + 32 * TC_KA <= TC_TMEM_COLS, "tensor memory columns");
 
-// Per-pass ring shapes.  Three rings: dequantised A slots (kA), B slots (kB: x, or h hi + lo,
-// or the group sums of the eps stages; kNb sub-tiles each) and packed-weight slots (kP, each
-// 4 stages of 128-byte rows).  Packed slots are freed by the dequantisers once they have
-// consumed them, so the packed stream runs ahead of the MMAs; B slots are freed by the MMAs.
-// The tile shape (128 rows x 256 tokens) reads each B row for 128 weight rows and each A row
-// for 256 tokens per MMA, which keeps the shared-memory traffic per MAC low enough for the
-// tensor core (shared-memory bandwidth, not the MMA rate, limits narrower tiles).
+// Per-pass ring shapes.  Two shared-memory rings: B slots (kB: x, or h hi + lo, or the group
+// sums of the eps stages; kNb sub-tiles each) and packed-weight slots (kP, each 4 stages of
+// 128-byte rows).  Packed slots are freed by the dequantisers once they have consumed them, so
+// the packed stream runs ahead of the MMAs; B slots are freed by the MMAs.  Shared-memory
+// bandwidth bounds the kernel: per stage the TMA writes and the MMAs read every B row once,
+// and the A operand no longer passes through shared memory at all.
 template <int PASS>
 struct TcCfg {
-    static constexpr int kA = PASS ? 3 : 4;
-    static constexpr int kB = PASS ? 2 : 3;
-    static constexpr int kP = PASS ? 2 : 3;
+    static constexpr int kB = PASS ? 3 : 5;
+    static constexpr int kP = PASS ? 3 : 4;
     static constexpr int kNb = PASS ? 2 : 1;
     static constexpr int kBSlot = kNb * TC_B_BYTES;
-    static constexpr int kOffB = kA * TC_A_BYTES;
+    static constexpr int kOffB = 0;
     static constexpr int kOffP = kOffB + kB * kBSlot;
     static constexpr int kOffStage = kOffP + kP * TC_P_BYTES;   // epilogue staging
     static constexpr int kSmem = kOffStage + (PASS ? 0 : TC_H_BYTES) + 1024;
@@ -114,7 +118,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
 
@@ -134,11 +137,14 @@ __host__ __device__ constexpr uint32_t idesc_f16(int n) {
     return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TC_M >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+// Same, with the A operand in tensor memory: lane i holds row i, two fp16 k-elements per
+// 32-bit column (lower k in the low half), 8 columns per 16-element k step.
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -160,6 +166,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 consecutive 32-bit columns of this thread's TMEM lane from v (not waited for).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+        "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+        "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
 }
 
 // OR of v over the 128 epilogue threads (named barrier 2), so that they all take the same
@@ -194,10 +212,6 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, __half2 s2) {
     return r;
 }
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
-}
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -283,7 +297,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     using C = TcCfg<PASS>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_p[C::kP], empty_p[C::kP], full_b[C::kB], empty_b[C::kB];
-    __shared__ __align__(8) uint64_t deq[C::kA], empty_a[C::kA];
+    __shared__ __align__(8) uint64_t deq[TC_KA], empty_a[TC_KA];
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int pref[kMaxExperts + 1];
@@ -306,8 +320,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_init(smem_u32(&full_b[s]), 1);
             mbar_init(smem_u32(&empty_b[s]), 1);     // tcgen05.commit of the stage's MMAs
         }
-        for (int s = 0; s < C::kA; ++s) {
-            mbar_init(smem_u32(&deq[s]), 8);         // one arrival per dequantiser warp
+        for (int s = 0; s < TC_KA; ++s) {
+            mbar_init(smem_u32(&deq[s]), 4);         // one arrival per warp of the stage's dequantiser set
             mbar_init(smem_u32(&empty_a[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -366,7 +380,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             for (int t = blockIdx.x; t < n_items && !poisoned; t += gridDim.x) {
                 const Item I = decode_item(a, pref, t);
                 const int tok0 = I.p0 + I.nt * TC_N;
-                const int boxes = I.n - I.nt * TC_N > 128 ? 2 : 1;   // 128-token boxes of this tile
+                const int boxes = (min(TC_N, I.n - I.nt * TC_N) + TC_BOX_ROWS - 1) / TC_BOX_ROWS;   // boxes of this tile
                 for (int st = 0; st < n_st; ++st, ++ib) {
                     const uint32_t s = ib % C::kB;
                     if (ib >= (uint32_t)C::kB) fail(mbar_wait(smem_u32(&empty_b[s]), ((ib / C::kB) - 1) & 1u));
@@ -377,7 +391,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     for (int sub = 0; sub < C::kNb; ++sub) {
                         const uint32_t dst = sbase + C::kOffB + s * C::kBSlot + sub * TC_B_BYTES;
                         for (int bx = 0; bx < boxes; ++bx) {
-                            const int y = tok0 + bx * 128;
+                            const int y = tok0 + bx * TC_BOX_ROWS;
                             const uint32_t d = dst + bx * TC_BOX_BYTES;
                             if (st < n_main)   // x, or h hi (sub 0) and h lo (sub 1)
                                 tma_load_2d(d, &map_b, (sub ? a.F : 0) + st * 64, y, bar);
@@ -396,26 +410,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint32_t it = 0, tile = 0;
             for (int t = blockIdx.x; t < n_items; t += gridDim.x, ++tile) {
                 const Item I = decode_item(a, pref, t);
-                const uint32_t idesc = idesc_f16(I.n - I.nt * TC_N > 128 ? TC_N : 128);
+                const int ntok = min(TC_N, I.n - I.nt * TC_N);
+                const uint32_t idesc = idesc_f16((ntok + TC_BOX_ROWS - 1) / TC_BOX_ROWS * TC_BOX_ROWS);
                 const uint32_t buf = tile & 1u;
                 if (tile >= 2 && !poisoned) fail(mbar_wait(smem_u32(&acc_empty[buf]), ((tile >> 1) - 1) & 1u));
                 tc_fence_after();
                 for (int st = 0; st < n_st; ++st, ++it) {
-                    const uint32_t s = it % C::kB, sa = it % C::kA;
-                    if (!poisoned) fail(mbar_wait(smem_u32(&deq[sa]), (it / C::kA) & 1u));
+                    const uint32_t s = it % C::kB, sa = it % TC_KA;
+                    if (!poisoned) fail(mbar_wait(smem_u32(&deq[sa]), (it / TC_KA) & 1u));
                     if (!poisoned) fail(mbar_wait(smem_u32(&full_b[s]), (it / C::kB) & 1u));
                     if (poisoned) continue;
                     tc_fence_after();
-                    const uint32_t abuf = sbase + sa * TC_A_BYTES;
+                    const uint32_t a_tmem = tmem + TC_A_COL + sa * 32u;
                     const uint32_t bbuf = sbase + C::kOffB + s * C::kBSlot;
                     const uint32_t d_tmem = tmem + buf * TC_N;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = sw128_desc(abuf + kk * 32);
 #pragma unroll
                         for (int b = 0; b < C::kNb; ++b) {
                             const uint64_t bd = sw128_desc(bbuf + b * TC_B_BYTES + kk * 32);
-                            umma_f16(d_tmem, ad, bd, idesc, (st > 0 || kk > 0 || b > 0) ? 1u : 0u);
+                            umma_f16_ta(d_tmem, a_tmem + kk * 8u, bd, idesc, (st > 0 || kk > 0 || b > 0) ? 1u : 0u);
                         }
                     }
                     umma_commit(smem_u32(&empty_b[s]));    // B slot free once these MMAs finish
@@ -426,9 +440,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
     } else if (warp < 10) {
         // ------------------------------------------------------------------ dequantisers
-        // 256 threads for 128 A rows: thread -> row r, half hf of the row's 8 packed words
-        const int r = (threadIdx.x - 64) & (TC_M - 1);
-        const int hf = (threadIdx.x - 64) >> 7;
+        // Two sets of 4 warps take alternate A stages (set = stage parity), 128 threads per
+        // stage, one A row each.  A warp reaches only its own quarter of the TMEM lanes
+        // (warp % 4), so thread -> row r = 32 (warp % 4) + lane; it writes the row's 64 weights
+        // of the stage (32 TMEM columns).
+        const int r = 32 * (warp & 3) + lane;
+        const uint32_t set = (uint32_t)(warp - 2) >> 2;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         uint32_t it = 0, ip = 0;   // stages (A ring), packed slots (4 main stages each)
         for (int ti = blockIdx.x; ti < n_items; ti += gridDim.x) {
             const Item I = decode_item(a, pref, ti);
@@ -452,56 +470,54 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint4* srow = reinterpret_cast<const uint4*>(sp + src * G);   // 8 bf16 per uint4
             const uint4* brow = reinterpret_cast<const uint4*>(bp + src * G);
             uint4 scl = __ldg(srow), scl_next = n_main > 8 ? __ldg(srow + 1) : make_uint4(0, 0, 0, 0);
-            uint4 es[4], eb[4];   // this half's scale / bias chunks for eps, loaded two stages early
             for (int st = 0; st < n_st; ++st, ++it) {
-                const uint32_t sa = it % C::kA;
+                const uint32_t sa = it % TC_KA;
                 if (st < n_main && (st & 7) == 0 && st > 0) {
                     scl = scl_next;
                     if (st + 8 < n_main) scl_next = __ldg(srow + (st >> 3) + 1);
                 }
-                if (st == n_main - 2) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        if (4 * hf + i < G / 8) {
-                            es[i] = __ldg(srow + 4 * hf + i);
-                            eb[i] = __ldg(brow + 4 * hf + i);
-                        }
-                }
-                // main stage: this half-row's 4 packed words, read before the A slot is waited
-                // for; the packed slot is handed back once the words have been consumed
-                uint4 w = make_uint4(0, 0, 0, 0);
-                const uint32_t sp_ = ip % C::kP;
+                const uint32_t ipc = ip;                  // packed slot of this stage
+                const uint32_t sp_ = ipc % C::kP;
+                if (st < n_main && (st & 3) == 3) ++ip;   // every thread tracks the packed slots
+                if ((it & 1u) != set) continue;           // the other set's stage
+                // main stage: the row's 8 packed words of group st % 4 (chunks 2q, 2q+1 of the
+                // 128-byte row, swizzled by row & 7), read before the A stage is waited for
+                uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
                 if (st < n_main) {
-                    if ((st & 3) == 0 && !poisoned) fail(mbar_wait(smem_u32(&full_p[sp_]), (ip / C::kP) & 1u));
+                    if (!poisoned) fail(mbar_wait(smem_u32(&full_p[sp_]), (ipc / C::kP) & 1u));
                     if (!poisoned) {
-                        // packed rows of 128 bytes (4 groups) with the 128-byte swizzle: chunk
-                        // 2q + hf of the row (group q = st % 4) sits at chunk ((2q + hf) ^ (row & 7))
                         const uint32_t pk = sbase + C::kOffP + sp_ * TC_P_BYTES + prow * 128u;
-                        w = lds128(pk + ((((uint32_t)(st & 3) * 2u + hf) ^ (prow & 7u)) << 4));
+                        const uint32_t q2 = (uint32_t)(st & 3) * 2u;
+                        w0 = lds128(pk + ((q2 ^ (prow & 7u)) << 4));
+                        w1 = lds128(pk + (((q2 + 1u) ^ (prow & 7u)) << 4));
                     }
                 }
-                if (it >= (uint32_t)C::kA && !poisoned) fail(mbar_wait(smem_u32(&empty_a[sa]), ((it / C::kA) - 1) & 1u));
-                if (!poisoned) {
-                    const uint32_t arow = sbase + sa * TC_A_BYTES + (uint32_t)r * 128u;
+                if (it >= (uint32_t)TC_KA && !poisoned) fail(mbar_wait(smem_u32(&empty_a[sa]), ((it / TC_KA) - 1) & 1u));
+                // tcgen05.st is warp-collective: the warp takes one decision
+                const bool skip = __any_sync(0xffffffffu, poisoned);
+                if (!skip) {
+                    tc_fence_after();   // the MMAs that read this stage before (commit) -> the stores
+                    uint32_t v[32];
                     if (st < n_main) {
                         const uint32_t sw = (&scl.x)[(st & 7) >> 1];
                         const float sf = __uint_as_float((st & 1) ? (sw & 0xFFFF0000u) : (sw << 16));
                         const __half2 s2 = __float2half2_rn(sf);   // exact: bf16 -> fp16
-                        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+                        const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint32_t ch = 4u * hf + c;   // word ch -> A chunk ch (8 inputs)
-                            sts128(arow + ((ch ^ (uint32_t)(r & 7)) << 4), dequant_word(wv[c], s2));
+                        for (int c = 0; c < 8; ++c) {   // word c -> 8 inputs = 4 columns
+                            const uint4 q = dequant_word(wv[c], s2);
+                            v[4 * c] = q.x; v[4 * c + 1] = q.y; v[4 * c + 2] = q.z; v[4 * c + 3] = q.w;
                         }
                     } else {
-                        // eps = b + 8 s for the row's G groups (zero beyond G), natural group order;
-                        // this half writes chunks 4 hf .. 4 hf + 3 (groups 32 hf ..)
+                        // eps = b + 8 s for the row's G groups (zero beyond G), natural group order:
+                        // chunk c = groups 8c .. 8c + 7
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
+                        for (int c = 0; c < 8; ++c) {
                             uint32_t hv[4] = {0u, 0u, 0u, 0u};
-                            if (4 * hf + c < G / 8) {
-                                const uint32_t sw[4] = {es[c].x, es[c].y, es[c].z, es[c].w};
-                                const uint32_t bw[4] = {eb[c].x, eb[c].y, eb[c].z, eb[c].w};
+                            if (c < G / 8) {
+                                const uint4 es = __ldg(srow + c), eb = __ldg(brow + c);
+                                const uint32_t sw[4] = {es.x, es.y, es.z, es.w};
+                                const uint32_t bw[4] = {eb.x, eb.y, eb.z, eb.w};
 #pragma unroll
                                 for (int q = 0; q < 4; ++q) {
                                     const float e0 = fmaf(8.f, __uint_as_float(sw[q] << 16), __uint_as_float(bw[q] << 16));
@@ -510,19 +526,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                     hv[q] = h2u(__floats2half2_rn(e0, e1));
                                 }
                             }
-                            const uint32_t ch = 4u * hf + c;
-                            sts128(arow + ((ch ^ (uint32_t)(r & 7)) << 4), make_uint4(hv[0], hv[1], hv[2], hv[3]));
+                            v[4 * c] = hv[0]; v[4 * c + 1] = hv[1]; v[4 * c + 2] = hv[2]; v[4 * c + 3] = hv[3];
                         }
                     }
-                    fence_proxy_async();   // generic-proxy writes -> visible to the tensor core
+                    tmem_st32(tmem + lane_base + TC_A_COL + sa * 32u, v);
+                    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+                    tc_fence_before();   // the stores -> the MMA issuer, through the arrival below
                 }
-                // one arrival per warp: __syncwarp orders the lanes' reads and writes (and their
-                // proxy fences) before lane 0's release
+                // one arrival per warp, after all lanes' stores completed
                 __syncwarp();
-                if (st < n_main && (st & 3) == 3) {   // the slot's last group consumed
-                    if (lane == 0) mbar_arrive(smem_u32(&empty_p[sp_]));
-                    ++ip;
-                }
+                if (st < n_main && (st & 3) >= 2 && lane == 0)   // this set's last group of the slot
+                    mbar_arrive(smem_u32(&empty_p[sp_]));
                 if (lane == 0) mbar_arrive(smem_u32(&deq[sa]));
             }
         }
@@ -693,9 +707,9 @@ cudaError_t launch_ffn_tc(const smoe_layer_desc& D, const FfnTcWeights& W, int B
         a.wrow0 = W.g_rows; a.wrow1 = W.u_rows; a.woff1 = W.u_off;
         a.s0 = W.sg; a.b0 = W.bg; a.s1 = W.su; a.b1 = W.bu;
         a.m_tiles = F / 64;
-        if (!encode_map(&mb, xg, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, d, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_map(&mshi, sxh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gx, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_map(&mslo, sxh + (size_t)BK * Gx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gx, 64, 128,
+        if (!encode_map(&mb, xg, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, d, 64, TC_BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_map(&mshi, sxh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gx, 64, TC_BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_map(&mslo, sxh + (size_t)BK * Gx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gx, 64, TC_BOX_ROWS,
                         CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         const int grid = std::max(1, std::min(sms, E * a.m_tiles * ((BK + TC_N - 1) / TC_N)));
@@ -705,9 +719,9 @@ cudaError_t launch_ffn_tc(const smoe_layer_desc& D, const FfnTcWeights& W, int B
         a.wrow0 = d; a.wrow1 = d; a.woff1 = 0;
         a.s0 = W.sd; a.b0 = W.bd; a.s1 = W.sd; a.b1 = W.bd;
         a.m_tiles = d / TC_M;
-        if (!encode_map(&mb, h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, 2 * F, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_map(&mshi, shh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gh, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_map(&mslo, shh + nw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gh, 64, 128,
+        if (!encode_map(&mb, h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, 2 * F, 64, TC_BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_map(&mshi, shh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gh, 64, TC_BOX_ROWS, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_map(&mslo, shh + nw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, Gh, 64, TC_BOX_ROWS,
                         CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         const int grid = std::max(1, std::min(sms, E * a.m_tiles * ((BK + TC_N - 1) / TC_N)));
