@@ -54,27 +54,32 @@ constexpr int TC_H_STRIDE = 33;             // pass 0 epilogue staging: 64 h col
 constexpr int TC_H_BYTES = 64 * TC_H_STRIDE * 4;   // column-major, padded (conflict-free both ways)
 constexpr int TC_THREADS = 480;
 constexpr uint32_t TC_TMEM_COLS = 512;       // 2 accumulator buffers of TC_N columns + the A ring
-constexpr int TC_KA = 4;                     // A stages in tensor memory
-constexpr uint32_t TC_A_COL = 2 * TC_N;      // first TMEM column of the A ring (32 columns per stage)
-static_assert(TC_A_COL + 32 * TC_KA <= TC_TMEM_COLS, "tensor memory columns");
+constexpr int TC_A_GROUPS = 4;               // A ring in tensor memory: 4 groups (32 columns each)
+constexpr uint32_t TC_A_COL = 2 * TC_N;      // first TMEM column of the A ring
+static_assert(TC_A_COL + 32 * TC_A_GROUPS <= TC_TMEM_COLS, "tensor memory columns");
 
-// Per-pass ring shapes.  Two shared-memory rings: B slots (kB: x, or h hi + lo, or the group
-// sums of the eps stages; kNb sub-tiles each) and packed-weight slots (kP, each 4 stages of
-// 128-byte rows).  Packed slots are freed by the dequantisers once they have consumed them, so
-// the packed stream runs ahead of the MMAs; B slots are freed by the MMAs.  Shared-memory
-// bandwidth bounds the kernel: per stage the TMA writes and the MMAs read every B row once,
-// and the A operand no longer passes through shared memory at all.
+// Per-pass stage shapes.  A stage is 8 MMAs (k = 16 each) over two B sub-tiles: gate/up takes
+// two input groups per stage (x of group 2j and 2j + 1 against their own A columns), down one
+// group (h hi and h lo against the same A columns); the last stage of a tile is the eps stage
+// (S hi and S lo against eps).  Issuing 8 MMAs per pair of barrier waits and commits keeps
+// the single issuing thread ahead of the tensor core.  Two shared-memory rings: B slots (kB,
+// two sub-tiles each) and packed-weight slots (kP, each 4 groups of 128-byte rows).  Packed
+// slots are freed by the dequantisers once they have consumed them, so the packed stream runs
+// ahead of the MMAs; B slots are freed by the MMAs.  The A operand never passes through
+// shared memory.
 template <int PASS>
 struct TcCfg {
-    static constexpr int kB = PASS ? 3 : 5;
-    static constexpr int kP = PASS ? 3 : 4;
-    static constexpr int kNb = PASS ? 2 : 1;
+    static constexpr int kGps = PASS ? 1 : 2;                 // groups per main stage
+    static constexpr int kKa = TC_A_GROUPS / kGps;            // A stages in tensor memory
+    static constexpr int kB = 3;
+    static constexpr int kP = 3;
+    static constexpr int kNb = 2;
     static constexpr int kBSlot = kNb * TC_B_BYTES;
     static constexpr int kOffB = 0;
     static constexpr int kOffP = kOffB + kB * kBSlot;
     static constexpr int kOffStage = kOffP + kP * TC_P_BYTES;   // epilogue staging
     static constexpr int kSmem = kOffStage + (PASS ? 0 : TC_H_BYTES) + 1024;
-    static constexpr int kCorr = PASS ? 1 : 2;                // eps stages (pass 0: S hi, S lo)
+    static constexpr int kCorr = 1;                           // eps stage
 };
 static_assert(TcCfg<0>::kSmem <= 227 * 1024 - 7168, "pass 0 shared memory");
 static_assert(TcCfg<1>::kSmem <= 227 * 1024 - 7168, "pass 1 shared memory");
@@ -297,7 +302,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     using C = TcCfg<PASS>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_p[C::kP], empty_p[C::kP], full_b[C::kB], empty_b[C::kB];
-    __shared__ __align__(8) uint64_t deq[TC_KA], empty_a[TC_KA];
+    __shared__ __align__(8) uint64_t deq[C::kKa], empty_a[C::kKa];
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int pref[kMaxExperts + 1];
@@ -308,8 +313,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int G = a.kdim / kGroup;     // <= 64, a multiple of 8
-    const int n_main = G;              // one stage per group
+    const int n_main = G / C::kGps;    // main stages
     const int n_st = n_main + C::kCorr;
+    constexpr int kSps = 4 / C::kGps;  // main stages per packed slot
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kP; ++s) {
@@ -320,7 +326,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_init(smem_u32(&full_b[s]), 1);
             mbar_init(smem_u32(&empty_b[s]), 1);     // tcgen05.commit of the stage's MMAs
         }
-        for (int s = 0; s < TC_KA; ++s) {
+        for (int s = 0; s < C::kKa; ++s) {
             mbar_init(smem_u32(&deq[s]), 4);         // one arrival per warp of the stage's dequantiser set
             mbar_init(smem_u32(&empty_a[s]), 1);
         }
@@ -356,7 +362,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint32_t ip = 0;
             for (int t = blockIdx.x; t < n_items && !poisoned; t += gridDim.x) {
                 const Item I = decode_item(a, pref, t);
-                for (int st = 0; st < n_main; st += 4, ++ip) {   // one slot per 4 groups
+                for (int st = 0; st < G; st += 4, ++ip) {   // one slot per 4 groups
                     const uint32_t s = ip % C::kP;
                     if (ip >= (uint32_t)C::kP) fail(mbar_wait(smem_u32(&empty_p[s]), ((ip / C::kP) - 1) & 1u));
                     if (poisoned) break;
@@ -393,11 +399,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         for (int bx = 0; bx < boxes; ++bx) {
                             const int y = tok0 + bx * TC_BOX_ROWS;
                             const uint32_t d = dst + bx * TC_BOX_BYTES;
-                            if (st < n_main)   // x, or h hi (sub 0) and h lo (sub 1)
-                                tma_load_2d(d, &map_b, (sub ? a.F : 0) + st * 64, y, bar);
-                            else if (PASS == 0)   // eps stages: S hi, then S lo
-                                tma_load_2d(d, st == n_main ? &map_shi : &map_slo, 0, y, bar);
-                            else
+                            if (st < n_main)   // x of groups 2st, 2st+1, or h hi (sub 0) and h lo (sub 1)
+                                tma_load_2d(d, &map_b, PASS ? (sub ? a.F : 0) + st * 64 : (2 * st + sub) * 64, y, bar);
+                            else   // eps stage: S hi, S lo
                                 tma_load_2d(d, sub ? &map_slo : &map_shi, 0, y, bar);
                         }
                     }
@@ -416,12 +420,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (tile >= 2 && !poisoned) fail(mbar_wait(smem_u32(&acc_empty[buf]), ((tile >> 1) - 1) & 1u));
                 tc_fence_after();
                 for (int st = 0; st < n_st; ++st, ++it) {
-                    const uint32_t s = it % C::kB, sa = it % TC_KA;
-                    if (!poisoned) fail(mbar_wait(smem_u32(&deq[sa]), (it / TC_KA) & 1u));
+                    const uint32_t s = it % C::kB, sa = it % C::kKa;
+                    if (!poisoned) fail(mbar_wait(smem_u32(&deq[sa]), (it / C::kKa) & 1u));
                     if (!poisoned) fail(mbar_wait(smem_u32(&full_b[s]), (it / C::kB) & 1u));
                     if (poisoned) continue;
                     tc_fence_after();
-                    const uint32_t a_tmem = tmem + TC_A_COL + sa * 32u;
+                    const uint32_t a_tmem = tmem + TC_A_COL + sa * 32u * C::kGps;
+                    const bool two = PASS == 0 && st < n_main;   // sub-tile b against A group b
                     const uint32_t bbuf = sbase + C::kOffB + s * C::kBSlot;
                     const uint32_t d_tmem = tmem + buf * TC_N;
 #pragma unroll
@@ -429,7 +434,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
                         for (int b = 0; b < C::kNb; ++b) {
                             const uint64_t bd = sw128_desc(bbuf + b * TC_B_BYTES + kk * 32);
-                            umma_f16_ta(d_tmem, a_tmem + kk * 8u, bd, idesc, (st > 0 || kk > 0 || b > 0) ? 1u : 0u);
+                            umma_f16_ta(d_tmem, a_tmem + (two ? 32u * b : 0u) + kk * 8u, bd, idesc,
+                                        (st > 0 || kk > 0 || b > 0) ? 1u : 0u);
                         }
                     }
                     umma_commit(smem_u32(&empty_b[s]));    // B slot free once these MMAs finish
@@ -443,11 +449,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // Two sets of 4 warps take alternate A stages (set = stage parity), 128 threads per
         // stage, one A row each.  A warp reaches only its own quarter of the TMEM lanes
         // (warp % 4), so thread -> row r = 32 (warp % 4) + lane; it writes the row's 64 weights
-        // of the stage (32 TMEM columns).
+        // of each group of the stage (32 TMEM columns per group).
         const int r = 32 * (warp & 3) + lane;
         const uint32_t set = (uint32_t)(warp - 2) >> 2;
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        uint32_t it = 0, ip = 0;   // stages (A ring), packed slots (4 main stages each)
+        uint32_t it = 0, ip = 0;   // stages (A ring), packed slots (4 groups each)
         for (int ti = blockIdx.x; ti < n_items; ti += gridDim.x) {
             const Item I = decode_item(a, pref, ti);
             // source row of A row r
@@ -469,48 +475,63 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             const uint4* srow = reinterpret_cast<const uint4*>(sp + src * G);   // 8 bf16 per uint4
             const uint4* brow = reinterpret_cast<const uint4*>(bp + src * G);
-            uint4 scl = __ldg(srow), scl_next = n_main > 8 ? __ldg(srow + 1) : make_uint4(0, 0, 0, 0);
+            uint4 scl = __ldg(srow), scl_next = G > 8 ? __ldg(srow + 1) : make_uint4(0, 0, 0, 0);
             for (int st = 0; st < n_st; ++st, ++it) {
-                const uint32_t sa = it % TC_KA;
-                if (st < n_main && (st & 7) == 0 && st > 0) {
+                const uint32_t sa = it % C::kKa;
+                const int g0 = st * C::kGps;              // first group of a main stage
+                if (st < n_main && (g0 & 7) == 0 && g0 > 0) {   // scales of groups g0 .. g0 + 7
                     scl = scl_next;
-                    if (st + 8 < n_main) scl_next = __ldg(srow + (st >> 3) + 1);
+                    if (g0 + 8 < G) scl_next = __ldg(srow + (g0 >> 3) + 1);
                 }
                 const uint32_t ipc = ip;                  // packed slot of this stage
                 const uint32_t sp_ = ipc % C::kP;
-                if (st < n_main && (st & 3) == 3) ++ip;   // every thread tracks the packed slots
+                if (st < n_main && st % kSps == kSps - 1) ++ip;   // every thread tracks the packed slots
                 if ((it & 1u) != set) continue;           // the other set's stage
-                // main stage: the row's 8 packed words of group st % 4 (chunks 2q, 2q+1 of the
-                // 128-byte row, swizzled by row & 7), read before the A stage is waited for
-                uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
+                // main stage: per group g the row's 8 packed words (chunks 2q, 2q+1 of the 128-byte
+                // row, q = g % 4, swizzled by row & 7), read before the A stage is waited for
+                uint4 w[C::kGps][2];
+#pragma unroll
+                for (int gi = 0; gi < C::kGps; ++gi) w[gi][0] = w[gi][1] = make_uint4(0, 0, 0, 0);
                 if (st < n_main) {
                     if (!poisoned) fail(mbar_wait(smem_u32(&full_p[sp_]), (ipc / C::kP) & 1u));
                     if (!poisoned) {
                         const uint32_t pk = sbase + C::kOffP + sp_ * TC_P_BYTES + prow * 128u;
-                        const uint32_t q2 = (uint32_t)(st & 3) * 2u;
-                        w0 = lds128(pk + ((q2 ^ (prow & 7u)) << 4));
-                        w1 = lds128(pk + (((q2 + 1u) ^ (prow & 7u)) << 4));
+#pragma unroll
+                        for (int gi = 0; gi < C::kGps; ++gi) {
+                            const uint32_t q2 = (uint32_t)((g0 + gi) & 3) * 2u;
+                            w[gi][0] = lds128(pk + ((q2 ^ (prow & 7u)) << 4));
+                            w[gi][1] = lds128(pk + (((q2 + 1u) ^ (prow & 7u)) << 4));
+                        }
                     }
                 }
-                if (it >= (uint32_t)TC_KA && !poisoned) fail(mbar_wait(smem_u32(&empty_a[sa]), ((it / TC_KA) - 1) & 1u));
+                if (it >= (uint32_t)C::kKa && !poisoned)
+                    fail(mbar_wait(smem_u32(&empty_a[sa]), ((it / C::kKa) - 1) & 1u));
                 // tcgen05.st is warp-collective: the warp takes one decision
                 const bool skip = __any_sync(0xffffffffu, poisoned);
                 if (!skip) {
                     tc_fence_after();   // the MMAs that read this stage before (commit) -> the stores
-                    uint32_t v[32];
+                    const uint32_t acol = tmem + lane_base + TC_A_COL + sa * 32u * C::kGps;
                     if (st < n_main) {
-                        const uint32_t sw = (&scl.x)[(st & 7) >> 1];
-                        const float sf = __uint_as_float((st & 1) ? (sw & 0xFFFF0000u) : (sw << 16));
-                        const __half2 s2 = __float2half2_rn(sf);   // exact: bf16 -> fp16
-                        const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {   // word c -> 8 inputs = 4 columns
-                            const uint4 q = dequant_word(wv[c], s2);
-                            v[4 * c] = q.x; v[4 * c + 1] = q.y; v[4 * c + 2] = q.z; v[4 * c + 3] = q.w;
+                        for (int gi = 0; gi < C::kGps; ++gi) {   // group g0 + gi -> 32 columns
+                            const int g = g0 + gi;
+                            const uint32_t sw = (&scl.x)[(g & 7) >> 1];
+                            const float sf = __uint_as_float((g & 1) ? (sw & 0xFFFF0000u) : (sw << 16));
+                            const __half2 s2 = __float2half2_rn(sf);   // exact: bf16 -> fp16
+                            const uint32_t wv[8] = {w[gi][0].x, w[gi][0].y, w[gi][0].z, w[gi][0].w,
+                                                    w[gi][1].x, w[gi][1].y, w[gi][1].z, w[gi][1].w};
+                            uint32_t v[32];
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {   // word c -> 8 inputs = 4 columns
+                                const uint4 q = dequant_word(wv[c], s2);
+                                v[4 * c] = q.x; v[4 * c + 1] = q.y; v[4 * c + 2] = q.z; v[4 * c + 3] = q.w;
+                            }
+                            tmem_st32(acol + 32u * gi, v);
                         }
                     } else {
                         // eps = b + 8 s for the row's G groups (zero beyond G), natural group order:
                         // chunk c = groups 8c .. 8c + 7
+                        uint32_t v[32];
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
                             uint32_t hv[4] = {0u, 0u, 0u, 0u};
@@ -528,14 +549,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             }
                             v[4 * c] = hv[0]; v[4 * c + 1] = hv[1]; v[4 * c + 2] = hv[2]; v[4 * c + 3] = hv[3];
                         }
+                        tmem_st32(acol, v);
                     }
-                    tmem_st32(tmem + lane_base + TC_A_COL + sa * 32u, v);
                     asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
                     tc_fence_before();   // the stores -> the MMA issuer, through the arrival below
                 }
                 // one arrival per warp, after all lanes' stores completed
                 __syncwarp();
-                if (st < n_main && (st & 3) >= 2 && lane == 0)   // this set's last group of the slot
+                if (st < n_main && st % kSps >= kSps - 2 && lane == 0)   // this set's last stage of the slot
                     mbar_arrive(smem_u32(&empty_p[sp_]));
                 if (lane == 0) mbar_arrive(smem_u32(&deq[sa]));
             }
