@@ -277,14 +277,23 @@ struct Tile {
 // g+8 of each m-tile ([m][row], 4 groups each); sums: the stage's activation group sums.
 // Per group: acc += (scale * 2^24) * C + bias * S, C the exact mma result in units of 2^-24
 // and S the tokens' group sums.
-template <int NT, bool LO>
+// PK (with LO, NT = 1, at most 4 tokens): the hi and lo terms share one 8-column n-tile,
+// columns 0-3 the hi terms of tokens 0-3 and columns 4-7 their lo terms, so each k-step is
+// one mma instead of two.  The lo columns get no bias term (S = 0 there: the group sum
+// already covers hi + lo); the caller adds column j + 4 into column j at the end.
+template <int NT, bool LO, bool PK>
 __device__ __forceinline__ void consume_stage(float (&acc)[2][NT][4], uint32_t wb0, uint32_t wb1, uint32_t xs,
                                               const uint2 (&sc)[2][2], const uint2 (&bi)[2][2], uint32_t sums,
                                               int g, int c) {
-    constexpr int NB = LO ? 2 : 1;   // activation terms per input
+    static_assert(!PK || (LO && NT == 1), "packed hi/lo columns: down pass, one n-tile");
+    constexpr int NB = (LO && !PK) ? 2 : 1;   // activation terms per input (separate n-tiles)
     float4 S[NT][2];                 // group sums of tokens 2c and 2c+1 of each n-tile, 4 groups
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
+        if (PK && c >= 2) {   // lo columns
+            S[nt][0] = S[nt][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            continue;
+        }
         const uint4 v0 = lds_u4(sums + (uint32_t)(nt * 8 + 2 * c) * 16u);
         const uint4 v1 = lds_u4(sums + (uint32_t)(nt * 8 + 2 * c + 1) * 16u);
         S[nt][0] = make_float4(__uint_as_float(v0.x), __uint_as_float(v0.y), __uint_as_float(v0.z),
@@ -297,12 +306,16 @@ __device__ __forceinline__ void consume_stage(float (&acc)[2][NT][4], uint32_t w
         uint32_t bf[NT][NB][8];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const int r = nt * 8 + g;
+            // B row g of the n-tile: token row r of box hl; packed: token g & 3 of the hi (g < 4)
+            // or lo (g >= 4) boxes.  The 128-byte swizzle XORs chunks with the row's low bits.
+            const int r = PK ? (g & 3) : nt * 8 + g;
+            const int sw = r & 7;
 #pragma unroll
             for (int hl = 0; hl < NB; ++hl) {
-                const uint32_t rb = xs + (hl * 4 + q) * kXBoxBytes + r * 128;
-                const uint4 v0 = lds_u4(rb + (((2 * c) ^ g) << 4));
-                const uint4 v1 = lds_u4(rb + (((2 * c + 1) ^ g) << 4));
+                const int box = PK ? (g >> 2) * 4 + q : hl * 4 + q;
+                const uint32_t rb = xs + box * kXBoxBytes + r * 128;
+                const uint4 v0 = lds_u4(rb + (((2 * c) ^ sw) << 4));
+                const uint4 v1 = lds_u4(rb + (((2 * c + 1) ^ sw) << 4));
                 bf[nt][hl][0] = v0.x; bf[nt][hl][1] = v0.y; bf[nt][hl][2] = v0.z; bf[nt][hl][3] = v0.w;
                 bf[nt][hl][4] = v1.x; bf[nt][hl][5] = v1.y; bf[nt][hl][6] = v1.z; bf[nt][hl][7] = v1.w;
             }
@@ -381,7 +394,7 @@ __device__ __forceinline__ bool mailbox_post(Mailbox& M, int uu) {
 // posts the tile to the publisher, which makes them visible device-wide and counts the tile
 // for the expert's down tiles.  Publishing from a warp of its own keeps the fence's wait for
 // outstanding stores off the consumers.
-template <int NT, int PASS, int MODE>
+template <int NT, int PASS, int MODE, bool PK = false>
 __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, uint32_t& it, bool& poisoned,
                                               const Tile& T, int pc, int n, int warp, int lane, float* red,
                                               int done_uu, Mailbox& M) {
@@ -444,7 +457,7 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
         bi[0][1] = lds_u2(tb + (uint32_t)(lrow0 + g + 8) * rs);
         bi[1][0] = lds_u2(tb + (uint32_t)(lrow1 + g) * rs);
         bi[1][1] = lds_u2(tb + (uint32_t)(lrow1 + g + 8) * rs);
-        consume_stage<NT, PASS == 1>(acc, base + wrow_off0, base + wrow_off1, base + C::kXOff, sc, bi,
+        consume_stage<NT, PASS == 1, PK>(acc, base + wrow_off0, base + wrow_off1, base + C::kXOff, sc, bi,
                                      base + C::kSumOff, g, c);
         __syncwarp();   // the warp's reads of the slot, then one arrival for the warp
         if (lane == 0) mbar_arrive(R.empty + 8 * slot);
@@ -510,6 +523,12 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
         // the fence makes them visible device-wide before the count
         if (done_uu >= 0 && tid == 0 && !mailbox_post(M, done_uu)) atomicOr(a.status, SMOE_FAULT_TIMEOUT);
     } else {
+        if (PK) {   // lo columns 4-7 (lanes c = 2, 3) into hi columns 0-3 (lanes c = 0, 1)
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[m][0][i] += __shfl_xor_sync(0xffffffffu, acc[m][0][i], 2);
+        }
 #pragma unroll
         for (int m = 0; m < 2; ++m)
 #pragma unroll
@@ -819,7 +838,10 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
         }
         if constexpr (MODE != kGateUp) {
             if (!gate_up) {
-                if (n <= 8) consume_chunk<1, 1, MODE>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
+                if (n <= 4)
+                    consume_chunk<1, 1, MODE, true>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
+                else if (n <= 8)
+                    consume_chunk<1, 1, MODE>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
                 else consume_chunk<2, 1, MODE>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
             }
         }

@@ -86,7 +86,7 @@ struct FfnTcWeights {
 };
 
 // Experts with at least this many list entries take the tcgen05 path (when the shape allows).
-constexpr int kTcMinTokens = 64;
+constexpr int kTcMinTokens = 32;
 bool tc_path_supported(const smoe_layer_desc& D);
 cudaError_t launch_ffn_tc(const smoe_layer_desc& D, const FfnTcWeights& W, int B, int pass,
                           const int32_t* union_ids, const int32_t* n_union, const int32_t* offsets,

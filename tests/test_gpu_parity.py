@@ -245,8 +245,8 @@ def test_hot_experts_many_tokens_per_expert():
 
 @pytest.mark.parametrize("layout", ["separate", "fused"])
 def test_tensor_core_path_many_tokens_per_expert(layout):
-    """512 tokens over 16 experts (top-4): every expert has ~128 entries and runs on the
-    tcgen05 path (d and ffn_dim multiples of 512, B >= 256)."""
+    """512 tokens over 16 experts (top-4): every expert has ~128 entries (>= 32) and runs on
+    the tcgen05 path (d and ffn_dim multiples of 512, B >= 256)."""
     w = W.scaled(W.WORKLOADS["toy"], ffn_dim=512, tokens=512, layout=layout)
     c = Case(w)
     out, idx, _ = c.run_layer()
@@ -265,7 +265,7 @@ def test_tensor_core_and_small_paths_mixed():
     o64, oidx, _, _ = c.oracle_layer()
     assert np.array_equal(idx.numpy(), oidx)
     counts = np.bincount(oidx.ravel(), minlength=w.num_experts)
-    assert counts.max() >= 64 and (counts[counts > 0] < 64).any()
+    assert counts.max() >= 32 and (counts[counts > 0] < 32).any()
     check_outputs(out.numpy(), o64, c.x.float().numpy())
 
 
