@@ -194,6 +194,9 @@ def run_gpu(args, w, world, rank, local):
     xb = torch.empty(B, d, dtype=torch.int16, device=dev)
     idx = torch.empty(B, K, dtype=torch.int32, device=dev)
     wt = torch.empty(B, K, dtype=torch.float32, device=dev)
+    # workloads with a ranked router: ranks K..K+spec-1 (ids and probabilities) every layer
+    spec_idx = torch.empty(B, w.spec, dtype=torch.int32, device=dev) if w.spec else None
+    spec_p = torch.empty(B, w.spec, dtype=torch.float32, device=dev) if w.spec else None
     stream = torch.cuda.current_stream()
     launches_per_layer = (1 if w.chained else 0) + 2 + 1 + 4
 
@@ -206,7 +209,10 @@ def run_gpu(args, w, world, rank, local):
                 xl = xb
             else:
                 xl = x_dev
-            smoe.smoe_route(desc, xl, ly["gate"], ly["bias"], idx, wt, ws)
+            if w.spec:
+                smoe.smoe_route_ranked(desc, xl, ly["gate"], ly["bias"], idx, wt, spec_idx, spec_p, ws)
+            else:
+                smoe.smoe_route(desc, xl, ly["gate"], ly["bias"], idx, wt, ws)
             smoe.smoe_expert_union(desc, idx, ly["uid"], ly["nu"], ly["off"], ly["tl"], ly["sl"], ws)
             if ev is not None:
                 ev[l][0].record(cur)
@@ -342,6 +348,7 @@ def run_gpu(args, w, world, rank, local):
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
         "config": {"workload": w.name, "tokens": B, "layers": L, "d_model": d, "experts": E, "top_k": K,
+                   "spec_ranks": w.spec,
                    "ffn_dim": F, "layout": w.layout, "weights": "4-bit affine g64, bf16 scales/biases",
                    "l2": f"inputs larger than L2: {L * E * eb / 1e9:.1f} GB of expert weights per step",
                    "parallelism": f"replicas x{world}",

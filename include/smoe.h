@@ -119,6 +119,21 @@ SMOE_API smoe_status smoe_route(const smoe_layer_desc* desc, const uint16_t* x, 
                        const float* gate_bias, int32_t B, int32_t* topk_idx, float* topk_w,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* Step 1 with the ranking continued past top_k (page "Data Flow", "Serial Step Trace": the
+ * exact gate matvec yields a ranked top-(8 + spec); the ranks beyond 8 are the bets
+ * prefetched for the next token).  topk_idx / topk_w as smoe_route (bit-identical), plus
+ *   n_spec   number of further ranks, 0 <= n_spec, top_k + n_spec <= min(num_experts, 32)
+ *   spec_idx int32 [B, n_spec] out: the experts of ranks top_k .. top_k + n_spec - 1, in
+ *            rank order (same ordering rule as topk_idx)
+ *   spec_p   fp32 [B, n_spec] out, or NULL: their probabilities under the softmax over all
+ *            num_experts logits (not renormalised)
+ * n_spec == 0 is smoe_route.  Errors as smoe_route; SMOE_ERR_INVALID_ARG for an n_spec out
+ * of range or a NULL spec_idx with n_spec > 0. */
+SMOE_API smoe_status smoe_route_ranked(const smoe_layer_desc* desc, const uint16_t* x, const float* gate_w,
+                       const float* gate_bias, int32_t B, int32_t n_spec, int32_t* topk_idx,
+                       float* topk_w, int32_t* spec_idx, float* spec_p, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
 /* Step 2, the expert union of a chunk.
  *   topk_idx   int32 [B, top_k] in
  *   union_ids  int32 [num_experts] out: ascending routed expert ids, first n_union valid

@@ -200,6 +200,26 @@ smoe_status smoe_route(const smoe_layer_desc* desc, const uint16_t* x, const flo
                                     ws_ptr<float>(workspace, L.logits), static_cast<cudaStream_t>(stream)));
 }
 
+smoe_status smoe_route_ranked(const smoe_layer_desc* desc, const uint16_t* x, const float* gate_w,
+                              const float* gate_bias, int32_t B, int32_t n_spec, int32_t* topk_idx, float* topk_w,
+                              int32_t* spec_idx, float* spec_p, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+    smoe_status st = check_desc(desc);
+    if (st != SMOE_OK) return st;
+    if (B < 0 || n_spec < 0) return SMOE_ERR_INVALID_ARG;
+    const int ranks = desc->top_k + n_spec;
+    if (ranks > desc->num_experts || ranks > kMaxRanks) return SMOE_ERR_INVALID_ARG;
+    if (n_spec > 0 && !spec_idx) return SMOE_ERR_INVALID_ARG;
+    if (B == 0) return SMOE_OK;
+    if (!x || !gate_w || !topk_idx || !topk_w) return SMOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(gate_w)) return SMOE_ERR_UNSUPPORTED;
+    WsLayout L;
+    if ((st = check_ws(*desc, B, workspace, workspace_bytes, &L)) != SMOE_OK) return st;
+    return cuda_status(launch_route(*desc, x, gate_w, gate_bias, B, topk_idx, topk_w,
+                                    ws_ptr<float>(workspace, L.logits), static_cast<cudaStream_t>(stream), 0,
+                                    n_spec, n_spec > 0 ? spec_idx : nullptr, n_spec > 0 ? spec_p : nullptr));
+}
+
 smoe_status smoe_expert_union(const smoe_layer_desc* desc, const int32_t* topk_idx, int32_t B, int32_t* union_ids,
                               int32_t* n_union, int32_t* offsets, int32_t* token_list, int32_t* slot_list,
                               void* workspace, size_t workspace_bytes, void* stream) {

@@ -206,12 +206,17 @@ __global__ void __launch_bounds__(256) gate_logits_staged_kernel(const uint16_t*
 int tile_tokens(int B) { return B <= 64 ? 8 : 64; }
 
 // One CTA per token.  Thread e sums expert e's split-K partials in split order (all loads
-// issued before the sum) and adds the bias; warp 0 then takes K rounds of a warp arg-max
-// (lane l holds experts l, l+32, ...; ties -> lower expert id) and the softmax weights.
+// issued before the sum) and adds the bias; warp 0 then takes K + n_spec rounds of a warp
+// arg-max (lane l holds experts l, l+32, ...; ties -> lower expert id): ranks 0..K-1 are the
+// routing with their softmax weights, ranks K..K+n_spec-1 the ranked continuation (page
+// "Data Flow", "Serial Step Trace": the gate matvec ranks top-(8+spec); ranks beyond 8 are
+// the bets for the next token) with their full-softmax probabilities.
 __global__ void __launch_bounds__(kMaxExperts) topk_kernel(const float* __restrict__ partial, int splits,
                                                            const float* __restrict__ bias, int B, int E, int K,
                                                            int norm, int32_t* __restrict__ idx_out,
-                                                           float* __restrict__ w_out) {
+                                                           float* __restrict__ w_out, int n_spec,
+                                                           int32_t* __restrict__ spec_idx,
+                                                           float* __restrict__ spec_p) {
     __shared__ float logit[kMaxExperts];
     const int t = blockIdx.x;
     const int e = threadIdx.x;
@@ -246,9 +251,9 @@ __global__ void __launch_bounds__(kMaxExperts) topk_kernel(const float* __restri
         if (live[i]) mx = fmaxf(mx, v[i]);
 #pragma unroll
     for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    // full softmax denominator (only needed without norm_topk_prob)
+    // full softmax denominator (without norm_topk_prob, and for the ranked continuation)
     float z_all = 0.f;
-    if (!norm) {
+    if (!norm || spec_p) {
 #pragma unroll
         for (int i = 0; i < PER; ++i)
             if (live[i]) z_all += expf(v[i] - mx);
@@ -257,7 +262,8 @@ __global__ void __launch_bounds__(kMaxExperts) topk_kernel(const float* __restri
     }
     float sel_v = 0.f;   // lane k keeps the k-th selection
     int sel_i = 0;
-    for (int k = 0; k < K; ++k) {
+    const int ranks = K + n_spec;   // <= 32
+    for (int k = 0; k < ranks; ++k) {
         float bv = -INFINITY;
         int bi = 0x7fffffff;
 #pragma unroll
@@ -278,8 +284,8 @@ __global__ void __launch_bounds__(kMaxExperts) topk_kernel(const float* __restri
                 if (i == (bi >> 5)) live[i] = false;
         }
     }
-    float p = (lane < K) ? expf(sel_v - mx) : 0.f;
-    float z = p;
+    const float p = (lane < ranks) ? expf(sel_v - mx) : 0.f;
+    float z = (lane < K) ? p : 0.f;
     if (norm) {
 #pragma unroll
         for (int off = 16; off; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
@@ -289,6 +295,9 @@ __global__ void __launch_bounds__(kMaxExperts) topk_kernel(const float* __restri
     if (lane < K) {
         idx_out[(size_t)t * K + lane] = sel_i;
         w_out[(size_t)t * K + lane] = p / z;
+    } else if (lane < ranks) {
+        spec_idx[(size_t)t * n_spec + (lane - K)] = sel_i;
+        if (spec_p) spec_p[(size_t)t * n_spec + (lane - K)] = p / z_all;
     }
 }
 
@@ -308,7 +317,7 @@ int route_splits(int B, int E, int d) {
 
 cudaError_t launch_route(const smoe_layer_desc& D, const uint16_t* x, const float* gate_w, const float* gate_bias,
                          int B, int32_t* topk_idx, float* topk_w, float* logits_ws, cudaStream_t stream,
-                         int split_cap) {
+                         int split_cap, int n_spec, int32_t* spec_idx, float* spec_p) {
     const int E = D.num_experts, d = D.d_model, K = D.top_k;
     int S = route_splits(B, E, d);
     while (split_cap > 0 && S > split_cap) S >>= 1;
@@ -322,7 +331,8 @@ cudaError_t launch_route(const smoe_layer_desc& D, const uint16_t* x, const floa
         gate_logits_staged_kernel<8, 4><<<grid, 256, smem, stream>>>(x, gate_w, B, E, d, kchunk, logits_ws);
     }
     const int threads = (E + 31) / 32 * 32;
-    topk_kernel<<<B, threads, 0, stream>>>(logits_ws, S, gate_bias, B, E, K, D.norm_topk_prob, topk_idx, topk_w);
+    topk_kernel<<<B, threads, 0, stream>>>(logits_ws, S, gate_bias, B, E, K, D.norm_topk_prob, topk_idx, topk_w,
+                                           n_spec, spec_idx, spec_p);
     return cudaGetLastError();
 }
 

@@ -50,9 +50,13 @@ inline T* ws_ptr(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast
 // ----------------------------------------------------------------------------- launchers
 // Each returns cudaGetLastError() after enqueueing its kernel(s) on `stream`.
 // split_cap > 0 limits the number of split-K partials (callers with a fixed scratch size).
+// n_spec > 0: also the ranks K..K+n_spec-1 (ids into spec_idx [B, n_spec], full-softmax
+// probabilities into spec_p unless NULL); K + n_spec <= kMaxRanks.
+constexpr int kMaxRanks = 32;
 cudaError_t launch_route(const smoe_layer_desc& D, const uint16_t* x, const float* gate_w,
                          const float* gate_bias, int B, int32_t* topk_idx, float* topk_w,
-                         float* logits_ws, cudaStream_t stream, int split_cap = 0);
+                         float* logits_ws, cudaStream_t stream, int split_cap = 0, int n_spec = 0,
+                         int32_t* spec_idx = nullptr, float* spec_p = nullptr);
 
 // scratch: int32 [1 + union_chunks(B*K) * E] for batches of more than 1024 entries (may be
 // NULL for smaller ones)

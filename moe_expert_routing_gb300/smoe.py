@@ -20,7 +20,7 @@ SMOE_OK, SMOE_ERR_INVALID_ARG, SMOE_ERR_UNSUPPORTED, SMOE_ERR_WORKSPACE, SMOE_ER
 SMOE_LAYOUT_SEPARATE, SMOE_LAYOUT_FUSED_GATE_UP = 0, 1
 SMOE_FAULT_EXPERT_INDEX, SMOE_FAULT_FP16_RANGE, SMOE_FAULT_TIMEOUT, SMOE_FAULT_TOKEN_INDEX = 1, 2, 4, 8
 
-EXPORTED = ("smoe_workspace_bytes", "smoe_route", "smoe_expert_union", "smoe_moe_ffn_batch", "smoe_moe_layer",
+EXPORTED = ("smoe_workspace_bytes", "smoe_route", "smoe_route_ranked", "smoe_expert_union", "smoe_moe_ffn_batch", "smoe_moe_layer",
             "smoe_rmsnorm_bf16", "smoe_clear_device_status", "smoe_read_device_status", "smoe_status_string",
             "smoe_route_noalloc")
 
@@ -57,6 +57,7 @@ def load_library(path: str = LIB_PATH):
         L.smoe_workspace_bytes.restype = sz
         L.smoe_workspace_bytes.argtypes = [vp, i32]
         L.smoe_route.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+        L.smoe_route_ranked.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp, sz, vp]
         L.smoe_expert_union.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]
         L.smoe_moe_ffn_batch.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.smoe_moe_layer.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
@@ -67,7 +68,7 @@ def load_library(path: str = LIB_PATH):
         L.smoe_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         L.smoe_status_string.restype = ctypes.c_char_p
         L.smoe_status_string.argtypes = [ctypes.c_int]
-        for name in ("smoe_route", "smoe_expert_union", "smoe_moe_ffn_batch", "smoe_moe_layer", "smoe_rmsnorm_bf16",
+        for name in ("smoe_route", "smoe_route_ranked", "smoe_expert_union", "smoe_moe_ffn_batch", "smoe_moe_layer", "smoe_rmsnorm_bf16",
                      "smoe_clear_device_status", "smoe_read_device_status"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -140,6 +141,14 @@ def alloc_workspace(desc: LayerDesc, max_tokens: int, device="cuda") -> torch.Te
 def smoe_route(desc, x, gate_w, gate_bias, topk_idx, topk_w, ws, stream=None):
     _check(load_library().smoe_route(ctypes.byref(desc), _p(x), _p(gate_w), _p(gate_bias), x.shape[0],
                                      _p(topk_idx), _p(topk_w), _p(ws), ws.numel(), _stream(stream)), "smoe_route")
+
+
+def smoe_route_ranked(desc, x, gate_w, gate_bias, topk_idx, topk_w, spec_idx, spec_p, ws, stream=None):
+    """smoe_route plus ranks top_k .. top_k + n_spec - 1 (n_spec = spec_idx.shape[1]); spec_p may be None."""
+    n_spec = 0 if spec_idx is None else spec_idx.shape[1]
+    _check(load_library().smoe_route_ranked(ctypes.byref(desc), _p(x), _p(gate_w), _p(gate_bias), x.shape[0], n_spec,
+                                            _p(topk_idx), _p(topk_w), _p(spec_idx), _p(spec_p), _p(ws), ws.numel(),
+                                            _stream(stream)), "smoe_route_ranked")
 
 
 def smoe_route_noalloc(desc, x, gate_w, gate_bias, topk_idx, topk_w, stream=None):

@@ -112,6 +112,7 @@ class Workload:
     chained: bool = False        # RMSNorm chaining between layers
     chain_center: bool = True    # the chaining norm removes the row mean first
     seed: int = 0
+    spec: int = 0                # ranks beyond top_k exported by the router (next-token bets)
 
     @property
     def expert_bytes(self) -> int:
@@ -133,6 +134,10 @@ WORKLOADS: Dict[str, Workload] = {
     # Qwen3.5-MoE-shaped prefill: fused gate_up, 40 chained layers
     "q35_prefill64": Workload("qwen35_moe_prefill_b64_l40", 2048, 256, 8, 512, 64, 40, "fused", 0.02,
                               chained=True, seed=3),
+    # Qwen3-235B-shaped decode chain: one token through all 94 MoE layers, the router also
+    # ranking 8 more experts per layer (the next token's prefetch bets)
+    "decode_b1_l94": Workload("qwen3_235b_decode_b1_l94", 4096, 128, 8, 1536, 1, 94, "separate", 0.02,
+                              chained=True, seed=5, spec=8),
     # long skewed prompt: 4096 tokens, Zipf(1.1) logit bias, 4 chained layers
     "long4096": Workload("qwen3_235b_zipf_b4096_l4", 4096, 128, 8, 1536, 4096, 4, "separate", 0.02,
                          zipf_s=1.1, chained=True, seed=4),

@@ -10,6 +10,8 @@ Each function cites the passage it follows (page title and section):
 * ``logits``/``topk``/``route`` -- "Layer-Major Batched Prefill", "Choreography Per Chunk"
   step 5 (real router gate on the true hidden state, norm_topk_prob re-normalisation);
   "Surface Scout", "The Model Config" (``norm_topk_prob`` field)
+* ``route_ranked`` -- "Data Flow", "Serial Step Trace" (ranked top-(8 + spec), the ranks
+  beyond 8 as next-token bets)
 * ``expert_union`` -- "Layer-Major Batched Prefill", "The Inversion" (dedupe into the
   expert UNION, each union expert applied to every routed token)
 * ``expert_ffn``   -- "SSD Streaming Expert Layers", "Math Contract" (down(silu(gate(x)) * up(x)))
@@ -130,6 +132,21 @@ def route(x_bf16, gate_w, gate_bias, K: int, norm_topk_prob: int = 1):
     lg = logits(x_bf16, gate_w, gate_bias)
     idx, w64, w32 = topk(lg, K, norm_topk_prob)
     return idx, w64, w32, lg
+
+
+def route_ranked(x_bf16, gate_w, gate_bias, K: int, n_spec: int, norm_topk_prob: int = 1):
+    """Exact routing with the ranking continued: (idx, w64, spec_idx, spec_p64, logits).
+
+    Page "Data Flow", "Serial Step Trace": the exact gate matvec produces a ranked
+    top-(8 + spec); ranks 8 and beyond are the next token's prefetch bets.  idx / w64 are
+    the routing of ``route``; spec_idx holds ranks K .. K + n_spec - 1 of the same order
+    (descending logit, ties -> lower id) and spec_p64 their probabilities under the
+    softmax over all experts (not renormalised).
+    """
+    lg = logits(x_bf16, gate_w, gate_bias)
+    idx, w64, _ = topk(lg, K, norm_topk_prob)
+    full, p64, _ = topk(lg, K + n_spec, 0)
+    return idx, w64, full[:, K:].copy(), p64[:, K:].copy(), lg
 
 
 def expert_union(idx, E: int):

@@ -88,6 +88,24 @@ def test_route_argument_errors(lib):
     assert lib.smoe_route(None, None, None, None, 1, None, None, None, 0, None) == smoe.SMOE_ERR_INVALID_ARG
 
 
+def test_route_ranked_argument_errors(lib):
+    d = _desc()   # top_k 8, 128 experts: at most 24 further ranks
+    vp = ctypes.c_void_p
+
+    def call(n_spec, spec=1024, B=4, x=1024):
+        return lib.smoe_route_ranked(ctypes.byref(d), vp(x), vp(1024), None, B, n_spec, vp(1024), vp(1024),
+                                     vp(spec), None, vp(4096), 1 << 30, None)
+
+    assert call(-1) == smoe.SMOE_ERR_INVALID_ARG
+    assert call(25) == smoe.SMOE_ERR_INVALID_ARG                 # top_k + n_spec > 32
+    assert call(8, spec=0) == smoe.SMOE_ERR_INVALID_ARG          # no spec_idx buffer
+    assert call(8, B=0, x=0) == smoe.SMOE_OK                     # B == 0: no-op
+    assert call(8, x=1032) == smoe.SMOE_ERR_UNSUPPORTED
+    small = _desc(num_experts=10, top_k=4)
+    assert lib.smoe_route_ranked(ctypes.byref(small), vp(1024), vp(1024), None, 4, 7, vp(1024), vp(1024), vp(1024),
+                                 None, vp(4096), 1 << 30, None) == smoe.SMOE_ERR_INVALID_ARG   # 11 ranks > 10
+
+
 def test_layer_and_ffn_argument_errors(lib):
     d = _desc()
     vp = ctypes.c_void_p

@@ -140,6 +140,41 @@ def test_route_norm_topk_prob_off_and_k_equals_e():
         np.testing.assert_allclose(wt.cpu().numpy(), ow64, rtol=W_RTOL, atol=1e-7)
 
 
+@pytest.mark.parametrize("name,B,n_spec,norm", [("decode_b1", 1, 8, 1), ("decode_b8", 8, 8, 1),
+                                                 ("prefill64", 64, 24, 1), ("toy", 16, 12, 0), ("long4096", 512, 8, 1)])
+def test_route_ranked_parity(name, B, n_spec, norm):
+    """Ranked continuation: the routing equals smoe_route's bit for bit; the ranks K..K+N-1
+    match the oracle exactly (inputs drawn with separated logits over ranks 1..K+N+1) and
+    their full-softmax probabilities to 1e-5."""
+    _need_gpu()
+    w = W.scaled(W.WORKLOADS[name], norm_topk_prob=norm)
+    K = w.top_k
+    gate = W.gen_gate(w, 0)
+    bias = W.gen_gate_bias(w, 0)
+    x, _ = resampled_x(W.scaled(w, top_k=K + n_spec), 0, B, gate, bias)
+    desc = smoe.make_desc(w.d_model, w.num_experts, K, w.ffn_dim, w.layout, norm)
+    ws = smoe.alloc_workspace(desc, B)
+    xd, gd, bd = x.to(DEV).view(torch.int16), gate.to(DEV), None if bias is None else bias.to(DEV)
+    idx0 = torch.empty(B, K, dtype=torch.int32, device=DEV)
+    wt0 = torch.empty(B, K, dtype=torch.float32, device=DEV)
+    smoe.smoe_route(desc, xd, gd, bd, idx0, wt0, ws)
+    idx = torch.empty(B, K, dtype=torch.int32, device=DEV)
+    wt = torch.empty(B, K, dtype=torch.float32, device=DEV)
+    sidx = torch.empty(B, n_spec, dtype=torch.int32, device=DEV)
+    sp = torch.empty(B, n_spec, dtype=torch.float32, device=DEV)
+    smoe.smoe_route_ranked(desc, xd, gd, bd, idx, wt, sidx, sp, ws)
+    sidx2 = torch.empty(B, n_spec, dtype=torch.int32, device=DEV)
+    smoe.smoe_route_ranked(desc, xd, gd, bd, idx, wt, sidx2, None, ws)   # probabilities not wanted
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx0) and torch.equal(wt, wt0)
+    assert torch.equal(sidx, sidx2)
+    oi, ow64, osi, osp, _ = oracle.route_ranked(x, gate, bias, K, n_spec, norm)
+    assert np.array_equal(idx.cpu().numpy(), oi)
+    np.testing.assert_allclose(wt.cpu().numpy(), ow64, rtol=W_RTOL, atol=1e-7)
+    assert np.array_equal(sidx.cpu().numpy(), osi)
+    np.testing.assert_allclose(sp.cpu().numpy(), osp, rtol=W_RTOL, atol=1e-9)
+
+
 # ----------------------------------------------------------------------------- union
 @pytest.mark.parametrize("B,K,E", [(1, 8, 128), (16, 4, 16), (64, 8, 128), (64, 8, 256), (37, 3, 9), (4096, 8, 128),
                                    (200, 16, 16)])
@@ -381,6 +416,11 @@ def test_chain_prefill64_teacher_forced():
 
 def test_chain_qwen35_fused_teacher_forced():
     _chain("q35_prefill64", 3)
+
+
+def test_chain_decode_b1_teacher_forced():
+    """One token through the first 4 layers of the 94-layer decode chain."""
+    _chain("decode_b1_l94", 4)
 
 
 def test_chain_long_skewed_sampled_rows():

@@ -137,6 +137,36 @@ def test_route_full_k_equals_softmax_and_argsort():
         assert np.allclose(w64[t], softmax(lg[t])[order], rtol=1e-13, atol=0)
 
 
+def test_route_ranked_closed_form():
+    """Logits [3,1,2,0], K=1, three more ranks: ids [0] then [2,1,3] with the full-softmax
+    probabilities e^2/S, e/S, 1/S (S = e^3 + e + e^2 + 1); the routing itself is route's."""
+    d, E = 64, 4
+    Wg = np.zeros((E, d), np.float32)
+    Wg[:, 0] = [3.0, 1.0, 2.0, 0.0]
+    idx, w64, sidx, sp, lg = oracle.route_ranked(_one_hot_x(d), Wg, None, 1, 3, 1)
+    e = math.e
+    S = e ** 3 + e + e ** 2 + 1
+    assert idx.tolist() == [[0]] and w64[0].tolist() == [1.0]
+    assert sidx.tolist() == [[2, 1, 3]]
+    assert sp[0] == pytest.approx([e ** 2 / S, e / S, 1 / S], rel=1e-14)
+
+
+def test_route_ranked_continues_the_stable_argsort():
+    """K + n_spec = E: routing ids followed by the ranked ids are the full stable argsort of
+    the logits (ties -> lower id), and the probabilities of all ranks sum to 1."""
+    rng = np.random.default_rng(5)
+    d, E, K = 64, 12, 3
+    Wg = rng.integers(-3, 4, size=(E, d)).astype(np.float32)   # integer logits: ties occur
+    x = _bf16_bits(rng.integers(-2, 3, size=(6, d)).astype(np.float32))
+    idx, w64, sidx, sp, lg = oracle.route_ranked(x, Wg, None, K, E - K, 0)
+    for t in range(6):
+        order = np.argsort(-lg[t], kind="stable")
+        assert idx[t].tolist() + sidx[t].tolist() == order.tolist()
+        assert np.allclose(np.concatenate([w64[t], sp[t]]), softmax(lg[t])[order], rtol=1e-13, atol=0)
+        assert abs(w64[t].sum() + sp[t].sum() - 1.0) < 1e-12
+    assert any(len(set(r)) < E for r in lg.tolist())   # the case really has ties
+
+
 def test_route_bruteforce_subsets():
     """Tiny E: the chosen set maximises the summed probability over all K-subsets."""
     rng = np.random.default_rng(2)
