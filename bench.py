@@ -176,11 +176,16 @@ def run_gpu(args, w, world, rank, local):
     B, L, K, E, d, F = w.tokens, w.layers, w.top_k, w.num_experts, w.d_model, w.ffn_dim
     desc = smoe.make_desc(d, E, K, F, w.layout, w.norm_topk_prob)
 
+    # shared expert (if the workload has one): column slices, its own descriptor and workspace
+    P = w.shared_slices
+    sdesc = smoe.make_desc(d, P, P, w.shared_ffn_dim // P, w.layout, 1) if P else None
+    sws = smoe.alloc_workspace(sdesc, B, dev) if P else None
     layers = []
     for l in range(L):
         wts = W.gen_layer_weights(w, l, device=dev)
         bias = W.gen_gate_bias(w, l)
         layers.append({
+            "shared": smoe.Weights(W.gen_shared_weights(w, l, device=dev)) if P else None,
             "weights": smoe.Weights(wts), "wts": wts, "gate": W.gen_gate(w, l, device=dev).contiguous(),
             "bias": None if bias is None else bias.to(dev),
             "uid": torch.zeros(E, dtype=torch.int32, device=dev), "nu": torch.zeros(1, dtype=torch.int32, device=dev),
@@ -198,7 +203,14 @@ def run_gpu(args, w, world, rank, local):
     spec_idx = torch.empty(B, w.spec, dtype=torch.int32, device=dev) if w.spec else None
     spec_p = torch.empty(B, w.spec, dtype=torch.float32, device=dev) if w.spec else None
     stream = torch.cuda.current_stream()
-    launches_per_layer = (1 if w.chained else 0) + 2 + 1 + 4
+    # kernels per layer: glue norm, router (2), union (1, or 3 above 1024 entries), FFN (gather,
+    # two passes or the both-pass + two tensor-core passes, combine), shared expert (slice
+    # routing + FFN)
+    def ffn_kernels(b, dd, ff):
+        tc = dd % 512 == 0 and ff % 512 == 0 and dd <= 4096 and ff <= 4096 and b >= 256
+        return 5 if tc else 4
+    launches_per_layer = ((1 if w.chained else 0) + 2 + (1 if B * K <= 1024 else 3) + ffn_kernels(B, d, F) +
+                          (1 + ffn_kernels(B, d, w.shared_ffn_dim // P) if P else 0))
 
     def step(x_dev, ev=None):
         cur = torch.cuda.current_stream()   # the capture stream while a graph is captured
@@ -218,6 +230,8 @@ def run_gpu(args, w, world, rank, local):
                 ev[l][0].record(cur)
             smoe.smoe_moe_ffn_batch(desc, ly["weights"], xl, ly["uid"], ly["nu"], ly["off"], ly["tl"], ly["sl"], wt,
                                     h, ws)
+            if P:
+                smoe.smoe_shared_expert_ffn(sdesc, ly["shared"], xl, h, sws)
             if ev is not None:
                 ev[l][1].record(cur)
 
@@ -280,13 +294,13 @@ def run_gpu(args, w, world, rank, local):
     U = [int(ly["nu"].item()) for ly in layers]
     eb = w.expert_bytes
     hbm, tf_burst, tf_sus, peak_kind = _peaks()
-    ffn_bytes = [u * eb + B * d * 2 + 2 * B * d * 4 for u in U]
+    ffn_bytes = [u * eb + w.shared_bytes + B * d * 2 + 2 * B * d * 4 for u in U]
     layer_bytes = [fb + E * d * 4 for fb in ffn_bytes]
-    layer_flops = 6 * B * K * d * F + 2 * B * d * E
+    layer_flops = 6 * B * K * d * F + 6 * B * d * w.shared_ffn_dim + 2 * B * d * E
     t_roof_step = sum(max(bb / (hbm * 1e9), layer_flops / (tf_sus * 1e12)) for bb in layer_bytes)
     ffn_ms_mean = sum(ffn_ms) / len(ffn_ms)
     ffn_bytes_mean = sum(ffn_bytes) / len(ffn_bytes)
-    ffn_flops = 6 * B * K * d * F
+    ffn_flops = 6 * B * K * d * F + 6 * B * d * w.shared_ffn_dim
     # the FFN step's binding roof: union expert bytes at HBM bandwidth, or its flops at the
     # sustained tensor rate (fp16 and bf16 run at the same nominal rate)
     tensor_bound = ffn_flops / (tf_sus * 1e12) > ffn_bytes_mean / (hbm * 1e9)
@@ -348,7 +362,8 @@ def run_gpu(args, w, world, rank, local):
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
         "config": {"workload": w.name, "tokens": B, "layers": L, "d_model": d, "experts": E, "top_k": K,
-                   "spec_ranks": w.spec,
+                   "spec_ranks": w.spec, "shared_ffn_dim": w.shared_ffn_dim,
+                   "norm_topk_prob": w.norm_topk_prob,
                    "ffn_dim": F, "layout": w.layout, "weights": "4-bit affine g64, bf16 scales/biases",
                    "l2": f"inputs larger than L2: {L * E * eb / 1e9:.1f} GB of expert weights per step",
                    "parallelism": f"replicas x{world}",
@@ -357,7 +372,8 @@ def run_gpu(args, w, world, rank, local):
         "union_sizes": U,
         "step_roofline_frac": t_roof_step / (ms_step * 1e-3),
         "roofline": dict(roof, traffic=traffic if not tensor_bound else None,
-                         kernel="expert FFN step (smoe_moe_ffn_batch: gather, gate/up+SwiGLU, down, combine)"),
+                         kernel="expert FFN step (smoe_moe_ffn_batch: gather, gate/up+SwiGLU, down, combine"
+                               + (", and smoe_shared_expert_ffn)" if P else ")")),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": B * d * 2, "d2h_bytes_per_step": B * d * 4},
         "gpu_launches": launches_per_layer * L * args.steps,

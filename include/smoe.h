@@ -163,6 +163,23 @@ SMOE_API smoe_status smoe_moe_ffn_batch(const smoe_layer_desc* desc, const smoe_
                                const float* topk_w, float* residual,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/* The shared expert (page "Data Flow", "Serial Step Trace": the shared expert FFN runs on
+ * every token and residual += shared_out + routed_out; page "Surface Scout", "The Model
+ * Config": shared_expert_ffn_dim, 0 when the model has none): residual += down(silu(gate x)
+ * * up x) for all B tokens, with no routing weight.
+ * Layout: a shared expert of ffn width P * F is passed as P column slices of width F, slice
+ * p holding FFN columns pF .. pF + F - 1: desc->num_experts = desc->top_k = P (P <= 16),
+ * desc->ffn_dim = F, and the weight tensors [P, ...] of smoe_expert_weights (gate / up rows
+ * pF.., down input columns pF..; separate or fused layout as desc->layout says).  Since
+ * SwiGLU acts column by column, the sum of the slices' outputs is the whole expert's; the
+ * slices give the down projection P times the output tiles.  The call routes every token
+ * to every slice with weight 1 in the workspace (sized by smoe_workspace_bytes(desc, B)),
+ * runs steps 3 + 4 and adds the slices' outputs in slice order.  desc->norm_topk_prob is
+ * ignored.  Errors as smoe_moe_ffn_batch; SMOE_ERR_INVALID_ARG if num_experts != top_k. */
+SMOE_API smoe_status smoe_shared_expert_ffn(const smoe_layer_desc* desc, const smoe_expert_weights* weights,
+                                            const uint16_t* x, int32_t B, float* residual, void* workspace,
+                                            size_t workspace_bytes, void* stream);
+
 /* The whole MoE block (steps 1-4) for B tokens: residual += MoE(x).
  * topk_idx / topk_w may be NULL (the routing then lives in the workspace only) or device
  * buffers [B, top_k] that receive it. */

@@ -282,6 +282,30 @@ smoe_status smoe_moe_layer(const smoe_layer_desc* desc, const smoe_expert_weight
     return cuda_status(e);
 }
 
+smoe_status smoe_shared_expert_ffn(const smoe_layer_desc* desc, const smoe_expert_weights* weights, const uint16_t* x,
+                                   int32_t B, float* residual, void* workspace, size_t workspace_bytes, void* stream) {
+    smoe_status st = check_desc(desc);
+    if (st != SMOE_OK) return st;
+    if (desc->num_experts != desc->top_k || B < 0) return SMOE_ERR_INVALID_ARG;
+    if (B == 0) return SMOE_OK;
+    if (!x || !residual) return SMOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(residual)) return SMOE_ERR_UNSUPPORTED;
+    FfnPointers P{};
+    if ((st = check_weights(*desc, weights, &P)) != SMOE_OK) return st;
+    WsLayout L;
+    if ((st = check_ws(*desc, B, workspace, workspace_bytes, &L)) != SMOE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t* uid = ws_ptr<int32_t>(workspace, L.union_ids);
+    int32_t* nu = ws_ptr<int32_t>(workspace, L.n_union);
+    int32_t* off = ws_ptr<int32_t>(workspace, L.offsets);
+    int32_t* tl = ws_ptr<int32_t>(workspace, L.token_list);
+    int32_t* sl = ws_ptr<int32_t>(workspace, L.slot_list);
+    float* w = ws_ptr<float>(workspace, L.topk_w);
+    cudaError_t e = launch_all_slices(B, desc->num_experts, uid, nu, off, tl, sl, w, s);
+    if (e == cudaSuccess) e = launch_ffn(*desc, P, x, B, uid, nu, off, tl, sl, w, residual, workspace, L, s, true);
+    return cuda_status(e);
+}
+
 smoe_status smoe_rmsnorm_bf16(const float* h, float eps, int32_t center, int32_t B, int32_t d, uint16_t* x_out,
                               void* stream) {
     if (B < 0 || d <= 0 || !(eps >= 0.f) || (center != 0 && center != 1)) return SMOE_ERR_INVALID_ARG;

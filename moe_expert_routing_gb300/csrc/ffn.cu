@@ -894,7 +894,7 @@ static bool encode_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataTyp
 cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uint16_t* x, int B,
                        const int32_t* union_ids, const int32_t* n_union, const int32_t* offsets,
                        const int32_t* token_list, const int32_t* slot_list, const float* topk_w,
-                       float* residual, void* ws, const WsLayout& L, cudaStream_t stream) {
+                       float* residual, void* ws, const WsLayout& L, cudaStream_t stream, bool all_tokens) {
     const int d = D.d_model, F = D.ffn_dim, K = D.top_k, E = D.num_experts;
     const int BK = B * K;
     const int max_u = BK < E ? BK : E;
@@ -948,8 +948,9 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
                                                                           ticket, E + 2);
 
     // experts with many tokens go to the tcgen05 path; with fewer than 256 tokens in the chunk
-    // an expert rarely reaches the threshold, so the extra launches are skipped
-    const int tc_min = (tc_path_supported(D) && B >= 256) ? kTcMinTokens : 0;
+    // a routed expert rarely reaches the threshold, so the extra launches are skipped (the
+    // slices of a shared expert hold every token and take it from kTcMinTokens tokens on)
+    const int tc_min = (tc_path_supported(D) && (B >= 256 || (all_tokens && B >= kTcMinTokens))) ? kTcMinTokens : 0;
     FfnTcWeights TW{};
     TW.map_gate = W.tc_gate; TW.map_up = W.tc_up; TW.map_down = W.tc_down;
     TW.sg = W.sg; TW.bg = W.bg; TW.g_rows = W.g_rows_per_expert;

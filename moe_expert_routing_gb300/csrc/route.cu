@@ -303,24 +303,28 @@ __global__ void __launch_bounds__(kMaxExperts) topk_kernel(const float* __restri
 
 }  // namespace
 
-int route_splits(int B, int E, int d) {
+// Split-K factor of the router for B tokens: the largest divisor s of d / quantum (a split
+// keeps a multiple of 128 inputs, 8 k-steps of 16 per load batch, and for the staged
+// large-batch kernel of 256, one staged piece) with s <= cap and at most ~4 CTAs per SM.
+int route_splits_capped(int B, int E, int d, int cap) {
     const int bt = tile_tokens(B);
     const int tiles = ((B + bt - 1) / bt) * ((E + kExpertsPerCta - 1) / kExpertsPerCta);
-    const int target = 2 * 152;
-    int s = 1;
-    // a split keeps a multiple of 128 inputs (8 k-steps of 16 per load batch) and, for the
-    // staged large-batch kernel, of 256 (one staged piece)
     const int quantum = bt == 64 ? 256 : 128;
-    while (s < kMaxSplits && s * tiles < target && (d / (2 * s)) % quantum == 0) s *= 2;
-    return s;
+    const int q = d % quantum ? 1 : d / quantum;
+    const int limit = cap > 0 && cap < kMaxSplits ? cap : kMaxSplits;
+    int best = 1;
+    for (int s = 1; s <= limit && s <= q; ++s)
+        if (q % s == 0 && (s == 1 || s * tiles <= 4 * 152)) best = s;
+    return best;
 }
+
+int route_splits(int B, int E, int d) { return route_splits_capped(B, E, d, 0); }
 
 cudaError_t launch_route(const smoe_layer_desc& D, const uint16_t* x, const float* gate_w, const float* gate_bias,
                          int B, int32_t* topk_idx, float* topk_w, float* logits_ws, cudaStream_t stream,
                          int split_cap, int n_spec, int32_t* spec_idx, float* spec_p) {
     const int E = D.num_experts, d = D.d_model, K = D.top_k;
-    int S = route_splits(B, E, d);
-    while (split_cap > 0 && S > split_cap) S >>= 1;
+    const int S = route_splits_capped(B, E, d, split_cap);
     const int bt = tile_tokens(B);
     dim3 grid((B + bt - 1) / bt, (E + kExpertsPerCta - 1) / kExpertsPerCta, S);
     const int kchunk = d / S;   // a multiple of 128 (route_splits)

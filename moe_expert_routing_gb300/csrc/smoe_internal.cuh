@@ -65,6 +65,10 @@ cudaError_t launch_union(const smoe_layer_desc& D, const int32_t* topk_idx, int 
                          int32_t* n_union, int32_t* offsets, int32_t* token_list, int32_t* slot_list,
                          uint32_t* status, int32_t* scratch, cudaStream_t stream);
 
+// Every token to every one of P slices with weight 1 (the routing of a shared expert).
+cudaError_t launch_all_slices(int B, int P, int32_t* union_ids, int32_t* n_union, int32_t* offsets,
+                              int32_t* token_list, int32_t* slot_list, float* w, cudaStream_t stream);
+
 // Expert weights as the FFN kernels consume them.  The packed words are read through TMA
 // tensor maps: 2-D u32 views [rows, in/8] of each weight tensor, box 32 words (4 groups) x
 // 128 rows (gate, up) or 256 rows (down), 128-byte swizzle.  Fused gate_up: map_gate == map_up over the gate_up tensor, the up rows
@@ -97,10 +101,12 @@ cudaError_t launch_ffn_tc(const smoe_layer_desc& D, const FfnTcWeights& W, int B
                           const int32_t* token_list, const int32_t* slot_list, void* ws, const WsLayout& L,
                           int tc_min, int sms, cudaStream_t stream);
 
+// all_tokens: every expert of the call holds all B tokens (the slices of a shared expert), so
+// the tensor-core path is worth launching whenever B reaches its threshold.
 cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uint16_t* x, int B,
                        const int32_t* union_ids, const int32_t* n_union, const int32_t* offsets,
                        const int32_t* token_list, const int32_t* slot_list, const float* topk_w,
-                       float* residual, void* ws, const WsLayout& L, cudaStream_t stream);
+                       float* residual, void* ws, const WsLayout& L, cudaStream_t stream, bool all_tokens = false);
 
 cudaError_t launch_rmsnorm(const float* h, float eps, int center, int B, int d, uint16_t* x_out,
                            cudaStream_t stream);

@@ -263,9 +263,36 @@ __global__ void __launch_bounds__(kThreads) chunk_scatter_kernel(const int32_t* 
     }
 }
 
+// Routing of a shared expert stored as P slices: every token to every slice with weight 1.
+// union_ids[p] = p, offsets[p] = p B, the list of slice p = tokens 0..B-1 in order with slot
+// p, weights w[t][p] = 1.
+__global__ void __launch_bounds__(256) all_slices_kernel(int B, int P, int32_t* __restrict__ union_ids,
+                                                         int32_t* __restrict__ n_union, int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ token_list,
+                                                         int32_t* __restrict__ slot_list, float* __restrict__ w) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i <= P) offsets[i] = i * B;
+    if (i < P) union_ids[i] = i;
+    if (i == 0) *n_union = P;
+    if (i < B * P) {
+        const int p = i / B, t = i - p * B;
+        token_list[i] = t;
+        slot_list[i] = p;
+        w[(size_t)t * P + p] = 1.f;
+    }
+}
+
 }  // namespace
 
 int union_chunks(int BK) { return (BK + kThreads - 1) / kThreads; }
+
+cudaError_t launch_all_slices(int B, int P, int32_t* union_ids, int32_t* n_union, int32_t* offsets,
+                              int32_t* token_list, int32_t* slot_list, float* w, cudaStream_t stream) {
+    const int n = B * P > P + 1 ? B * P : P + 1;
+    all_slices_kernel<<<(n + 255) / 256, 256, 0, stream>>>(B, P, union_ids, n_union, offsets, token_list, slot_list,
+                                                           w);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_union(const smoe_layer_desc& D, const int32_t* topk_idx, int B, int32_t* union_ids,
                          int32_t* n_union, int32_t* offsets, int32_t* token_list, int32_t* slot_list,

@@ -21,7 +21,7 @@ SMOE_LAYOUT_SEPARATE, SMOE_LAYOUT_FUSED_GATE_UP = 0, 1
 SMOE_FAULT_EXPERT_INDEX, SMOE_FAULT_FP16_RANGE, SMOE_FAULT_TIMEOUT, SMOE_FAULT_TOKEN_INDEX = 1, 2, 4, 8
 
 EXPORTED = ("smoe_workspace_bytes", "smoe_route", "smoe_route_ranked", "smoe_expert_union", "smoe_moe_ffn_batch", "smoe_moe_layer",
-            "smoe_rmsnorm_bf16", "smoe_clear_device_status", "smoe_read_device_status", "smoe_status_string",
+            "smoe_shared_expert_ffn", "smoe_rmsnorm_bf16", "smoe_clear_device_status", "smoe_read_device_status", "smoe_status_string",
             "smoe_route_noalloc")
 
 
@@ -61,6 +61,7 @@ def load_library(path: str = LIB_PATH):
         L.smoe_expert_union.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]
         L.smoe_moe_ffn_batch.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.smoe_moe_layer.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
+        L.smoe_shared_expert_ffn.argtypes = [vp, vp, vp, i32, vp, vp, sz, vp]
         L.smoe_rmsnorm_bf16.argtypes = [vp, ctypes.c_float, i32, i32, i32, vp, vp]
         L.smoe_route_noalloc.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp]
         L.smoe_route_noalloc.restype = ctypes.c_int
@@ -68,8 +69,9 @@ def load_library(path: str = LIB_PATH):
         L.smoe_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         L.smoe_status_string.restype = ctypes.c_char_p
         L.smoe_status_string.argtypes = [ctypes.c_int]
-        for name in ("smoe_route", "smoe_route_ranked", "smoe_expert_union", "smoe_moe_ffn_batch", "smoe_moe_layer", "smoe_rmsnorm_bf16",
-                     "smoe_clear_device_status", "smoe_read_device_status"):
+        for name in ("smoe_route", "smoe_route_ranked", "smoe_expert_union", "smoe_moe_ffn_batch", "smoe_moe_layer",
+                     "smoe_shared_expert_ffn", "smoe_rmsnorm_bf16", "smoe_clear_device_status",
+                     "smoe_read_device_status"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -176,6 +178,13 @@ def smoe_moe_layer(desc, weights: Weights, x, gate_w, gate_bias, residual, ws, t
     _check(load_library().smoe_moe_layer(ctypes.byref(desc), ctypes.byref(weights.struct), _p(x), _p(gate_w),
                                          _p(gate_bias), x.shape[0], _p(residual), _p(topk_idx), _p(topk_w), _p(ws),
                                          ws.numel(), _stream(stream)), "smoe_moe_layer")
+
+
+def smoe_shared_expert_ffn(desc, weights: Weights, x, residual, ws, stream=None):
+    """residual += shared expert(x) for every row of x (weights as P column slices, see smoe.h)."""
+    _check(load_library().smoe_shared_expert_ffn(ctypes.byref(desc), ctypes.byref(weights.struct), _p(x), x.shape[0],
+                                                 _p(residual), _p(ws), ws.numel(), _stream(stream)),
+           "smoe_shared_expert_ffn")
 
 
 def smoe_rmsnorm_bf16(h, x_out, eps: float = 1e-6, center: int = 0, stream=None):

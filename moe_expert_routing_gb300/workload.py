@@ -113,6 +113,16 @@ class Workload:
     chain_center: bool = True    # the chaining norm removes the row mean first
     seed: int = 0
     spec: int = 0                # ranks beyond top_k exported by the router (next-token bets)
+    shared_ffn_dim: int = 0      # shared expert ffn width, 0 = none
+    shared_slices: int = 0       # the shared expert is stored as this many column slices
+
+    @property
+    def shared_bytes(self) -> int:
+        """Bytes of the shared expert's packed weights, scales and biases (0 without one)."""
+        if not self.shared_ffn_dim:
+            return 0
+        d, f, g = self.d_model, self.shared_ffn_dim, self.group_size
+        return 3 * (f * d // 2 + f * (d // g) * 4)
 
     @property
     def expert_bytes(self) -> int:
@@ -138,6 +148,10 @@ WORKLOADS: Dict[str, Workload] = {
     # ranking 8 more experts per layer (the next token's prefetch bets)
     "decode_b1_l94": Workload("qwen3_235b_decode_b1_l94", 4096, 128, 8, 1536, 1, 94, "separate", 0.02,
                               chained=True, seed=5, spec=8),
+    # Qwen2-MoE-shaped prefill chunk (57B-A14B layer shape): 64 experts, top-8 without
+    # norm_topk_prob, and a shared expert of ffn 20480 stored as 8 slices of 2560
+    "qwen2_prefill64": Workload("qwen2_57b_a14b_prefill_b64_l8", 3584, 64, 8, 2560, 64, 8, "separate", 0.02,
+                                norm_topk_prob=0, chained=True, seed=6, shared_ffn_dim=20480, shared_slices=8),
     # long skewed prompt: 4096 tokens, Zipf(1.1) logit bias, 4 chained layers
     "long4096": Workload("qwen3_235b_zipf_b4096_l4", 4096, 128, 8, 1536, 4096, 4, "separate", 0.02,
                          zipf_s=1.1, chained=True, seed=4),
@@ -234,6 +248,19 @@ def gen_proj(w: Workload, layer: int, proj: str, experts=None, device="cpu"):
     z = torch.sqrt(-2.0 * torch.log(u1)) * torch.cos((2.0 * math.pi) * u2)
     b = _bf16_bits(-8.0 * s.to(torch.float64) + 1e-3 * z)
     return (words.reshape(n, out, inn // 8), s.reshape(n, out, inn // g), b.reshape(n, out, inn // g))
+
+
+def shared_workload(w: Workload) -> Workload:
+    """The shared expert's slices as a workload of their own: shared_slices experts of ffn
+    width shared_ffn_dim / shared_slices, drawn from streams of their own (seed offset)."""
+    P = w.shared_slices
+    return dataclasses.replace(w, num_experts=P, top_k=P, ffn_dim=w.shared_ffn_dim // P, seed=w.seed + 0x10000,
+                               shared_ffn_dim=0, shared_slices=0, spec=0)
+
+
+def gen_shared_weights(w: Workload, layer: int, device="cpu", layout=None) -> Dict[str, torch.Tensor]:
+    """The shared expert of one layer as its column slices (tensors [P, ...], layout of w)."""
+    return gen_layer_weights(shared_workload(w), layer, device=device, layout=layout)
 
 
 def gen_layer_weights(w: Workload, layer: int, experts=None, device="cpu", layout=None) -> Dict[str, torch.Tensor]:

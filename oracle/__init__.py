@@ -19,6 +19,9 @@ Each function cites the passage it follows (page title and section):
   weights into the residual); token-major vs layer-major: "Layer-Major Batched Prefill",
   "The Inversion" and "Measured Result" (identical outputs)
 * ``rmsnorm_bf16`` -- "Data Flow", "Serial Step Trace" (RMS norm before the FFN block)
+* ``shared_dense_layer`` / ``shared_expert_ffn`` -- "Data Flow", "Serial Step Trace" (the
+  shared expert FFN on every token, residual += shared_out + routed_out); "Surface Scout",
+  "The Model Config" (shared_expert_ffn_dim)
 """
 from __future__ import annotations
 
@@ -225,6 +228,34 @@ def moe_layer(layer: Layer, x_bf16, idx, w64, residual, mode: str = "layer", thr
     if rc:
         raise ValueError(f"oracle_moe_combine rc={rc}")
     return out, out64, ys
+
+
+def shared_dense_layer(slices: Dict, d_model: int, P: int, F: int, layout: str = "separate") -> Layer:
+    """The shared expert as ONE dense expert of ffn width P * F, reassembled from its P
+    column slices (slice p = FFN columns pF .. pF + F - 1): gate / up rows of the slices
+    stacked in slice order, down input columns (packed words, scale and bias groups)
+    concatenated in slice order.  Returned in the separate layout."""
+    a = {k: _np(v, np.uint32 if k.startswith("w_") else np.uint16) for k, v in slices.items()}
+    if layout == "fused":
+        gu = {k[0]: a[f"{k}_gate_up"] for k in ("w", "s", "b")}
+        gate = {c: np.ascontiguousarray(gu[c][:, :F]) for c in gu}
+        up = {c: np.ascontiguousarray(gu[c][:, F:]) for c in gu}
+    else:
+        gate = {c: a[f"{c}_gate"] for c in ("w", "s", "b")}
+        up = {c: a[f"{c}_up"] for c in ("w", "s", "b")}
+    dense = {}
+    for c in ("w", "s", "b"):
+        dense[f"{c}_gate"] = np.ascontiguousarray(gate[c].reshape(1, P * F, -1))
+        dense[f"{c}_up"] = np.ascontiguousarray(up[c].reshape(1, P * F, -1))
+        dense[f"{c}_down"] = np.ascontiguousarray(np.concatenate(list(a[f"{c}_down"]), axis=-1)[None])
+    assert dense["w_down"].shape == (1, d_model, P * F // 8)
+    return Layer(d_model, 1, 1, P * F, dense, "separate", 1)
+
+
+def shared_expert_ffn(dense: Layer, x_bf16) -> np.ndarray:
+    """y [B, d] (double): the shared expert applied to every row of x."""
+    B = _np(x_bf16, np.uint16).shape[0]
+    return expert_ffn(dense, 0, x_bf16, list(range(B)))
 
 
 def rmsnorm_bf16(h, eps: float = 1e-6, center: bool = False) -> np.ndarray:

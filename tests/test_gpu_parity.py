@@ -304,6 +304,56 @@ def test_tensor_core_and_small_paths_mixed():
     check_outputs(out.numpy(), o64, c.x.float().numpy())
 
 
+# ----------------------------------------------------------------------------- shared expert
+@pytest.mark.parametrize("layout,B,F", [("separate", 16, 256), ("fused", 37, 256), ("separate", 512, 512)])
+def test_shared_expert_parity(layout, B, F):
+    """residual += shared expert (3 column slices) on every token: few-token path, fused
+    layout with a ragged batch, and the tcgen05 path (every slice holds B >= 256 entries)."""
+    _need_gpu()
+    P = 3
+    w = W.scaled(W.WORKLOADS["toy"], shared_ffn_dim=P * F, shared_slices=P, layout=layout, tokens=B)
+    x = W.gen_x(w, 0, B)
+    sl = W.gen_shared_weights(w, 0)
+    desc = smoe.make_desc(w.d_model, P, P, F, layout, 1)
+    ws = smoe.alloc_workspace(desc, B)
+    weights = smoe.Weights({k: v.to(DEV) for k, v in sl.items()})
+    res = x.float().to(DEV)
+    smoe.smoe_clear_device_status(ws)
+    smoe.smoe_shared_expert_ffn(desc, weights, x.to(DEV).view(torch.int16), res, ws)
+    assert smoe.smoe_read_device_status(ws) == 0
+    dense = oracle.shared_dense_layer(sl, w.d_model, P, F, layout)
+    r0 = x.float().numpy().astype(np.float64)
+    check_outputs(res.cpu().numpy(), r0 + oracle.shared_expert_ffn(dense, x), r0)
+
+
+def test_qwen2_layer_with_shared_expert():
+    """Qwen2-MoE-shaped layer: top-8 of 64 without norm_topk_prob, then the 20480-wide shared
+    expert (8 slices): residual + routed + shared against the oracle on sampled rows."""
+    w = W.WORKLOADS["qwen2_prefill64"]
+    c = Case(w, B=64)
+    P, F = w.shared_slices, w.shared_ffn_dim // w.shared_slices
+    sl = W.gen_shared_weights(w, 0, device=DEV)
+    sdesc = smoe.make_desc(w.d_model, P, P, F, w.layout, 1)
+    sws = smoe.alloc_workspace(sdesc, 64)
+    res = c.x.float().to(DEV)
+    idx = torch.empty(64, w.top_k, dtype=torch.int32, device=DEV)
+    wt = torch.empty(64, w.top_k, dtype=torch.float32, device=DEV)
+    smoe.smoe_clear_device_status(c.ws)
+    smoe.smoe_clear_device_status(sws)
+    smoe.smoe_moe_layer(c.desc, c.weights, c.x_dev(), c.gate_d, None, res, c.ws, idx, wt)
+    smoe.smoe_shared_expert_ffn(sdesc, smoe.Weights(sl), c.x_dev(), res, sws)
+    assert smoe.smoe_read_device_status(c.ws) == 0 and smoe.smoe_read_device_status(sws) == 0
+    rows = list(range(0, 64, 4))
+    o64, oidx, ow64, _ = c.oracle_layer(rows=rows)
+    assert np.array_equal(idx.cpu().numpy(), oidx)
+    np.testing.assert_allclose(wt.cpu().numpy(), ow64, rtol=W_RTOL, atol=1e-7)
+    sliced = oracle.Layer(w.d_model, P, P, F, {k: v.cpu() for k, v in sl.items()}, w.layout, 1)
+    shared = np.zeros((64, w.d_model))
+    for p in range(P):
+        shared[rows] += oracle.expert_ffn(sliced, p, c.x, rows)
+    check_outputs(res.cpu().numpy(), o64 + shared, c.x.float().numpy(), rows=rows)
+
+
 def test_top1_routing():
     w = W.scaled(W.WORKLOADS["toy"], top_k=1)
     c = Case(w)

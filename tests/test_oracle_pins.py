@@ -286,6 +286,64 @@ def test_silu_matches_library_on_random_weights():
     assert np.allclose(got, want, rtol=1e-11, atol=1e-11)
 
 
+# ------------------------------------------------------------------ shared expert (column slices)
+def _random_slices(P, F, d, seed, layout="separate"):
+    """P random column slices of a shared expert (distinct nibbles, exact bf16 scales) and
+    the dense fp64 matrices they stand for, built here by plain numpy stacking."""
+    rng = np.random.default_rng(seed)
+    qg, qu = rng.integers(0, 16, (P, F, d)), rng.integers(0, 16, (P, F, d))
+    qd = rng.integers(0, 16, (P, d, F))
+    sg, su = rng.integers(1, 64, (P, F, d // 64)) / 1024.0, rng.integers(1, 64, (P, F, d // 64)) / 1024.0
+    sd = rng.integers(1, 64, (P, d, F // 64)) / 1024.0
+    bg, bu, bd = -8 * sg + 1.0 / 256, -8 * su - 1.0 / 512, -8 * sd + 1.0 / 512
+    w = {"w_down": np.stack([_pack_rows(q) for q in qd]), "s_down": _bf16_bits(sd), "b_down": _bf16_bits(bd)}
+    g = (np.stack([_pack_rows(q) for q in qg]), _bf16_bits(sg), _bf16_bits(bg))
+    u = (np.stack([_pack_rows(q) for q in qu]), _bf16_bits(su), _bf16_bits(bu))
+    if layout == "separate":
+        w.update(w_gate=g[0], s_gate=g[1], b_gate=g[2], w_up=u[0], s_up=u[1], b_up=u[2])
+    else:
+        w.update(w_gate_up=np.concatenate([g[0], u[0]], 1), s_gate_up=np.concatenate([g[1], u[1]], 1),
+                 b_gate_up=np.concatenate([g[2], u[2]], 1))
+    deq = lambda q, s, b: np.repeat(s, 64, axis=-1) * q + np.repeat(b, 64, axis=-1)
+    Wg = np.concatenate(list(deq(qg, sg, bg)), axis=0)      # [P F, d]: slice p = rows pF..
+    Wu = np.concatenate(list(deq(qu, su, bu)), axis=0)
+    Wd = np.concatenate(list(deq(qd, sd, bd)), axis=1)      # [d, P F]: slice p = columns pF..
+    return w, (Wg, Wu, Wd)
+
+
+@pytest.mark.parametrize("layout", ["separate", "fused"])
+def test_shared_dense_matches_numpy(layout):
+    """The reassembled shared expert equals a numpy dense SwiGLU of the stacked slices."""
+    P, F, d = 3, 64, 128
+    w, (Wg, Wu, Wd) = _random_slices(P, F, d, 21, layout)
+    dense = oracle.shared_dense_layer(w, d, P, F, layout)
+    rng = np.random.default_rng(22)
+    x = _bf16_bits(rng.normal(size=(4, d)).astype(np.float32).round(2))
+    xf = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    g, v = xf @ Wg.T, xf @ Wu.T
+    want = (g * expit(g) * v) @ Wd.T
+    assert np.allclose(oracle.shared_expert_ffn(dense, x), want, rtol=1e-11, atol=1e-11)
+
+
+def test_shared_equals_weight_one_route_over_slices():
+    """SwiGLU acts column by column: the sum of the slices' outputs (each slice an expert of
+    the sliced layer, every token routed to all P with weight 1) is the dense expert."""
+    P, F, d = 4, 64, 128
+    w, _ = _random_slices(P, F, d, 23)
+    dense = oracle.shared_dense_layer(w, d, P, F)
+    sliced = oracle.Layer(d, P, P, F, w, "separate", 0)
+    rng = np.random.default_rng(24)
+    x = _bf16_bits(rng.normal(size=(5, d)).astype(np.float32).round(2))
+    res = rng.normal(size=(5, d)).astype(np.float32)
+    idx = np.tile(np.arange(P, dtype=np.int32), (5, 1))
+    _, out64, _ = oracle.moe_layer(sliced, x, idx, np.ones((5, P)), res)
+    assert np.allclose(out64 - res, oracle.shared_expert_ffn(dense, x), rtol=1e-11, atol=1e-11)
+    # a planted mistake: slices stacked in the wrong order give another expert
+    swapped = {k: (v[::-1].copy() if k.endswith("_down") else v) for k, v in w.items()}
+    bad = oracle.shared_dense_layer(swapped, d, P, F)
+    assert not np.allclose(oracle.shared_expert_ffn(bad, x), oracle.shared_expert_ffn(dense, x), rtol=1e-3)
+
+
 # ------------------------------------------------------------------ whole layer
 def _toy_case(w=None, layout=None, tokens=None):
     w = w or W.WORKLOADS["toy"]
