@@ -48,8 +48,59 @@ def _dist():
     return world, rank, local
 
 
+class NvmlClocks:
+    """SM clock and clock-event reasons sampled through NVML (ctypes, read-only queries) every
+    5 ms from a thread, while the timed region runs."""
+
+    SM = 1   # NVML_CLOCK_SM
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device):
+        import ctypes
+        import threading
+        import torch
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(torch_device)
+        bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0".encode()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle for " + bus.decode())
+        self.get_reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.ct = ctypes
+        mx = ctypes.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.SM, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+        self.sm, self.reasons, self.stop_flag = [], set(), False
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def _run(self):
+        ct = self.ct
+        clk, r = ct.c_uint(), ct.c_ulonglong()
+        while not self.stop_flag:
+            if self.lib.nvmlDeviceGetClockInfo(self.h, self.SM, ct.byref(clk)) == 0:
+                self.sm.append(float(clk.value))
+            if self.get_reasons(self.h, ct.byref(r)) == 0:
+                self.reasons.update(n for bit, n in self.REASONS.items() if r.value & bit)
+            time.sleep(0.005)
+
+    def stop(self):
+        self.stop_flag = True
+        self.thread.join()
+        if not self.sm:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"], "source": "nvml"}
+        s = sorted(self.sm)
+        return {"sm_mhz": s[len(s) // 2], "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(s), "source": "nvml, 5 ms"}
+
+
 class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region (fallback
+    when NVML cannot be loaded)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -91,12 +142,21 @@ class Clocks:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         sm.sort()
-        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(smax), "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(smax), "reasons": sorted(reasons), "samples": len(sm),
+                "source": "nvidia-smi, 200 ms"}
+
+
+def start_clocks(torch_device, gpu_index: int):
+    try:
+        return NvmlClocks(torch_device)
+    except Exception:
+        return Clocks(gpu_index)
 
 
 def _traffic_from_profile(kernel_src: str, workload: str):
-    """DRAM bytes per FFN-step launch recorded in the committed ncu summary of this workload,
-    if the kernel source is unchanged since the capture (sha256 of csrc/ffn.cu must match)."""
+    """(DRAM bytes per FFN-step launch, union size of that launch) recorded in the committed
+    ncu summary of this workload, if the kernel source is unchanged since the capture (sha256
+    of csrc/ffn.cu must match); else None."""
     path = os.path.join(ROOT, "profiles", "expert_ffn_prefill64.md")
     try:
         text = open(path).read()
@@ -107,28 +167,50 @@ def _traffic_from_profile(kernel_src: str, workload: str):
         return None
     m_sha = re.search(r"ffn\.cu sha256:\s*([0-9a-f]{64})", text)
     m_b = re.search(r"dram bytes per smoe_moe_ffn_batch launch:\s*([0-9]+)", text)
-    if not m_sha or not m_b:
+    m_u = re.search(r"union experts of the captured launch:\s*([0-9]+)", text)
+    if not m_sha or not m_b or not m_u:
         return None
     sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-    return int(m_b.group(1)) if sha == m_sha.group(1) else None
+    return (int(m_b.group(1)), int(m_u.group(1))) if sha == m_sha.group(1) else None
 
 
 # ------------------------------------------------------------------------------ oracle timing
-def oracle_sample(w, layer, x, gate, bias, wts_cpu, rows, threads=0):
-    """Time the oracle (layer-major, all host cores) on `rows` of one layer: (seconds, cores)."""
+def oracle_layers(w, x_rows, layer_source, budget_s: float, threads: int = 0):
+    """Time the oracle (layer-major, all host cores) on the given token rows through the
+    workload's stack, layer after layer (glue norm for chained stacks, routing, routed
+    experts, shared expert), until about budget_s seconds of CPU work: returns (token-layers
+    timed, seconds, cores).  layer_source(l) gives layer l's host tensors (copied outside the
+    timed region): (weights, gate, bias, shared slices or None)."""
+    import numpy as np
     import oracle
-    lay = oracle.Layer.from_workload(w, wts_cpu)
-    t0 = time.perf_counter()
-    idx, w64, _, _ = oracle.route(x[rows], gate, bias, w.top_k, w.norm_topk_prob)
-    xs = x[rows]
-    oracle.moe_layer(lay, xs, idx, w64, xs.float(), threads=threads)
-    dt = time.perf_counter() - t0
-    return dt, (threads if threads > 0 else oracle.hardware_threads())
+    cores = threads if threads > 0 else oracle.hardware_threads()
+    B = x_rows.shape[0]
+    x0 = x_rows.contiguous()
+    h = x0.float().numpy()
+    P = w.shared_slices
+    spent, n_layers = 0.0, 0
+    for l in range(w.layers):
+        wts, gate, bias, shared = layer_source(l)
+        lay = oracle.Layer.from_workload(w, wts)
+        sl = oracle.Layer(w.d_model, P, P, w.shared_ffn_dim // P, shared, w.layout, 0) if P else None
+        all_slices = np.tile(np.arange(P, dtype=np.int32), (B, 1)) if P else None
+        t0 = time.perf_counter()
+        xl = oracle.rmsnorm_bf16(h, 1e-6, center=w.chain_center) if w.chained else x0
+        idx, w64, _, _ = oracle.route(xl, gate, bias, w.top_k, w.norm_topk_prob)
+        out, _, _ = oracle.moe_layer(lay, xl, idx, w64, h, threads=threads)
+        if P:
+            out, _, _ = oracle.moe_layer(sl, xl, all_slices, np.ones((B, P)), out, threads=threads)
+        h = out
+        spent += time.perf_counter() - t0
+        n_layers += 1
+        if spent >= budget_s:
+            break
+    return B * n_layers, spent, cores
 
 
-def _sample_rows(w, budget_s: float = 15.0):
-    """Rows of one layer the oracle finishes in about budget_s on the host (rough model)."""
-    macs_per_token = 3 * w.d_model * w.ffn_dim * w.top_k
+def _sample_rows(w, budget_s: float = 6.0):
+    """Token rows whose first layer the oracle finishes in about budget_s on the host."""
+    macs_per_token = 3 * w.d_model * (w.ffn_dim * w.top_k + w.shared_ffn_dim)
     return max(1, min(w.tokens, int(budget_s * 2.0e9 / macs_per_token)))
 
 
@@ -137,27 +219,35 @@ def run_reference(args, w):
     from moe_expert_routing_gb300 import workload as W
 
     gdev = "cuda" if torch.cuda.is_available() else "cpu"
-    n = _sample_rows(w, budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
-    rows = list(range(n))
-    gate = W.gen_gate(w, 0)
-    bias = W.gen_gate_bias(w, 0)
-    x = W.gen_x(w, 0, w.tokens)
-    wts = {k: v.cpu() for k, v in W.gen_layer_weights(w, 0, device=gdev).items()}
+    per_step = max(3.0, 60.0 / max(1, args.steps + args.warmup))
+    n = _sample_rows(w, budget_s=per_step / 2)
+    x = W.gen_x(w, 0, n)
+    cache = {}
+
+    def layer_source(l):
+        if l not in cache:
+            wts = {k: v.cpu() for k, v in W.gen_layer_weights(w, l, device=gdev).items()}
+            sh = ({k: v.cpu() for k, v in W.gen_shared_weights(w, l, device=gdev).items()}
+                  if w.shared_slices else None)
+            cache[l] = (wts, W.gen_gate(w, l), W.gen_gate_bias(w, l), sh)
+        return cache[l]
+
     for _ in range(args.warmup):
-        oracle_sample(w, 0, x, gate, bias, wts, rows)
-    times, cores = [], 0
+        oracle_layers(w, x, layer_source, per_step)
+    rates, cores, units, spent = [], 0, 0, 0.0
     for _ in range(args.steps):
-        dt, cores = oracle_sample(w, 0, x, gate, bias, wts, rows)
-        times.append(dt)
-    t = sum(times) / len(times)
-    value = n / t
+        units, spent, cores = oracle_layers(w, x, layer_source, per_step)
+        rates.append(units / spent)
+    value = sum(rates) / len(rates)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": spent * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "tokens": w.tokens, "layers": w.layers, "sample_tokens": n},
+        "config": {"workload": w.name, "tokens": w.tokens, "layers": w.layers, "sample_tokens": n,
+                   "sample_token_layers": units},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"layer 0, first {n} of {w.tokens} tokens, layer-major oracle (fp64)"},
+                         "sample": f"first {n} of {w.tokens} tokens through the first {units // n} of {w.layers} "
+                                   f"layers, layer-major fp64 oracle, {spent:.1f} s per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -266,7 +356,7 @@ def run_gpu(args, w, world, rank, local):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks = Clocks(local) if rank == 0 else None
+    clocks = start_clocks(dev, local) if rank == 0 else None
     time.sleep(0.3 if clocks else 0.0)
     t_start.record(stream)
     for s in range(args.steps):
@@ -343,20 +433,23 @@ def run_gpu(args, w, world, rank, local):
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         n = _sample_rows(w)
-        ly = layers[0]
-        wts_cpu = {k: v.cpu() for k, v in ly["wts"].items()}
-        xs = (x_in.view(torch.bfloat16) if not w.chained else None)
-        if xs is None:   # chained stacks: layer 0 consumes RMSNorm(x); use the device's own glue output
-            h.copy_(x_in.view(torch.bfloat16))
-            smoe.smoe_rmsnorm_bf16(h, xb, 1e-6, center=int(w.chain_center))
-            xs = xb.view(torch.bfloat16)
-        xs = xs.cpu()
-        dt, cores = oracle_sample(w, 0, xs, ly["gate"].cpu(), None if ly["bias"] is None else ly["bias"].cpu(),
-                                  wts_cpu, list(range(n)))
-        cpu = {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"layer 0, first {n} of {B} tokens ({n} token-layers), layer-major fp64 oracle, "
-                         f"{dt:.1f} s"}
-    traffic = _traffic_from_profile(os.path.join(ROOT, "moe_expert_routing_gb300", "csrc", "ffn.cu"), w.name)
+
+        def layer_source(l):
+            ly = layers[l]
+            return ({k: v.cpu() for k, v in ly["wts"].items()}, ly["gate"].cpu(),
+                    None if ly["bias"] is None else ly["bias"].cpu(),
+                    {k: v.cpu() for k, v in ly["shared"].tensors.items()} if ly["shared"] is not None else None)
+
+        units, dt, cores = oracle_layers(w, x_in.view(torch.bfloat16)[:n].cpu(), layer_source, 12.0)
+        cpu = {"value": units / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"first {n} of {B} tokens through the first {units // n} of {L} layers "
+                         f"({units} token-layers), layer-major fp64 oracle, {dt:.1f} s"}
+    rec = _traffic_from_profile(os.path.join(ROOT, "moe_expert_routing_gb300", "csrc", "ffn.cu"), w.name)
+    traffic = None
+    if rec is not None:
+        # the capture is of one layer; scale to the timed layers' mean union by algorithmic bytes
+        cap_bytes, cap_u = rec
+        traffic = cap_bytes * ffn_bytes_mean / (cap_u * eb + w.shared_bytes + B * d * 2 + 2 * B * d * 4)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",

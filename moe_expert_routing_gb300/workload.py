@@ -35,7 +35,7 @@ import torch
 MASK32 = 0xFFFFFFFF
 
 # tensor ids mixed into the stream key
-T_X, T_GATE_W, T_ZIPF = 1, 2, 3
+T_X, T_GATE_W, T_ZIPF, T_X_SEQ = 1, 2, 3, 4
 T_WORDS, T_SCALE, T_BIASN = 10, 11, 12
 PROJ_ID = {"up": 0, "gate": 1, "down": 2}
 
@@ -186,6 +186,20 @@ def gen_x(w: Workload, layer: int, tokens: int, attempts: Optional[torch.Tensor]
     u2 = (h2 >> 8).to(torch.float64) * (1.0 / 16777216.0)
     z = torch.sqrt(-2.0 * torch.log(u1)) * torch.cos((2.0 * math.pi) * u2)
     return _bf16_bits(z)
+
+
+def gen_x_sequence(w: Workload, layer: int, tokens: int, rho: float, device="cpu") -> torch.Tensor:
+    """A correlated decode sequence of hidden rows, bf16 [tokens, d]: x_0 = z_0,
+    x_t = rho x_{t-1} + sqrt(1 - rho^2) z_t (z ~ N(0, 1) per element, so every x_t ~ N(0, 1)),
+    in float64 before the rounding.  rho = 0 gives independent tokens."""
+    d = w.d_model
+    z = normal(stream_key(w.seed, layer, T_X_SEQ), tokens * d, device).reshape(tokens, d)
+    x = torch.empty_like(z)
+    c = math.sqrt(max(0.0, 1.0 - rho * rho))
+    x[0] = z[0]
+    for t in range(1, tokens):
+        x[t] = rho * x[t - 1] + c * z[t]
+    return _bf16_bits(x)
 
 
 def gen_gate(w: Workload, layer: int, device="cpu") -> torch.Tensor:

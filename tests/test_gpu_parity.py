@@ -175,6 +175,32 @@ def test_route_ranked_parity(name, B, n_spec, norm):
     np.testing.assert_allclose(sp.cpu().numpy(), osp, rtol=W_RTOL, atol=1e-9)
 
 
+def test_routing_stats_of_a_correlated_sequence():
+    """Next-token coverage on a correlated decode sequence routed by the GPU equals the same
+    statistics of the oracle's routing (Qwen3-235B-shaped router, top-8 plus 8 ranks)."""
+    _need_gpu()
+    from moe_expert_routing_gb300 import routing_stats as RS
+    w = W.WORKLOADS["decode_b1"]
+    T, N = 128, 8
+    gate = W.gen_gate(w, 0)
+    x = W.gen_x_sequence(w, 0, T, 0.9)
+    desc = smoe.make_desc(w.d_model, w.num_experts, w.top_k, w.ffn_dim, w.layout, w.norm_topk_prob)
+    ws = smoe.alloc_workspace(desc, T)
+    idx = torch.empty(T, w.top_k, dtype=torch.int32, device=DEV)
+    wt = torch.empty(T, w.top_k, dtype=torch.float32, device=DEV)
+    sidx = torch.empty(T, N, dtype=torch.int32, device=DEV)
+    smoe.smoe_route_ranked(desc, x.to(DEV).view(torch.int16), gate.to(DEV), None, idx, wt, sidx, None, ws)
+    oi, _, osi, _, lg = oracle.route_ranked(x, gate, None, w.top_k, N, w.norm_topk_prob)
+    sure = logit_gaps(lg, w.top_k + N) >= 1e-4          # no near-tie among ranks 1..K+N+1
+    assert sure.mean() > 0.9
+    gi, gs = idx.cpu().numpy(), sidx.cpu().numpy()
+    assert np.array_equal(gi[sure], oi[sure]) and np.array_equal(gs[sure], osi[sure])
+    if sure.all():
+        assert RS.sequence_stats(gi, gs) == RS.sequence_stats(oi, osi)
+    st = RS.sequence_stats(gi, gs)
+    assert 0.0 < st["adjacent_reuse"] <= st["ranked_coverage"] <= 1.0
+
+
 # ----------------------------------------------------------------------------- union
 @pytest.mark.parametrize("B,K,E", [(1, 8, 128), (16, 4, 16), (64, 8, 128), (64, 8, 256), (37, 3, 9), (4096, 8, 128),
                                    (200, 16, 16)])
