@@ -41,6 +41,17 @@ def _peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def max_over_ranks(value: float, world: int, device="cpu") -> float:
+    """The largest of every rank's value (the slowest rank's time); the value itself at N = 1."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -371,10 +382,7 @@ def run_gpu(args, w, world, rank, local):
         dist.barrier()
     ms_total = t_start.elapsed_time(t_end)
     ffn_ms = [evs[s][l][0].elapsed_time(evs[s][l][1]) for s in range(args.steps) for l in range(L)]
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(ms_total, world, dev)
     ms_step = ms_total / args.steps
     bits = smoe.smoe_read_device_status(ws)
     if bits:
