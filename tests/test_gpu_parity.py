@@ -380,6 +380,21 @@ def test_qwen2_layer_with_shared_expert():
     check_outputs(res.cpu().numpy(), o64 + shared, c.x.float().numpy(), rows=rows)
 
 
+@pytest.mark.parametrize("B,K,E,d,F", [
+    (64, 16, 256, 512, 256),    # the largest top_k and expert count; 1024 entries: one-CTA union
+    (129, 8, 64, 512, 256),     # 1032 entries: the chunked union just past the one-CTA limit
+    (24, 4, 16, 256, 256),      # d_model = ffn_dim = 256: 8-byte scale rows in both passes
+])
+def test_layer_parity_at_the_limits(B, K, E, d, F):
+    w = W.scaled(W.WORKLOADS["toy"], top_k=K, num_experts=E, d_model=d, ffn_dim=F, tokens=B)
+    c = Case(w)
+    out, idx, wt = c.run_layer()
+    o64, oidx, ow64, _ = c.oracle_layer()
+    assert np.array_equal(idx.numpy(), oidx)
+    np.testing.assert_allclose(wt.numpy(), ow64, rtol=W_RTOL, atol=1e-7)
+    check_outputs(out.numpy(), o64, c.x.float().numpy())
+
+
 def test_top1_routing():
     w = W.scaled(W.WORKLOADS["toy"], top_k=1)
     c = Case(w)
