@@ -206,20 +206,24 @@ __global__ void __launch_bounds__(256) gate_logits_staged_kernel(const uint16_t*
 int tile_tokens(int B) { return B <= 64 ? 8 : 64; }
 
 // One CTA per token.  Thread e sums expert e's split-K partials in split order (all loads
-// issued before the sum) and adds the bias; warp 0 then takes K + n_spec rounds of a warp
-// arg-max (lane l holds experts l, l+32, ...; ties -> lower expert id): ranks 0..K-1 are the
-// routing with their softmax weights, ranks K..K+n_spec-1 the ranked continuation (page
-// "Data Flow", "Serial Step Trace": the gate matvec ranks top-(8+spec); ranks beyond 8 are
-// the bets for the next token) with their full-softmax probabilities.
+// issued before the sum) and adds the bias; then every expert's rank is counted in parallel
+// (rank(e) = experts with a larger logit, or an equal logit and a lower id: descending
+// order, ties -> lower expert id) and the experts of ranks 0 .. K + n_spec - 1 are placed
+// in rank order; warp 0 computes the softmax weights.  Ranks 0..K-1 are the routing, ranks
+// K..K+n_spec-1 the ranked continuation (page "Data Flow", "Serial Step Trace": the gate
+// matvec ranks top-(8+spec); ranks beyond 8 are the bets for the next token) with their
+// full-softmax probabilities.
 __global__ void __launch_bounds__(kMaxExperts) topk_kernel(const float* __restrict__ partial, int splits,
                                                            const float* __restrict__ bias, int B, int E, int K,
                                                            int norm, int32_t* __restrict__ idx_out,
                                                            float* __restrict__ w_out, int n_spec,
                                                            int32_t* __restrict__ spec_idx,
                                                            float* __restrict__ spec_p) {
-    __shared__ float logit[kMaxExperts];
+    __shared__ __align__(16) float logit[kMaxExperts];
+    __shared__ int by_rank[kMaxRanks];
     const int t = blockIdx.x;
     const int e = threadIdx.x;
+    const int ranks = K + n_spec;   // <= 32
     if (e < E) {
         float p[kMaxSplits];
 #pragma unroll
@@ -232,59 +236,39 @@ __global__ void __launch_bounds__(kMaxExperts) topk_kernel(const float* __restri
         if (bias) s += bias[e];
         logit[e] = s;
     }
+    if (e < kMaxRanks) by_rank[e] = 0;   // (only a non-finite logit could leave a rank unfilled)
+    __syncthreads();
+    if (e < E) {
+        const float v = logit[e];
+        int r = 0;
+        int j = 0;
+        for (; j + 4 <= E; j += 4) {   // the whole row, four logits per (broadcast) load
+            const float4 u = *reinterpret_cast<const float4*>(logit + j);
+            r += (u.x > v) || (u.x == v && j < e);
+            r += (u.y > v) || (u.y == v && j + 1 < e);
+            r += (u.z > v) || (u.z == v && j + 2 < e);
+            r += (u.w > v) || (u.w == v && j + 3 < e);
+        }
+        for (; j < E; ++j) r += (logit[j] > v) || (logit[j] == v && j < e);
+        if (r < ranks) by_rank[r] = e;
+    }
     __syncthreads();
     if (threadIdx.x >= 32) return;
     const int lane = threadIdx.x;
     constexpr int PER = kMaxExperts / 32;
-    float v[PER];
-    bool live[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int ex = lane + 32 * i;
-        live[i] = ex < E;
-        v[i] = live[i] ? logit[ex] : 0.f;
-    }
-    // max logit over all experts
-    float mx = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < PER; ++i)
-        if (live[i]) mx = fmaxf(mx, v[i]);
-#pragma unroll
-    for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    // full softmax denominator (without norm_topk_prob, and for the ranked continuation)
+    // max logit over all experts (the rank-0 logit) and, where needed, the full softmax
+    // denominator: lane l sums experts l, l+32, ..., then a butterfly over the lanes
+    const float mx = logit[by_rank[0]];
     float z_all = 0.f;
     if (!norm || spec_p) {
 #pragma unroll
         for (int i = 0; i < PER; ++i)
-            if (live[i]) z_all += expf(v[i] - mx);
+            if (lane + 32 * i < E) z_all += expf(logit[lane + 32 * i] - mx);
 #pragma unroll
         for (int off = 16; off; off >>= 1) z_all += __shfl_xor_sync(0xffffffffu, z_all, off);
     }
-    float sel_v = 0.f;   // lane k keeps the k-th selection
-    int sel_i = 0;
-    const int ranks = K + n_spec;   // <= 32
-    for (int k = 0; k < ranks; ++k) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int ex = lane + 32 * i;
-            if (live[i] && (v[i] > bv || (v[i] == bv && ex < bi))) { bv = v[i]; bi = ex; }
-        }
-#pragma unroll
-        for (int off = 16; off; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
-        if (lane == k) { sel_v = bv; sel_i = bi; }
-        if ((bi & 31) == lane) {
-#pragma unroll
-            for (int i = 0; i < PER; ++i)
-                if (i == (bi >> 5)) live[i] = false;
-        }
-    }
-    const float p = (lane < ranks) ? expf(sel_v - mx) : 0.f;
+    const int sel_i = lane < ranks ? by_rank[lane] : 0;   // lane k: the expert of rank k
+    const float p = (lane < ranks) ? expf(logit[sel_i] - mx) : 0.f;
     float z = (lane < K) ? p : 0.f;
     if (norm) {
 #pragma unroll
