@@ -154,7 +154,7 @@ def smoe_route_ranked(desc, x, gate_w, gate_bias, topk_idx, topk_w, spec_idx, sp
 
 
 def smoe_route_noalloc(desc, x, gate_w, gate_bias, topk_idx, topk_w, stream=None):
-    """smoe_route without a workspace (fixed 1 MiB scratch inside the library; see smoe.h)."""
+    """smoe_route without a workspace (a fixed 4 MiB scratch array inside the library; see smoe.h)."""
     _check(load_library().smoe_route_noalloc(ctypes.byref(desc), _p(x), _p(gate_w), _p(gate_bias), x.shape[0],
                                              _p(topk_idx), _p(topk_w), _stream(stream)), "smoe_route_noalloc")
 
