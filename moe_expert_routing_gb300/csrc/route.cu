@@ -48,16 +48,16 @@ __device__ __forceinline__ void split3(float2 v, uint32_t& hi, uint32_t& mid, ui
     lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// CTA: 8 warps x 16 experts, 8*NT tokens, one k-split of kchunk inputs.  Warp: A = 16 gate
+// CTA: WARPS warps x 16 experts, 8*NT tokens, one k-split of kchunk inputs.  Warp: A = 16 gate
 // rows (three bf16 terms), B = NT 8-token tiles of x, fp32 accumulators.  The loads of KB
 // k-steps are issued together before their products, so a warp has KB steps of its weight
 // and activation reads in flight (kchunk is a multiple of 16 * KB).
-template <int NT, int KB>
-__global__ void __launch_bounds__(256) gate_logits_kernel(const uint16_t* __restrict__ x,
-                                                          const float* __restrict__ W, int B, int E, int d,
-                                                          int kchunk, float* __restrict__ partial) {
+template <int NT, int KB, int WARPS = 8>
+__global__ void __launch_bounds__(32 * WARPS) gate_logits_kernel(const uint16_t* __restrict__ x,
+                                                                 const float* __restrict__ W, int B, int E, int d,
+                                                                 int kchunk, float* __restrict__ partial) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-    const int e0 = blockIdx.y * kExpertsPerCta + warp * 16;
+    const int e0 = blockIdx.y * (WARPS * 16) + warp * 16;
     if (e0 >= E) return;
     const int t0 = blockIdx.x * 8 * NT;
     const int k_begin = blockIdx.z * kchunk, k_end = k_begin + kchunk;
@@ -312,7 +312,11 @@ cudaError_t launch_route(const smoe_layer_desc& D, const uint16_t* x, const floa
     const int bt = tile_tokens(B);
     dim3 grid((B + bt - 1) / bt, (E + kExpertsPerCta - 1) / kExpertsPerCta, S);
     const int kchunk = d / S;   // a multiple of 128 (route_splits)
-    if (bt == 8) {
+    if (bt == 8 && B <= 8) {
+        // one token tile: CTAs of 2 warps (32 experts) spread the gate read over 4x the SMs
+        dim3 g2(grid.x, (E + 31) / 32, S);
+        gate_logits_kernel<1, 8, 2><<<g2, 64, 0, stream>>>(x, gate_w, B, E, d, kchunk, logits_ws);
+    } else if (bt == 8) {
         gate_logits_kernel<1, 8><<<grid, 256, 0, stream>>>(x, gate_w, B, E, d, kchunk, logits_ws);
     } else {
         const int smem = 64 * kPieceStride * 2;   // 33 KB: below the default dynamic limit

@@ -12,7 +12,7 @@
 // so each list is in ascending token order and the output is deterministic: within a
 // 1024-entry chunk, equal ids are ranked with __match_any_sync inside each warp and a
 // per-expert prefix over the 32 warps.
-//   up to 1024 entries:  union_kernel, one CTA
+//   up to 1024 entries:  union_kernel, one CTA (128 threads up to 128 entries: decode)
 //   more:                chunk_hist_kernel (one CTA per 1024-entry chunk: per-chunk counts)
 //                        -> chunk_scan_kernel (one CTA: union, list offsets, chunk bases)
 //                        -> chunk_scatter_kernel (one CTA per chunk)
@@ -24,7 +24,8 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 
-__global__ void __launch_bounds__(kThreads) union_kernel(const int32_t* __restrict__ idx, int BK, int E,
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) union_kernel(const int32_t* __restrict__ idx, int BK, int E,
                                                          int32_t* __restrict__ union_ids,
                                                          int32_t* __restrict__ n_union,
                                                          int32_t* __restrict__ offsets,
@@ -35,20 +36,21 @@ __global__ void __launch_bounds__(kThreads) union_kernel(const int32_t* __restri
     __shared__ int list_off[kMaxExperts];  // start of expert e's list
     __shared__ int running[kMaxExperts];   // entries of expert e placed so far
     __shared__ int chunk_base[kMaxExperts];
-    __shared__ int wcount[kWarps][kMaxExperts];
+    constexpr int WARPS = THREADS / 32;
+    __shared__ int wcount[WARPS][kMaxExperts];
     __shared__ int bad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     if (tid == 0) bad = 0;
-    for (int e = tid; e < kMaxExperts; e += kThreads) {
+    for (int e = tid; e < kMaxExperts; e += THREADS) {
         count[e] = 0;
         running[e] = 0;
     }
-    for (int i = tid; i < kWarps * kMaxExperts; i += kThreads) (&wcount[0][0])[i] = 0;
+    for (int i = tid; i < WARPS * kMaxExperts; i += THREADS) (&wcount[0][0])[i] = 0;
     __syncthreads();
 
     // histogram + validation
-    for (int i = tid; i < BK; i += kThreads) {
+    for (int i = tid; i < BK; i += THREADS) {
         const int e = idx[i];
         if (e < 0 || e >= E) bad = 1;
         else atomicAdd(&count[e], 1);
@@ -102,17 +104,17 @@ __global__ void __launch_bounds__(kThreads) union_kernel(const int32_t* __restri
     }
     __syncthreads();
 
-    // stable scatter, 1024 entries per round
-    for (int base = 0; base < BK; base += kThreads) {
+    // stable scatter, THREADS entries per round
+    for (int base = 0; base < BK; base += THREADS) {
         const int i = base + tid;
         const int e = (i < BK) ? idx[i] : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         const int rank = __popc(peers & ((1u << lane) - 1u));
         if (e >= 0 && rank == 0) wcount[warp][e] = __popc(peers);
         __syncthreads();
-        for (int x = tid; x < E; x += kThreads) {
+        for (int x = tid; x < E; x += THREADS) {
             int s = 0;
-            for (int w = 0; w < kWarps; ++w) {
+            for (int w = 0; w < WARPS; ++w) {
                 const int cnt = wcount[w][x];
                 wcount[w][x] = s;
                 s += cnt;
@@ -127,8 +129,8 @@ __global__ void __launch_bounds__(kThreads) union_kernel(const int32_t* __restri
             slot_list[pos] = i - (i / K) * K;
         }
         __syncthreads();
-        for (int x = tid; x < E; x += kThreads)
-            for (int w = 0; w < kWarps; ++w) wcount[w][x] = 0;
+        for (int x = tid; x < E; x += THREADS)
+            for (int w = 0; w < WARPS; ++w) wcount[w][x] = 0;
         __syncthreads();
     }
 }
@@ -299,8 +301,12 @@ cudaError_t launch_union(const smoe_layer_desc& D, const int32_t* topk_idx, int 
                          uint32_t* status, int32_t* scratch, cudaStream_t stream) {
     const int BK = B * D.top_k, E = D.num_experts;
     if (BK <= kThreads || !scratch) {
-        union_kernel<<<1, kThreads, 0, stream>>>(topk_idx, BK, E, union_ids, n_union, offsets, token_list,
-                                                 slot_list, D.top_k, status);
+        if (BK <= 128)
+            union_kernel<128><<<1, 128, 0, stream>>>(topk_idx, BK, E, union_ids, n_union, offsets, token_list,
+                                                     slot_list, D.top_k, status);
+        else
+            union_kernel<kThreads><<<1, kThreads, 0, stream>>>(topk_idx, BK, E, union_ids, n_union, offsets,
+                                                               token_list, slot_list, D.top_k, status);
         return cudaGetLastError();
     }
     // scratch: [0] bad flag, then the per-chunk counts / bases [chunks][E]
