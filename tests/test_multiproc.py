@@ -48,7 +48,7 @@ def test_max_over_ranks_single_process():
 def _run_reference(rank, world):
     env = dict(os.environ, RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank), CUDA_VISIBLE_DEVICES="")
     return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "toy",
-                           "--steps", "1", "--warmup", "0", "--gpus", str(world)],
+                           "--steps", "1", "--warmup", "0", "--gpus", str(world), "--ref-seconds", "1"],
                           capture_output=True, text=True, env=env, timeout=600)
 
 
