@@ -243,9 +243,20 @@ struct Item {
 };
 
 // Work items: for every union expert with n >= tc_min, m_tiles x ceil(n / TC_N) tiles.  The
-// per-expert prefix (up to 256 experts) is built by warp 0 in shared memory.
+// per-expert prefix (up to 256 experts) is built by warp 0 in shared memory, next to copies of
+// the union ids and list offsets (pref[0..nu], uid = pref + kMaxExperts + 1, off = uid +
+// kMaxExperts + 1), so the per-tile decoding in every role reads shared memory only.
 __device__ int build_items(const TcArgs& a, int* pref) {
     __shared__ int total;
+    int* uid = pref + kMaxExperts + 1;
+    int* off = uid + kMaxExperts + 1;
+    {
+        const int nu = *a.n_union;
+        for (int u = threadIdx.x; u <= nu; u += blockDim.x) {
+            off[u] = a.offsets[u];
+            if (u < nu) uid[u] = a.union_ids[u];
+        }
+    }
     if (threadIdx.x < 32) {
         const int nu = *a.n_union;
         int run = 0;
@@ -284,10 +295,12 @@ __device__ __forceinline__ Item decode_item(const TcArgs& a, const int* pref, in
     }
     // skip experts with no items (pref[u] == pref[u+1])
     while (lo + 1 < nu && pref[lo + 1] <= t) ++lo;
+    const int* uid = pref + kMaxExperts + 1;
+    const int* off = uid + kMaxExperts + 1;
     Item it;
-    it.e = a.union_ids[lo];
-    it.p0 = a.offsets[lo];
-    it.n = a.offsets[lo + 1] - it.p0;
+    it.e = uid[lo];
+    it.p0 = off[lo];
+    it.n = off[lo + 1] - it.p0;
     const int r = t - pref[lo];
     it.nt = r / a.m_tiles;
     it.mt = r - it.nt * a.m_tiles;
@@ -305,7 +318,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     __shared__ __align__(8) uint64_t deq[C::kKa], empty_a[C::kKa];
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
     __shared__ uint32_t tmem_base_sh;
-    __shared__ int pref[kMaxExperts + 1];
+    __shared__ int pref[3 * (kMaxExperts + 1)];   // item prefix, union ids, list offsets
     __shared__ int tok_sh[2][TC_N], slot_sh[2][TC_N];
     __shared__ float gsum_sh[4][32];   // pass 0 epilogue: partial group sums [column quarter][token]
 
