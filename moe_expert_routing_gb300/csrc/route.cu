@@ -206,13 +206,17 @@ __global__ void __launch_bounds__(256) gate_logits_staged_kernel(const uint16_t*
 int tile_tokens(int B) { return B <= 64 ? 8 : 64; }
 
 // One CTA per token.  Thread e sums expert e's split-K partials in split order (all loads
-// issued before the sum) and adds the bias; then every expert's rank is counted in parallel
-// (rank(e) = experts with a larger logit, or an equal logit and a lower id: descending
-// order, ties -> lower expert id) and the experts of ranks 0 .. K + n_spec - 1 are placed
-// in rank order; warp 0 computes the softmax weights.  Ranks 0..K-1 are the routing, ranks
+// issued before the sum) and adds the bias.  The experts of ranks 0 .. K + n_spec - 1
+// (descending logit, ties -> lower expert id) are then found either by counting every
+// expert's rank in parallel (RANK: rank(e) = experts with a larger logit, or an equal logit
+// and a lower id; quickest for small batches, where one CTA's latency is the cost) or by
+// K + n_spec rounds of a warp arg-max over lanes holding experts l, l+32, ... (fewer
+// instructions per token for large batches); both give the same experts in the same order.
+// Warp 0 computes the softmax weights.  Ranks 0..K-1 are the routing, ranks
 // K..K+n_spec-1 the ranked continuation (page "Data Flow", "Serial Step Trace": the gate
 // matvec ranks top-(8+spec); ranks beyond 8 are the bets for the next token) with their
 // full-softmax probabilities.
+template <bool RANK>
 __global__ void __launch_bounds__(kMaxExperts) topk_kernel(const float* __restrict__ partial, int splits,
                                                            const float* __restrict__ bias, int B, int E, int K,
                                                            int norm, int32_t* __restrict__ idx_out,
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(kMaxExperts) topk_kernel(const float* __restri
     }
     if (e < kMaxRanks) by_rank[e] = 0;   // (only a non-finite logit could leave a rank unfilled)
     __syncthreads();
-    if (e < E) {
+    if (RANK && e < E) {
         const float v = logit[e];
         int r = 0;
         int j = 0;
@@ -256,18 +260,54 @@ __global__ void __launch_bounds__(kMaxExperts) topk_kernel(const float* __restri
     if (threadIdx.x >= 32) return;
     const int lane = threadIdx.x;
     constexpr int PER = kMaxExperts / 32;
-    // max logit over all experts (the rank-0 logit) and, where needed, the full softmax
-    // denominator: lane l sums experts l, l+32, ..., then a butterfly over the lanes
-    const float mx = logit[by_rank[0]];
+    float v[PER];   // lane l holds experts l, l+32, ...
+    bool live[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        live[i] = lane + 32 * i < E;
+        v[i] = live[i] ? logit[lane + 32 * i] : 0.f;
+    }
+    // max logit over all experts and, where needed, the full softmax denominator (butterflies)
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+        if (live[i]) mx = fmaxf(mx, v[i]);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     float z_all = 0.f;
     if (!norm || spec_p) {
 #pragma unroll
         for (int i = 0; i < PER; ++i)
-            if (lane + 32 * i < E) z_all += expf(logit[lane + 32 * i] - mx);
+            if (live[i]) z_all += expf(v[i] - mx);
 #pragma unroll
         for (int off = 16; off; off >>= 1) z_all += __shfl_xor_sync(0xffffffffu, z_all, off);
     }
-    const int sel_i = lane < ranks ? by_rank[lane] : 0;   // lane k: the expert of rank k
+    int sel_i = 0;   // lane k: the expert of rank k
+    if (RANK) {
+        sel_i = lane < ranks ? by_rank[lane] : 0;
+    } else {
+        for (int k = 0; k < ranks; ++k) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int ex = lane + 32 * i;
+                if (live[i] && (v[i] > bv || (v[i] == bv && ex < bi))) { bv = v[i]; bi = ex; }
+            }
+#pragma unroll
+            for (int off = 16; off; off >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+            }
+            if (lane == k) sel_i = bi < E ? bi : 0;   // (no live finite logit left: NaN input)
+            if ((bi & 31) == lane) {
+#pragma unroll
+                for (int i = 0; i < PER; ++i)
+                    if (i == (bi >> 5)) live[i] = false;
+            }
+        }
+    }
     const float p = (lane < ranks) ? expf(logit[sel_i] - mx) : 0.f;
     float z = (lane < K) ? p : 0.f;
     if (norm) {
@@ -323,8 +363,8 @@ cudaError_t launch_route(const smoe_layer_desc& D, const uint16_t* x, const floa
         gate_logits_staged_kernel<8, 4><<<grid, 256, smem, stream>>>(x, gate_w, B, E, d, kchunk, logits_ws);
     }
     const int threads = (E + 31) / 32 * 32;
-    topk_kernel<<<B, threads, 0, stream>>>(logits_ws, S, gate_bias, B, E, K, D.norm_topk_prob, topk_idx, topk_w,
-                                           n_spec, spec_idx, spec_p);
+    (B <= 512 ? topk_kernel<true> : topk_kernel<false>)<<<B, threads, 0, stream>>>(
+        logits_ws, S, gate_bias, B, E, K, D.norm_topk_prob, topk_idx, topk_w, n_spec, spec_idx, spec_p);
     return cudaGetLastError();
 }
 
