@@ -157,14 +157,16 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
     if (blockIdx.x == 0)   // work queue of the expert passes that follow
         for (int i = threadIdx.x; i < n_ticket; i += blockDim.x) ticket[i] = 0;
     const int lane = threadIdx.x & 31;
-    const int total = offsets[*n_union];
     const int cpr = d / 8;   // 8-element chunks per row, a multiple of 32
     const int G = d / kGroup;
     const int segs = (cpr + 32 * U - 1) / (32 * U);   // warps per row
-    for (int wg = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; wg < total * segs;
-         wg += (gridDim.x * blockDim.x) >> 5) {
+    int wg = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    // the warp's first entry's token is loaded alongside the list length (lists hold BK entries)
+    const int t_first = wg / segs < BK ? token_list[wg / segs] : -1;
+    const int total = offsets[*n_union];
+    for (bool first = true; wg < total * segs; wg += (gridDim.x * blockDim.x) >> 5, first = false) {
         const int p = wg / segs, seg = wg - p * segs;
-        int t = token_list[p];
+        int t = first ? t_first : token_list[p];
         if (t < 0 || t >= B) {   // a caller-supplied list that does not match B: flag, use row 0
             if (lane == 0) atomicOr(status, SMOE_FAULT_TOKEN_INDEX);
             t = 0;
@@ -853,7 +855,9 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
 
 // ----------------------------------------------------------------------------- combine
 // Skipped entirely (residual untouched) when the union did not cover all B*K entries, i.e.
-// after a flagged routing fault.
+// after a flagged routing fault.  A thread issues the loads of up to 8 slots (and the
+// union check) together before its rank-ordered FMA chain, so it waits on one L2 round
+// trip instead of one per slot.
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ w,
                                                       const int32_t* __restrict__ n_union,
                                                       const int32_t* __restrict__ offsets, int B, int K, int d,
@@ -861,18 +865,31 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;   // float4 index
     const size_t n4 = (size_t)B * d / 4;
     if (i >= n4) return;
-    if (offsets[*n_union] != B * K) return;
+    const int covered = offsets[*n_union];
     const int t = (int)(i / (d / 4));
     const int c4 = (int)(i - (size_t)t * (d / 4));
+    const float* wt = w + (size_t)t * K;
+    const float4* yt = reinterpret_cast<const float4*>(y + (size_t)t * K * d) + c4;
     float4 acc = reinterpret_cast<float4*>(residual)[i];
-    for (int k = 0; k < K; ++k) {
-        const float wk = w[(size_t)t * K + k];
-        const float4 v = reinterpret_cast<const float4*>(y + ((size_t)t * K + k) * d)[c4];
-        acc.x = fmaf(wk, v.x, acc.x);
-        acc.y = fmaf(wk, v.y, acc.y);
-        acc.z = fmaf(wk, v.z, acc.z);
-        acc.w = fmaf(wk, v.w, acc.w);
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        float wk[8];
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (k0 + j < K) {
+                wk[j] = wt[k0 + j];
+                v[j] = yt[(size_t)(k0 + j) * (d / 4)];
+            }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (k0 + j < K) {
+                acc.x = fmaf(wk[j], v[j].x, acc.x);
+                acc.y = fmaf(wk[j], v[j].y, acc.y);
+                acc.z = fmaf(wk[j], v[j].z, acc.z);
+                acc.w = fmaf(wk[j], v[j].w, acc.w);
+            }
     }
+    if (covered != B * K) return;
     reinterpret_cast<float4*>(residual)[i] = acc;
 }
 

@@ -12,7 +12,8 @@
 // so each list is in ascending token order and the output is deterministic: within a
 // 1024-entry chunk, equal ids are ranked with __match_any_sync inside each warp and a
 // per-expert prefix over the 32 warps.
-//   up to 1024 entries:  union_kernel, one CTA (128 threads up to 128 entries: decode)
+//   up to 128 entries:   union_warp_kernel, one warp, registers and shuffles only (decode)
+//   up to 1024 entries:  union_kernel, one CTA
 //   more:                chunk_hist_kernel (one CTA per 1024-entry chunk: per-chunk counts)
 //                        -> chunk_scan_kernel (one CTA: union, list offsets, chunk bases)
 //                        -> chunk_scatter_kernel (one CTA per chunk)
@@ -23,6 +24,90 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
+
+// Up to 128 entries: lane l holds entries l, l+32, l+64, l+96.  Every entry is compared with
+// every other (one shuffle per source entry): less = entries with a smaller expert id (its
+// expert's list offset), eqb = earlier entries with the same id; less + eqb is its position
+// in the stable expert-major order, and eqb == 0 marks the first entry of its expert, which
+// writes the union slot.  The union position of expert e is the number of distinct ids below
+// e, read from a 256-bit set of the ids present (OR-reduced over the warp).
+__global__ void __launch_bounds__(32) union_warp_kernel(const int32_t* __restrict__ idx, int BK, int E,
+                                                        int32_t* __restrict__ union_ids,
+                                                        int32_t* __restrict__ n_union,
+                                                        int32_t* __restrict__ offsets,
+                                                        int32_t* __restrict__ token_list,
+                                                        int32_t* __restrict__ slot_list, int K,
+                                                        uint32_t* __restrict__ status) {
+    constexpr int PER = 4;
+    constexpr int WORDS = kMaxExperts / 32;
+    const int lane = threadIdx.x;
+    int e[PER];
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int i = lane + 32 * j;
+        e[j] = i < BK ? idx[i] : -1;
+        if (i < BK && (e[j] < 0 || e[j] >= E)) bad = true;
+    }
+    if (__any_sync(0xffffffffu, bad)) {
+        if (lane == 0) {
+            atomicOr(status, SMOE_FAULT_EXPERT_INDEX);
+            *n_union = 0;
+            offsets[0] = 0;
+        }
+        return;
+    }
+    int less[PER], eqb[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) less[j] = eqb[j] = 0;
+#pragma unroll
+    for (int sj = 0; sj < PER; ++sj) {
+        if (32 * sj >= BK) break;
+        const int n = BK - 32 * sj < 32 ? BK - 32 * sj : 32;
+        for (int s = 0; s < n; ++s) {
+            const int es = __shfl_sync(0xffffffffu, e[sj], s);
+            const int is = 32 * sj + s;
+#pragma unroll
+            for (int j = 0; j < PER; ++j) {
+                less[j] += es < e[j];
+                eqb[j] += es == e[j] && is < lane + 32 * j;
+            }
+        }
+    }
+    uint32_t present[WORDS];
+    int nu = 0;
+#pragma unroll
+    for (int w = 0; w < WORDS; ++w) {
+        uint32_t mine = 0;
+#pragma unroll
+        for (int j = 0; j < PER; ++j)
+            if (lane + 32 * j < BK && (e[j] >> 5) == w) mine |= 1u << (e[j] & 31);
+        present[w] = __reduce_or_sync(0xffffffffu, mine);
+        nu += __popc(present[w]);
+    }
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int i = lane + 32 * j;
+        if (i >= BK) continue;
+        const int pos = less[j] + eqb[j];
+        token_list[pos] = i / K;
+        slot_list[pos] = i - (i / K) * K;
+        if (eqb[j] == 0) {
+            int u = 0;
+#pragma unroll
+            for (int w = 0; w < WORDS; ++w) {
+                if (w < (e[j] >> 5)) u += __popc(present[w]);
+                else if (w == (e[j] >> 5)) u += __popc(present[w] & ((1u << (e[j] & 31)) - 1u));
+            }
+            union_ids[u] = e[j];
+            offsets[u] = less[j];
+        }
+    }
+    if (lane == 0) {
+        *n_union = nu;
+        offsets[nu] = BK;
+    }
+}
 
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS) union_kernel(const int32_t* __restrict__ idx, int BK, int E,
@@ -302,8 +387,8 @@ cudaError_t launch_union(const smoe_layer_desc& D, const int32_t* topk_idx, int 
     const int BK = B * D.top_k, E = D.num_experts;
     if (BK <= kThreads || !scratch) {
         if (BK <= 128)
-            union_kernel<128><<<1, 128, 0, stream>>>(topk_idx, BK, E, union_ids, n_union, offsets, token_list,
-                                                     slot_list, D.top_k, status);
+            union_warp_kernel<<<1, 32, 0, stream>>>(topk_idx, BK, E, union_ids, n_union, offsets, token_list,
+                                                    slot_list, D.top_k, status);
         else
             union_kernel<kThreads><<<1, kThreads, 0, stream>>>(topk_idx, BK, E, union_ids, n_union, offsets,
                                                                token_list, slot_list, D.top_k, status);

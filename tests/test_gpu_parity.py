@@ -203,7 +203,7 @@ def test_routing_stats_of_a_correlated_sequence():
 
 # ----------------------------------------------------------------------------- union
 @pytest.mark.parametrize("B,K,E", [(1, 8, 128), (16, 4, 16), (64, 8, 128), (64, 8, 256), (37, 3, 9), (4096, 8, 128),
-                                   (200, 16, 16)])
+                                   (200, 16, 16), (1, 1, 1), (3, 5, 200), (8, 8, 256), (16, 8, 128), (33, 4, 256)])
 def test_union_parity(B, K, E):
     _need_gpu()
     rng = np.random.default_rng(B * 1000 + K * 10 + E)
