@@ -5,8 +5,9 @@
 A step is one pass of the whole hot path over one batch: for every layer of the workload's
 stack, RMSNorm glue (chained stacks), exact routing, the expert union, the expert FFN and
 the weighted combine, all through libsmoe's C ABI.  Inputs are seeded and synthetic (the
-workload generator), resident in HBM when the timed region starts; the expert weights of a
-stack are far larger than L2, so no flush is needed between steps.
+workload generator), resident in HBM when the timed region starts.  A step of a stack reads
+far more expert weights than L2 holds; a step that reads less than ~1 GB (one decode layer) is
+timed on its own after a write that evicts L2.
 
 The JSON line reports MoE-layer tokens/s (token-layers per second) for the whole job, the
 union-expert bytes/s, the roofline of the expert FFN step, the end-to-end figure through
@@ -352,6 +353,15 @@ def run_gpu(args, w, world, rank, local):
 
     evs = [[[ffn_event(), ffn_event()] for _ in range(L)] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # A step that reads less than ~1 GB (every routed expert distinct, plus the gate matrices)
+    # could find the previous step's experts in the 129 MB L2: such steps are timed one by one,
+    # with a 256 MiB write between them (outside their events) that evicts L2.
+    eb = w.expert_bytes
+    step_bytes_max = L * (min(B * K, E) * eb + w.shared_bytes + E * d * 4)
+    flush = step_bytes_max < 1e9
+    flush_buf = torch.empty(256 * 2**20 // 4, dtype=torch.int32, device=dev) if flush else None
+    step_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)] if flush else None
     graphs = []
     if not args.eager:
         # one CUDA graph per timed step (each with its own FFN events), captured from the
@@ -373,16 +383,21 @@ def run_gpu(args, w, world, rank, local):
     time.sleep(0.3 if clocks else 0.0)
     t_start.record(stream)
     for s in range(args.steps):
+        if flush:
+            flush_buf.fill_(s)
+            step_evs[s][0].record(stream)
         if graphs:
             graphs[s].replay()
         else:
             step(x_in, evs[s])
+        if flush:
+            step_evs[s][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None
     if world > 1:
         dist.barrier()
-    ms_total = t_start.elapsed_time(t_end)
+    ms_total = (sum(a.elapsed_time(b) for a, b in step_evs) if flush else t_start.elapsed_time(t_end))
     ffn_ms = [evs[s][l][0].elapsed_time(evs[s][l][1]) for s in range(args.steps) for l in range(L)]
     ms_total = max_over_ranks(ms_total, world, dev)
     ms_step = ms_total / args.steps
@@ -392,7 +407,6 @@ def run_gpu(args, w, world, rank, local):
 
     # ---- algorithmic work (measured union sizes)
     U = [int(ly["nu"].item()) for ly in layers]
-    eb = w.expert_bytes
     hbm, tf_burst, tf_sus, peak_kind = _peaks()
     ffn_bytes = [u * eb + w.shared_bytes + B * d * 2 + 2 * B * d * 4 for u in U]
     layer_bytes = [fb + E * d * 4 for fb in ffn_bytes]
@@ -426,15 +440,25 @@ def run_gpu(args, w, world, rank, local):
         out_host.copy_(h, non_blocking=True)
     torch.cuda.synchronize()
     e2e_steps = max(3, min(args.steps, 10))
+    e2e_total = 0.0
     e_s.record(stream)
     for _ in range(e2e_steps):
+        if flush:
+            flush_buf.fill_(1)
+            e_s.record(stream)
         x_dev2.copy_(x_host, non_blocking=True)
         step(x_dev2)
         out_host.copy_(h, non_blocking=True)
+        if flush:
+            e_e.record(stream)
         torch.cuda.current_stream().synchronize()
-    e_e.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e_s.elapsed_time(e_e) / e2e_steps
+        if flush:
+            e2e_total += e_s.elapsed_time(e_e)
+    if not flush:
+        e_e.record(stream)
+        torch.cuda.synchronize()
+        e2e_total = e_s.elapsed_time(e_e)
+    e2e_ms = e2e_total / e2e_steps
     e2e_value = world * B * L / (e2e_ms * 1e-3)
 
     if rank != 0:
@@ -473,7 +497,9 @@ def run_gpu(args, w, world, rank, local):
                    "spec_ranks": w.spec, "shared_ffn_dim": w.shared_ffn_dim,
                    "norm_topk_prob": w.norm_topk_prob,
                    "ffn_dim": F, "layout": w.layout, "weights": "4-bit affine g64, bf16 scales/biases",
-                   "l2": f"inputs larger than L2: {L * E * eb / 1e9:.1f} GB of expert weights per step",
+                   "l2": (f"L2 flushed between timed steps (256 MiB write outside the step events): a step "
+                          f"reads at most {step_bytes_max / 1e6:.0f} MB" if flush else
+                          f"inputs larger than L2: {sum(U) * eb / 1e9:.1f} GB of union expert weights per step"),
                    "parallelism": f"replicas x{world}",
                    "launch": "eager" if args.eager else "one CUDA graph per step, replayed"},
         "union_expert_gbs": union_gbs,
