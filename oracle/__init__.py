@@ -22,6 +22,10 @@ Each function cites the passage it follows (page title and section):
 * ``shared_dense_layer`` / ``shared_expert_ffn`` -- "Data Flow", "Serial Step Trace" (the
   shared expert FFN on every token, residual += shared_out + routed_out); "Surface Scout",
   "The Model Config" (shared_expert_ffn_dim)
+* ``SlotPool``     -- "Data Flow", "Ring Buffer State Machine" (slots keyed by (layer, expert)
+  retained as cache entries; EMPTY slots first, else the least-recently-used idle slot is
+  evicted; freshly loaded slots carry the new tick) and "Handling Misses"; "Layer-Major
+  Batched Prefill", "Retention, never replay" (keep what was read, never wipe per token)
 """
 from __future__ import annotations
 
@@ -166,6 +170,55 @@ def expert_union(idx, E: int):
         raise ValueError(f"oracle_union rc={rc}")
     n = int(nu[0])
     return uid[:n].copy(), off[:n + 1].copy(), tl[:B * K].copy(), sl[:B * K].copy()
+
+
+class SlotPool:
+    """Residency of (layer, expert) keys in a pool of n_slots weight slots (plain Python).
+
+    One ``plan`` per layer call, in the order the pages give: the tick advances; every key of
+    the call's union that a slot already holds is a hit (its slot is re-stamped with the tick);
+    the misses, in union order, take the idle slots (slots holding no key of this union) in
+    order of (stamp, slot id) -- empty slots carry stamp -1, so they come first, then the least
+    recently used; equal stamps (slots loaded by the same call) go lowest slot id first.  A
+    taken slot's previous key stops being resident; the slot now holds the missed key with the
+    new tick.  Returns (slot of each union position, [(key, slot)] copies in miss order).
+    """
+
+    def __init__(self, n_keys: int, n_slots: int):
+        self.n_keys, self.n_slots = n_keys, n_slots
+        self.tick = 0
+        self.slot_of = [-1] * n_keys
+        self.owner = [-1] * n_slots
+        self.stamp = [-1] * n_slots
+
+    def plan(self, keys: Sequence[int]):
+        keys = [int(k) for k in keys]
+        if len(set(keys)) != len(keys) or any(not 0 <= k < self.n_keys for k in keys):
+            raise ValueError("a union holds distinct keys in range")
+        self.tick += 1
+        slots = [-1] * len(keys)
+        in_use = set()
+        for u, k in enumerate(keys):
+            if self.slot_of[k] >= 0:
+                slots[u] = self.slot_of[k]
+                in_use.add(slots[u])
+        idle = sorted((self.stamp[s], s) for s in range(self.n_slots) if s not in in_use)
+        misses = [u for u in range(len(keys)) if slots[u] < 0]
+        if len(misses) > len(idle):
+            raise ValueError("more misses than idle slots")
+        copies = []
+        for m, u in enumerate(misses):
+            s = idle[m][1]
+            old = self.owner[s]
+            if old >= 0:
+                self.slot_of[old] = -1
+            self.owner[s] = keys[u]
+            self.slot_of[keys[u]] = s
+            slots[u] = s
+            copies.append((keys[u], s))
+        for s in slots:
+            self.stamp[s] = self.tick
+        return slots, copies
 
 
 class Layer:

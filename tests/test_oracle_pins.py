@@ -471,3 +471,79 @@ def test_oracle_row_subset_matches_full():
     full = oracle.moe_layer(layer, x, idx, w64, res)[1]
     part = oracle.moe_layer(layer, x, idx, w64, res, rows=[3, 7, 11])[1]
     assert np.array_equal(part[[3, 7, 11]], full[[3, 7, 11]])
+
+
+# ----------------------------------------------------------------------------- slot pool
+# Worked by hand from the retention rule of "Data Flow", "Ring Buffer State Machine": empty
+# slots first, then the least recently used idle slot; slots of the current union are in use.
+SLOT_POOL_CASE = [   # (keys of the call, slots expected, copies expected); 3 slots
+    ([0, 1], [0, 1], [(0, 0), (1, 1)]),     # tick 1: both miss, empty slots 0 and 1
+    ([1, 2], [1, 2], [(2, 2)]),             # tick 2: 1 hits; 2 takes empty slot 2 (stamp -1 < 1)
+    ([0, 3], [0, 1], [(3, 1)]),             # tick 3: 0 hits; slots 1, 2 idle at stamp 2 -> lower id
+    ([4], [2], [(4, 2)]),                   # tick 4: slot 2 (stamp 2) is older than 0, 1 (stamp 3)
+    ([1, 3], [0, 1], [(1, 0)]),             # tick 5: 3 hits in slot 1; 1 was evicted, takes slot 0 (3)
+]
+
+
+def test_slot_pool_hand_worked():
+    pool = oracle.SlotPool(n_keys=8, n_slots=3)
+    for keys, slots, copies in SLOT_POOL_CASE:
+        got_s, got_c = pool.plan(keys)
+        assert got_s == slots and got_c == copies, (keys, got_s, got_c)
+
+
+def test_slot_pool_keys_of_different_layers_are_distinct():
+    E = 4
+    pool = oracle.SlotPool(n_keys=2 * E, n_slots=2)
+    assert pool.plan([1]) == ([0], [(1, 0)])              # layer 0, expert 1
+    assert pool.plan([E + 1]) == ([1], [(E + 1, 1)])      # layer 1, expert 1: its own slot
+    assert pool.plan([1, 2]) == ([0, 1], [(2, 1)])        # layer 0 again: hit, and 2 evicts (1, 1)
+
+
+def test_slot_pool_planted_mru_eviction_fails_the_pin():
+    class MostRecent(oracle.SlotPool):   # a plausible mistake: evict the newest idle slot
+        def plan(self, keys):
+            saved = self.stamp
+            self.stamp = [-s if s >= 0 else -(10 ** 9) for s in saved]
+            try:
+                return super().plan(keys)
+            finally:
+                fresh = self.stamp
+                self.stamp = [self.tick if f == self.tick else saved[i] for i, f in enumerate(fresh)]
+
+    pool = MostRecent(n_keys=8, n_slots=3)
+    results = [pool.plan(keys) for keys, _, _ in SLOT_POOL_CASE]
+    assert results != [(s, c) for _, s, c in SLOT_POOL_CASE]
+
+
+def test_slot_pool_retains_a_cycle_that_fits():
+    # unions over 6 distinct keys, pool of 6: after the first pass nothing is copied again
+    cycle = [[0, 2, 4], [1, 2, 3], [4, 5], [0, 5]]
+    pool = oracle.SlotPool(n_keys=16, n_slots=6)
+    first = sum(len(pool.plan(u)[1]) for u in cycle)
+    assert first == 6
+    for _ in range(3):
+        assert sum(len(pool.plan(u)[1]) for u in cycle) == 0
+
+
+def test_slot_pool_invariants_random():
+    rng = np.random.default_rng(11)
+    n_keys, n_slots = 40, 12
+    pool = oracle.SlotPool(n_keys, n_slots)
+    for step in range(300):
+        keys = sorted(rng.choice(n_keys, size=int(rng.integers(1, 9)), replace=False).tolist())
+        before_owner, before_stamp = list(pool.owner), list(pool.stamp)
+        resident_before = {k for k in before_owner if k >= 0}
+        slots, copies = pool.plan(keys)
+        # every key of the union is resident in the slot returned for it
+        assert all(pool.owner[s] == k and pool.slot_of[k] == s for k, s in zip(keys, slots))
+        assert len(set(slots)) == len(slots)
+        # copies are exactly the keys not resident before, in union order
+        assert [k for k, _ in copies] == [k for k in keys if k not in resident_before]
+        # the slots taken are the (stamp, id)-smallest of the slots no hit used
+        hit_slots = {before_owner.index(k) for k in keys if k in resident_before}
+        idle = sorted((before_stamp[s], s) for s in range(n_slots) if s not in hit_slots)
+        assert [s for _, s in copies] == [s for _, s in idle[:len(copies)]]
+        # residency table and slot owners agree
+        assert sum(1 for k in range(n_keys) if pool.slot_of[k] >= 0) == sum(1 for o in pool.owner if o >= 0)
+        assert all(pool.stamp[s] == pool.tick for s in slots)
