@@ -164,6 +164,24 @@ def start_clocks(torch_device, gpu_index: int):
         return Clocks(gpu_index)
 
 
+def _host_link_gbs(torch, dev) -> float:
+    """Pinned host -> device copy bandwidth (GB/s), best of 3 copies of 1 GiB: the denominator
+    of the streamed-expert copy."""
+    n = 1 << 30
+    hbuf = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    dbuf = torch.empty(n, dtype=torch.uint8, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = float("inf")
+    for _ in range(3):
+        e0.record()
+        dbuf.copy_(hbuf, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    del hbuf, dbuf
+    return n / (best * 1e-3) / 1e9
+
+
 def _traffic_from_profile(kernel_src: str, workload: str):
     """(DRAM bytes per FFN-step launch, union size of that launch) recorded in the committed
     ncu summary of this workload, if the kernel source is unchanged since the capture (sha256
@@ -280,24 +298,56 @@ def run_gpu(args, w, world, rank, local):
     B, L, K, E, d, F = w.tokens, w.layers, w.top_k, w.num_experts, w.d_model, w.ffn_dim
     desc = smoe.make_desc(d, E, K, F, w.layout, w.norm_topk_prob)
 
+    # streamed experts: every layer's experts in pinned host memory, one pool of S HBM slots
+    # shared by the layers (keys layer * E + expert)
+    S = w.stream_slots
+    streamed = S > 0
     # shared expert (if the workload has one): column slices, its own descriptor and workspace
     P = w.shared_slices
     sdesc = smoe.make_desc(d, P, P, w.shared_ffn_dim // P, w.layout, 1) if P else None
     sws = smoe.alloc_workspace(sdesc, B, dev) if P else None
+    def pinned_copy(v):
+        hv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+        hv.copy_(v)
+        return hv
+
     layers = []
     for l in range(L):
         wts = W.gen_layer_weights(w, l, device=dev)
+        host = None
+        if streamed:   # the layer's experts live in host memory only
+            wts = {k: pinned_copy(v) for k, v in wts.items()}
+            host = smoe.HostWeights(wts)
         bias = W.gen_gate_bias(w, l)
         layers.append({
             "shared": smoe.Weights(W.gen_shared_weights(w, l, device=dev)) if P else None,
-            "weights": smoe.Weights(wts), "wts": wts, "gate": W.gen_gate(w, l, device=dev).contiguous(),
+            "weights": None if streamed else smoe.Weights(wts), "host": host, "wts": wts,
+            "gate": W.gen_gate(w, l, device=dev).contiguous(),
+            "cl": torch.zeros(1 + 2 * E, dtype=torch.int32, device=dev),
             "bias": None if bias is None else bias.to(dev),
             "uid": torch.zeros(E, dtype=torch.int32, device=dev), "nu": torch.zeros(1, dtype=torch.int32, device=dev),
             "off": torch.zeros(E + 1, dtype=torch.int32, device=dev),
             "tl": torch.zeros(B * K, dtype=torch.int32, device=dev),
             "sl": torch.zeros(B * K, dtype=torch.int32, device=dev),
         })
-    x_in = W.gen_x(w, 0, B, device=dev).view(torch.int16).contiguous()
+    if streamed:
+        pool_t = smoe.pool_tensors(layers[0]["wts"], S, dev)
+        pool = smoe.Weights(pool_t)
+        pdesc = smoe.make_desc(d, S, K, F, w.layout, w.norm_topk_prob)
+        pws = smoe.alloc_workspace(pdesc, B, dev)
+        n_keys = L * E
+        sstate = smoe.alloc_stream_state(n_keys, S, dev)
+        slot_ids = torch.zeros(E, dtype=torch.int32, device=dev)
+        # one token per step from a correlated sequence: warm-up, 3 graph warm-ups, timed, e2e
+        T = max(3, args.warmup) + 3 + args.steps + 16
+        x_seq = W.gen_x_sequence(w, 0, T, w.seq_rho).to(dev).view(torch.int16).contiguous()
+        x_in = x_seq[0:1]
+    else:
+        x_in = W.gen_x(w, 0, B, device=dev).view(torch.int16).contiguous()
+
+    def x_of(i):
+        return x_seq[i % T:i % T + 1] if streamed else x_in
+
     ws = smoe.alloc_workspace(desc, B, dev)
     h = torch.empty(B, d, dtype=torch.float32, device=dev)
     xb = torch.empty(B, d, dtype=torch.int16, device=dev)
@@ -314,9 +364,10 @@ def run_gpu(args, w, world, rank, local):
         tc = dd % 512 == 0 and ff % 512 == 0 and dd <= 4096 and ff <= 4096 and b >= 256
         return 5 if tc else 4
     launches_per_layer = ((1 if w.chained else 0) + 2 + (1 if B * K <= 1024 else 3) + ffn_kernels(B, d, F) +
-                          (1 + ffn_kernels(B, d, w.shared_ffn_dim // P) if P else 0))
+                          (1 + ffn_kernels(B, d, w.shared_ffn_dim // P) if P else 0) + (2 if streamed else 0))
 
-    def step(x_dev, ev=None):
+    def step(x_dev, ev=None, rec=None):
+        # rec: per layer (n_union, copy list) buffers of this step (streamed), kept for the stats
         cur = torch.cuda.current_stream()   # the capture stream while a graph is captured
         h.copy_(x_dev.view(torch.bfloat16))
         for l, ly in enumerate(layers):
@@ -329,29 +380,50 @@ def run_gpu(args, w, world, rank, local):
                 smoe.smoe_route_ranked(desc, xl, ly["gate"], ly["bias"], idx, wt, spec_idx, spec_p, ws)
             else:
                 smoe.smoe_route(desc, xl, ly["gate"], ly["bias"], idx, wt, ws)
-            smoe.smoe_expert_union(desc, idx, ly["uid"], ly["nu"], ly["off"], ly["tl"], ly["sl"], ws)
+            nu = rec[l][0] if rec is not None else ly["nu"]
+            smoe.smoe_expert_union(desc, idx, ly["uid"], nu, ly["off"], ly["tl"], ly["sl"], ws)
+            if streamed:
+                cl = rec[l][1] if rec is not None else ly["cl"]
+                smoe.smoe_stream_plan(desc, B, l * E, ly["uid"], nu, sstate, n_keys, S, slot_ids, cl, ws)
+                if ev is not None:
+                    ev[l][2].record(cur)
+                smoe.smoe_stream_copy(desc, ly["host"], pool, S, cl, ws)
+                if ev is not None:
+                    ev[l][3].record(cur)
             if ev is not None:
                 ev[l][0].record(cur)
-            smoe.smoe_moe_ffn_batch(desc, ly["weights"], xl, ly["uid"], ly["nu"], ly["off"], ly["tl"], ly["sl"], wt,
-                                    h, ws)
+            if streamed:
+                smoe.smoe_moe_ffn_batch(pdesc, pool, xl, slot_ids, nu, ly["off"], ly["tl"], ly["sl"], wt, h, pws)
+            else:
+                smoe.smoe_moe_ffn_batch(desc, ly["weights"], xl, ly["uid"], nu, ly["off"], ly["tl"], ly["sl"], wt,
+                                        h, ws)
             if P:
                 smoe.smoe_shared_expert_ffn(sdesc, ly["shared"], xl, h, sws)
             if ev is not None:
                 ev[l][1].record(cur)
 
     smoe.smoe_clear_device_status(ws)
-    for _ in range(max(3, args.warmup)):
-        step(x_in)
-    bits = smoe.smoe_read_device_status(ws)
+    if streamed:
+        smoe.smoe_clear_device_status(pws)
+    n_warm = max(3, args.warmup)
+    for i in range(n_warm):
+        step(x_of(i))
+    bits = smoe.smoe_read_device_status(ws) | (smoe.smoe_read_device_status(pws) if streamed else 0)
     if bits:
         raise RuntimeError(f"device status {bits:#x} during warm-up")
+    c2c_peak = _host_link_gbs(torch, dev) if streamed else None
 
     # ---- timed region: inputs resident in HBM
     def ffn_event():
         # recorded inside a captured graph: an external event record node keeps it timeable
         return torch.cuda.Event(enable_timing=True, external=not args.eager)
 
-    evs = [[[ffn_event(), ffn_event()] for _ in range(L)] for _ in range(args.steps)]
+    # streamed: 3 extra graphs replayed as warm-up (each graph is one token of the sequence, so
+    # the timed graphs must not be replayed before the timed region)
+    n_graphs = args.steps + (3 if streamed else 0)
+    evs = [[[ffn_event() for _ in range(4 if streamed else 2)] for _ in range(L)] for _ in range(n_graphs)]
+    recs = [[(torch.zeros(1, dtype=torch.int32, device=dev), torch.zeros(1 + 2 * E, dtype=torch.int32, device=dev))
+             for _ in range(L)] for _ in range(n_graphs)] if streamed else [None] * n_graphs
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # A step that reads less than ~1 GB (every routed expert distinct, plus the gate matrices)
     # could find the previous step's experts in the 129 MB L2: such steps are timed one by one,
@@ -368,14 +440,16 @@ def run_gpu(args, w, world, rank, local):
         # same library calls; replaying them removes the host launch gaps between kernels
         cap = torch.cuda.Stream()
         cap.wait_stream(stream)
-        for s in range(args.steps):
+        for s in range(n_graphs):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=cap):
-                step(x_in, evs[s])
+                step(x_of(n_warm + s), evs[s], recs[s])
             graphs.append(g)
         stream.wait_stream(cap)
         for g in graphs[:3]:   # upload / warm the graphs
             g.replay()
+        if streamed:   # the warm-up tokens; the timed graphs follow them in the sequence
+            graphs, evs, recs = graphs[3:], evs[3:], recs[3:]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -389,7 +463,7 @@ def run_gpu(args, w, world, rank, local):
         if graphs:
             graphs[s].replay()
         else:
-            step(x_in, evs[s])
+            step(x_of(n_warm + s), evs[s], recs[s])
         if flush:
             step_evs[s][1].record(stream)
     t_end.record(stream)
@@ -401,12 +475,18 @@ def run_gpu(args, w, world, rank, local):
     ffn_ms = [evs[s][l][0].elapsed_time(evs[s][l][1]) for s in range(args.steps) for l in range(L)]
     ms_total = max_over_ranks(ms_total, world, dev)
     ms_step = ms_total / args.steps
-    bits = smoe.smoe_read_device_status(ws)
+    bits = smoe.smoe_read_device_status(ws) | (smoe.smoe_read_device_status(pws) if streamed else 0)
     if bits:
         raise RuntimeError(f"device status {bits:#x} in the timed region")
 
     # ---- algorithmic work (measured union sizes)
-    U = [int(ly["nu"].item()) for ly in layers]
+    if streamed:
+        U = [int(recs[-1][l][0].item()) for l in range(L)]
+        n_copied = sum(int(recs[s][l][1][0].item()) for s in range(args.steps) for l in range(L))
+        n_routed = sum(int(recs[s][l][0].item()) for s in range(args.steps) for l in range(L))
+        copy_ms = sum(evs[s][l][2].elapsed_time(evs[s][l][3]) for s in range(args.steps) for l in range(L))
+    else:
+        U = [int(ly["nu"].item()) for ly in layers]
     hbm, tf_burst, tf_sus, peak_kind = _peaks()
     ffn_bytes = [u * eb + w.shared_bytes + B * d * 2 + 2 * B * d * 4 for u in U]
     layer_bytes = [fb + E * d * 4 for fb in ffn_bytes]
@@ -430,23 +510,29 @@ def run_gpu(args, w, world, rank, local):
     union_gbs = world * sum(U) * eb / (ms_step * 1e-3) / 1e9
 
     # ---- end to end through host buffers: pinned H2D of x, D2H of the final hidden state
-    x_host = x_in.cpu().pin_memory()
+    # (streamed: the tokens after the timed ones, one per step)
+    tok0 = n_warm + 3 + args.steps
+    x_host = (x_seq.cpu() if streamed else x_in.cpu()).pin_memory()
+
+    def x_host_of(i):
+        return x_host[i % T:i % T + 1] if streamed else x_host
+
     out_host = torch.empty(B, d, dtype=torch.float32).pin_memory()
     x_dev2 = torch.empty_like(x_in)
     e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for _ in range(2):
-        x_dev2.copy_(x_host, non_blocking=True)
+    for i in range(2):
+        x_dev2.copy_(x_host_of(tok0 + i), non_blocking=True)
         step(x_dev2)
         out_host.copy_(h, non_blocking=True)
     torch.cuda.synchronize()
     e2e_steps = max(3, min(args.steps, 10))
     e2e_total = 0.0
     e_s.record(stream)
-    for _ in range(e2e_steps):
+    for i in range(e2e_steps):
         if flush:
             flush_buf.fill_(1)
             e_s.record(stream)
-        x_dev2.copy_(x_host, non_blocking=True)
+        x_dev2.copy_(x_host_of(tok0 + 2 + i), non_blocking=True)
         step(x_dev2)
         out_host.copy_(h, non_blocking=True)
         if flush:
@@ -489,12 +575,30 @@ def run_gpu(args, w, world, rank, local):
         # the capture is of one layer; scale to the timed layers' mean union by algorithmic bytes
         cap_bytes, cap_u = rec
         traffic = cap_bytes * ffn_bytes_mean / (cap_u * eb + w.shared_bytes + B * d * 2 + 2 * B * d * 4)
+    ffn_roof = dict(roof, traffic=traffic if not tensor_bound else None,
+                    kernel="expert FFN step (smoe_moe_ffn_batch: gather, gate/up+SwiGLU, down, combine"
+                           + (", and smoe_shared_expert_ffn)" if P else ")"))
+    stream_info = None
+    if streamed:
+        # the dominant kernel of a streamed step is the slot copy: host-link bound
+        c2c = n_copied * eb / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else 0.0
+        stream_info = {"slots": S, "keys": n_keys, "seq_rho": w.seq_rho,
+                       "hit_rate": 1.0 - n_copied / max(1, n_routed),
+                       "experts_copied_per_step": n_copied / args.steps,
+                       "host_bytes_per_step": n_copied * eb / args.steps,
+                       "ffn_roofline": ffn_roof}
+        roof_line = {"bound": "c2c", "achieved": c2c, "peak": c2c_peak, "unit": "GB/s",
+                     "frac": c2c / c2c_peak if c2c_peak else None, "traffic": None,
+                     "peak_kind": "measured in this run: pinned host -> device cudaMemcpyAsync, 1 GiB, best of 3",
+                     "kernel": "smoe_stream_copy (missed experts, pinned host memory -> HBM slots)"}
+    else:
+        roof_line = ffn_roof
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
         "config": {"workload": w.name, "tokens": B, "layers": L, "d_model": d, "experts": E, "top_k": K,
-                   "spec_ranks": w.spec, "shared_ffn_dim": w.shared_ffn_dim,
+                   "spec_ranks": w.spec, "shared_ffn_dim": w.shared_ffn_dim, "stream_slots": S,
                    "norm_topk_prob": w.norm_topk_prob,
                    "ffn_dim": F, "layout": w.layout, "weights": "4-bit affine g64, bf16 scales/biases",
                    "l2": (f"L2 flushed between timed steps (256 MiB write outside the step events): a step "
@@ -504,10 +608,11 @@ def run_gpu(args, w, world, rank, local):
                    "launch": "eager" if args.eager else "one CUDA graph per step, replayed"},
         "union_expert_gbs": union_gbs,
         "union_sizes": U,
-        "step_roofline_frac": t_roof_step / (ms_step * 1e-3),
-        "roofline": dict(roof, traffic=traffic if not tensor_bound else None,
-                         kernel="expert FFN step (smoe_moe_ffn_batch: gather, gate/up+SwiGLU, down, combine"
-                               + (", and smoe_shared_expert_ffn)" if P else ")")),
+        # streamed: the step cannot beat its bytes over the host link either
+        "step_roofline_frac": max(t_roof_step, (n_copied * eb / args.steps / (c2c_peak * 1e9)) if streamed else 0.0)
+                              / (ms_step * 1e-3),
+        "roofline": roof_line,
+        "stream": stream_info,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": B * d * 2, "d2h_bytes_per_step": B * d * 4},
         "gpu_launches": launches_per_layer * L * args.steps,

@@ -72,6 +72,7 @@ typedef enum {
 #define SMOE_FAULT_FP16_RANGE   0x2u  /* |silu(g) * v| exceeded the fp16 range           */
 #define SMOE_FAULT_TIMEOUT      0x4u  /* a bounded wait for an async weight copy gave up   */
 #define SMOE_FAULT_TOKEN_INDEX  0x8u  /* a token list entry outside [0, B)                 */
+#define SMOE_FAULT_SLOT_POOL    0x10u /* a streamed-expert plan or copy entry out of range */
 
 /* Layer descriptor: the subset of the model config the MoE block needs
  * (page "Surface Scout", "The Model Config": d_model, ffn_dim, max_experts_per_layer,
@@ -197,6 +198,63 @@ SMOE_API smoe_status smoe_moe_layer(const smoe_layer_desc* desc, const smoe_expe
  * synthetic layers whose weights are not zero-mean, see the design notes). */
 SMOE_API smoe_status smoe_rmsnorm_bf16(const float* h, float eps, int32_t center, int32_t B, int32_t d,
                                        uint16_t* x_out, void* stream);
+
+/* ---- Experts streamed from host memory into a pool of HBM slots ------------------------
+ * Page "Data Flow", "Ring Buffer State Machine": the expert weights live in a ring of slots
+ * keyed by (layer, expert); a slot keeps its expert after use and a later request for the same
+ * key is a hit; a miss takes an EMPTY slot, else the least recently used idle slot (never one
+ * the current pass reads), and a freshly loaded slot carries the new tick.  "Handling Misses":
+ * correctness never depends on the cache.  Page "Layer-Major Batched Prefill", "Retention,
+ * never replay": reuse comes from keeping what was read, never from guessing.
+ * Here the layers' expert tensors stay in pinned host memory (on GB300: Grace memory, read by
+ * the GPU over NVLink-C2C) and a pool of n_slots experts lives in HBM.  Per layer, after
+ * smoe_expert_union:
+ *   smoe_stream_plan  -> slot_ids (the union's experts as slots of the pool) + copy_list
+ *   smoe_stream_copy  -> the missed experts' bytes from host memory into their slots
+ *   smoe_moe_ffn_batch with a pool descriptor (num_experts = n_slots), the pool tensors and
+ *                       slot_ids as union_ids: the same results, bit for bit, as the
+ *                       resident layer
+ * Everything is decided on the device (no host synchronisation); calls on one state must be
+ * ordered on one stream.
+ *
+ * State: int32 [4 + n_keys + 2 * n_slots] device buffer of smoe_stream_state_bytes(n_keys,
+ * n_slots) bytes (0 for invalid sizes), set up by smoe_stream_init and owned by the caller.  A
+ * key is key_base + expert (for instance layer * num_experts + expert); n_slots <= 256. */
+SMOE_API size_t smoe_stream_state_bytes(int32_t n_keys, int32_t n_slots);
+
+/* Empty pool: no key resident, every slot empty, tick 0 (asynchronous). */
+SMOE_API smoe_status smoe_stream_init(void* state, int32_t n_keys, int32_t n_slots, void* stream);
+
+/* Residency plan of one layer call.  The tick advances by one; every union expert that a slot
+ * holds is a hit and its slot is re-stamped; the misses, in union order, take the idle slots
+ * (slots no hit of this call uses) in order of (stamp, slot id) -- empty slots first, then the
+ * least recently used, slots of equal stamp lowest id first -- evicting their previous keys.
+ *   union_ids, n_union  as produced by smoe_expert_union for desc, B
+ *   slot_ids   int32 [num_experts]: slot of union position u (u < n_union)
+ *   copy_list  int32 [1 + 2 * num_experts]: [0] = number of misses m, then m pairs (expert,
+ *              slot) in union order, the input of smoe_stream_copy
+ * SMOE_ERR_INVALID_ARG if key_base + num_experts > n_keys or n_slots < min(B * top_k,
+ * num_experts) (a union must fit).  A union id outside [0, num_experts) or a state set up for
+ * other sizes sets SMOE_FAULT_SLOT_POOL, slot_ids -1 and no copies.  workspace: the layer's
+ * (status word). */
+SMOE_API smoe_status smoe_stream_plan(const smoe_layer_desc* desc, int32_t B, int32_t key_base,
+                                      const int32_t* union_ids, const int32_t* n_union, void* state,
+                                      int32_t n_keys, int32_t n_slots, int32_t* slot_ids, int32_t* copy_list,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Copy the experts of copy_list from the layer's tensors into their pool slots.
+ *   host_weights  the layer's [num_experts, ...] tensors (layout of desc) in pinned host memory
+ *                 (or device / managed memory); the GPU reads them directly
+ *   pool_weights  device tensors of the same layout with n_slots experts: slot s of a tensor
+ *                 holds the bytes of the copied expert's row block
+ *   copy_list     as written by smoe_stream_plan
+ * SMOE_ERR_UNSUPPORTED for unaligned tensors or host memory the GPU cannot address
+ * (unregistered pageable memory).  An entry outside range sets SMOE_FAULT_SLOT_POOL and is
+ * skipped.  workspace: the layer's (status word). */
+SMOE_API smoe_status smoe_stream_copy(const smoe_layer_desc* desc, const smoe_expert_weights* host_weights,
+                                      const smoe_expert_weights* pool_weights, int32_t n_slots,
+                                      const int32_t* copy_list, void* workspace, size_t workspace_bytes,
+                                      void* stream);
 
 /* Step 1 without a workspace, for callers that cannot allocate device memory (a plugin
  * inside a host application that owns the device-memory budget, or a latency-critical loop

@@ -5,6 +5,8 @@
 #include <cudaTypedefs.h>
 #include <stddef.h>
 
+#include <algorithm>
+
 namespace smoe {
 namespace {
 
@@ -69,6 +71,44 @@ bool encode_group_map(CUtensorMap* map, const uint16_t* p, int64_t rows, int64_t
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Device-accessible address of memory the streamed-expert copy touches: pinned (registered)
+// host memory (read over NVLink-C2C / PCIe), device or managed memory; NULL otherwise.
+const void* device_view(const void* p) {
+    if (!p) return nullptr;
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged)
+        return at.devicePointer;
+    return nullptr;
+}
+
+// The tensors of one layer's experts as (host tensor, pool tensor, bytes per expert), in the
+// order of smoe_expert_weights' layout: words, scales, biases of each projection.
+int expert_tensors(const smoe_layer_desc& D, const smoe_expert_weights& H, const smoe_expert_weights& P,
+                   const void* (&src)[kStreamRegions], void* (&dst)[kStreamRegions], int64_t (&bytes)[kStreamRegions]) {
+    const int64_t d = D.d_model, F = D.ffn_dim;
+    int n = 0;
+    auto add = [&](const void* s, const void* t, int64_t rows, int64_t in) {
+        src[n] = s; dst[n] = const_cast<void*>(t); bytes[n] = rows * in / 2; ++n;                  // packed words
+    };
+    auto add_g = [&](const void* s, const void* t, int64_t rows, int64_t in) {
+        src[n] = s; dst[n] = const_cast<void*>(t); bytes[n] = rows * (in / kGroup) * 2; ++n;      // bf16 per group
+    };
+    if (D.layout == SMOE_LAYOUT_SEPARATE) {
+        add(H.w_gate, P.w_gate, F, d); add_g(H.s_gate, P.s_gate, F, d); add_g(H.b_gate, P.b_gate, F, d);
+        add(H.w_up, P.w_up, F, d);     add_g(H.s_up, P.s_up, F, d);     add_g(H.b_up, P.b_up, F, d);
+    } else {
+        add(H.w_gate_up, P.w_gate_up, 2 * F, d);
+        add_g(H.s_gate_up, P.s_gate_up, 2 * F, d);
+        add_g(H.b_gate_up, P.b_gate_up, 2 * F, d);
+    }
+    add(H.w_down, P.w_down, d, F); add_g(H.s_down, P.s_down, d, F); add_g(H.b_down, P.b_down, d, F);
+    return n;
 }
 
 smoe_status check_weights(const smoe_layer_desc& D, const smoe_expert_weights* W, FfnPointers* P) {
@@ -313,6 +353,77 @@ smoe_status smoe_rmsnorm_bf16(const float* h, float eps, int32_t center, int32_t
     if (!h || !x_out) return SMOE_ERR_INVALID_ARG;
     if (d % 4 || !aligned16(h) || (reinterpret_cast<uintptr_t>(x_out) & 7u)) return SMOE_ERR_UNSUPPORTED;
     return cuda_status(launch_rmsnorm(h, eps, center, B, d, x_out, static_cast<cudaStream_t>(stream)));
+}
+
+size_t smoe_stream_state_bytes(int32_t n_keys, int32_t n_slots) {
+    if (n_keys <= 0 || n_slots <= 0 || n_slots > kMaxExperts) return 0;
+    return stream_state_words(n_keys, n_slots) * sizeof(int32_t);
+}
+
+smoe_status smoe_stream_init(void* state, int32_t n_keys, int32_t n_slots, void* stream) {
+    if (!state || n_keys <= 0 || n_slots <= 0 || (reinterpret_cast<uintptr_t>(state) & 3u)) return SMOE_ERR_INVALID_ARG;
+    if (n_slots > kMaxExperts) return SMOE_ERR_UNSUPPORTED;
+    return cuda_status(launch_stream_init(static_cast<int32_t*>(state), n_keys, n_slots,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+smoe_status smoe_stream_plan(const smoe_layer_desc* desc, int32_t B, int32_t key_base, const int32_t* union_ids,
+                             const int32_t* n_union, void* state, int32_t n_keys, int32_t n_slots, int32_t* slot_ids,
+                             int32_t* copy_list, void* workspace, size_t workspace_bytes, void* stream) {
+    smoe_status st = check_desc(desc);
+    if (st != SMOE_OK) return st;
+    if (B < 0 || n_keys <= 0 || n_slots <= 0 || key_base < 0) return SMOE_ERR_INVALID_ARG;
+    if (n_slots > kMaxExperts) return SMOE_ERR_UNSUPPORTED;
+    if ((int64_t)key_base + desc->num_experts > n_keys) return SMOE_ERR_INVALID_ARG;
+    // every union fits: at most min(B * top_k, num_experts) experts, all held at once
+    const int64_t need = std::min<int64_t>((int64_t)B * desc->top_k, desc->num_experts);
+    if (n_slots < need) return SMOE_ERR_INVALID_ARG;
+    if (B == 0) return SMOE_OK;
+    if (!union_ids || !n_union || !state || !slot_ids || !copy_list || (reinterpret_cast<uintptr_t>(state) & 3u))
+        return SMOE_ERR_INVALID_ARG;
+    WsLayout L;
+    if ((st = check_ws(*desc, B, workspace, workspace_bytes, &L)) != SMOE_OK) return st;
+    return cuda_status(launch_stream_plan(static_cast<int32_t*>(state), n_keys, n_slots, key_base, desc->num_experts,
+                                          union_ids, n_union, slot_ids, copy_list,
+                                          ws_ptr<uint32_t>(workspace, L.status), static_cast<cudaStream_t>(stream)));
+}
+
+smoe_status smoe_stream_copy(const smoe_layer_desc* desc, const smoe_expert_weights* host_weights,
+                             const smoe_expert_weights* pool_weights, int32_t n_slots, const int32_t* copy_list,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    smoe_status st = check_desc(desc);
+    if (st != SMOE_OK) return st;
+    if (!host_weights || !pool_weights || !copy_list || n_slots <= 0) return SMOE_ERR_INVALID_ARG;
+    if (n_slots > kMaxExperts) return SMOE_ERR_UNSUPPORTED;
+    const void* src[kStreamRegions];
+    void* dst[kStreamRegions];
+    int64_t bytes[kStreamRegions];
+    const int n = expert_tensors(*desc, *host_weights, *pool_weights, src, dst, bytes);
+    for (int r = 0; r < n; ++r) {
+        if (!src[r] || !dst[r]) return SMOE_ERR_INVALID_ARG;
+        if (!aligned16(src[r]) || !aligned16(dst[r]) || bytes[r] % 16) return SMOE_ERR_UNSUPPORTED;
+    }
+    WsLayout L;
+    if ((st = check_ws(*desc, 1, workspace, workspace_bytes, &L)) != SMOE_OK) return st;
+    StreamCopyArgs a{};
+    a.n_regions = n;
+    a.pieces_per_copy = 0;
+    for (int r = 0; r < n; ++r) {
+        // host tensors must be pinned (or device / managed) memory: the kernel reads them directly
+        const void* s = device_view(src[r]);
+        const void* t = device_view(dst[r]);
+        if (!s || !t) return SMOE_ERR_UNSUPPORTED;
+        a.region[r].src = static_cast<const uint4*>(s);
+        a.region[r].dst = static_cast<uint4*>(const_cast<void*>(t));
+        a.region[r].n16 = bytes[r] / 16;
+        a.region[r].pieces = (int)stream_pieces(bytes[r] / 16);
+        a.pieces_per_copy += a.region[r].pieces;
+    }
+    a.list = copy_list;
+    a.E = desc->num_experts;
+    a.S = n_slots;
+    a.status = ws_ptr<uint32_t>(workspace, L.status);
+    return cuda_status(launch_stream_copy(a, static_cast<cudaStream_t>(stream)));
 }
 
 smoe_status smoe_clear_device_status(void* workspace, void* stream) {

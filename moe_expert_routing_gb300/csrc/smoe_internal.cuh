@@ -111,6 +111,34 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
 cudaError_t launch_rmsnorm(const float* h, float eps, int center, int B, int d, uint16_t* x_out,
                            cudaStream_t stream);
 
+// ----------------------------------------------------------------------------- streamed experts
+// One weight tensor of a layer for the slot copy: expert e's part starts at src + e * n16 in
+// host memory (device-accessible address), slot s's at dst + s * n16 in the pool; n16 =
+// 16-byte units per expert, pieces = 32 KB pieces per expert.
+struct StreamRegion {
+    const uint4* src;
+    uint4* dst;
+    int64_t n16;
+    int pieces;
+};
+constexpr int kStreamRegions = 9;   // separate layout: 3 projections x (words, scales, biases)
+struct StreamCopyArgs {
+    StreamRegion region[kStreamRegions];
+    int n_regions;
+    int pieces_per_copy;            // sum of the regions' pieces
+    const int32_t* list;            // [0] n, then (expert, slot) pairs
+    int E;                          // experts of the layer (host tensors)
+    int S;                          // slots of the pool
+    uint32_t* status;
+};
+size_t stream_state_words(int n_keys, int n_slots);
+int64_t stream_pieces(int64_t n16);
+cudaError_t launch_stream_init(int32_t* state, int n_keys, int n_slots, cudaStream_t stream);
+cudaError_t launch_stream_plan(int32_t* state, int n_keys, int n_slots, int key_base, int E, const int32_t* union_ids,
+                               const int32_t* n_union, int32_t* slot_ids, int32_t* copy_list, uint32_t* status,
+                               cudaStream_t stream);
+cudaError_t launch_stream_copy(const StreamCopyArgs& a, cudaStream_t stream);
+
 // ----------------------------------------------------------------------------- device helpers
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
     return __uint_as_float(bits16 << 16);

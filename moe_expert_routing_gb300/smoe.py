@@ -19,10 +19,12 @@ LIB_PATH = os.path.join(_HERE, "_build", "libsmoe.so")
 SMOE_OK, SMOE_ERR_INVALID_ARG, SMOE_ERR_UNSUPPORTED, SMOE_ERR_WORKSPACE, SMOE_ERR_CUDA, SMOE_ERR_DEVICE_FAULT = range(6)
 SMOE_LAYOUT_SEPARATE, SMOE_LAYOUT_FUSED_GATE_UP = 0, 1
 SMOE_FAULT_EXPERT_INDEX, SMOE_FAULT_FP16_RANGE, SMOE_FAULT_TIMEOUT, SMOE_FAULT_TOKEN_INDEX = 1, 2, 4, 8
+SMOE_FAULT_SLOT_POOL = 0x10
 
 EXPORTED = ("smoe_workspace_bytes", "smoe_route", "smoe_route_ranked", "smoe_expert_union", "smoe_moe_ffn_batch", "smoe_moe_layer",
             "smoe_shared_expert_ffn", "smoe_rmsnorm_bf16", "smoe_clear_device_status", "smoe_read_device_status", "smoe_status_string",
-            "smoe_route_noalloc")
+            "smoe_route_noalloc", "smoe_stream_state_bytes", "smoe_stream_init", "smoe_stream_plan",
+            "smoe_stream_copy")
 
 
 class SmoeError(RuntimeError):
@@ -65,13 +67,18 @@ def load_library(path: str = LIB_PATH):
         L.smoe_rmsnorm_bf16.argtypes = [vp, ctypes.c_float, i32, i32, i32, vp, vp]
         L.smoe_route_noalloc.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp]
         L.smoe_route_noalloc.restype = ctypes.c_int
+        L.smoe_stream_state_bytes.restype = sz
+        L.smoe_stream_state_bytes.argtypes = [i32, i32]
+        L.smoe_stream_init.argtypes = [vp, i32, i32, vp]
+        L.smoe_stream_plan.argtypes = [vp, i32, i32, vp, vp, vp, i32, i32, vp, vp, vp, sz, vp]
+        L.smoe_stream_copy.argtypes = [vp, vp, vp, i32, vp, vp, sz, vp]
         L.smoe_clear_device_status.argtypes = [vp, vp]
         L.smoe_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         L.smoe_status_string.restype = ctypes.c_char_p
         L.smoe_status_string.argtypes = [ctypes.c_int]
         for name in ("smoe_route", "smoe_route_ranked", "smoe_expert_union", "smoe_moe_ffn_batch", "smoe_moe_layer",
                      "smoe_shared_expert_ffn", "smoe_rmsnorm_bf16", "smoe_clear_device_status",
-                     "smoe_read_device_status"):
+                     "smoe_read_device_status", "smoe_stream_init", "smoe_stream_plan", "smoe_stream_copy"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -111,6 +118,15 @@ def make_desc(d_model: int, num_experts: int, top_k: int, ffn_dim: int, layout: 
                      SMOE_LAYOUT_SEPARATE if layout == "separate" else SMOE_LAYOUT_FUSED_GATE_UP)
 
 
+def _hp(t: torch.Tensor):
+    """Host address of a contiguous pinned CPU tensor (the streamed-expert copy reads it)."""
+    if t.is_cuda or not t.is_pinned():
+        raise ValueError("host expert tensors must be pinned CPU tensors")
+    if not t.is_contiguous():
+        raise ValueError("libsmoe takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
 @dataclass
 class Weights:
     """Expert weight tensors of one layer (CUDA); names as in smoe_expert_weights."""
@@ -122,7 +138,30 @@ class Weights:
         for name, _ in ExpertWeights._fields_:
             t = self.tensors.get(name)
             if t is not None:
-                setattr(self.struct, name, _p(t).value)
+                setattr(self.struct, name, self._ptr(t).value)
+
+    @staticmethod
+    def _ptr(t):
+        return _p(t)
+
+
+class HostWeights(Weights):
+    """Expert weight tensors of one layer in pinned host memory (smoe_stream_copy's source)."""
+
+    @staticmethod
+    def _ptr(t):
+        return _hp(t)
+
+
+def pin_weights(tensors: Dict[str, torch.Tensor]) -> HostWeights:
+    """Pinned host copies of a layer's expert tensors."""
+    return HostWeights({k: v.cpu().pin_memory() for k, v in tensors.items()})
+
+
+def pool_tensors(tensors: Dict[str, torch.Tensor], n_slots: int, device="cuda") -> Dict[str, torch.Tensor]:
+    """Empty device tensors shaped like a layer's expert tensors with n_slots experts."""
+    return {k: torch.empty((n_slots,) + tuple(v.shape[1:]), dtype=v.dtype, device=device)
+            for k, v in tensors.items()}
 
 
 # ------------------------------------------------------------------------------ C ABI calls
@@ -190,6 +229,38 @@ def smoe_shared_expert_ffn(desc, weights: Weights, x, residual, ws, stream=None)
 def smoe_rmsnorm_bf16(h, x_out, eps: float = 1e-6, center: int = 0, stream=None):
     _check(load_library().smoe_rmsnorm_bf16(_p(h), ctypes.c_float(eps), int(center), h.shape[0], h.shape[1],
                                             _p(x_out), _stream(stream)), "smoe_rmsnorm_bf16")
+
+
+def smoe_stream_state_bytes(n_keys: int, n_slots: int) -> int:
+    return int(load_library().smoe_stream_state_bytes(n_keys, n_slots))
+
+
+def alloc_stream_state(n_keys: int, n_slots: int, device="cuda", stream=None) -> torch.Tensor:
+    """A device state buffer for n_keys (layer, expert) keys and n_slots pool slots, initialised
+    to an empty pool."""
+    n = smoe_stream_state_bytes(n_keys, n_slots)
+    if n == 0:
+        raise SmoeError(SMOE_ERR_INVALID_ARG, "smoe_stream_state_bytes")
+    st = torch.empty(n // 4, dtype=torch.int32, device=device)
+    smoe_stream_init(st, n_keys, n_slots, stream)
+    return st
+
+
+def smoe_stream_init(state, n_keys: int, n_slots: int, stream=None):
+    _check(load_library().smoe_stream_init(_p(state), n_keys, n_slots, _stream(stream)), "smoe_stream_init")
+
+
+def smoe_stream_plan(desc, B: int, key_base: int, union_ids, n_union, state, n_keys: int, n_slots: int, slot_ids,
+                     copy_list, ws, stream=None):
+    _check(load_library().smoe_stream_plan(ctypes.byref(desc), B, key_base, _p(union_ids), _p(n_union), _p(state),
+                                           n_keys, n_slots, _p(slot_ids), _p(copy_list), _p(ws), ws.numel(),
+                                           _stream(stream)), "smoe_stream_plan")
+
+
+def smoe_stream_copy(desc, host_weights: Weights, pool_weights: Weights, n_slots: int, copy_list, ws, stream=None):
+    _check(load_library().smoe_stream_copy(ctypes.byref(desc), ctypes.byref(host_weights.struct),
+                                           ctypes.byref(pool_weights.struct), n_slots, _p(copy_list), _p(ws),
+                                           ws.numel(), _stream(stream)), "smoe_stream_copy")
 
 
 def smoe_clear_device_status(ws, stream=None):

@@ -115,6 +115,8 @@ class Workload:
     spec: int = 0                # ranks beyond top_k exported by the router (next-token bets)
     shared_ffn_dim: int = 0      # shared expert ffn width, 0 = none
     shared_slices: int = 0       # the shared expert is stored as this many column slices
+    stream_slots: int = 0        # > 0: experts in pinned host memory, a pool of this many HBM slots
+    seq_rho: float = 0.0         # streamed decode: AR(1) correlation of consecutive tokens
 
     @property
     def shared_bytes(self) -> int:
@@ -152,6 +154,11 @@ WORKLOADS: Dict[str, Workload] = {
     # norm_topk_prob, and a shared expert of ffn 20480 stored as 8 slices of 2560
     "qwen2_prefill64": Workload("qwen2_57b_a14b_prefill_b64_l8", 3584, 64, 8, 2560, 64, 8, "separate", 0.02,
                                 norm_topk_prob=0, chained=True, seed=6, shared_ffn_dim=20480, shared_slices=8),
+    # the decode chain with its experts in pinned host memory (Grace memory on GB300, read over
+    # NVLink-C2C): 8 chained layers, one token per step from a correlated sequence, one pool of
+    # 256 HBM slots shared by the layers
+    "stream_b1_l8": Workload("qwen3_235b_stream_decode_b1_l8", 4096, 128, 8, 1536, 1, 8, "separate", 0.02,
+                             chained=True, seed=7, stream_slots=256, seq_rho=0.9),
     # long skewed prompt: 4096 tokens, Zipf(1.1) logit bias, 4 chained layers
     "long4096": Workload("qwen3_235b_zipf_b4096_l4", 4096, 128, 8, 1536, 4096, 4, "separate", 0.02,
                          zipf_s=1.1, chained=True, seed=4),

@@ -163,3 +163,42 @@ def test_binding_refuses_cpu_tensors(lib):
     with pytest.raises(ValueError):
         smoe.smoe_rmsnorm_bf16(torch.zeros(2, 512), torch.zeros(2, 512, dtype=torch.int16))
     del d
+
+
+def test_stream_argument_errors(lib):
+    vp = ctypes.c_void_p
+    d = _desc()   # 128 experts, top-8
+    E, K = d.num_experts, d.top_k
+    assert lib.smoe_stream_state_bytes(0, 8) == 0
+    assert lib.smoe_stream_state_bytes(10, 0) == 0
+    assert lib.smoe_stream_state_bytes(10, 257) == 0
+    assert lib.smoe_stream_state_bytes(10, 8) == 4 * (4 + 10 + 2 * 8)
+    assert lib.smoe_stream_init(None, 10, 8, None) == smoe.SMOE_ERR_INVALID_ARG
+    assert lib.smoe_stream_init(vp(1026), 10, 8, None) == smoe.SMOE_ERR_INVALID_ARG
+    assert lib.smoe_stream_init(vp(1024), 10, 257, None) == smoe.SMOE_ERR_UNSUPPORTED
+
+    def plan(B=4, key_base=0, n_keys=2 * E, n_slots=64, uid=vp(1), ws=vp(4096)):
+        return lib.smoe_stream_plan(ctypes.byref(d), B, key_base, uid, vp(1), vp(1024), n_keys, n_slots, vp(1),
+                                    vp(1), ws, 1 << 30, None)
+    assert plan(key_base=E + 1) == smoe.SMOE_ERR_INVALID_ARG          # keys of the layer beyond n_keys
+    assert plan(key_base=-1) == smoe.SMOE_ERR_INVALID_ARG
+    assert plan(B=4, n_slots=4 * K - 1) == smoe.SMOE_ERR_INVALID_ARG  # a union of 32 experts cannot fit
+    assert plan(B=64, n_slots=E - 1) == smoe.SMOE_ERR_INVALID_ARG     # min(B K, E) = E
+    assert plan(n_slots=257) == smoe.SMOE_ERR_UNSUPPORTED
+    assert plan(B=0, uid=None) == smoe.SMOE_OK                         # empty batch: nothing to plan
+    assert plan(uid=None) == smoe.SMOE_ERR_INVALID_ARG
+    assert plan(ws=vp(4097)) == smoe.SMOE_ERR_WORKSPACE
+
+    W = smoe.ExpertWeights()
+    assert lib.smoe_stream_copy(ctypes.byref(d), None, ctypes.byref(W), 64, vp(1), vp(4096), 1 << 30,
+                                None) == smoe.SMOE_ERR_INVALID_ARG
+    assert lib.smoe_stream_copy(ctypes.byref(d), ctypes.byref(W), ctypes.byref(W), 64, vp(1), vp(4096), 1 << 30,
+                                None) == smoe.SMOE_ERR_INVALID_ARG      # separate layout, NULL tensors
+    H = smoe.ExpertWeights()
+    for name, _ in smoe.ExpertWeights._fields_:
+        setattr(H, name, 4096)
+    H.w_down = 4096 + 8                                                  # misaligned
+    assert lib.smoe_stream_copy(ctypes.byref(d), ctypes.byref(H), ctypes.byref(H), 64, vp(1), vp(4096), 1 << 30,
+                                None) == smoe.SMOE_ERR_UNSUPPORTED
+    assert lib.smoe_stream_copy(ctypes.byref(d), ctypes.byref(H), ctypes.byref(H), 300, vp(1), vp(4096), 1 << 30,
+                                None) == smoe.SMOE_ERR_UNSUPPORTED
