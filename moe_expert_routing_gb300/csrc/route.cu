@@ -14,8 +14,9 @@
 //                       partials are summed in a fixed order by the top-k kernel, so results
 //                       are deterministic.
 //   topk_kernel         one CTA per token: sums the partials (+ bias) with one thread per
-//                       expert, then K rounds of a warp arg-max (ties -> lower expert id),
-//                       softmax weights.
+//                       expert, selects the experts of ranks 0..K-1 (descending logit, ties ->
+//                       lower expert id; by parallel rank counting for small batches, by K
+//                       rounds of a warp arg-max for large ones), softmax weights.
 #include "smoe_internal.cuh"
 
 #include <math.h>
