@@ -100,7 +100,7 @@ def test_stream_plan_bad_union_id_sets_fault():
     smoe.smoe_clear_device_status(ws)
 
 
-STREAM_CASES = [("toy", None, 24), ("decode_b8", None, 72), ("q35_prefill64", 8, 128)]
+STREAM_CASES = [("toy", None, 24), ("decode_b8", None, 72), ("q35_prefill64", 8, 128), ("long4096", 512, 128)]
 
 
 @pytest.mark.parametrize("name,B,S", STREAM_CASES)
