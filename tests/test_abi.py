@@ -202,3 +202,11 @@ def test_stream_argument_errors(lib):
                                 None) == smoe.SMOE_ERR_UNSUPPORTED
     assert lib.smoe_stream_copy(ctypes.byref(d), ctypes.byref(H), ctypes.byref(H), 300, vp(1), vp(4096), 1 << 30,
                                 None) == smoe.SMOE_ERR_UNSUPPORTED
+
+
+def test_host_weights_must_be_pinned(lib):
+    import torch
+    with pytest.raises(ValueError):
+        smoe.HostWeights({"w_down": torch.zeros(4, 8, dtype=torch.int32)})   # pageable CPU memory
+    with pytest.raises(ValueError):
+        smoe.HostWeights({"w_down": torch.zeros(4, 8, dtype=torch.int32)[:, ::2]})
