@@ -474,20 +474,15 @@ def test_oracle_row_subset_matches_full():
 
 
 # ----------------------------------------------------------------------------- slot pool
-# Worked by hand from the retention rule of "Data Flow", "Ring Buffer State Machine": empty
-# slots first, then the least recently used idle slot; slots of the current union are in use.
-SLOT_POOL_CASE = [   # (keys of the call, slots expected, copies expected); 3 slots
-    ([0, 1], [0, 1], [(0, 0), (1, 1)]),     # tick 1: both miss, empty slots 0 and 1
-    ([1, 2], [1, 2], [(2, 2)]),             # tick 2: 1 hits; 2 takes empty slot 2 (stamp -1 < 1)
-    ([0, 3], [0, 1], [(3, 1)]),             # tick 3: 0 hits; slots 1, 2 idle at stamp 2 -> lower id
-    ([4], [2], [(4, 2)]),                   # tick 4: slot 2 (stamp 2) is older than 0, 1 (stamp 3)
-    ([1, 3], [0, 1], [(1, 0)]),             # tick 5: 3 hits in slot 1; 1 was evicted, takes slot 0 (3)
-]
+def _slot_pool_case():
+    fx = json.load(open(os.path.join(GOLDEN, "slot_pool_handworked.json")))
+    return fx["n_keys"], fx["n_slots"], [(c["keys"], c["slots"], [tuple(p) for p in c["copies"]]) for c in fx["calls"]]
 
 
 def test_slot_pool_hand_worked():
-    pool = oracle.SlotPool(n_keys=8, n_slots=3)
-    for keys, slots, copies in SLOT_POOL_CASE:
+    n_keys, n_slots, calls = _slot_pool_case()
+    pool = oracle.SlotPool(n_keys=n_keys, n_slots=n_slots)
+    for keys, slots, copies in calls:
         got_s, got_c = pool.plan(keys)
         assert got_s == slots and got_c == copies, (keys, got_s, got_c)
 
@@ -511,9 +506,10 @@ def test_slot_pool_planted_mru_eviction_fails_the_pin():
                 fresh = self.stamp
                 self.stamp = [self.tick if f == self.tick else saved[i] for i, f in enumerate(fresh)]
 
-    pool = MostRecent(n_keys=8, n_slots=3)
-    results = [pool.plan(keys) for keys, _, _ in SLOT_POOL_CASE]
-    assert results != [(s, c) for _, s, c in SLOT_POOL_CASE]
+    n_keys, n_slots, calls = _slot_pool_case()
+    pool = MostRecent(n_keys=n_keys, n_slots=n_slots)
+    results = [pool.plan(keys) for keys, _, _ in calls]
+    assert results != [(s, c) for _, s, c in calls]
 
 
 def test_slot_pool_retains_a_cycle_that_fits():
