@@ -20,7 +20,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import subprocess
 import sys
 import time
@@ -182,25 +181,24 @@ def _host_link_gbs(torch, dev) -> float:
     return n / (best * 1e-3) / 1e9
 
 
-def _traffic_from_profile(kernel_src: str, workload: str):
-    """(DRAM bytes per FFN-step launch, union size of that launch) recorded in the committed
-    ncu summary of this workload, if the kernel source is unchanged since the capture (sha256
-    of csrc/ffn.cu must match); else None."""
-    path = os.path.join(ROOT, "profiles", "expert_ffn_prefill64.md")
+def _traffic_from_profile(workload: str):
+    """(DRAM bytes per FFN-step launch, union size of that launch) from the JSON record written
+    beside the committed ncu summary of this workload, if every kernel source it names is
+    unchanged since the capture (sha256 match); else None."""
+    path = os.path.join(ROOT, "profiles", f"expert_ffn_{workload}.traffic.json")
     try:
-        text = open(path).read()
-    except OSError:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    m_wl = re.search(r"workload:\s*(\S+)", text)
-    if not m_wl or m_wl.group(1) != workload:
+    try:
+        for src, sha in rec["sources_sha256"].items():
+            with open(os.path.join(ROOT, src), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != sha:
+                    return None
+        return int(rec["dram_bytes_per_ffn_call"]), int(rec["union_experts"])
+    except (OSError, KeyError, TypeError, ValueError):
         return None
-    m_sha = re.search(r"ffn\.cu sha256:\s*([0-9a-f]{64})", text)
-    m_b = re.search(r"dram bytes per smoe_moe_ffn_batch launch:\s*([0-9]+)", text)
-    m_u = re.search(r"union experts of the captured launch:\s*([0-9]+)", text)
-    if not m_sha or not m_b or not m_u:
-        return None
-    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-    return (int(m_b.group(1)), int(m_u.group(1))) if sha == m_sha.group(1) else None
 
 
 # ------------------------------------------------------------------------------ oracle timing
@@ -357,22 +355,30 @@ def run_gpu(args, w, world, rank, local):
     spec_idx = torch.empty(B, w.spec, dtype=torch.int32, device=dev) if w.spec else None
     spec_p = torch.empty(B, w.spec, dtype=torch.float32, device=dev) if w.spec else None
     stream = torch.cuda.current_stream()
-    # kernels per layer: glue norm, router (2), union (1, or 3 above 1024 entries), FFN (gather,
-    # two passes or the both-pass + two tensor-core passes, combine), shared expert (slice
-    # routing + FFN)
+    # kernels per layer: router (2), union (1, or 3 above 1024 entries), FFN (gather, two passes
+    # or the both-pass + two tensor-core passes, combine), shared expert (slice routing + FFN),
+    # glue norm where it is not fused into the combine, slot plan + copy for streamed experts
     def ffn_kernels(b, dd, ff):
         tc = dd % 512 == 0 and ff % 512 == 0 and dd <= 4096 and ff <= 4096 and b >= 256
         return 5 if tc else 4
-    launches_per_layer = ((1 if w.chained else 0) + 2 + (1 if B * K <= 1024 else 3) + ffn_kernels(B, d, F) +
-                          (1 + ffn_kernels(B, d, w.shared_ffn_dim // P) if P else 0) + (2 if streamed else 0))
+    # chained stacks without a shared expert: the norm that feeds layer l+1 runs in layer l's
+    # combine kernel (smoe_moe_ffn_batch_norm); with a shared expert it follows the shared expert
+    fused_norm = w.chained and not P
+    launches_per_layer = (2 + (1 if B * K <= 1024 else 3) + ffn_kernels(B, d, F) +
+                          (1 + ffn_kernels(B, d, w.shared_ffn_dim // P) if P else 0) + (2 if streamed else 0) +
+                          (1 if w.chained and not fused_norm else 0))
+    launches_per_step = launches_per_layer * L + (1 if fused_norm else 0)
 
     def step(x_dev, ev=None, rec=None):
         # rec: per layer (n_union, copy list) buffers of this step (streamed), kept for the stats
         cur = torch.cuda.current_stream()   # the capture stream while a graph is captured
         h.copy_(x_dev.view(torch.bfloat16))
+        if fused_norm:
+            smoe.smoe_rmsnorm_bf16(h, xb, 1e-6, center=int(w.chain_center))
         for l, ly in enumerate(layers):
             if w.chained:
-                smoe.smoe_rmsnorm_bf16(h, xb, 1e-6, center=int(w.chain_center))
+                if not fused_norm:
+                    smoe.smoe_rmsnorm_bf16(h, xb, 1e-6, center=int(w.chain_center))
                 xl = xb
             else:
                 xl = x_dev
@@ -392,11 +398,12 @@ def run_gpu(args, w, world, rank, local):
                     ev[l][3].record(cur)
             if ev is not None:
                 ev[l][0].record(cur)
-            if streamed:
-                smoe.smoe_moe_ffn_batch(pdesc, pool, xl, slot_ids, nu, ly["off"], ly["tl"], ly["sl"], wt, h, pws)
+            wdesc, wts_l, uids, wsl = (pdesc, pool, slot_ids, pws) if streamed else (desc, ly["weights"], ly["uid"], ws)
+            if fused_norm and l + 1 < L:   # this layer's combine also writes layer l+1's input
+                smoe.smoe_moe_ffn_batch_norm(wdesc, wts_l, xl, uids, nu, ly["off"], ly["tl"], ly["sl"], wt, h, xb,
+                                             wsl, 1e-6, int(w.chain_center))
             else:
-                smoe.smoe_moe_ffn_batch(desc, ly["weights"], xl, ly["uid"], nu, ly["off"], ly["tl"], ly["sl"], wt,
-                                        h, ws)
+                smoe.smoe_moe_ffn_batch(wdesc, wts_l, xl, uids, nu, ly["off"], ly["tl"], ly["sl"], wt, h, wsl)
             if P:
                 smoe.smoe_shared_expert_ffn(sdesc, ly["shared"], xl, h, sws)
             if ev is not None:
@@ -488,7 +495,9 @@ def run_gpu(args, w, world, rank, local):
     else:
         U = [int(ly["nu"].item()) for ly in layers]
     hbm, tf_burst, tf_sus, peak_kind = _peaks()
-    ffn_bytes = [u * eb + w.shared_bytes + B * d * 2 + 2 * B * d * 4 for u in U]
+    # (+ the next layer's input, bf16, where the combine also writes it)
+    ffn_bytes = [u * eb + w.shared_bytes + B * d * 2 + 2 * B * d * 4 + (B * d * 2 if fused_norm and l + 1 < L else 0)
+                 for l, u in enumerate(U)]
     layer_bytes = [fb + E * d * 4 for fb in ffn_bytes]
     layer_flops = 6 * B * K * d * F + 6 * B * d * w.shared_ffn_dim + 2 * B * d * E
     t_roof_step = sum(max(bb / (hbm * 1e9), layer_flops / (tf_sus * 1e12)) for bb in layer_bytes)
@@ -569,7 +578,7 @@ def run_gpu(args, w, world, rank, local):
         cpu = {"value": units / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"first {n} of {B} tokens, {units // n} layer passes over the {L}-layer stack "
                          f"({units} token-layers), layer-major fp64 oracle, {dt:.1f} s"}
-    rec = _traffic_from_profile(os.path.join(ROOT, "moe_expert_routing_gb300", "csrc", "ffn.cu"), w.name)
+    rec = _traffic_from_profile(args.workload)
     traffic = None
     if rec is not None:
         # the capture is of one layer; scale to the timed layers' mean union by algorithmic bytes
@@ -615,7 +624,7 @@ def run_gpu(args, w, world, rank, local):
         "stream": stream_info,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": B * d * 2, "d2h_bytes_per_step": B * d * 4},
-        "gpu_launches": launches_per_layer * L * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

@@ -25,9 +25,9 @@
  *     Only smoe_read_device_status synchronises.
  *   - Argument errors are found on the host before anything is launched: the call returns
  *     an error status and enqueues nothing.  Faults found on the device (an expert index
- *     outside [0, E), an fp16 overflow of the SwiGLU activation) set bits in the status word
- *     kept at the start of the workspace; the kernels then skip the bad work and return,
- *     they never trap.  smoe_read_device_status reports them.
+ *     outside [0, E), a value outside the fp16 range of the tensor-core operands) set bits in
+ *     the status word kept at the start of the workspace; the kernels then skip the bad work
+ *     and return, they never trap.  smoe_read_device_status reports them.
  *   - bf16 values are passed as uint16_t bit patterns.
  *   - Supported shapes: group_size 64; d_model and ffn_dim each 256 or a multiple of 512
  *     (a row of scales or biases is 8 bytes or a multiple of 16); 1 <= top_k
@@ -69,9 +69,13 @@ typedef enum {
 
 /* Device status bits (smoe_read_device_status). */
 #define SMOE_FAULT_EXPERT_INDEX 0x1u  /* a routed expert id outside [0, num_experts)      */
-#define SMOE_FAULT_FP16_RANGE   0x2u  /* |silu(g) * v| exceeded the fp16 range           */
+#define SMOE_FAULT_FP16_RANGE   0x2u  /* an input x, one of its 64-group sums or a SwiGLU
+                                         activation silu(g) * v is outside the fp16 range
+                                         (or not finite); the outputs are then not
+                                         meaningful                                        */
 #define SMOE_FAULT_TIMEOUT      0x4u  /* a bounded wait for an async weight copy gave up   */
-#define SMOE_FAULT_TOKEN_INDEX  0x8u  /* a token list entry outside [0, B)                 */
+#define SMOE_FAULT_TOKEN_INDEX  0x8u  /* a token list entry outside [0, B): row 0 is read
+                                         in its place and the residual is not meaningful   */
 #define SMOE_FAULT_SLOT_POOL    0x10u /* a streamed-expert plan or copy entry out of range */
 
 /* Layer descriptor: the subset of the model config the MoE block needs
@@ -164,6 +168,25 @@ SMOE_API smoe_status smoe_moe_ffn_batch(const smoe_layer_desc* desc, const smoe_
                                const float* topk_w, float* residual,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/* Steps 3 + 4 followed by the norm that feeds the next block (page "Data Flow", "Serial Step
+ * Trace": the hidden state is RMS-normed before every FFN block): smoe_moe_ffn_batch, then
+ *   x_next = bf16(norm(residual))  exactly as smoe_rmsnorm_bf16(residual, eps, center) computes it
+ * (bit for bit), in the same kernel as the weighted combine (d_model <= 4096; wider rows run the
+ * standalone norm after the combine).
+ *   x_next  bf16 [B, d_model] out, 8-byte aligned; it may be the same buffer as x, which is no
+ *           longer read when x_next is written
+ *   eps, center  as smoe_rmsnorm_bf16
+ * Other arguments and errors as smoe_moe_ffn_batch; SMOE_ERR_INVALID_ARG for a NULL x_next, a
+ * negative eps or center outside {0, 1}.  After a routing fault (SMOE_FAULT_EXPERT_INDEX) the
+ * residual is left unchanged and x_next is not meaningful. */
+SMOE_API smoe_status smoe_moe_ffn_batch_norm(const smoe_layer_desc* desc, const smoe_expert_weights* weights,
+                                             const uint16_t* x, int32_t B, const int32_t* union_ids,
+                                             const int32_t* n_union, const int32_t* offsets,
+                                             const int32_t* token_list, const int32_t* slot_list,
+                                             const float* topk_w, float* residual, float eps, int32_t center,
+                                             uint16_t* x_next, void* workspace, size_t workspace_bytes,
+                                             void* stream);
+
 /* The shared expert (page "Data Flow", "Serial Step Trace": the shared expert FFN runs on
  * every token and residual += shared_out + routed_out; page "Surface Scout", "The Model
  * Config": shared_expert_ffn_dim, 0 when the model has none): residual += down(silu(gate x)
@@ -194,8 +217,11 @@ SMOE_API smoe_status smoe_moe_layer(const smoe_layer_desc* desc, const smoe_expe
  *   c = center ? mean_i h[t][i] : 0
  *   x_out[t][i] = bf16( (h[t][i] - c) / sqrt(mean_i (h[t][i] - c)^2 + eps) )
  *   h fp32 [B, d], x_out bf16 [B, d].  fp32 arithmetic, bf16 round to nearest even.
- * center = 0 is the pages' RMS norm; center = 1 first removes the row mean (used to chain
- * synthetic layers whose weights are not zero-mean, see the design notes). */
+ * center = 0 is the pages' RMS norm; center = 1 first removes the row mean.  Synthetic
+ * expert weights with q uniform on 0..15 and bias -8 scale have mean -scale/2, so every layer
+ * output carries a per-token common mode; chained through a plain RMS norm it turns the next
+ * layer's inputs into same-sign vectors that route to ever fewer experts.  Removing the row
+ * mean keeps the chained inputs zero-mean, as real hidden states are. */
 SMOE_API smoe_status smoe_rmsnorm_bf16(const float* h, float eps, int32_t center, int32_t B, int32_t d,
                                        uint16_t* x_out, void* stream);
 
@@ -264,10 +290,12 @@ SMOE_API smoe_status smoe_stream_copy(const smoe_layer_desc* desc, const smoe_ex
  * every GPU that loads it until the process exits).  A call needs B * num_experts <= 2^20
  * (B <= 8192 at 128 experts) and returns SMOE_ERR_UNSUPPORTED beyond that, without launching.
  * Up to B = 256 at 128 experts the results equal smoe_route's; beyond, fewer split-K partials
- * fit and the logits differ from smoe_route's by fp32 summation order only.  The first call on a device looks up
- * the array's address (cudaGetSymbolAddress) with that device current: make it before any
- * stream capture.  All calls share the array: calls that overlap on the GPU race and must be
- * ordered by the caller.  Allocates nothing. */
+ * fit and the logits differ from smoe_route's by fp32 summation order only.  The first call
+ * on a device looks up the array's address (cudaGetSymbolAddress) with that device current:
+ * make it before any stream capture.  The address is kept per CUDA context; after a device
+ * reset the next call is a first call again.  All calls share the array: calls that overlap
+ * on the GPU race and must be ordered by the caller.  Argument errors as smoe_route (no
+ * workspace errors).  Allocates nothing. */
 SMOE_API smoe_status smoe_route_noalloc(const smoe_layer_desc* desc, const uint16_t* x, const float* gate_w,
                                         const float* gate_bias, int32_t B, int32_t* topk_idx, float* topk_w,
                                         void* stream);

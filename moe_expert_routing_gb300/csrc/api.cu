@@ -16,6 +16,8 @@ size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
 // Descriptor checks shared by every call.  INVALID_ARG for values that make no sense,
 // UNSUPPORTED for sensible shapes the kernels do not handle.
 smoe_status check_desc(const smoe_layer_desc* D) {
@@ -33,6 +35,8 @@ smoe_status check_desc(const smoe_layer_desc* D) {
     if ((int64_t)D->d_model * D->ffn_dim > (int64_t)1 << 30) return SMOE_ERR_UNSUPPORTED;
     return SMOE_OK;
 }
+
+namespace {
 
 smoe_status check_ws(const smoe_layer_desc& D, int B, void* ws, size_t ws_bytes, WsLayout* L) {
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return SMOE_ERR_WORKSPACE;
@@ -291,6 +295,31 @@ smoe_status smoe_moe_ffn_batch(const smoe_layer_desc* desc, const smoe_expert_we
     if ((st = check_ws(*desc, B, workspace, workspace_bytes, &L)) != SMOE_OK) return st;
     return cuda_status(launch_ffn(*desc, P, x, B, union_ids, n_union, offsets, token_list, slot_list, topk_w,
                                   residual, workspace, L, static_cast<cudaStream_t>(stream)));
+}
+
+smoe_status smoe_moe_ffn_batch_norm(const smoe_layer_desc* desc, const smoe_expert_weights* weights,
+                                    const uint16_t* x, int32_t B, const int32_t* union_ids, const int32_t* n_union,
+                                    const int32_t* offsets, const int32_t* token_list, const int32_t* slot_list,
+                                    const float* topk_w, float* residual, float eps, int32_t center,
+                                    uint16_t* x_next, void* workspace, size_t workspace_bytes, void* stream) {
+    smoe_status st = check_desc(desc);
+    if (st != SMOE_OK) return st;
+    if (B < 0 || !(eps >= 0.f) || (center != 0 && center != 1)) return SMOE_ERR_INVALID_ARG;
+    if (B == 0) return SMOE_OK;
+    if (!x || !union_ids || !n_union || !offsets || !token_list || !slot_list || !topk_w || !residual || !x_next)
+        return SMOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(residual) || (reinterpret_cast<uintptr_t>(x_next) & 7u))
+        return SMOE_ERR_UNSUPPORTED;
+    FfnPointers P{};
+    if ((st = check_weights(*desc, weights, &P)) != SMOE_OK) return st;
+    WsLayout L;
+    if ((st = check_ws(*desc, B, workspace, workspace_bytes, &L)) != SMOE_OK) return st;
+    NextNorm next;
+    next.x_next = x_next;
+    next.eps = eps;
+    next.center = center;
+    return cuda_status(launch_ffn(*desc, P, x, B, union_ids, n_union, offsets, token_list, slot_list, topk_w,
+                                  residual, workspace, L, static_cast<cudaStream_t>(stream), false, next));
 }
 
 smoe_status smoe_moe_layer(const smoe_layer_desc* desc, const smoe_expert_weights* weights, const uint16_t* x,

@@ -188,12 +188,14 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
                 const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
                 __half hv[8];
                 float sa = 0.f;
+                float vmax = 0.f;
 #pragma unroll
                 for (int m = 0; m < 8; ++m) {
                     const float v = bf16_bits_to_float((m & 1) ? (wv[m >> 1] >> 16) : (wv[m >> 1] & 0xFFFFu));
                     const __half h = __float2half_rn((m & 1) ? v * 0.0625f : v);
                     hv[perm8(m)] = h;
                     sa += (m & 1) ? __half2float(h) * 16.f : __half2float(h);
+                    vmax = fmaxf(vmax, fabsf(v));
                 }
                 uint4 o;
                 o.x = (uint32_t)__half_as_ushort(hv[0]) | ((uint32_t)__half_as_ushort(hv[1]) << 16);
@@ -203,6 +205,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
                 orow[ch] = o;
 #pragma unroll
                 for (int off = 1; off < 8; off <<= 1) sa += __shfl_xor_sync(0xffffffffu, sa, off);
+                // an input (or a group sum, which the tensor cores take as fp16) outside the fp16
+                // range, or not finite (fmaxf drops NaN, the sum keeps it)
+                if (__any_sync(0xffffffffu, !(vmax <= 65504.f) || !(fabsf(sa) <= 65504.f)) && lane == 0)
+                    atomicOr(status, SMOE_FAULT_FP16_RANGE);
                 if ((lane & 7) == 0) {
                     const size_t i = (size_t)p * G + ch / 8;
                     sx[i] = sa;
@@ -221,8 +227,12 @@ constexpr int kMailbox = 4;                                // finished gate/up t
 
 // Which passes a launch of the expert-pass kernel runs.
 constexpr int kGateUp = 1, kDown = 2, kBoth = 3;
+constexpr bool has_publisher(int mode) { return mode == kBoth; }
+constexpr bool gate_up_only(int mode) { return mode == kGateUp; }
+constexpr bool down_only(int mode) { return mode == kDown; }
+constexpr bool claims(int mode) { return mode == kBoth; }   // atomic queue, down tiles wait per expert
 // consumer warps + a producer warp (+ a publisher warp when both passes share a launch)
-constexpr int pass_threads(int mode) { return 32 * (kConsumerWarps + 1 + (mode == kBoth)); }
+constexpr int pass_threads(int mode) { return 32 * (kConsumerWarps + 1 + has_publisher(mode)); }
 constexpr int kWBytes = 256 * 128;         // 256 weight rows x 32 u32 words (4 groups)
 constexpr int kXBoxBytes = 16 * 128;       // 16 activation rows x 64 fp16 (one group)
 constexpr int kTokChunk = 16;              // tokens per pass over the weights
@@ -236,9 +246,9 @@ constexpr int kSbBytes = 256 * 16;         // 256 rows x up to 8 bf16 (a table o
 // down tiles use 3 stages sized for them.
 template <int MODE>
 struct StageCfg {
-    static constexpr int kCount = MODE == kGateUp ? 4 : 3;
+    static constexpr int kCount = gate_up_only(MODE) ? 4 : 3;
     static constexpr int kXOff = kWBytes;
-    static constexpr int kSOff = kXOff + (MODE == kGateUp ? 4 : 8) * kXBoxBytes;
+    static constexpr int kSOff = kXOff + (gate_up_only(MODE) ? 4 : 8) * kXBoxBytes;
     static constexpr int kBOff = kSOff + kSbBytes;
     static constexpr int kSumOff = kBOff + kSbBytes;
     static constexpr int kSumBytes = kTokChunk * 4 * 4;
@@ -249,6 +259,7 @@ struct StageCfg {
 };
 static_assert(StageCfg<kGateUp>::kSmem <= 227 * 1024 - 3072, "gate/up pass shared memory");
 static_assert(StageCfg<kBoth>::kSmem <= 227 * 1024 - 3072, "expert pass shared memory");
+
 
 struct PassArgs {
     int64_t wrow0;        // pass 0: gate rows per expert in map_w0; pass 1: d
@@ -663,13 +674,13 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
 
     const int nu = *f.p[0].n_union;
     const int t0 = f.p[0].tiles_per_expert, n0 = nu * t0;
-    const int first_item = MODE == kDown ? n0 : 0;
-    const int n_items = MODE == kGateUp ? n0 : n0 + nu * f.p[1].tiles_per_expert;
-    int32_t* queue = f.ticket + (MODE == kDown ? 1 : 0);
+    const int first_item = down_only(MODE) ? n0 : 0;
+    const int n_items = gate_up_only(MODE) ? n0 : n0 + nu * f.p[1].tiles_per_expert;
+    int32_t* queue = f.ticket + (down_only(MODE) ? 1 : 0);
     uint32_t it = 0;
     bool poisoned = false;
 
-    if (MODE == kBoth && warp == kConsumerWarps + 1) {
+    if (has_publisher(MODE) && warp == kConsumerWarps + 1) {
         // ---------------------------------------------------------------- publisher (one thread)
         if (lane == 0) {
             for (uint32_t k = 0;; ++k) {
@@ -696,7 +707,7 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
             // one-pass launches: static round-robin (uniform items, no queue latency); both
             // passes: the ordered queue that makes the cross-CTA waits safe
             int sk = 0;
-            auto take = [&]() { return MODE == kBoth ? atomicAdd(queue, 1) : (int)(blockIdx.x + gridDim.x * sk++); };
+            auto take = [&]() { return claims(MODE) ? atomicAdd(queue, 1) : (int)(blockIdx.x + gridDim.x * sk++); };
             Claim cur = claim_item(f, first_item + take(), n0, n_items);
             int next_item = first_item + take();
             for (;;) {
@@ -714,7 +725,7 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
                 T.mine = a.tc_min <= 0 || T.p1 - T.p0 < a.tc_min;
                 if (!T.ok) atomicOr(a.status, SMOE_FAULT_EXPERT_INDEX);
                 if (T.ok && T.mine) {
-                    if (MODE == kBoth && cur.pass == 1) {
+                    if (claims(MODE) && cur.pass == 1) {
                         // every gate/up tile of this expert has published h and its group sums
                         // (an acquire load, not a fence: a fence would also wait for this
                         // thread's copies in flight)
@@ -756,7 +767,7 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
                             slot_meta[slot][5] = T.row;
                             mbar_expect_tx(full, tx);
                             const int tx0 = packed ? 0 : (st * 4) & ~7;   // 16-byte window of the stage's groups
-                            if (MODE == kGateUp || (MODE == kBoth && cur.pass == 0)) {
+                            if (gate_up_only(MODE) || (MODE == kBoth && cur.pass == 0)) {
                                 tma_load_2d(base, &map_gate, st * 32, (int)r0, full);
                                 tma_load_2d(base + 128 * 128, &map_up, st * 32, (int)r1, full);
                                 tma_load_2d(base + C::kSOff, &map_sg, tx0, ty0, full);
@@ -768,7 +779,7 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
                                     tma_load_2d(base + C::kXOff + q * kXBoxBytes, &map_xg, (st * 4 + q) * 64, pc,
                                                 full);
                                 tma_load_2d(base + C::kSumOff, &map_sx, st * 4, pc, full);
-                            } else if (MODE != kGateUp) {
+                            } else if (!gate_up_only(MODE)) {
                                 tma_load_2d(base, &map_down, st * 32, (int)r0, full);
                                 tma_load_2d(base + C::kSOff, &map_sd, tx0, ty0, full);
                                 tma_load_2d(base + C::kBOff, &map_bd, tx0, ty0, full);
@@ -814,7 +825,7 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
         // they run the same chunks and meet at the same named barriers; a down-only launch has
         // none, and each warp decides for itself (no cross-warp sync per chunk)
         const bool late = !mbar_wait(R.full + 8 * slot, (it / C::kCount) & 1u);
-        if (MODE == kDown ? __any_sync(0xffffffffu, late) : consumers_any(late)) {
+        if (down_only(MODE) ? __any_sync(0xffffffffu, late) : consumers_any(late)) {
             if (threadIdx.x == 0) atomicOr(f.p[0].status, SMOE_FAULT_TIMEOUT);
             break;
         }
@@ -829,16 +840,16 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
         T.p1 = meta[4];
         T.row = meta[5];
         const int n = min(kTokChunk, T.p1 - pc);
-        const bool gate_up = MODE == kGateUp || (MODE == kBoth && item < n0);
-        if constexpr (MODE != kDown) {
+        const bool gate_up = gate_up_only(MODE) || (MODE == kBoth && item < n0);
+        if constexpr (!down_only(MODE)) {
             if (gate_up) {
                 // both passes in this launch: publish the tile after its last chunk
-                const int done_uu = MODE == kBoth && pc + kTokChunk >= T.p1 ? item / t0 : -1;
+                const int done_uu = has_publisher(MODE) && pc + kTokChunk >= T.p1 ? item / t0 : -1;
                 if (n <= 8) consume_chunk<1, 0, MODE>(f.p[0], R, it, poisoned, T, pc, n, warp, lane, red, done_uu, M);
                 else consume_chunk<2, 0, MODE>(f.p[0], R, it, poisoned, T, pc, n, warp, lane, red, done_uu, M);
             }
         }
-        if constexpr (MODE != kGateUp) {
+        if constexpr (!gate_up_only(MODE)) {
             if (!gate_up) {
                 if (n <= 4)
                     consume_chunk<1, 1, MODE, true>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
@@ -850,7 +861,7 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
         if (poisoned) break;
     }
     // no more tiles to publish
-    if (MODE == kBoth && threadIdx.x == 0 && !mailbox_post(M, -1)) atomicOr(f.p[0].status, SMOE_FAULT_TIMEOUT);
+    if (has_publisher(MODE) && threadIdx.x == 0 && !mailbox_post(M, -1)) atomicOr(f.p[0].status, SMOE_FAULT_TIMEOUT);
 }
 
 // ----------------------------------------------------------------------------- combine
@@ -893,6 +904,86 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     reinterpret_cast<float4*>(residual)[i] = acc;
 }
 
+// The combine followed by the norm that feeds the next block, one CTA of 256 threads per token
+// row (d <= 4096: a thread holds up to 4 float4 of the row): residual[t] += sum_k w y (the
+// combine_kernel's rank-ordered FMA chain), then x_next[t] = bf16(norm(residual[t])) with
+// rmsnorm_bf16_kernel's loop order and reductions, so both outputs equal combine_kernel +
+// rmsnorm_bf16_kernel bit for bit.  After a flagged routing fault (the union did not cover all
+// B*K entries) neither residual nor x_next is written.
+__global__ void __launch_bounds__(256) combine_norm_kernel(const float* __restrict__ y, const float* __restrict__ w,
+                                                           const int32_t* __restrict__ n_union,
+                                                           const int32_t* __restrict__ offsets, int B, int K, int d,
+                                                           float* __restrict__ residual, float eps, int center,
+                                                           uint16_t* __restrict__ x_next) {
+    __shared__ float red[8];
+    const int t = blockIdx.x;
+    const int n4 = d / 4;   // <= 1024
+    const bool covered = offsets[*n_union] == B * K;
+    const float* wt = w + (size_t)t * K;
+    float4* row = reinterpret_cast<float4*>(residual + (size_t)t * d);
+    float4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int i = threadIdx.x + 256 * j;
+        if (i >= n4) break;
+        const float4* yt = reinterpret_cast<const float4*>(y + (size_t)t * K * d) + i;
+        float4 acc = row[i];
+        for (int k0 = 0; k0 < K; k0 += 8) {
+            float wk[8];
+            float4 yv[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (k0 + q < K) {
+                    wk[q] = wt[k0 + q];
+                    yv[q] = yt[(size_t)(k0 + q) * n4];
+                }
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (k0 + q < K) {
+                    acc.x = fmaf(wk[q], yv[q].x, acc.x);
+                    acc.y = fmaf(wk[q], yv[q].y, acc.y);
+                    acc.z = fmaf(wk[q], yv[q].z, acc.z);
+                    acc.w = fmaf(wk[q], yv[q].w, acc.w);
+                }
+        }
+        v[j] = acc;
+    }
+    if (!covered) return;   // the same decision in every thread of the CTA
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (threadIdx.x + 256 * j < n4) row[threadIdx.x + 256 * j] = v[j];
+    float mean = 0.f;
+    if (center) {
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (threadIdx.x + 256 * j < n4) s += (v[j].x + v[j].y) + (v[j].z + v[j].w);
+        mean = block_sum256(s, red) / (float)d;
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (threadIdx.x + 256 * j < n4) {
+            const float a = v[j].x - mean, b = v[j].y - mean, c = v[j].z - mean, e = v[j].w - mean;
+            ss = fmaf(a, a, ss);
+            ss = fmaf(b, b, ss);
+            ss = fmaf(c, c, ss);
+            ss = fmaf(e, e, ss);
+        }
+    const float tot = block_sum256(ss, red);
+    const float inv = 1.0f / sqrtf(tot / (float)d + eps);
+    uint2* out = reinterpret_cast<uint2*>(x_next + (size_t)t * d);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (threadIdx.x + 256 * j < n4) {
+            const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn((v[j].x - mean) * inv));
+            const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn((v[j].y - mean) * inv));
+            const uint32_t c = __bfloat16_as_ushort(__float2bfloat16_rn((v[j].z - mean) * inv));
+            const uint32_t e = __bfloat16_as_ushort(__float2bfloat16_rn((v[j].w - mean) * inv));
+            out[threadIdx.x + 256 * j] = make_uint2(a | (b << 16), c | (e << 16));
+        }
+}
+
 }  // namespace
 
 // 2-D tensor map over a row-major buffer [rows, cols] of `esize`-byte elements.
@@ -911,7 +1002,8 @@ static bool encode_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataTyp
 cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uint16_t* x, int B,
                        const int32_t* union_ids, const int32_t* n_union, const int32_t* offsets,
                        const int32_t* token_list, const int32_t* slot_list, const float* topk_w,
-                       float* residual, void* ws, const WsLayout& L, cudaStream_t stream, bool all_tokens) {
+                       float* residual, void* ws, const WsLayout& L, cudaStream_t stream, bool all_tokens,
+                       const NextNorm& next) {
     const int d = D.d_model, F = D.ffn_dim, K = D.top_k, E = D.num_experts;
     const int BK = B * K;
     const int max_u = BK < E ? BK : E;
@@ -931,6 +1023,7 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     if (!(attr_done.load() & bit)) {
         cudaError_t e = cudaFuncSetAttribute(ffn_expert_kernel<kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              StageCfg<kGateUp>::kSmem);
+
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(ffn_expert_kernel<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      StageCfg<kDown>::kSmem);
@@ -993,6 +1086,7 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     fa.p[1] = b;
     fa.ticket = ticket;
     const int t0 = a.tiles_per_expert, t1 = b.tiles_per_expert;
+
     if (tc_min > 0) {
         // long prompts: experts with a few tokens each run both passes from one queue
         const int grid = std::min(sms, max_u * (t0 + t1));
@@ -1015,9 +1109,19 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
         }
     }
 
+    if (next.x_next && d <= 4096) {
+        combine_norm_kernel<<<B, 256, 0, stream>>>(y, topk_w, n_union, offsets, B, K, d, residual, next.eps,
+                                                   next.center, next.x_next);
+        return cudaGetLastError();
+    }
     const size_t n4 = (size_t)B * d / 4;
     combine_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, stream>>>(y, topk_w, n_union, offsets, B, K, d,
                                                                       residual);
+    if (next.x_next) {   // wider rows: the standalone norm after the combine
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return launch_rmsnorm(residual, next.eps, next.center, B, d, next.x_next, stream);
+    }
     return cudaGetLastError();
 }
 

@@ -317,6 +317,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     __shared__ __align__(8) uint64_t full_p[C::kP], empty_p[C::kP], full_b[C::kB], empty_b[C::kB];
     __shared__ __align__(8) uint64_t deq[C::kKa], empty_a[C::kKa];
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
+    __shared__ __align__(8) uint64_t mma_drain;   // commit of every MMA the issuer launched
     __shared__ uint32_t tmem_base_sh;
     __shared__ int pref[3 * (kMaxExperts + 1)];   // item prefix, union ids, list offsets
     __shared__ int tok_sh[2][TC_N], slot_sh[2][TC_N];
@@ -347,6 +348,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_init(smem_u32(&acc_full[b]), 1);
             mbar_init(smem_u32(&acc_empty[b]), 4);   // one arrival per epilogue warp
         }
+        mbar_init(smem_u32(&mma_drain), 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     if (warp == 1) {
@@ -391,6 +393,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                 }
             }
+            // the copies issued into the last kP slots land (bounded waits) before the CTA may
+            // exit and release its shared memory, also when another role gave up early
+            for (uint32_t i = ip > (uint32_t)C::kP ? ip - C::kP : 0u; i < ip; ++i)
+                mbar_wait(smem_u32(&full_p[i % C::kP]), (i / C::kP) & 1u);
         }
     } else if (warp == 14) {
         // ------------------------------------------------------------------ activation producer
@@ -420,6 +426,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                 }
             }
+            // as above: the issued activation copies land before the exit
+            for (uint32_t i = ib > (uint32_t)C::kB ? ib - C::kB : 0u; i < ib; ++i)
+                mbar_wait(smem_u32(&full_b[i % C::kB]), (i / C::kB) & 1u);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
@@ -456,6 +465,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 if (!poisoned) umma_commit(smem_u32(&acc_full[buf]));   // accumulators of this tile ready
             }
+            // every MMA this thread issued has completed (and stopped reading tensor and shared
+            // memory) before the CTA releases them, also when another role gave up early
+            umma_commit(smem_u32(&mma_drain));
+            mbar_wait(smem_u32(&mma_drain), 0u);
         }
     } else if (warp < 10) {
         // ------------------------------------------------------------------ dequantisers

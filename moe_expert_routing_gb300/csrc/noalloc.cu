@@ -14,10 +14,12 @@
 // fp32 summation order of the logits.
 //
 // Set-up: the first call on a device (with that device current) looks up the array's device
-// address with cudaGetSymbolAddress and caches it; make that first call before any stream
-// capture.  In host code the name g_route_scratch is only a host-side stand-in for the
-// symbol, never a usable device address, which is why the looked-up address is passed to
-// the kernels.
+// address with cudaGetSymbolAddress and caches it, keyed by the unique id of the device's
+// current CUDA context; make that first call before any stream capture.  A device reset (or
+// any teardown of the context) gives the next call a new context id, so the address is looked
+// up again (again a first call: before any capture).  In host code the name g_route_scratch
+// is only a host-side stand-in for the symbol, never a usable device address, which is why
+// the looked-up address is passed to the kernels.
 //
 // Sharing: every call on a device uses the same array and leaves the last call's partial
 // logits in it.  Nothing has to start at zero (each call overwrites every partial it reads),
@@ -38,19 +40,51 @@ static __device__ __align__(256) float g_route_scratch[kNoallocScratchFloats];
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 float* g_scratch_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_scratch_ctx[kMaxDevices] = {0};   // context id the address belongs to
 
-// Device address of g_route_scratch on the current device (looked up once per device).
+// Unique id of the calling thread's current CUDA context (0 if there is none yet or the driver
+// cannot say).
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = []() {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    }();
+    static PFN_cuCtxGetId_v12000 get_id = []() {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    }();
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_route_scratch in the current device's context (looked up once per
+// context).
 cudaError_t scratch_for_current_device(float** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
+    // before the runtime's first use of the device there is no current context (id 0): the
+    // look-up below creates it, and its id is read afterwards
+    const unsigned long long ctx = current_context_id();
+    if (!g_scratch_ptr[dev] || ctx == 0 || g_scratch_ctx[dev] != ctx) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_route_scratch);
         if (e != cudaSuccess) return e;
         g_scratch_ptr[dev] = static_cast<float*>(p);
+        g_scratch_ctx[dev] = current_context_id();
     }
     *out = g_scratch_ptr[dev];
     return cudaSuccess;
@@ -64,12 +98,8 @@ using namespace smoe;
 extern "C" SMOE_API smoe_status smoe_route_noalloc(const smoe_layer_desc* desc, const uint16_t* x,
                                                    const float* gate_w, const float* gate_bias, int32_t B,
                                                    int32_t* topk_idx, float* topk_w, void* stream) {
-    if (!desc) return SMOE_ERR_INVALID_ARG;
-    if (desc->d_model <= 0 || desc->num_experts <= 0 || desc->top_k <= 0 || desc->top_k > desc->num_experts ||
-        desc->ffn_dim <= 0 || desc->group_size <= 0 || (desc->norm_topk_prob != 0 && desc->norm_topk_prob != 1) ||
-        (desc->layout != SMOE_LAYOUT_SEPARATE && desc->layout != SMOE_LAYOUT_FUSED_GATE_UP))
-        return SMOE_ERR_INVALID_ARG;
-    if (smoe_workspace_bytes(desc, 1) == 0) return SMOE_ERR_UNSUPPORTED;   // shape the kernels do not take
+    const smoe_status st = check_desc(desc);
+    if (st != SMOE_OK) return st;
     if (B < 0) return SMOE_ERR_INVALID_ARG;
     if (B == 0) return SMOE_OK;
     if (!x || !gate_w || !topk_idx || !topk_w) return SMOE_ERR_INVALID_ARG;

@@ -6,20 +6,8 @@
 namespace smoe {
 namespace {
 
-// One CTA per row, float4 loads; the row mean (if centring) and the sum of squares are
-// reduced across the CTA in fp32.
-__device__ __forceinline__ float block_sum(float v, float* red) {
-#pragma unroll
-    for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) tot += red[w];
-    return tot;
-}
-
+// One CTA of 256 threads per row, float4 loads; the row mean (if centring) and the sum of
+// squares are reduced across the CTA in fp32 (block_sum256).
 __global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const float* __restrict__ h, float eps, int center, int d,
                                                            uint16_t* __restrict__ x_out) {
     __shared__ float red[8];
@@ -32,7 +20,7 @@ __global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const float* __restri
             const float4 v = row[i];
             s += (v.x + v.y) + (v.z + v.w);
         }
-        mean = block_sum(s, red) / (float)d;
+        mean = block_sum256(s, red) / (float)d;
     }
     float ss = 0.f;
     for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
@@ -43,7 +31,7 @@ __global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const float* __restri
         ss = fmaf(c, c, ss);
         ss = fmaf(e, e, ss);
     }
-    const float tot = block_sum(ss, red);
+    const float tot = block_sum256(ss, red);
     const float inv = 1.0f / sqrtf(tot / (float)d + eps);
     uint2* out = reinterpret_cast<uint2*>(x_out + (size_t)t * d);
     for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {

@@ -53,10 +53,9 @@ __device__ __forceinline__ void split3(float2 v, uint32_t& hi, uint32_t& mid, ui
 // rows (three bf16 terms), B = NT 8-token tiles of x, fp32 accumulators.  The loads of KB
 // k-steps are issued together before their products, so a warp has KB steps of its weight
 // and activation reads in flight (kchunk is a multiple of 16 * KB).
-template <int NT, int KB, int WARPS = 8>
-__global__ void __launch_bounds__(32 * WARPS) gate_logits_kernel(const uint16_t* __restrict__ x,
-                                                                 const float* __restrict__ W, int B, int E, int d,
-                                                                 int kchunk, float* __restrict__ partial) {
+template <int NT, int KB, int WARPS>
+__device__ __forceinline__ void gate_tile(const uint16_t* __restrict__ x, const float* __restrict__ W, int B, int E,
+                                          int d, int kchunk, float* __restrict__ partial) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const int e0 = blockIdx.y * (WARPS * 16) + warp * 16;
     if (e0 >= E) return;
@@ -119,6 +118,13 @@ __global__ void __launch_bounds__(32 * WARPS) gate_logits_kernel(const uint16_t*
         }
 }
 
+template <int NT, int KB, int WARPS = 8>
+__global__ void __launch_bounds__(32 * WARPS) gate_logits_kernel(const uint16_t* __restrict__ x,
+                                                                 const float* __restrict__ W, int B, int E, int d,
+                                                                 int kchunk, float* __restrict__ partial) {
+    gate_tile<NT, KB, WARPS>(x, W, B, E, d, kchunk, partial);
+}
+
 // Large batches: the same tile with the CTA's 64 token rows staged in shared memory piece by
 // piece (256 inputs at a time, cp.async), so the 8 warps read each activation once from
 // global memory instead of once per warp.  Rows padded by 16 bytes: the 8 rows a fragment
@@ -158,6 +164,14 @@ __global__ void __launch_bounds__(256) gate_logits_staged_kernel(const uint16_t*
         asm volatile("cp.async.wait_all;\n" ::: "memory");
         __syncthreads();
         if (e0 < E) {
+            // each piece accumulates on its own (48 MMAs), then adds into acc in IEEE fp32: the
+            // tensor core's accumulation is not IEEE-rounded, and one chain over thousands of
+            // inputs (a single split) drifts by ~1e-4 of the logit
+            float pacc[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) pacc[nt][i] = 0.f;
             for (int kb = 0; kb < kPiece; kb += 16 * KB) {
                 float2 wv[KB][4];
 #pragma unroll
@@ -185,10 +199,14 @@ __global__ void __launch_bounds__(256) gate_logits_staged_kernel(const uint16_t*
                         const uint32_t b1 = *reinterpret_cast<const uint32_t*>(xr + 8);
 #pragma unroll
                         for (int term = 2; term >= 0; --term)   // small terms first
-                            mma_bf16(acc[nt], a[term][0], a[term][1], a[term][2], a[term][3], b0, b1);
+                            mma_bf16(pacc[nt], a[term][0], a[term][1], a[term][2], a[term][3], b0, b1);
                     }
                 }
             }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[nt][i] += pacc[nt][i];
         }
         __syncthreads();   // the piece is consumed before the next one is staged
     }
@@ -204,62 +222,23 @@ __global__ void __launch_bounds__(256) gate_logits_staged_kernel(const uint16_t*
         }
 }
 
+// Tokens per CTA tile of the router: 8-token tiles up to 64 tokens (many small CTAs spread the
+// gate read widest; at 64 tokens one staged 64-token tile per split measured 4.8 us slower per
+// layer), 64-token tiles with the activations staged in shared memory beyond.
 int tile_tokens(int B) { return B <= 64 ? 8 : 64; }
 
-// One CTA per token.  Thread e sums expert e's split-K partials in split order (all loads
-// issued before the sum) and adds the bias.  The experts of ranks 0 .. K + n_spec - 1
-// (descending logit, ties -> lower expert id) are then found either by counting every
-// expert's rank in parallel (RANK: rank(e) = experts with a larger logit, or an equal logit
-// and a lower id; quickest for small batches, where one CTA's latency is the cost) or by
-// K + n_spec rounds of a warp arg-max over lanes holding experts l, l+32, ... (fewer
-// instructions per token for large batches); both give the same experts in the same order.
-// Warp 0 computes the softmax weights.  Ranks 0..K-1 are the routing, ranks
-// K..K+n_spec-1 the ranked continuation (page "Data Flow", "Serial Step Trace": the gate
-// matvec ranks top-(8+spec); ranks beyond 8 are the bets for the next token) with their
-// full-softmax probabilities.
+// Selection and weights of one token by one warp, from its E logits in shared memory (and, with
+// RANK, the experts of ranks 0..K+n_spec-1 already placed in by_rank): the max logit and, where
+// needed, the full softmax denominator by butterflies; without RANK, K + n_spec rounds of a
+// warp arg-max over lanes holding experts l, l+32, ...; lane k then holds rank k's expert and
+// computes its weight.
 template <bool RANK>
-__global__ void __launch_bounds__(kMaxExperts) topk_kernel(const float* __restrict__ partial, int splits,
-                                                           const float* __restrict__ bias, int B, int E, int K,
-                                                           int norm, int32_t* __restrict__ idx_out,
-                                                           float* __restrict__ w_out, int n_spec,
-                                                           int32_t* __restrict__ spec_idx,
-                                                           float* __restrict__ spec_p) {
-    __shared__ __align__(16) float logit[kMaxExperts];
-    __shared__ int by_rank[kMaxRanks];
-    const int t = blockIdx.x;
-    const int e = threadIdx.x;
+__device__ __forceinline__ void topk_select_warp(const float* logit, const int* by_rank, int t, int E, int K, int norm,
+                                                 int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+                                                 int n_spec, int32_t* __restrict__ spec_idx,
+                                                 float* __restrict__ spec_p) {
+    const int lane = threadIdx.x & 31;
     const int ranks = K + n_spec;   // <= 32
-    if (e < E) {
-        float p[kMaxSplits];
-#pragma unroll
-        for (int sp = 0; sp < kMaxSplits; ++sp)
-            if (sp < splits) p[sp] = __ldg(partial + ((size_t)sp * B + t) * E + e);
-        float s = 0.f;
-#pragma unroll
-        for (int sp = 0; sp < kMaxSplits; ++sp)
-            if (sp < splits) s += p[sp];
-        if (bias) s += bias[e];
-        logit[e] = s;
-    }
-    if (e < kMaxRanks) by_rank[e] = 0;   // (only a non-finite logit could leave a rank unfilled)
-    __syncthreads();
-    if (RANK && e < E) {
-        const float v = logit[e];
-        int r = 0;
-        int j = 0;
-        for (; j + 4 <= E; j += 4) {   // the whole row, four logits per (broadcast) load
-            const float4 u = *reinterpret_cast<const float4*>(logit + j);
-            r += (u.x > v) || (u.x == v && j < e);
-            r += (u.y > v) || (u.y == v && j + 1 < e);
-            r += (u.z > v) || (u.z == v && j + 2 < e);
-            r += (u.w > v) || (u.w == v && j + 3 < e);
-        }
-        for (; j < E; ++j) r += (logit[j] > v) || (logit[j] == v && j < e);
-        if (r < ranks) by_rank[r] = e;
-    }
-    __syncthreads();
-    if (threadIdx.x >= 32) return;
-    const int lane = threadIdx.x;
     constexpr int PER = kMaxExperts / 32;
     float v[PER];   // lane l holds experts l, l+32, ...
     bool live[PER];
@@ -324,6 +303,62 @@ __global__ void __launch_bounds__(kMaxExperts) topk_kernel(const float* __restri
         spec_idx[(size_t)t * n_spec + (lane - K)] = sel_i;
         if (spec_p) spec_p[(size_t)t * n_spec + (lane - K)] = p / z_all;
     }
+}
+
+// One CTA per token.  Thread e sums expert e's split-K partials in split order (all loads
+// issued before the sum) and adds the bias.  The experts of ranks 0 .. K + n_spec - 1
+// (descending logit, ties -> lower expert id) are then found either by counting every
+// expert's rank in parallel (RANK: rank(e) = experts with a larger logit, or an equal logit
+// and a lower id; quickest for small batches, where one CTA's latency is the cost) or by
+// K + n_spec rounds of a warp arg-max over lanes holding experts l, l+32, ... (fewer
+// instructions per token for large batches); both give the same experts in the same order.
+// Warp 0 computes the softmax weights.  Ranks 0..K-1 are the routing, ranks
+// K..K+n_spec-1 the ranked continuation (page "Data Flow", "Serial Step Trace": the gate
+// matvec ranks top-(8+spec); ranks beyond 8 are the bets for the next token) with their
+// full-softmax probabilities.
+template <bool RANK>
+__global__ void __launch_bounds__(kMaxExperts) topk_kernel(const float* __restrict__ partial, int splits,
+                                                           const float* __restrict__ bias, int B, int E, int K,
+                                                           int norm, int32_t* __restrict__ idx_out,
+                                                           float* __restrict__ w_out, int n_spec,
+                                                           int32_t* __restrict__ spec_idx,
+                                                           float* __restrict__ spec_p) {
+    __shared__ __align__(16) float logit[kMaxExperts];
+    __shared__ int by_rank[kMaxRanks];
+    const int t = blockIdx.x;
+    const int e = threadIdx.x;
+    const int ranks = K + n_spec;   // <= 32
+    if (e < E) {
+        float p[kMaxSplits];
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplits; ++sp)
+            if (sp < splits) p[sp] = __ldg(partial + ((size_t)sp * B + t) * E + e);
+        float s = 0.f;
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplits; ++sp)
+            if (sp < splits) s += p[sp];
+        if (bias) s += bias[e];
+        logit[e] = s;
+    }
+    if (e < kMaxRanks) by_rank[e] = 0;   // (only a non-finite logit could leave a rank unfilled)
+    __syncthreads();
+    if (RANK && e < E) {
+        const float v = logit[e];
+        int r = 0;
+        int j = 0;
+        for (; j + 4 <= E; j += 4) {   // the whole row, four logits per (broadcast) load
+            const float4 u = *reinterpret_cast<const float4*>(logit + j);
+            r += (u.x > v) || (u.x == v && j < e);
+            r += (u.y > v) || (u.y == v && j + 1 < e);
+            r += (u.z > v) || (u.z == v && j + 2 < e);
+            r += (u.w > v) || (u.w == v && j + 3 < e);
+        }
+        for (; j < E; ++j) r += (logit[j] > v) || (logit[j] == v && j < e);
+        if (r < ranks) by_rank[r] = e;
+    }
+    __syncthreads();
+    if (threadIdx.x >= 32) return;
+    topk_select_warp<RANK>(logit, by_rank, t, E, K, norm, idx_out, w_out, n_spec, spec_idx, spec_p);
 }
 
 }  // namespace

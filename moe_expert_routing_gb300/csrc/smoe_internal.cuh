@@ -40,6 +40,8 @@ struct WsLayout {
     size_t total;
 };
 
+// Descriptor validation shared by every entry point (SMOE_OK, INVALID_ARG or UNSUPPORTED).
+smoe_status check_desc(const smoe_layer_desc* D);
 int route_splits(int B, int E, int d);
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 WsLayout ws_layout(const smoe_layer_desc& D, int max_tokens);
@@ -103,10 +105,18 @@ cudaError_t launch_ffn_tc(const smoe_layer_desc& D, const FfnTcWeights& W, int B
 
 // all_tokens: every expert of the call holds all B tokens (the slices of a shared expert), so
 // the tensor-core path is worth launching whenever B reaches its threshold.
+// x_next (optional): after the combine, x_next = bf16(norm(residual)) as launch_rmsnorm computes
+// it (eps, center), fused into the combine kernel for d_model <= 4096.
+struct NextNorm {
+    uint16_t* x_next = nullptr;
+    float eps = 0.f;
+    int center = 0;
+};
 cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uint16_t* x, int B,
                        const int32_t* union_ids, const int32_t* n_union, const int32_t* offsets,
                        const int32_t* token_list, const int32_t* slot_list, const float* topk_w,
-                       float* residual, void* ws, const WsLayout& L, cudaStream_t stream, bool all_tokens = false);
+                       float* residual, void* ws, const WsLayout& L, cudaStream_t stream, bool all_tokens = false,
+                       const NextNorm& next = NextNorm());
 
 cudaError_t launch_rmsnorm(const float* h, float eps, int center, int B, int d, uint16_t* x_out,
                            cudaStream_t stream);
@@ -142,6 +152,21 @@ cudaError_t launch_stream_copy(const StreamCopyArgs& a, cudaStream_t stream);
 // ----------------------------------------------------------------------------- device helpers
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
     return __uint_as_float(bits16 << 16);
+}
+
+// Sum of v over a CTA of 256 threads (warp butterflies, then the 8 warp sums in warp order),
+// returned to every thread; red: 8 floats of shared memory.  The RMS-norm kernels use it so
+// that a norm fused into another kernel gives the standalone norm's results bit for bit.
+__device__ __forceinline__ float block_sum256(float v, float* red) {
+#pragma unroll
+    for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    return tot;
 }
 
 }  // namespace smoe

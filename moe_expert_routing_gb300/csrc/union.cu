@@ -17,7 +17,7 @@
 //   more:                chunk_hist_kernel (one CTA per 1024-entry chunk: per-chunk counts)
 //                        -> chunk_scan_kernel (one CTA: union, list offsets, chunk bases)
 //                        -> chunk_scatter_kernel (one CTA per chunk)
-#include "smoe_internal.cuh"
+#include "union_block.cuh"
 
 namespace smoe {
 namespace {
@@ -25,12 +25,7 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 
-// Up to 128 entries: lane l holds entries l, l+32, l+64, l+96.  Every entry is compared with
-// every other (one shuffle per source entry): less = entries with a smaller expert id (its
-// expert's list offset), eqb = earlier entries with the same id; less + eqb is its position
-// in the stable expert-major order, and eqb == 0 marks the first entry of its expert, which
-// writes the union slot.  The union position of expert e is the number of distinct ids below
-// e, read from a 256-bit set of the ids present (OR-reduced over the warp).
+// Up to 128 entries: one warp (union_of_warp); up to 1024: one CTA (union_of_block).
 __global__ void __launch_bounds__(32) union_warp_kernel(const int32_t* __restrict__ idx, int BK, int E,
                                                         int32_t* __restrict__ union_ids,
                                                         int32_t* __restrict__ n_union,
@@ -38,75 +33,7 @@ __global__ void __launch_bounds__(32) union_warp_kernel(const int32_t* __restric
                                                         int32_t* __restrict__ token_list,
                                                         int32_t* __restrict__ slot_list, int K,
                                                         uint32_t* __restrict__ status) {
-    constexpr int PER = 4;
-    constexpr int WORDS = kMaxExperts / 32;
-    const int lane = threadIdx.x;
-    int e[PER];
-    bool bad = false;
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-        const int i = lane + 32 * j;
-        e[j] = i < BK ? idx[i] : -1;
-        if (i < BK && (e[j] < 0 || e[j] >= E)) bad = true;
-    }
-    if (__any_sync(0xffffffffu, bad)) {
-        if (lane == 0) {
-            atomicOr(status, SMOE_FAULT_EXPERT_INDEX);
-            *n_union = 0;
-            offsets[0] = 0;
-        }
-        return;
-    }
-    int less[PER], eqb[PER];
-#pragma unroll
-    for (int j = 0; j < PER; ++j) less[j] = eqb[j] = 0;
-#pragma unroll
-    for (int sj = 0; sj < PER; ++sj) {
-        if (32 * sj >= BK) break;
-        const int n = BK - 32 * sj < 32 ? BK - 32 * sj : 32;
-        for (int s = 0; s < n; ++s) {
-            const int es = __shfl_sync(0xffffffffu, e[sj], s);
-            const int is = 32 * sj + s;
-#pragma unroll
-            for (int j = 0; j < PER; ++j) {
-                less[j] += es < e[j];
-                eqb[j] += es == e[j] && is < lane + 32 * j;
-            }
-        }
-    }
-    uint32_t present[WORDS];
-    int nu = 0;
-#pragma unroll
-    for (int w = 0; w < WORDS; ++w) {
-        uint32_t mine = 0;
-#pragma unroll
-        for (int j = 0; j < PER; ++j)
-            if (lane + 32 * j < BK && (e[j] >> 5) == w) mine |= 1u << (e[j] & 31);
-        present[w] = __reduce_or_sync(0xffffffffu, mine);
-        nu += __popc(present[w]);
-    }
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-        const int i = lane + 32 * j;
-        if (i >= BK) continue;
-        const int pos = less[j] + eqb[j];
-        token_list[pos] = i / K;
-        slot_list[pos] = i - (i / K) * K;
-        if (eqb[j] == 0) {
-            int u = 0;
-#pragma unroll
-            for (int w = 0; w < WORDS; ++w) {
-                if (w < (e[j] >> 5)) u += __popc(present[w]);
-                else if (w == (e[j] >> 5)) u += __popc(present[w] & ((1u << (e[j] & 31)) - 1u));
-            }
-            union_ids[u] = e[j];
-            offsets[u] = less[j];
-        }
-    }
-    if (lane == 0) {
-        *n_union = nu;
-        offsets[nu] = BK;
-    }
+    union_of_warp(idx, BK, E, union_ids, n_union, offsets, token_list, slot_list, K, status);
 }
 
 template <int THREADS>
@@ -117,107 +44,7 @@ __global__ void __launch_bounds__(THREADS) union_kernel(const int32_t* __restric
                                                          int32_t* __restrict__ token_list,
                                                          int32_t* __restrict__ slot_list, int K,
                                                          uint32_t* __restrict__ status) {
-    __shared__ int count[kMaxExperts];
-    __shared__ int list_off[kMaxExperts];  // start of expert e's list
-    __shared__ int running[kMaxExperts];   // entries of expert e placed so far
-    __shared__ int chunk_base[kMaxExperts];
-    constexpr int WARPS = THREADS / 32;
-    __shared__ int wcount[WARPS][kMaxExperts];
-    __shared__ int bad;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-    if (tid == 0) bad = 0;
-    for (int e = tid; e < kMaxExperts; e += THREADS) {
-        count[e] = 0;
-        running[e] = 0;
-    }
-    for (int i = tid; i < WARPS * kMaxExperts; i += THREADS) (&wcount[0][0])[i] = 0;
-    __syncthreads();
-
-    // histogram + validation
-    for (int i = tid; i < BK; i += THREADS) {
-        const int e = idx[i];
-        if (e < 0 || e >= E) bad = 1;
-        else atomicAdd(&count[e], 1);
-    }
-    __syncthreads();
-    if (bad) {
-        if (tid == 0) {
-            atomicOr(status, SMOE_FAULT_EXPERT_INDEX);
-            *n_union = 0;
-            offsets[0] = 0;
-        }
-        return;
-    }
-
-    // exclusive scans over experts (E <= 256) by warp 0: union positions and list offsets
-    if (warp == 0) {
-        constexpr int PER = kMaxExperts / 32;
-        int c[PER], used = 0, tot = 0;
-#pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            const int e = lane * PER + j;
-            c[j] = (e < E) ? count[e] : 0;
-            used += c[j] > 0;
-            tot += c[j];
-        }
-        int used_incl = used, tot_incl = tot;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int a = __shfl_up_sync(0xffffffffu, used_incl, off);
-            const int b = __shfl_up_sync(0xffffffffu, tot_incl, off);
-            if (lane >= off) { used_incl += a; tot_incl += b; }
-        }
-        int u = used_incl - used, o = tot_incl - tot;
-#pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            const int e = lane * PER + j;
-            if (e < E) {
-                list_off[e] = o;
-                if (c[j] > 0) {
-                    union_ids[u] = e;
-                    offsets[u] = o;
-                    ++u;
-                }
-                o += c[j];
-            }
-        }
-        if (lane == 31) {
-            *n_union = u;
-            offsets[u] = o;
-        }
-    }
-    __syncthreads();
-
-    // stable scatter, THREADS entries per round
-    for (int base = 0; base < BK; base += THREADS) {
-        const int i = base + tid;
-        const int e = (i < BK) ? idx[i] : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        const int rank = __popc(peers & ((1u << lane) - 1u));
-        if (e >= 0 && rank == 0) wcount[warp][e] = __popc(peers);
-        __syncthreads();
-        for (int x = tid; x < E; x += THREADS) {
-            int s = 0;
-            for (int w = 0; w < WARPS; ++w) {
-                const int cnt = wcount[w][x];
-                wcount[w][x] = s;
-                s += cnt;
-            }
-            chunk_base[x] = running[x];
-            running[x] += s;
-        }
-        __syncthreads();
-        if (e >= 0) {
-            const int pos = list_off[e] + chunk_base[e] + wcount[warp][e] + rank;
-            token_list[pos] = i / K;
-            slot_list[pos] = i - (i / K) * K;
-        }
-        __syncthreads();
-        for (int x = tid; x < E; x += THREADS)
-            for (int w = 0; w < WARPS; ++w) wcount[w][x] = 0;
-        __syncthreads();
-    }
+    union_of_block<THREADS>(idx, BK, E, union_ids, n_union, offsets, token_list, slot_list, K, status);
 }
 
 

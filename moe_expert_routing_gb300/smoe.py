@@ -21,10 +21,10 @@ SMOE_LAYOUT_SEPARATE, SMOE_LAYOUT_FUSED_GATE_UP = 0, 1
 SMOE_FAULT_EXPERT_INDEX, SMOE_FAULT_FP16_RANGE, SMOE_FAULT_TIMEOUT, SMOE_FAULT_TOKEN_INDEX = 1, 2, 4, 8
 SMOE_FAULT_SLOT_POOL = 0x10
 
-EXPORTED = ("smoe_workspace_bytes", "smoe_route", "smoe_route_ranked", "smoe_expert_union", "smoe_moe_ffn_batch", "smoe_moe_layer",
-            "smoe_shared_expert_ffn", "smoe_rmsnorm_bf16", "smoe_clear_device_status", "smoe_read_device_status", "smoe_status_string",
-            "smoe_route_noalloc", "smoe_stream_state_bytes", "smoe_stream_init", "smoe_stream_plan",
-            "smoe_stream_copy")
+EXPORTED = ("smoe_workspace_bytes", "smoe_route", "smoe_route_ranked", "smoe_expert_union", "smoe_moe_ffn_batch",
+            "smoe_moe_ffn_batch_norm", "smoe_moe_layer", "smoe_shared_expert_ffn", "smoe_rmsnorm_bf16",
+            "smoe_clear_device_status", "smoe_read_device_status", "smoe_status_string", "smoe_route_noalloc",
+            "smoe_stream_state_bytes", "smoe_stream_init", "smoe_stream_plan", "smoe_stream_copy")
 
 
 class SmoeError(RuntimeError):
@@ -62,6 +62,8 @@ def load_library(path: str = LIB_PATH):
         L.smoe_route_ranked.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp, sz, vp]
         L.smoe_expert_union.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]
         L.smoe_moe_ffn_batch.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.smoe_moe_ffn_batch_norm.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, i32, vp,
+                                              vp, sz, vp]
         L.smoe_moe_layer.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
         L.smoe_shared_expert_ffn.argtypes = [vp, vp, vp, i32, vp, vp, sz, vp]
         L.smoe_rmsnorm_bf16.argtypes = [vp, ctypes.c_float, i32, i32, i32, vp, vp]
@@ -76,7 +78,8 @@ def load_library(path: str = LIB_PATH):
         L.smoe_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         L.smoe_status_string.restype = ctypes.c_char_p
         L.smoe_status_string.argtypes = [ctypes.c_int]
-        for name in ("smoe_route", "smoe_route_ranked", "smoe_expert_union", "smoe_moe_ffn_batch", "smoe_moe_layer",
+        for name in ("smoe_route", "smoe_route_ranked", "smoe_expert_union", "smoe_moe_ffn_batch",
+                     "smoe_moe_ffn_batch_norm", "smoe_moe_layer",
                      "smoe_shared_expert_ffn", "smoe_rmsnorm_bf16", "smoe_clear_device_status",
                      "smoe_read_device_status", "smoe_stream_init", "smoe_stream_plan", "smoe_stream_copy"):
             getattr(L, name).restype = ctypes.c_int
@@ -210,6 +213,16 @@ def smoe_moe_ffn_batch(desc, weights: Weights, x, union_ids, n_union, offsets, t
                                              _p(union_ids), _p(n_union), _p(offsets), _p(token_list),
                                              _p(slot_list), _p(topk_w), _p(residual), _p(ws), ws.numel(),
                                              _stream(stream)), "smoe_moe_ffn_batch")
+
+
+def smoe_moe_ffn_batch_norm(desc, weights: Weights, x, union_ids, n_union, offsets, token_list, slot_list, topk_w,
+                            residual, x_next, ws, eps: float = 1e-6, center: int = 0, stream=None):
+    """smoe_moe_ffn_batch, then x_next = bf16(norm(residual)) (the next block's input; may be x)."""
+    _check(load_library().smoe_moe_ffn_batch_norm(ctypes.byref(desc), ctypes.byref(weights.struct), _p(x),
+                                                  x.shape[0], _p(union_ids), _p(n_union), _p(offsets),
+                                                  _p(token_list), _p(slot_list), _p(topk_w), _p(residual),
+                                                  ctypes.c_float(eps), int(center), _p(x_next), _p(ws), ws.numel(),
+                                                  _stream(stream)), "smoe_moe_ffn_batch_norm")
 
 
 def smoe_moe_layer(desc, weights: Weights, x, gate_w, gate_bias, residual, ws, topk_idx=None, topk_w=None,

@@ -23,7 +23,7 @@
 //                                                     FFN block)
 //   * RMSNorm with unit weight between chained layers (page "Data Flow", "Serial Step Trace")
 //
-// Readings where the pages are silent (each also listed in the design notes):
+// Readings where the pages are silent (the plainest reading the rest of the pages supports):
 //   nibble i of a row lives in word i/8 at bits 4*(i%8) (low nibble first);
 //   w = scale * q + bias;  top-k ordered by probability descending, equal values by the
 //   lower expert id; selection by logit (softmax is strictly increasing, so the order by

@@ -88,6 +88,34 @@ def test_route_argument_errors(lib):
     assert lib.smoe_route(None, None, None, None, 1, None, None, None, 0, None) == smoe.SMOE_ERR_INVALID_ARG
 
 
+def test_route_noalloc_argument_errors(lib):
+    """The no-allocation router validates like smoe_route (same descriptor check) and refuses
+    batches whose partial logits do not fit its fixed 2^20-float scratch, all before touching
+    CUDA."""
+    d = _desc()   # 128 experts
+    vp = ctypes.c_void_p
+
+    def call(desc=d, B=4, x=1024, w=1024, idx=1024, wt=1024):
+        return lib.smoe_route_noalloc(None if desc is None else ctypes.byref(desc), vp(x), vp(w), None, B, vp(idx),
+                                      vp(wt), None)
+
+    assert call(desc=None) == smoe.SMOE_ERR_INVALID_ARG
+    assert call(desc=_desc(top_k=0)) == smoe.SMOE_ERR_INVALID_ARG
+    assert call(desc=_desc(norm_topk_prob=3)) == smoe.SMOE_ERR_INVALID_ARG
+    assert call(desc=_desc(group_size=32)) == smoe.SMOE_ERR_UNSUPPORTED
+    assert call(desc=_desc(num_experts=300)) == smoe.SMOE_ERR_UNSUPPORTED
+    assert call(B=-1) == smoe.SMOE_ERR_INVALID_ARG
+    assert call(B=0, x=0, idx=0) == smoe.SMOE_OK          # B == 0: no-op
+    assert call(x=0) == smoe.SMOE_ERR_INVALID_ARG
+    assert call(w=0) == smoe.SMOE_ERR_INVALID_ARG
+    assert call(idx=0) == smoe.SMOE_ERR_INVALID_ARG
+    assert call(wt=0) == smoe.SMOE_ERR_INVALID_ARG
+    assert call(x=1032) == smoe.SMOE_ERR_UNSUPPORTED      # 8-byte aligned only
+    assert call(w=1028) == smoe.SMOE_ERR_UNSUPPORTED
+    assert call(B=8193) == smoe.SMOE_ERR_UNSUPPORTED      # 8193 x 128 > 2^20 partial logits
+    assert call(B=4097, desc=_desc(num_experts=256)) == smoe.SMOE_ERR_UNSUPPORTED
+
+
 def test_route_ranked_argument_errors(lib):
     d = _desc()   # top_k 8, 128 experts: at most 24 further ranks
     vp = ctypes.c_void_p
@@ -132,6 +160,27 @@ def test_layer_and_ffn_argument_errors(lib):
     rc = lib.smoe_moe_ffn_batch(ctypes.byref(d), ctypes.byref(w), vp(1024), 4, None, vp(1), vp(1), vp(1), vp(1),
                                 vp(1), vp(1024), vp(4096), 1 << 30, None)
     assert rc == smoe.SMOE_ERR_INVALID_ARG
+
+
+def test_ffn_batch_norm_argument_errors(lib):
+    d = _desc()
+    vp, f = ctypes.c_void_p, ctypes.c_float
+    w = smoe.ExpertWeights()
+    for name, _ in smoe.ExpertWeights._fields_:
+        setattr(w, name, 4096)
+
+    def call(x_next=2048, eps=1e-6, center=1, B=4, weights=w):
+        return lib.smoe_moe_ffn_batch_norm(ctypes.byref(d), ctypes.byref(weights), vp(1024), B, vp(1), vp(1), vp(1),
+                                           vp(1), vp(1), vp(1), vp(1024), f(eps), center, vp(x_next), vp(4096),
+                                           1 << 30, None)
+
+    assert call(x_next=0) == smoe.SMOE_ERR_INVALID_ARG
+    assert call(eps=-1.0) == smoe.SMOE_ERR_INVALID_ARG
+    assert call(center=2) == smoe.SMOE_ERR_INVALID_ARG
+    assert call(B=-1) == smoe.SMOE_ERR_INVALID_ARG
+    assert call(B=0, x_next=0) == smoe.SMOE_OK                     # B == 0: no-op
+    assert call(x_next=2052) == smoe.SMOE_ERR_UNSUPPORTED          # 4-byte aligned only
+    assert call(weights=smoe.ExpertWeights()) == smoe.SMOE_ERR_INVALID_ARG
 
 
 def test_union_and_norm_argument_errors(lib):

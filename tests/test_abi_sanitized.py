@@ -1,8 +1,8 @@
 """The C ABI's host-side argument validation under AddressSanitizer and UndefinedBehaviorSanitizer.
 
-`csrc/api.cu` (every entry point's validation) is recompiled with the sanitizers and linked with
-the library's other objects; a child interpreter with the sanitizer runtimes preloaded drives the
-argument-error paths of every call through plain ctypes.  These paths return before any CUDA
+`csrc/api.cu` and `csrc/noalloc.cu` (every entry point's validation) are recompiled with the
+sanitizers and linked with the library's other objects; a child interpreter with the sanitizer
+runtimes preloaded drives the argument-error paths of every call through plain ctypes.  These paths return before any CUDA
 call, so no GPU is needed; an out-of-bounds access or undefined behaviour in them aborts the child.
 """
 import glob
@@ -70,6 +70,13 @@ for name, _ in W._fields_:
 h.w_down = 4096 + 8
 assert L.smoe_stream_copy(r(d), r(h), r(h), 64, vp(1), vp(4096), sz(1 << 30), None) == UNSUPPORTED
 assert L.smoe_stream_copy(r(d), r(w), r(w), 64, vp(1), vp(4096), sz(1 << 30), None) == INVALID
+assert L.smoe_route_noalloc(None, vp(1024), vp(1024), None, 4, vp(1024), vp(1024), None) == INVALID
+assert L.smoe_route_noalloc(r(bad[0]), vp(1024), vp(1024), None, 4, vp(1024), vp(1024), None) == UNSUPPORTED
+assert L.smoe_route_noalloc(r(d), vp(1024), vp(1024), None, -1, vp(1024), vp(1024), None) == INVALID
+assert L.smoe_route_noalloc(r(d), None, None, None, 0, None, None, None) == OK
+assert L.smoe_route_noalloc(r(d), vp(1024), vp(1024), None, 4, None, vp(1024), None) == INVALID
+assert L.smoe_route_noalloc(r(d), vp(1032), vp(1024), None, 4, vp(1024), vp(1024), None) == UNSUPPORTED
+assert L.smoe_route_noalloc(r(d), vp(1024), vp(1024), None, 8193, vp(1024), vp(1024), None) == UNSUPPORTED
 for s in range(7):
     assert L.smoe_status_string(s)
 print("sanitized abi ok")
@@ -88,14 +95,18 @@ def test_abi_validation_under_asan_and_ubsan(tmp_path):
     if not asan or not ubsan or not os.path.exists(B.NVCC):
         pytest.skip("nvcc or the gcc sanitizer runtimes are not installed")
     B.build()   # the library's objects
-    api_o = str(tmp_path / "api_san.o")
-    # (nvcc splits -Xcompiler values at commas: one flag per sanitizer)
-    cmd = [B.NVCC, *B.ARCH, *B.FLAGS, "-Xcompiler", "-fsanitize=address", "-Xcompiler", "-fsanitize=undefined",
-           "-Xcompiler", "-fno-omit-frame-pointer", "-c", os.path.join(B.CSRC, "api.cu"), "-o", api_o]
-    subprocess.run(cmd, check=True, capture_output=True)
-    objs = [o for o in glob.glob(os.path.join(B.OUT_DIR, "*.o")) if os.path.basename(o) != "api.o"]
+    san = ("api", "noalloc")
+    san_objs = []
+    for name in san:
+        o = str(tmp_path / f"{name}_san.o")
+        # (nvcc splits -Xcompiler values at commas: one flag per sanitizer)
+        cmd = [B.NVCC, *B.ARCH, *B.FLAGS, "-Xcompiler", "-fsanitize=address", "-Xcompiler", "-fsanitize=undefined",
+               "-Xcompiler", "-fno-omit-frame-pointer", "-c", os.path.join(B.CSRC, name + ".cu"), "-o", o]
+        subprocess.run(cmd, check=True, capture_output=True)
+        san_objs.append(o)
+    objs = [o for o in glob.glob(os.path.join(B.OUT_DIR, "*.o")) if os.path.basename(o)[:-2] not in san]
     lib = str(tmp_path / "libsmoe_san.so")
-    subprocess.run([B.NVCC, *B.ARCH, "-shared", "-cudart", "shared", "-o", lib, api_o, *objs], check=True,
+    subprocess.run([B.NVCC, *B.ARCH, "-shared", "-cudart", "shared", "-o", lib, *san_objs, *objs], check=True,
                    capture_output=True)
     undef = subprocess.run(["nm", "-D", "--undefined-only", lib], capture_output=True, text=True).stdout
     assert "__asan_" in undef and "__ubsan_" in undef   # the validation code is instrumented

@@ -3,11 +3,12 @@
 Routing indices, the union and the token lists must match bit-exactly (layer-0 inputs are
 drawn with a logit gap >= 1e-3 between adjacent ranks 1..K+1); routing weights to 1e-5
 relative; layer outputs to relative L2 <= 5e-3 (on the layer delta and on the output) and
-max-abs <= 2e-2.  Chained stacks are checked layer by layer, teacher-forced: the oracle's
-layer l consumes the GPU's own hidden state h_l.  Tokens whose oracle gap between ranks K and
-K+1 is below 1e-4 are exempt from the index comparison (they must stay under 0.1%); for the
-others the expert set must match exactly and two ranks may only appear swapped where their
-oracle logits tie within 1e-4.
+max-abs <= 2e-2 (absolute, at every layer).  Chained stacks are checked layer by layer,
+teacher-forced (the oracle's layer l consumes the GPU's own hidden state h_l), and end to end
+(each side runs its own chain; tokens whose routing flips at some layer are counted).  In the
+teacher-forced check, tokens whose oracle gap between ranks K and K+1 is below 1e-4 are exempt
+from the index comparison, and so are tokens with the same expert set whose ranks swapped on
+oracle logits that tie within 1e-4; both together must stay under 0.1% of the token-layers.
 """
 import numpy as np
 import pytest
@@ -76,12 +77,8 @@ class Case:
         return out64, idx, w64, lg
 
 
-def check_outputs(gpu_out, oracle_out64, residual, rows=None, abs_scale=1.0):
-    """rel-L2 <= 5e-3 on the delta and the output; max-abs <= 2e-2 * abs_scale.
-
-    abs_scale is 1 at the input scale the workloads state (single layers, layer 0 of a
-    chain); for teacher-forced chained layers it is RMS(delta_l) / RMS(delta_0), see
-    _chain."""
+def check_outputs(gpu_out, oracle_out64, residual, rows=None):
+    """rel-L2 <= 5e-3 on the delta and the output; max-abs <= 2e-2 (absolute)."""
     g = np.asarray(gpu_out, np.float64)
     o = np.asarray(oracle_out64, np.float64)
     r = np.asarray(residual, np.float64)
@@ -93,7 +90,7 @@ def check_outputs(gpu_out, oracle_out64, residual, rows=None, abs_scale=1.0):
     mab = max_abs(g, o)
     assert d_rel <= REL_L2_TOL, f"delta rel-L2 {d_rel:.3e}"
     assert o_rel <= REL_L2_TOL, f"output rel-L2 {o_rel:.3e}"
-    assert mab <= MAX_ABS_TOL * abs_scale, f"max-abs {mab:.3e} (scale {abs_scale:.3g})"
+    assert mab <= MAX_ABS_TOL, f"max-abs {mab:.3e}"
     return d_rel, mab
 
 
@@ -256,6 +253,56 @@ def test_union_bad_index_sets_fault_and_leaves_residual():
     assert smoe.smoe_read_device_status(c.ws) == 0
 
 
+def _routed_lists(c, x_dev):
+    """Route and build the union of case c for the given device input; returns the buffers."""
+    B, K, E = c.B, c.w.top_k, c.w.num_experts
+    idx = torch.empty(B, K, dtype=torch.int32, device=DEV)
+    wt = torch.empty(B, K, dtype=torch.float32, device=DEV)
+    smoe.smoe_route(c.desc, x_dev, c.gate_d, c.bias_d, idx, wt, c.ws)
+    uid = torch.zeros(E, dtype=torch.int32, device=DEV)
+    nu = torch.zeros(1, dtype=torch.int32, device=DEV)
+    off = torch.zeros(E + 1, dtype=torch.int32, device=DEV)
+    tl = torch.zeros(B * K, dtype=torch.int32, device=DEV)
+    sl = torch.zeros(B * K, dtype=torch.int32, device=DEV)
+    smoe.smoe_expert_union(c.desc, idx, uid, nu, off, tl, sl, c.ws)
+    return wt, uid, nu, off, tl, sl
+
+
+@pytest.mark.parametrize("value", [-600.0, 70000.0])
+def test_fp16_range_fault_bit(value):
+    """Hidden states far outside the workloads' N(0, 1) scale, made on the host: at x = -600
+    the SwiGLU activations reach ~1e6 (the synthetic weights have mean -0.5 scale, so gate
+    and up both grow like 3 |x| per row) and do not fit fp16; x = 70000 does not fit fp16
+    itself.  The FFN sets SMOE_FAULT_FP16_RANGE and returns; nothing hangs."""
+    c = Case(W.WORKLOADS["toy"], gap=False)
+    x = torch.full((c.B, c.w.d_model), value, dtype=torch.bfloat16)
+    xd = x.to(DEV).view(torch.int16)
+    smoe.smoe_clear_device_status(c.ws)
+    wt, uid, nu, off, tl, sl = _routed_lists(c, xd)
+    res = x.float().to(DEV)
+    smoe.smoe_moe_ffn_batch(c.desc, c.weights, xd, uid, nu, off, tl, sl, wt, res, c.ws)
+    bits = smoe.smoe_read_device_status(c.ws)
+    assert bits & smoe.SMOE_FAULT_FP16_RANGE, f"status {bits:#x}"
+    assert not bits & smoe.SMOE_FAULT_TIMEOUT
+    smoe.smoe_clear_device_status(c.ws)
+    assert smoe.smoe_read_device_status(c.ws) == 0
+
+
+def test_token_index_fault_bit():
+    """A caller-built token list with an entry outside [0, B): the FFN sets
+    SMOE_FAULT_TOKEN_INDEX, reads row 0 in its place and returns; nothing hangs."""
+    c = Case(W.WORKLOADS["toy"], gap=False)
+    xd = c.x_dev()
+    smoe.smoe_clear_device_status(c.ws)
+    wt, uid, nu, off, tl, sl = _routed_lists(c, xd)
+    tl[5] = c.B + 3
+    res = c.x.float().to(DEV)
+    smoe.smoe_moe_ffn_batch(c.desc, c.weights, xd, uid, nu, off, tl, sl, wt, res, c.ws)
+    bits = smoe.smoe_read_device_status(c.ws)
+    assert bits & smoe.SMOE_FAULT_TOKEN_INDEX, f"status {bits:#x}"
+    assert not bits & smoe.SMOE_FAULT_TIMEOUT
+
+
 # ----------------------------------------------------------------------------- whole layer
 LAYER_CASES = [
     ("toy", None), ("decode_b1", None), ("decode_b8", None), ("prefill64", None), ("q35_prefill64", None),
@@ -290,6 +337,30 @@ def test_ffn_batch_step_by_step_matches_layer():
     smoe.smoe_moe_ffn_batch(c.desc, c.weights, c.x_dev(), uid, nu, off, tl, sl, wt, res, c.ws)
     out_layer, _, _ = c.run_layer()
     assert torch.equal(res.cpu(), out_layer)
+
+
+@pytest.mark.parametrize("name,B,d,center,alias", [("toy", 16, None, 1, False), ("prefill64", 64, None, 1, True),
+                                                   ("q35_prefill64", 37, None, 0, True), ("toy", 5, 8192, 1, False)])
+def test_ffn_batch_norm_equals_ffn_then_norm(name, B, d, center, alias):
+    """smoe_moe_ffn_batch_norm gives smoe_moe_ffn_batch's residual and smoe_rmsnorm_bf16's
+    next-block input bit for bit (the fused kernel for d_model <= 4096, the standalone norm
+    after the combine beyond), also when x_next is the input buffer x itself."""
+    w = W.WORKLOADS[name] if d is None else W.scaled(W.WORKLOADS[name], d_model=d)
+    c = Case(w, B=B)
+    xd = c.x_dev()
+    wt, uid, nu, off, tl, sl = _routed_lists(c, xd)
+    smoe.smoe_clear_device_status(c.ws)
+    res_a = c.x.float().to(DEV) * 3.0
+    res_b = res_a.clone()
+    smoe.smoe_moe_ffn_batch(c.desc, c.weights, xd, uid, nu, off, tl, sl, wt, res_a, c.ws)
+    xn_a = torch.empty_like(xd)
+    smoe.smoe_rmsnorm_bf16(res_a, xn_a, 1e-6, center=center)
+    x_in = xd.clone()
+    xn_b = x_in if alias else torch.full_like(xd, -1)
+    smoe.smoe_moe_ffn_batch_norm(c.desc, c.weights, x_in, uid, nu, off, tl, sl, wt, res_b, xn_b, c.ws, 1e-6, center)
+    assert smoe.smoe_read_device_status(c.ws) == 0
+    assert torch.equal(res_a, res_b)
+    assert torch.equal(xn_a, xn_b)
 
 
 def test_hot_experts_many_tokens_per_expert():
@@ -437,13 +508,56 @@ def test_graph_replay_equals_direct():
 
 
 # ----------------------------------------------------------------------------- chained stacks
-def _chain(name, layers, B=None, sample_rows=None):
+# Per-layer figures of the chained tests (layer, max-abs, delta rel-L2, delta RMS), printed at
+# the end of each test so that a run with -s records them.
+CHAIN_RECORD = {}
+
+
+def tile_covering_rows(idx: np.ndarray, E: int, extra: int = 512, tile: int = 192, tc_min: int = 32,
+                       hottest: int = 2) -> list:
+    """Token rows that exercise every output column of the tensor-core tiles.
+
+    From the (oracle) routing idx [B, K]: an expert's token list is its tokens in ascending
+    order, and list position p sits in tile p // tile at column p % tile.  The rows chosen hit
+    every column residue 0..tile-1 of the `hottest` experts with the longest lists (residue r
+    taken in tile r % tiles, so the residues spread over the tiles), the first and the last
+    position of every tile of every expert with at least tc_min entries (so each one's last
+    short tile is hit), and evenly spaced rows up to `extra` more."""
+    B = idx.shape[0]
+    lists = [np.nonzero((idx == e).any(axis=1))[0] for e in range(E)]
+    counts = np.array([len(t) for t in lists])
+    rows = set()
+    for e in np.argsort(-counts, kind="stable")[:hottest]:
+        n = counts[e]
+        tiles = (n + tile - 1) // tile
+        for r in range(min(tile, n)):
+            p = (r % tiles) * tile + r
+            rows.add(int(lists[e][p if p < n else r]))
+    for e in np.nonzero(counts >= tc_min)[0]:
+        n = counts[e]
+        for t0 in range(0, n, tile):
+            rows.add(int(lists[e][t0]))
+            rows.add(int(lists[e][min(n, t0 + tile) - 1]))
+    step = max(1, B // extra)
+    rows.update(range(0, B, step))
+    return sorted(rows)
+
+
+def _chain(name, layers, B=None, sample_rows=None, cover_tiles=False):
+    """Teacher-forced check of a chained stack, layer by layer: the oracle's layer l consumes
+    the GPU's own x_l and h_l.  Routing indices must match exactly; a token whose oracle gap
+    between ranks K and K+1 is below 1e-4 is exempt, and so is a token whose expert set
+    matches but two ranks swapped where their oracle logits tie within 1e-4 (fp32 against
+    fp64 logits on a near-tie); exempt and swapped tokens together stay within 0.1% of the
+    token-layers.  Outputs within the literal tolerances (rel-L2 5e-3, max-abs 2e-2) on
+    `sample_rows` (all rows if None), or on rows chosen per layer by tile_covering_rows."""
     w = W.WORKLOADS[name]
     B = B or w.tokens
     first = Case(w, 0, B)
     h = first.x.float().to(DEV)
     xb = torch.empty(B, w.d_model, dtype=torch.int16, device=DEV)
-    exempt, total, worst, rms0 = 0, 0, 0.0, 1.0
+    exempt, swapped, total, worst = 0, 0, 0, 0.0
+    record = []
     for l in range(layers):
         c = first if l == 0 else Case(w, l, B, x=first.x)
         smoe.smoe_rmsnorm_bf16(h, xb, 1e-6, center=int(w.chain_center))
@@ -463,29 +577,94 @@ def _chain(name, layers, B=None, sample_rows=None):
         s = -np.sort(-lg, axis=1)
         near = (s[:, w.top_k - 1] - s[:, w.top_k]) < 1e-4
         gi = idx.cpu().numpy()
+        swap = np.zeros(B, bool)
         for t in np.nonzero(np.any(gi != oi, axis=1) & ~near)[0]:
             # same expert set; ranks may only swap where the oracle logits tie within 1e-4
             assert set(gi[t].tolist()) == set(oi[t].tolist()), f"layer {l} token {t}: expert set differs"
             diff = gi[t] != oi[t]
             assert np.all(np.abs(lg[t, gi[t][diff]] - lg[t, oi[t][diff]]) < 1e-4), \
                 f"layer {l} token {t}: rank order differs on separated logits"
+            swap[t] = True
         exempt += int(near.sum())
+        swapped += int(swap.sum())
         total += B
-        rows = sample_rows if sample_rows is not None else list(range(B))
-        rows = [r for r in rows if not near[r]]
+        if cover_tiles:
+            rows = tile_covering_rows(oi, w.num_experts)
+        else:
+            rows = sample_rows if sample_rows is not None else list(range(B))
+        rows = [r for r in rows if not near[r] and not swap[r]]
         _, o64, _ = oracle.moe_layer(c.layer_o, x_l, oi, ow64, h_in, rows=rows)
-        # The workloads' weights have mean -0.5*scale (nibbles average 7.5, the bias centres
-        # them at 8), so every layer output carries a common mode; the residual stream grows
-        # with depth.  The absolute bound is applied at layer 0's scale and scaled with the
-        # delta RMS after that.
+        d_rel, mab = check_outputs(h.cpu().numpy(), o64, h_in.numpy(), rows=rows)
         delta = o64[rows] - h_in.numpy()[rows]
-        rms = float(np.sqrt(np.mean(delta ** 2)))
-        if l == 0:
-            rms0 = rms
-        d_rel, mab = check_outputs(h.cpu().numpy(), o64, h_in.numpy(), rows=rows, abs_scale=max(1.0, rms / rms0))
+        record.append((l, len(rows), mab, d_rel, float(np.sqrt(np.mean(delta ** 2)))))
         worst = max(worst, d_rel)
-    assert exempt <= max(1, 0.001 * total), f"{exempt} near-tie token-layers"
+    CHAIN_RECORD[name] = record
+    for l, n, mab, d_rel, rms in record:
+        print(f"[chain {name}] layer {l}: rows {n}, max-abs {mab:.3e}, delta rel-L2 {d_rel:.3e}, delta RMS {rms:.3g}")
+    print(f"[chain {name}] near-tie tokens {exempt}, swapped ranks {swapped}, of {total} token-layers")
+    assert exempt + swapped <= max(1, 0.001 * total), f"{exempt} near-tie + {swapped} swapped token-layers"
     return worst
+
+
+def _chain_free(name, layers, rows=None):
+    """The stack run end to end on each side, with no teacher forcing: the GPU's chain (glue
+    norm and smoe_moe_layer per layer, all B tokens) against the oracle's own chain over the
+    sampled rows (tokens are independent through the stack, so the oracle runs the rows alone).
+
+    The two chains round their layer inputs to bf16 independently (fp32 against fp64 norms),
+    so from layer 1 on their inputs differ in a few elements by one bf16 ulp, and the
+    difference grows through the stack.  A token whose routing differs from the oracle's at
+    some layer has flipped: its later layers use other experts, so it is counted and left out
+    of the output comparison.  Every flip must be explained by the inputs: the oracle's
+    smallest adjacent logit gap among ranks 1..K+1 on its own input is below twice the
+    largest change of any logit between the two inputs (both evaluated by the oracle), plus
+    the 1e-4 near-tie margin of the GPU's fp32 logits.  The tokens that never flip match the
+    oracle's output and the stack's total update (output - input) to rel-L2 5e-3."""
+    w = W.WORKLOADS[name]
+    B = w.tokens
+    rows = list(range(B)) if rows is None else list(rows)
+    first = Case(w, 0, B)
+    h = first.x.float().to(DEV)
+    xb = torch.empty(B, w.d_model, dtype=torch.int16, device=DEV)
+    h_o = first.x.float().numpy()[rows]
+    h0 = h_o.astype(np.float64)
+    flipped = np.zeros(len(rows), bool)
+    for l in range(layers):
+        c = first if l == 0 else Case(w, l, B, x=first.x)
+        smoe.smoe_rmsnorm_bf16(h, xb, 1e-6, center=int(w.chain_center))
+        idx = torch.empty(B, w.top_k, dtype=torch.int32, device=DEV)
+        wt = torch.empty(B, w.top_k, dtype=torch.float32, device=DEV)
+        smoe.smoe_clear_device_status(c.ws)
+        smoe.smoe_moe_layer(c.desc, c.weights, xb, c.gate_d, c.bias_d, h, c.ws, idx, wt)
+        assert smoe.smoe_read_device_status(c.ws) == 0
+        xo = torch.from_numpy(oracle.rmsnorm_bf16(h_o.astype(np.float32), 1e-6, center=w.chain_center)
+                              .view(np.int16)).view(torch.bfloat16)
+        xg = xb.cpu()[rows].view(torch.bfloat16)
+        oi, ow64, _, lg_o = oracle.route(xo, c.gate, c.bias, w.top_k, w.norm_topk_prob)
+        lg_g = oracle.logits(xg, c.gate, c.bias)
+        new = np.any(idx.cpu().numpy()[rows] != oi, axis=1) & ~flipped
+        pert = np.max(np.abs(lg_g - lg_o), axis=1)
+        gap = logit_gaps(lg_o, w.top_k)
+        for t in np.nonzero(new)[0]:
+            assert gap[t] < 2 * pert[t] + 1e-4, \
+                f"layer {l} row {rows[t]}: routing flipped at logit gap {gap[t]:.3e} > 2 x input change {pert[t]:.3e}"
+        flipped |= new
+        out, _, _ = oracle.moe_layer(c.layer_o, xo, oi, ow64, h_o.astype(np.float32))
+        h_o = out.astype(np.float64)
+        keep = ~flipped
+        g = h.cpu().numpy()[rows].astype(np.float64)
+        print(f"[chain-free {name}] layer {l}: flipped {int(flipped.sum())} of {len(rows)}, output rel-L2 "
+              f"{rel_l2(g[keep], h_o[keep]):.3e}, max logit change {pert.max():.2e}")
+    g = h.cpu().numpy()[rows].astype(np.float64)
+    keep = ~flipped
+    o_rel = rel_l2(g[keep], h_o[keep])
+    d_rel = rel_l2(g[keep] - h0[keep], h_o[keep] - h0[keep])
+    mab = max_abs(g[keep], h_o[keep])
+    print(f"[chain-free {name}] {layers} layers, {len(rows)} tokens: flipped {int(flipped.sum())}, output rel-L2 "
+          f"{o_rel:.3e}, update rel-L2 {d_rel:.3e}, max-abs {mab:.3e}, output RMS {np.sqrt(np.mean(h_o ** 2)):.3g}")
+    assert keep.sum() >= len(rows) // 4, "too few tokens kept their routing to compare outputs"
+    assert o_rel <= REL_L2_TOL and d_rel <= REL_L2_TOL, (o_rel, d_rel)
+    return flipped.sum(), o_rel, mab
 
 
 @pytest.mark.parametrize("center", [0, 1])
@@ -514,6 +693,18 @@ def test_chain_decode_b1_teacher_forced():
     _chain("decode_b1_l94", 4)
 
 
-def test_chain_long_skewed_sampled_rows():
-    """4096 tokens with the Zipf logit bias: hot experts far above 16 tokens."""
-    _chain("long4096", 2, sample_rows=list(range(0, 4096, 256)))
+def test_chain_long_skewed_tile_covering_rows():
+    """4096 tokens with the Zipf logit bias, layers 0 and 1 at full size: rows chosen from the
+    oracle's token lists to hit every tile column of the hottest experts and every
+    tensor-core expert's last short tile (hot experts far above the 32-entry threshold)."""
+    _chain("long4096", 2, cover_tiles=True)
+
+
+def test_chain_free_prefill64_all_layers():
+    """The 8-layer B=64 stack end to end, GPU chain against oracle chain."""
+    _chain_free("prefill64", 8)
+
+
+def test_chain_free_long4096_sampled_rows():
+    """The 4-layer 4096-token Zipf stack end to end on 256 sampled tokens."""
+    _chain_free("long4096", 4, rows=range(0, 4096, 16))

@@ -65,16 +65,40 @@ def test_route_noalloc_large_batch_matches_oracle():
     np.testing.assert_allclose(wt.cpu().numpy(), ow64, rtol=W_RTOL, atol=1e-7)
 
 
-def test_route_noalloc_rejects_oversize_batch():
+@pytest.mark.parametrize("B", [8192])
+def test_route_noalloc_whole_scratch_matches_oracle(B):
+    """The largest batch the fixed scratch takes at 128 experts: 8192 x 128 = 2^20 partial
+    logits, one split-K partial, the whole array used; indices exact, weights to 1e-5."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import oracle
+    w = W.WORKLOADS["long4096"]
+    gate = W.gen_gate(w, 0)
+    bias = W.gen_gate_bias(w, 0)
+    x, _ = resampled_x(w, 0, B, gate, bias)
+    desc = smoe.make_desc(w.d_model, w.num_experts, w.top_k, w.ffn_dim)
+    idx = torch.empty(B, w.top_k, dtype=torch.int32, device=DEV)
+    wt = torch.empty(B, w.top_k, dtype=torch.float32, device=DEV)
+    smoe.smoe_route_noalloc(desc, x.to(DEV).view(torch.int16), gate.to(DEV), bias.to(DEV), idx, wt)
+    oi, ow64, _, _ = oracle.route(x, gate, bias, w.top_k, 1)
+    assert np.array_equal(idx.cpu().numpy(), oi)
+    np.testing.assert_allclose(wt.cpu().numpy(), ow64, rtol=W_RTOL, atol=1e-7)
+
+
+@pytest.mark.parametrize("B", [8193, 16384])
+def test_route_noalloc_rejects_oversize_batch(B):
+    """One token past the scratch (8193 x 128 > 2^20 floats even with one split) is refused
+    with SMOE_ERR_UNSUPPORTED before anything is launched."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     w = W.WORKLOADS["prefill64"]
     desc = smoe.make_desc(w.d_model, w.num_experts, w.top_k, w.ffn_dim)
-    B = 16384   # 16384 tokens x 128 experts > 2^20 floats even with one split
     x = torch.zeros(B, w.d_model, dtype=torch.int16, device=DEV)
     gate = torch.zeros(w.num_experts, w.d_model, dtype=torch.float32, device=DEV)
-    idx = torch.empty(B, w.top_k, dtype=torch.int32, device=DEV)
+    idx = torch.full((B, w.top_k), -1, dtype=torch.int32, device=DEV)
     wt = torch.empty(B, w.top_k, dtype=torch.float32, device=DEV)
     with pytest.raises(smoe.SmoeError) as ei:
         smoe.smoe_route_noalloc(desc, x, gate, None, idx, wt)
     assert ei.value.status == smoe.SMOE_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert torch.all(idx == -1)   # nothing was launched
