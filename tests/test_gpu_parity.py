@@ -340,12 +340,17 @@ def test_ffn_batch_step_by_step_matches_layer():
 
 
 @pytest.mark.parametrize("name,B,d,center,alias", [("toy", 16, None, 1, False), ("prefill64", 64, None, 1, True),
-                                                   ("q35_prefill64", 37, None, 0, True), ("toy", 5, 8192, 1, False)])
+                                                   ("q35_prefill64", 37, None, 0, True), ("toy", 5, 8192, 1, False),
+                                                   ("toy512", 512, None, 1, True), ("toy512", 384, None, 0, False)])
 def test_ffn_batch_norm_equals_ffn_then_norm(name, B, d, center, alias):
     """smoe_moe_ffn_batch_norm gives smoe_moe_ffn_batch's residual and smoe_rmsnorm_bf16's
-    next-block input bit for bit (the fused kernel for d_model <= 4096, the standalone norm
-    after the combine beyond), also when x_next is the input buffer x itself."""
-    w = W.WORKLOADS[name] if d is None else W.scaled(W.WORKLOADS[name], d_model=d)
+    next-block input bit for bit (the combine + norm kernel for d_model <= 4096, the standalone
+    norm after the combine beyond; also with hot experts on the tensor-core path at B >= 256),
+    also when x_next is the input buffer x itself."""
+    if name == "toy512":   # d, ffn_dim multiples of 512: hot experts on the tensor-core path
+        w = W.scaled(W.WORKLOADS["toy"], ffn_dim=512, tokens=B, num_experts=32, zipf_s=1.1)
+    else:
+        w = W.WORKLOADS[name] if d is None else W.scaled(W.WORKLOADS[name], d_model=d)
     c = Case(w, B=B)
     xd = c.x_dev()
     wt, uid, nu, off, tl, sl = _routed_lists(c, xd)
@@ -488,6 +493,15 @@ def test_layer_is_deterministic():
     a, _, _ = c.run_layer()
     b, _, _ = c.run_layer()
     assert torch.equal(a, b)
+
+
+def test_tensor_core_layer_is_deterministic():
+    """Hot experts on the tensor-core path, cold ones on the few-token queue: repeated calls
+    agree bit for bit."""
+    w = W.scaled(W.WORKLOADS["toy"], ffn_dim=512, tokens=384, num_experts=32, zipf_s=1.1)
+    c = Case(w)
+    outs = [c.run_layer()[0] for _ in range(3)]
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
 def test_graph_replay_equals_direct():
