@@ -433,7 +433,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t it = 0, tile = 0;
+            uint32_t tile = 0, s = 0, sa = 0, ph_b = 0, ph_a = 0;
+            const uint64_t bdesc0 = sw128_desc(sbase + C::kOffB);
             for (int t = blockIdx.x; t < n_items; t += gridDim.x, ++tile) {
                 const Item I = decode_item(a, pref, t);
                 const int ntok = min(TC_N, I.n - I.nt * TC_N);
@@ -441,27 +442,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t buf = tile & 1u;
                 if (tile >= 2 && !poisoned) fail(mbar_wait(smem_u32(&acc_empty[buf]), ((tile >> 1) - 1) & 1u));
                 tc_fence_after();
-                for (int st = 0; st < n_st; ++st, ++it) {
-                    const uint32_t s = it % C::kB, sa = it % C::kKa;
-                    if (!poisoned) fail(mbar_wait(smem_u32(&deq[sa]), (it / C::kKa) & 1u));
-                    if (!poisoned) fail(mbar_wait(smem_u32(&full_b[s]), (it / C::kB) & 1u));
-                    if (poisoned) continue;
-                    tc_fence_after();
-                    const uint32_t a_tmem = tmem + TC_A_COL + sa * 32u * C::kGps;
-                    const bool two = PASS == 0 && st < n_main;   // sub-tile b against A group b
-                    const uint32_t bbuf = sbase + C::kOffB + s * C::kBSlot;
-                    const uint32_t d_tmem = tmem + buf * TC_N;
+                const uint32_t d_tmem = tmem + buf * TC_N;
+                for (int st = 0; st < n_st; ++st) {
+                    if (!poisoned) fail(mbar_wait(smem_u32(&deq[sa]), ph_a));
+                    if (!poisoned) fail(mbar_wait(smem_u32(&full_b[s]), ph_b));
+                    if (!poisoned) {
+                        tc_fence_after();
+                        const uint32_t a_tmem = tmem + TC_A_COL + sa * 32u * C::kGps;
+                        const bool two = PASS == 0 && st < n_main;   // sub-tile b against A group b
+                        const uint64_t bd0 = bdesc0 + (uint64_t)((s * (uint32_t)C::kBSlot) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
+                        for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
-                        for (int b = 0; b < C::kNb; ++b) {
-                            const uint64_t bd = sw128_desc(bbuf + b * TC_B_BYTES + kk * 32);
-                            umma_f16_ta(d_tmem, a_tmem + (two ? 32u * b : 0u) + kk * 8u, bd, idesc,
-                                        (st > 0 || kk > 0 || b > 0) ? 1u : 0u);
+                            for (int b = 0; b < C::kNb; ++b) {
+                                umma_f16_ta(d_tmem, a_tmem + (two ? 32u * b : 0u) + kk * 8u,
+                                            bd0 + (uint64_t)((b * TC_B_BYTES + kk * 32) >> 4), idesc,
+                                            (st > 0 || kk > 0 || b > 0) ? 1u : 0u);
+                            }
                         }
+                        umma_commit(smem_u32(&empty_b[s]));    // B slot free once these MMAs finish
+                        umma_commit(smem_u32(&empty_a[sa]));   // and the dequantised slot
                     }
-                    umma_commit(smem_u32(&empty_b[s]));    // B slot free once these MMAs finish
-                    umma_commit(smem_u32(&empty_a[sa]));   // and the dequantised slot
+                    if (++s == (uint32_t)C::kB) { s = 0; ph_b ^= 1u; }
+                    if (++sa == (uint32_t)C::kKa) { sa = 0; ph_a ^= 1u; }
                 }
                 if (!poisoned) umma_commit(smem_u32(&acc_full[buf]));   // accumulators of this tile ready
             }

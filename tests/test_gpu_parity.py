@@ -406,6 +406,49 @@ def test_tensor_core_and_small_paths_mixed():
     check_outputs(out.numpy(), o64, c.x.float().numpy())
 
 
+def _reshape_scales(c: "Case"):
+    """Weight rows outside the sampled scale range, in every projection of every expert:
+    rows 7j whose group scales (and biases) fall by 2^-(g mod 16) along the row (a 2^15
+    spread), rows 11j + 3 that are constant (s = 0, b = +-0.01) and rows 13j + 5 with
+    scales and biases times 4.  The oracle and the device get the same tensors."""
+    for name in list(c.wts_cpu):
+        if not name.startswith("s_"):
+            continue
+        s = c.wts_cpu[name].to(torch.float64).clone()
+        b = c.wts_cpu["b_" + name[2:]].to(torch.float64).clone()
+        _, out, G = s.shape
+        f = torch.pow(2.0, -(torch.arange(G, dtype=torch.float64) % 16))
+        s[:, 0::7, :] *= f
+        b[:, 0::7, :] *= f
+        s[:, 3::11, :] = 0.0
+        b[:, 3::11, :] = 0.01 * torch.where(torch.arange(G) % 2 == 0, 1.0, -1.0).to(torch.float64)
+        s[:, 5::13, :] *= 4.0
+        b[:, 5::13, :] *= 4.0
+        c.wts_cpu[name] = W._bf16_bits(s)
+        c.wts_cpu["b_" + name[2:]] = W._bf16_bits(b)
+    c.wts_gpu = {k: v.to(DEV) for k, v in c.wts_cpu.items()}
+    c.weights = smoe.Weights(c.wts_gpu)
+    c.layer_o = oracle.Layer.from_workload(c.w, c.wts_cpu)
+
+
+@pytest.mark.parametrize("layout,zipf", [("separate", 0.0), ("fused", 0.0), ("separate", 1.1)])
+def test_tensor_core_path_rows_outside_the_sampled_scale_range(layout, zipf):
+    """Weights outside the sampled scale range on the tcgen05 path: groups whose scale is 2^-15
+    of the row's largest (s (q - 8) among the fp16 subnormals), constant rows whose whole
+    weight is the per-group term b + 8 s, and rows with four times the scales; with zipf = 1.1
+    the cold experts take the mma.sync path over the same tensors."""
+    w = W.scaled(W.WORKLOADS["toy"], ffn_dim=512, tokens=512 if zipf == 0.0 else 384,
+                 num_experts=16 if zipf == 0.0 else 32, layout=layout, zipf_s=zipf)
+    c = Case(w)
+    _reshape_scales(c)
+    out, idx, _ = c.run_layer()
+    o64, oidx, _, _ = c.oracle_layer()
+    assert np.array_equal(idx.numpy(), oidx)
+    counts = np.bincount(oidx.ravel(), minlength=w.num_experts)
+    assert counts.max() >= 32
+    check_outputs(out.numpy(), o64, c.x.float().numpy())
+
+
 # ----------------------------------------------------------------------------- shared expert
 @pytest.mark.parametrize("layout,B,F", [("separate", 16, 256), ("fused", 37, 256), ("separate", 512, 512)])
 def test_shared_expert_parity(layout, B, F):
