@@ -74,8 +74,10 @@ typedef enum {
                                          (or not finite); the outputs are then not
                                          meaningful                                        */
 #define SMOE_FAULT_TIMEOUT      0x4u  /* a bounded wait for an async weight copy gave up   */
-#define SMOE_FAULT_TOKEN_INDEX  0x8u  /* a token list entry outside [0, B): row 0 is read
-                                         in its place and the residual is not meaningful   */
+#define SMOE_FAULT_TOKEN_INDEX  0x8u  /* a token list entry outside [0, B) or a slot list
+                                         entry outside [0, top_k): row 0 is read in its
+                                         place, the entry's output is dropped and the
+                                         residual is not meaningful                         */
 #define SMOE_FAULT_SLOT_POOL    0x10u /* a streamed-expert plan or copy entry out of range */
 
 /* Layer descriptor: the subset of the model config the MoE block needs
@@ -154,7 +156,9 @@ SMOE_API smoe_status smoe_expert_union(const smoe_layer_desc* desc, const int32_
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /* Steps 3 + 4: every union expert applied once to its token list, outputs weighted by
- * topk_w and added to the residual in rank order k = 0..top_k-1.
+ * topk_w and added to the residual in rank order k = 0..top_k-1: the down projection's epilogue
+ * stores each slot already weighted, w[t][k] * y_k (fp32 product), and one reduction per row adds
+ * the top_k weighted slots into residual[t] in rank order (deterministic).
  *   x         bf16 [B, d_model] (the same rows that were routed)
  *   union ... slot_list: as produced by smoe_expert_union
  *   topk_w    fp32 [B, top_k]

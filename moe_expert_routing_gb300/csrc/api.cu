@@ -212,6 +212,8 @@ WsLayout ws_layout(const smoe_layer_desc& D, int max_tokens) {
     L.s16x = take(2 * BK * (d / kGroup) * 2);
     L.s16h = take(2 * BK * (F / kGroup) * 2);
     L.y = take(BK * d * 4);
+    L.entl = take(BK * 4);
+    L.wl = take(BK * 4);
     L.ticket = take((E + 2) * 4);
     L.uscratch = take((1 + (size_t)union_chunks((int)BK) * E) * 4);
     L.total = o;

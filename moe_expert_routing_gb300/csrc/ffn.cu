@@ -142,7 +142,9 @@ __device__ __forceinline__ uint4 lds_u4(uint32_t a) {
 // One warp per segment of 32 x U 8-element chunks of a list entry p: xg[p] = pair-permuted
 // fp16(x[token_list[p]]) with the odd elements of every 8 divided by 16; sx[p][g] = sum of the
 // values the stored halves stand for in group g (8 consecutive lanes hold a group's chunks),
-// also as fp16 hi and lo planes s16[0|1][p][g].  The warp issues all U of its loads before
+// also as fp16 hi and lo planes s16[0|1][p][g].  The first segment's warp also writes the
+// entry's output row t*K + k (entl[p], -1 for a token or slot index out of range, flagged) and
+// routing weight (wl[p]), so the down passes read both by list position.  The warp issues all U of its loads before
 // converting, so the kernel streams instead of waiting on one dependent load chain per 16
 // bytes; small batches use U = 1 (more warps), large ones U = 16 (fewer index loads).
 template <int U>
@@ -150,6 +152,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
                                                      const int32_t* __restrict__ n_union,
                                                      const int32_t* __restrict__ offsets,
                                                      const int32_t* __restrict__ token_list,
+                                                     const int32_t* __restrict__ slot_list,
+                                                     const float* __restrict__ topk_w, int K,
+                                                     int32_t* __restrict__ entl, float* __restrict__ wl,
                                                      uint32_t* __restrict__ status,
                                                      __half* __restrict__ xg, float* __restrict__ sx,
                                                      __half* __restrict__ s16, int BK, int32_t* __restrict__ ticket,
@@ -167,6 +172,13 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
     for (bool first = true; wg < total * segs; wg += (gridDim.x * blockDim.x) >> 5, first = false) {
         const int p = wg / segs, seg = wg - p * segs;
         int t = first ? t_first : token_list[p];
+        if (seg == 0 && lane == 0) {   // the entry's output row and routing weight
+            const int k = slot_list[p];
+            const bool ok = t >= 0 && t < B && k >= 0 && k < K;
+            entl[p] = ok ? t * K + k : -1;
+            wl[p] = ok ? topk_w[(size_t)t * K + k] : 0.f;
+            if (!ok && t >= 0 && t < B) atomicOr(status, SMOE_FAULT_TOKEN_INDEX);   // slot out of range
+        }
         if (t < 0 || t >= B) {   // a caller-supplied list that does not match B: flag, use row 0
             if (lane == 0) atomicOr(status, SMOE_FAULT_TOKEN_INDEX);
             t = 0;
@@ -274,7 +286,9 @@ struct PassArgs {
     const int32_t* union_ids; const int32_t* n_union; const int32_t* offsets;
     const int32_t* token_list; const int32_t* slot_list;
     __half* h_out; float* hsum_out;   // pass 0 outputs
-    float* y_out;                     // pass 1 output [B*K, d]
+    float* y_out;                     // pass 1 output [B*K, d]: w[t,k] y_k(x_t), the weighted slot
+    const int32_t* entl;              // output row t*K + k of list position p (-1: rejected)
+    const float* wl;                  // routing weight of list position p
     uint32_t* status;
 };
 
@@ -434,18 +448,21 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
     }
     wrow_off0 = (uint32_t)lrow0 * 128u;
     wrow_off1 = (uint32_t)lrow1 * 128u;
-    // pass 1: token and slot of this thread's output columns, loaded before the k loop
-    int tok[NT][2], slt[NT][2];
+    // pass 1: output row t*K + k (-1 past the chunk or for an index the gather rejected) and
+    // routing weight of this thread's output columns, loaded before the k loop and first used
+    // after it
+    int ent[NT][2];
+    float wgt[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const int slot = nt * 8 + 2 * c + j;
-            tok[nt][j] = -1;
-            slt[nt][j] = 0;
+            ent[nt][j] = -1;
+            wgt[nt][j] = 0.f;
             if (PASS == 1 && slot < n) {
-                tok[nt][j] = a.token_list[pc + slot];
-                slt[nt][j] = a.slot_list[pc + slot];
+                ent[nt][j] = a.entl[pc + slot];
+                wgt[nt][j] = a.wl[pc + slot];
             }
         }
     const bool packed = a.kdim / kGroup == 4;   // tables [256][4]: the whole row
@@ -548,10 +565,10 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int t = tok[nt][i & 1], k = slt[nt][i & 1];   // t < 0: slot past the chunk
-                    if (t < 0 || t >= a.B || k < 0 || k >= a.K) continue;   // flagged by the gather
+                    const int e = ent[nt][i & 1];
+                    if (e < 0) continue;
                     const int r = T.row + warp * 32 + m * 16 + g + ((i & 2) ? 8 : 0);
-                    a.y_out[((size_t)t * a.K + k) * a.d + r] = acc[m][nt][i];
+                    a.y_out[(size_t)e * a.d + r] = acc[m][nt][i] * wgt[nt][i & 1];
                 }
     }
 }
@@ -865,11 +882,14 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
 }
 
 // ----------------------------------------------------------------------------- combine
+// The down passes' epilogues store every slot already weighted (w[t,k] y_k, the weighted half
+// of the combine); this is the deterministic rank-order reduction that adds a token's K
+// weighted slots into its residual row: residual[t] += sum_k (w y)_k in rank order k = 0..K-1.
 // Skipped entirely (residual untouched) when the union did not cover all B*K entries, i.e.
-// after a flagged routing fault.  A thread issues the loads of up to 8 slots (and the
-// union check) together before its rank-ordered FMA chain, so it waits on one L2 round
-// trip instead of one per slot.
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ w,
+// after a flagged routing fault.  A thread issues the loads of up to 8 slots (and the union
+// check) together before its rank-ordered chain of adds, so it waits on one L2 round trip
+// instead of one per slot.
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y,
                                                       const int32_t* __restrict__ n_union,
                                                       const int32_t* __restrict__ offsets, int B, int K, int d,
                                                       float* __restrict__ residual) {
@@ -879,25 +899,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     const int covered = offsets[*n_union];
     const int t = (int)(i / (d / 4));
     const int c4 = (int)(i - (size_t)t * (d / 4));
-    const float* wt = w + (size_t)t * K;
     const float4* yt = reinterpret_cast<const float4*>(y + (size_t)t * K * d) + c4;
     float4 acc = reinterpret_cast<float4*>(residual)[i];
     for (int k0 = 0; k0 < K; k0 += 8) {
-        float wk[8];
         float4 v[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-            if (k0 + j < K) {
-                wk[j] = wt[k0 + j];
-                v[j] = yt[(size_t)(k0 + j) * (d / 4)];
-            }
+            if (k0 + j < K) v[j] = yt[(size_t)(k0 + j) * (d / 4)];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             if (k0 + j < K) {
-                acc.x = fmaf(wk[j], v[j].x, acc.x);
-                acc.y = fmaf(wk[j], v[j].y, acc.y);
-                acc.z = fmaf(wk[j], v[j].z, acc.z);
-                acc.w = fmaf(wk[j], v[j].w, acc.w);
+                acc.x += v[j].x;
+                acc.y += v[j].y;
+                acc.z += v[j].z;
+                acc.w += v[j].w;
             }
     }
     if (covered != B * K) return;
@@ -905,12 +920,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 }
 
 // The combine followed by the norm that feeds the next block, one CTA of 256 threads per token
-// row (d <= 4096: a thread holds up to 4 float4 of the row): residual[t] += sum_k w y (the
-// combine_kernel's rank-ordered FMA chain), then x_next[t] = bf16(norm(residual[t])) with
+// row (d <= 4096: a thread holds up to 4 float4 of the row): residual[t] += sum_k (w y)_k (the
+// combine_kernel's rank-ordered chain of adds), then x_next[t] = bf16(norm(residual[t])) with
 // rmsnorm_bf16_kernel's loop order and reductions, so both outputs equal combine_kernel +
 // rmsnorm_bf16_kernel bit for bit.  After a flagged routing fault (the union did not cover all
 // B*K entries) neither residual nor x_next is written.
-__global__ void __launch_bounds__(256) combine_norm_kernel(const float* __restrict__ y, const float* __restrict__ w,
+__global__ void __launch_bounds__(256) combine_norm_kernel(const float* __restrict__ y,
                                                            const int32_t* __restrict__ n_union,
                                                            const int32_t* __restrict__ offsets, int B, int K, int d,
                                                            float* __restrict__ residual, float eps, int center,
@@ -919,7 +934,6 @@ __global__ void __launch_bounds__(256) combine_norm_kernel(const float* __restri
     const int t = blockIdx.x;
     const int n4 = d / 4;   // <= 1024
     const bool covered = offsets[*n_union] == B * K;
-    const float* wt = w + (size_t)t * K;
     float4* row = reinterpret_cast<float4*>(residual + (size_t)t * d);
     float4 v[4];
 #pragma unroll
@@ -929,21 +943,17 @@ __global__ void __launch_bounds__(256) combine_norm_kernel(const float* __restri
         const float4* yt = reinterpret_cast<const float4*>(y + (size_t)t * K * d) + i;
         float4 acc = row[i];
         for (int k0 = 0; k0 < K; k0 += 8) {
-            float wk[8];
             float4 yv[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-                if (k0 + q < K) {
-                    wk[q] = wt[k0 + q];
-                    yv[q] = yt[(size_t)(k0 + q) * n4];
-                }
+                if (k0 + q < K) yv[q] = yt[(size_t)(k0 + q) * n4];
 #pragma unroll
             for (int q = 0; q < 8; ++q)
                 if (k0 + q < K) {
-                    acc.x = fmaf(wk[q], yv[q].x, acc.x);
-                    acc.y = fmaf(wk[q], yv[q].y, acc.y);
-                    acc.z = fmaf(wk[q], yv[q].z, acc.z);
-                    acc.w = fmaf(wk[q], yv[q].w, acc.w);
+                    acc.x += yv[q].x;
+                    acc.y += yv[q].y;
+                    acc.z += yv[q].z;
+                    acc.w += yv[q].w;
                 }
         }
         v[j] = acc;
@@ -1053,7 +1063,9 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     const int segs = (d / 8 + 32 * (big ? 16 : 1) - 1) / (32 * (big ? 16 : 1));
     const int gather_blocks = std::max(1, std::min((BK * segs + 7) / 8, sms * 16));
     (big ? gather_kernel<16> : gather_kernel<1>)<<<gather_blocks, 256, 0, stream>>>(x, d, B, n_union, offsets,
-                                                                                     token_list, status,
+                                                                                     token_list, slot_list, topk_w, K,
+                                                                                     ws_ptr<int32_t>(ws, L.entl),
+                                                                                     ws_ptr<float>(ws, L.wl), status,
                                                                           xg, sx, ws_ptr<__half>(ws, L.s16x), BK,
                                                                           ticket, E + 2);
 
@@ -1076,6 +1088,7 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     a.union_ids = union_ids; a.n_union = n_union; a.offsets = offsets;
     a.token_list = token_list; a.slot_list = slot_list;
     a.h_out = h; a.hsum_out = sh; a.y_out = y; a.status = status;
+    a.entl = ws_ptr<int32_t>(ws, L.entl); a.wl = ws_ptr<float>(ws, L.wl);
     PassArgs b = a;
     b.wrow0 = d; b.wrow1 = d; b.woff1 = 0;
     b.s0 = W.sd; b.b0 = W.bd; b.s1 = W.sd; b.b1 = W.bd;
@@ -1110,12 +1123,12 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     }
 
     if (next.x_next && d <= 4096) {
-        combine_norm_kernel<<<B, 256, 0, stream>>>(y, topk_w, n_union, offsets, B, K, d, residual, next.eps,
+        combine_norm_kernel<<<B, 256, 0, stream>>>(y, n_union, offsets, B, K, d, residual, next.eps,
                                                    next.center, next.x_next);
         return cudaGetLastError();
     }
     const size_t n4 = (size_t)B * d / 4;
-    combine_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, stream>>>(y, topk_w, n_union, offsets, B, K, d,
+    combine_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, stream>>>(y, n_union, offsets, B, K, d,
                                                                       residual);
     if (next.x_next) {   // wider rows: the standalone norm after the combine
         cudaError_t e = cudaGetLastError();

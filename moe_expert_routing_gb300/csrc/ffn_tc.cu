@@ -73,7 +73,7 @@ struct TcCfg {
     static constexpr int kKa = TC_A_GROUPS / kGps;            // A stages in tensor memory
     static constexpr int kB = 3;
     static constexpr int kP = 3;
-    static constexpr int kNb = 2;
+    static constexpr int kNb = 2;                             // B sub-tiles per stage (8 MMAs)
     static constexpr int kBSlot = kNb * TC_B_BYTES;
     static constexpr int kOffB = 0;
     static constexpr int kOffP = kOffB + kB * kBSlot;
@@ -83,6 +83,7 @@ struct TcCfg {
 };
 static_assert(TcCfg<0>::kSmem <= 227 * 1024 - 7168, "pass 0 shared memory");
 static_assert(TcCfg<1>::kSmem <= 227 * 1024 - 7168, "pass 1 shared memory");
+static_assert(TcCfg<0>::kNb == 2 && TcCfg<1>::kNb == 2, "a stage is 4 k steps x 2 sub-tiles = 8 MMAs (umma_stage8)");
 
 // ----------------------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -142,14 +143,31 @@ __host__ __device__ constexpr uint32_t idesc_f16(int n) {
     return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TC_M >> 4) << 24);
 }
 
-// Same, with the A operand in tensor memory: lane i holds row i, two fp16 k-elements per
-// 32-bit column (lower k in the low half), 8 columns per 16-element k step.
-__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                            uint32_t accumulate) {
+// The A operand comes from tensor memory: lane i holds row i, two fp16 k-elements per 32-bit
+// column (lower k in the low half), 8 columns per 16-element k step.
+// One pipeline stage: 8 MMAs with the A operand in tensor memory (a[m], b[m] for m = 0..7, the
+// first one initialising D when accumulate is 0) and the commits of the stage's B and A slots,
+// in one asm block.  Issued back to back like this, 8 MMAs of N = 192 cost the issuing thread
+// less time than the tensor core takes to run them, so work queues up ahead of the tensor core;
+// as separate statements, each with its own predicate, every MMA took the thread longer than
+// the tensor core did.
+__device__ __forceinline__ void umma_stage8(uint32_t d_tmem, const uint32_t (&a)[8], const uint64_t (&b)[8],
+                                            uint32_t idesc, uint32_t accumulate, uint32_t bar_b, uint32_t bar_a) {
     asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+        "{\n .reg .pred p, q;\n setp.ne.b32 p, %18, 0;\n setp.eq.b32 q, %18, %18;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %9, %17, p;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %10, %17, q;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %17, q;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %17, q;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %17, q;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %17, q;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %17, q;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %17, q;\n"
+        " tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%19];\n"
+        " tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%20];\n}\n" ::"r"(d_tmem),
+        "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]), "l"(b[1]),
+        "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(accumulate), "r"(bar_b),
+        "r"(bar_a)
         : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -234,7 +252,9 @@ struct TcArgs {
     const int32_t* token_list; const int32_t* slot_list;
     __half* h_out;                    // pass 0: [B*K, 2F] hi | lo
     __half* hsum_out;                 // pass 0: group sums of h, fp16 planes [2][B*K, F/64]
-    float* y_out;                     // pass 1: [B*K, d]
+    float* y_out;                     // pass 1: [B*K, d], each slot weighted: w[t,k] y_k
+    const int32_t* entl;              // output row t*K + k of list position p (-1: rejected)
+    const float* wl;                  // routing weight of list position p
     uint32_t* status;
 };
 
@@ -320,7 +340,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     __shared__ __align__(8) uint64_t mma_drain;   // commit of every MMA the issuer launched
     __shared__ uint32_t tmem_base_sh;
     __shared__ int pref[3 * (kMaxExperts + 1)];   // item prefix, union ids, list offsets
-    __shared__ int tok_sh[2][TC_N], slot_sh[2][TC_N];
+    __shared__ int ent_sh[2][TC_N];   // pass 1: output row t*K + k of each column (-1: none)
+    __shared__ float w_sh[2][TC_N];   // pass 1: routing weight of each column
     __shared__ float gsum_sh[4][32];   // pass 0 epilogue: partial group sums [column quarter][token]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -451,17 +472,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         const uint32_t a_tmem = tmem + TC_A_COL + sa * 32u * C::kGps;
                         const bool two = PASS == 0 && st < n_main;   // sub-tile b against A group b
                         const uint64_t bd0 = bdesc0 + (uint64_t)((s * (uint32_t)C::kBSlot) >> 4);
+                        uint32_t av[8];
+                        uint64_t bv[8];
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
                             for (int b = 0; b < C::kNb; ++b) {
-                                umma_f16_ta(d_tmem, a_tmem + (two ? 32u * b : 0u) + kk * 8u,
-                                            bd0 + (uint64_t)((b * TC_B_BYTES + kk * 32) >> 4), idesc,
-                                            (st > 0 || kk > 0 || b > 0) ? 1u : 0u);
+                                av[kk * 2 + b] = a_tmem + (two ? 32u * b : 0u) + kk * 8u;
+                                bv[kk * 2 + b] = bd0 + (uint64_t)((b * TC_B_BYTES + kk * 32) >> 4);
                             }
                         }
-                        umma_commit(smem_u32(&empty_b[s]));    // B slot free once these MMAs finish
-                        umma_commit(smem_u32(&empty_a[sa]));   // and the dequantised slot
+                        // the MMAs, then the commits: B slot and dequantised slot free once they finish
+                        umma_stage8(d_tmem, av, bv, idesc, st > 0 ? 1u : 0u, smem_u32(&empty_b[s]),
+                                    smem_u32(&empty_a[sa]));
                     }
                     if (++s == (uint32_t)C::kB) { s = 0; ph_b ^= 1u; }
                     if (++sa == (uint32_t)C::kKa) { sa = 0; ph_a ^= 1u; }
@@ -602,11 +625,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint32_t buf = tile & 1u;
             const int tok0 = I.p0 + I.nt * TC_N;
             const int ntok = min(TC_N, I.n - I.nt * TC_N);
-            // token / slot of the tile's entries (pass 1 output rows)
+            // output row and routing weight of the tile's entries (pass 1)
             if (PASS == 1) {
                 for (int j = et; j < TC_N; j += 128) {
-                    tok_sh[buf][j] = j < ntok ? a.token_list[tok0 + j] : 0;
-                    slot_sh[buf][j] = j < ntok ? a.slot_list[tok0 + j] : 0;
+                    ent_sh[buf][j] = j < ntok ? a.entl[tok0 + j] : -1;
+                    w_sh[buf][j] = j < ntok ? a.wl[tok0 + j] : 0.f;
                 }
                 asm volatile("bar.sync 2, 128;\n" ::: "memory");
             }
@@ -678,9 +701,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         for (int k = 0; k < 32; ++k) {
                             const int tk = c0 + k;
                             if (tk < ntok) {
-                                const int tok = tok_sh[buf][tk], sl = slot_sh[buf][tk];
-                                if (tok >= 0 && tok < a.B && sl >= 0 && sl < a.K)
-                                    a.y_out[((size_t)tok * a.K + sl) * a.d + r] = v[k];
+                                const int e = ent_sh[buf][tk];
+                                if (e >= 0) a.y_out[(size_t)e * a.d + r] = v[k] * w_sh[buf][tk];
                             }
                         }
                     }
@@ -750,6 +772,7 @@ cudaError_t launch_ffn_tc(const smoe_layer_desc& D, const FfnTcWeights& W, int B
     a.tc_min = tc_min;
     a.union_ids = union_ids; a.n_union = n_union; a.offsets = offsets;
     a.token_list = token_list; a.slot_list = slot_list;
+    a.entl = ws_ptr<int32_t>(ws, L.entl); a.wl = ws_ptr<float>(ws, L.wl);
     a.h_out = h; a.hsum_out = shh; a.y_out = ws_ptr<float>(ws, L.y);
     a.status = ws_ptr<uint32_t>(ws, L.status);
     CUtensorMap mb, mshi, mslo;

@@ -34,7 +34,9 @@ struct WsLayout {
     size_t sh;            // fp32 [B * K, F / 64]: per-group sums of the activations
     size_t s16x;          // fp16 [2][B * K, d / 64]: input group sums as hi and lo planes
     size_t s16h;          // fp16 [2][B * K, F / 64]: activation group sums as hi and lo planes
-    size_t y;             // fp32 [B * K, d]: unweighted expert outputs, row t*K + k
+    size_t y;             // fp32 [B * K, d]: weighted expert outputs w[t,k] y_k, row t*K + k
+    size_t entl;          // int32 [B * K]: entry t*K + k of list position p (-1: index rejected)
+    size_t wl;            // fp32 [B * K]: routing weight w[t,k] of list position p
     size_t ticket;        // int32 [2 + E]: work queues of the expert passes and per-expert counts
     size_t uscratch;      // int32 [1 + chunks * E]: the union's per-chunk counts (B * K > 1024)
     size_t total;

@@ -288,14 +288,19 @@ def test_fp16_range_fault_bit(value):
     assert smoe.smoe_read_device_status(c.ws) == 0
 
 
-def test_token_index_fault_bit():
-    """A caller-built token list with an entry outside [0, B): the FFN sets
-    SMOE_FAULT_TOKEN_INDEX, reads row 0 in its place and returns; nothing hangs."""
+@pytest.mark.parametrize("which", ["token", "slot"])
+def test_token_index_fault_bit(which):
+    """A caller-built list with a token entry outside [0, B) or a slot entry outside [0, K):
+    the FFN sets SMOE_FAULT_TOKEN_INDEX, drops that entry's output (reading row 0 in place of
+    a bad token) and returns; nothing hangs."""
     c = Case(W.WORKLOADS["toy"], gap=False)
     xd = c.x_dev()
     smoe.smoe_clear_device_status(c.ws)
     wt, uid, nu, off, tl, sl = _routed_lists(c, xd)
-    tl[5] = c.B + 3
+    if which == "token":
+        tl[5] = c.B + 3
+    else:
+        sl[5] = c.w.top_k
     res = c.x.float().to(DEV)
     smoe.smoe_moe_ffn_batch(c.desc, c.weights, xd, uid, nu, off, tl, sl, wt, res, c.ws)
     bits = smoe.smoe_read_device_status(c.ws)
