@@ -7,7 +7,8 @@
 //
 // Exact fp16 weights.  w = s q + b = s (q - 8) + (b + 8 s).  s is bf16 (8-bit significand)
 // and q - 8 a 4-bit signed integer, so s (q - 8) has at most 11 significant bits and is
-// exactly an fp16 number; the rest, eps = b + 8 s, depends only on (row, group).  Hence
+// exactly an fp16 number within fp16's normal range (scales from 2^-14 up; smaller ones round
+// among the subnormals); the rest, eps = b + 8 s, depends only on (row, group).  Hence
 //   sum_i w_i x_i = sum_i [s (q_i - 8)]_fp16 x_i  +  sum_g eps_g S_g,   S_g = sum_{i in g} x_i,
 // the first term one long fp16 contraction with fp32 accumulation in tensor memory, the
 // second a small [rows x groups] x [groups x tokens] product that runs as one extra k-stage
