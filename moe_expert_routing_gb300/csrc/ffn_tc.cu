@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     using C = TcCfg<PASS>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_p[C::kP], empty_p[C::kP], full_b[C::kB], empty_b[C::kB];
-    __shared__ __align__(8) uint64_t deq[C::kKa], empty_a[C::kKa];
+    __shared__ __align__(8) uint64_t empty_a[C::kKa];
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
     __shared__ __align__(8) uint64_t mma_drain;   // commit of every MMA the issuer launched
     __shared__ uint32_t tmem_base_sh;
@@ -359,11 +359,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_init(smem_u32(&empty_p[s]), 8);     // every dequantiser warp has consumed the slot
         }
         for (int s = 0; s < C::kB; ++s) {
-            mbar_init(smem_u32(&full_b[s]), 1);
+            // the stage's activation copies (one arrival with their byte count) and its
+            // dequantised A (one arrival per warp of the stage's dequantiser set): the MMA
+            // issuer waits on one barrier per stage
+            mbar_init(smem_u32(&full_b[s]), 1 + 4);
             mbar_init(smem_u32(&empty_b[s]), 1);     // tcgen05.commit of the stage's MMAs
         }
         for (int s = 0; s < C::kKa; ++s) {
-            mbar_init(smem_u32(&deq[s]), 4);         // one arrival per warp of the stage's dequantiser set
             mbar_init(smem_u32(&empty_a[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -455,7 +457,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t tile = 0, s = 0, sa = 0, ph_b = 0, ph_a = 0;
+            uint32_t tile = 0, s = 0, sa = 0, ph_b = 0;
             const uint64_t bdesc0 = sw128_desc(sbase + C::kOffB);
             for (int t = blockIdx.x; t < n_items; t += gridDim.x, ++tile) {
                 const Item I = decode_item(a, pref, t);
@@ -466,8 +468,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + buf * TC_N;
                 for (int st = 0; st < n_st; ++st) {
-                    if (!poisoned) fail(mbar_wait(smem_u32(&deq[sa]), ph_a));
-                    if (!poisoned) fail(mbar_wait(smem_u32(&full_b[s]), ph_b));
+                    if (!poisoned) fail(mbar_wait(smem_u32(&full_b[s]), ph_b));   // activations and A
                     if (!poisoned) {
                         tc_fence_after();
                         const uint32_t a_tmem = tmem + TC_A_COL + sa * 32u * C::kGps;
@@ -488,7 +489,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                     smem_u32(&empty_a[sa]));
                     }
                     if (++s == (uint32_t)C::kB) { s = 0; ph_b ^= 1u; }
-                    if (++sa == (uint32_t)C::kKa) { sa = 0; ph_a ^= 1u; }
+                    if (++sa == (uint32_t)C::kKa) sa = 0;
                 }
                 if (!poisoned) umma_commit(smem_u32(&acc_full[buf]));   // accumulators of this tile ready
             }
@@ -611,7 +612,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 __syncwarp();
                 if (st < n_main && st % kSps >= kSps - 2 && lane == 0)   // this set's last stage of the slot
                     mbar_arrive(smem_u32(&empty_p[sp_]));
-                if (lane == 0) mbar_arrive(smem_u32(&deq[sa]));
+                if (lane == 0) {
+                    // A of stage it is in place.  Stage it's barrier slot last served stage
+                    // it - kB; with an A ring at least as deep as the activation ring (the down
+                    // pass: 4 A stages, 3 activation slots) this set can run far enough ahead of
+                    // the MMA issuer to arrive while that phase is still open, so it first waits
+                    // (bounded) for it; with fewer A stages (gate/up: 2), reaching stage it at all
+                    // means the issuer has passed stage it - 2, so that phase is complete.
+                    if (C::kKa >= C::kB && it >= (uint32_t)C::kB && !poisoned)
+                        fail(mbar_wait(smem_u32(&full_b[it % C::kB]), ((it / C::kB) - 1) & 1u));
+                    mbar_arrive(smem_u32(&full_b[it % C::kB]));
+                }
             }
         }
     } else {
