@@ -341,8 +341,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     __shared__ __align__(8) uint64_t mma_drain;   // commit of every MMA the issuer launched
     __shared__ uint32_t tmem_base_sh;
     __shared__ int pref[3 * (kMaxExperts + 1)];   // item prefix, union ids, list offsets
-    __shared__ int ent_sh[2][TC_N];   // pass 1: output row t*K + k of each column (-1: none)
-    __shared__ float w_sh[2][TC_N];   // pass 1: routing weight of each column
+    __shared__ __align__(16) int ent_sh[2][TC_N];   // pass 1: output row t*K + k of each column (-1: none)
+    __shared__ __align__(16) float w_sh[2][TC_N];   // pass 1: routing weight of each column
     __shared__ float gsum_sh[4][32];   // pass 0 epilogue: partial group sums [column quarter][token]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -708,14 +708,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             a.hsum_out[(size_t)a.B * a.K * Gh + i] = __float2half_rn(g4 - __half2float(sh));
                         }
                     } else {
-                        const int r = I.mt * TC_M + lr;   // output row
+                        // output row r of the 32 columns' entries (-1 past the tile's tokens), their
+                        // rows and weights read 4 columns at a time
+                        float* yr = a.y_out + (I.mt * TC_M + lr);
+                        const int4* ep = reinterpret_cast<const int4*>(&ent_sh[buf][c0]);
+                        const float4* wp = reinterpret_cast<const float4*>(&w_sh[buf][c0]);
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) {
-                            const int tk = c0 + k;
-                            if (tk < ntok) {
-                                const int e = ent_sh[buf][tk];
-                                if (e >= 0) a.y_out[(size_t)e * a.d + r] = v[k] * w_sh[buf][tk];
-                            }
+                        for (int k4 = 0; k4 < 8; ++k4) {
+                            const int4 e4 = ep[k4];
+                            const float4 w4 = wp[k4];
+                            if (e4.x >= 0) yr[(size_t)e4.x * a.d] = v[4 * k4] * w4.x;
+                            if (e4.y >= 0) yr[(size_t)e4.y * a.d] = v[4 * k4 + 1] * w4.y;
+                            if (e4.z >= 0) yr[(size_t)e4.z * a.d] = v[4 * k4 + 2] * w4.z;
+                            if (e4.w >= 0) yr[(size_t)e4.w * a.d] = v[4 * k4 + 3] * w4.w;
                         }
                     }
                 }
