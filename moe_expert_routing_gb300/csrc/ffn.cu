@@ -919,26 +919,26 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     reinterpret_cast<float4*>(residual)[i] = acc;
 }
 
-// The combine followed by the norm that feeds the next block, one CTA of 256 threads per token
-// row (d <= 4096: a thread holds up to 4 float4 of the row): residual[t] += sum_k (w y)_k (the
+// The combine followed by the norm that feeds the next block, one CTA of 512 threads per token
+// row (d <= 4096: a thread holds up to 2 float4 of the row): residual[t] += sum_k (w y)_k (the
 // combine_kernel's rank-ordered chain of adds), then x_next[t] = bf16(norm(residual[t])) with
 // rmsnorm_bf16_kernel's loop order and reductions, so both outputs equal combine_kernel +
 // rmsnorm_bf16_kernel bit for bit.  After a flagged routing fault (the union did not cover all
 // B*K entries) neither residual nor x_next is written.
-__global__ void __launch_bounds__(256) combine_norm_kernel(const float* __restrict__ y,
+__global__ void __launch_bounds__(512) combine_norm_kernel(const float* __restrict__ y,
                                                            const int32_t* __restrict__ n_union,
                                                            const int32_t* __restrict__ offsets, int B, int K, int d,
                                                            float* __restrict__ residual, float eps, int center,
                                                            uint16_t* __restrict__ x_next) {
-    __shared__ float red[8];
+    __shared__ float red[16];
     const int t = blockIdx.x;
     const int n4 = d / 4;   // <= 1024
     const bool covered = offsets[*n_union] == B * K;
     float4* row = reinterpret_cast<float4*>(residual + (size_t)t * d);
-    float4 v[4];
+    float4 v[2];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int i = threadIdx.x + 256 * j;
+    for (int j = 0; j < 2; ++j) {
+        const int i = threadIdx.x + 512 * j;
         if (i >= n4) break;
         const float4* yt = reinterpret_cast<const float4*>(y + (size_t)t * K * d) + i;
         float4 acc = row[i];
@@ -960,37 +960,37 @@ __global__ void __launch_bounds__(256) combine_norm_kernel(const float* __restri
     }
     if (!covered) return;   // the same decision in every thread of the CTA
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        if (threadIdx.x + 256 * j < n4) row[threadIdx.x + 256 * j] = v[j];
+    for (int j = 0; j < 2; ++j)
+        if (threadIdx.x + 512 * j < n4) row[threadIdx.x + 512 * j] = v[j];
     float mean = 0.f;
     if (center) {
         float s = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (threadIdx.x + 256 * j < n4) s += (v[j].x + v[j].y) + (v[j].z + v[j].w);
-        mean = block_sum256(s, red) / (float)d;
+        for (int j = 0; j < 2; ++j)
+            if (threadIdx.x + 512 * j < n4) s += (v[j].x + v[j].y) + (v[j].z + v[j].w);
+        mean = block_sum512(s, red) / (float)d;
     }
     float ss = 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        if (threadIdx.x + 256 * j < n4) {
+    for (int j = 0; j < 2; ++j)
+        if (threadIdx.x + 512 * j < n4) {
             const float a = v[j].x - mean, b = v[j].y - mean, c = v[j].z - mean, e = v[j].w - mean;
             ss = fmaf(a, a, ss);
             ss = fmaf(b, b, ss);
             ss = fmaf(c, c, ss);
             ss = fmaf(e, e, ss);
         }
-    const float tot = block_sum256(ss, red);
+    const float tot = block_sum512(ss, red);
     const float inv = 1.0f / sqrtf(tot / (float)d + eps);
     uint2* out = reinterpret_cast<uint2*>(x_next + (size_t)t * d);
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        if (threadIdx.x + 256 * j < n4) {
+    for (int j = 0; j < 2; ++j)
+        if (threadIdx.x + 512 * j < n4) {
             const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn((v[j].x - mean) * inv));
             const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn((v[j].y - mean) * inv));
             const uint32_t c = __bfloat16_as_ushort(__float2bfloat16_rn((v[j].z - mean) * inv));
             const uint32_t e = __bfloat16_as_ushort(__float2bfloat16_rn((v[j].w - mean) * inv));
-            out[threadIdx.x + 256 * j] = make_uint2(a | (b << 16), c | (e << 16));
+            out[threadIdx.x + 512 * j] = make_uint2(a | (b << 16), c | (e << 16));
         }
 }
 
@@ -1123,7 +1123,7 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     }
 
     if (next.x_next && d <= 4096) {
-        combine_norm_kernel<<<B, 256, 0, stream>>>(y, n_union, offsets, B, K, d, residual, next.eps,
+        combine_norm_kernel<<<B, 512, 0, stream>>>(y, n_union, offsets, B, K, d, residual, next.eps,
                                                    next.center, next.x_next);
         return cudaGetLastError();
     }

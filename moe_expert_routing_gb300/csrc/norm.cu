@@ -6,11 +6,11 @@
 namespace smoe {
 namespace {
 
-// One CTA of 256 threads per row, float4 loads; the row mean (if centring) and the sum of
-// squares are reduced across the CTA in fp32 (block_sum256).
-__global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const float* __restrict__ h, float eps, int center, int d,
+// One CTA of 512 threads per row, float4 loads; the row mean (if centring) and the sum of
+// squares are reduced across the CTA in fp32 (block_sum512).
+__global__ void __launch_bounds__(512) rmsnorm_bf16_kernel(const float* __restrict__ h, float eps, int center, int d,
                                                            uint16_t* __restrict__ x_out) {
-    __shared__ float red[8];
+    __shared__ float red[16];
     const int t = blockIdx.x;
     const float4* row = reinterpret_cast<const float4*>(h + (size_t)t * d);
     float mean = 0.f;
@@ -20,7 +20,7 @@ __global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const float* __restri
             const float4 v = row[i];
             s += (v.x + v.y) + (v.z + v.w);
         }
-        mean = block_sum256(s, red) / (float)d;
+        mean = block_sum512(s, red) / (float)d;
     }
     float ss = 0.f;
     for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const float* __restri
         ss = fmaf(c, c, ss);
         ss = fmaf(e, e, ss);
     }
-    const float tot = block_sum256(ss, red);
+    const float tot = block_sum512(ss, red);
     const float inv = 1.0f / sqrtf(tot / (float)d + eps);
     uint2* out = reinterpret_cast<uint2*>(x_out + (size_t)t * d);
     for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(const float* __restri
 
 cudaError_t launch_rmsnorm(const float* h, float eps, int center, int B, int d, uint16_t* x_out,
                            cudaStream_t stream) {
-    rmsnorm_bf16_kernel<<<B, 256, 0, stream>>>(h, eps, center, d, x_out);
+    rmsnorm_bf16_kernel<<<B, 512, 0, stream>>>(h, eps, center, d, x_out);
     return cudaGetLastError();
 }
 

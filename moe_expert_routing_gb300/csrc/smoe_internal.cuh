@@ -156,10 +156,10 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
     return __uint_as_float(bits16 << 16);
 }
 
-// Sum of v over a CTA of 256 threads (warp butterflies, then the 8 warp sums in warp order),
-// returned to every thread; red: 8 floats of shared memory.  The RMS-norm kernels use it so
+// Sum of v over a CTA of 512 threads (warp butterflies, then the 16 warp sums in warp order),
+// returned to every thread; red: 16 floats of shared memory.  The RMS-norm kernels use it so
 // that a norm fused into another kernel gives the standalone norm's results bit for bit.
-__device__ __forceinline__ float block_sum256(float v, float* red) {
+__device__ __forceinline__ float block_sum512(float v, float* red) {
 #pragma unroll
     for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
     __syncthreads();
@@ -167,7 +167,7 @@ __device__ __forceinline__ float block_sum256(float v, float* red) {
     __syncthreads();
     float tot = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) tot += red[w];
+    for (int w = 0; w < 16; ++w) tot += red[w];
     return tot;
 }
 
