@@ -569,7 +569,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
                         for (int gi = 0; gi < C::kGps; ++gi) {   // group g0 + gi -> 32 columns
                             const int g = g0 + gi;
-                            const uint32_t sw = (&scl.x)[(g & 7) >> 1];
+                            const uint32_t wsel = (uint32_t)(g & 7) >> 1;   // selects, not a local-memory index
+                            const uint32_t sw = wsel == 0 ? scl.x : wsel == 1 ? scl.y : wsel == 2 ? scl.z : scl.w;
                             const float sf = __uint_as_float((g & 1) ? (sw & 0xFFFF0000u) : (sw << 16));
                             const __half2 s2 = __float2half2_rn(sf);   // exact: bf16 -> fp16
                             const uint32_t wv[8] = {w[gi][0].x, w[gi][0].y, w[gi][0].z, w[gi][0].w,
