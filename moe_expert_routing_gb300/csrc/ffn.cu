@@ -246,30 +246,33 @@ constexpr bool claims(int mode) { return mode == kBoth; }   // atomic queue, dow
 // consumer warps + a producer warp (+ a publisher warp when both passes share a launch)
 constexpr int pass_threads(int mode) { return 32 * (kConsumerWarps + 1 + has_publisher(mode)); }
 constexpr int kWBytes = 256 * 128;         // 256 weight rows x 32 u32 words (4 groups)
-constexpr int kXBoxBytes = 16 * 128;       // 16 activation rows x 64 fp16 (one group)
-constexpr int kTokChunk = 16;              // tokens per pass over the weights
+constexpr int kTokChunk = 16;              // tokens per pass over the weights (down-only launches: 8)
 constexpr int kSbBytes = 256 * 16;         // 256 rows x up to 8 bf16 (a table of scales or biases)
 
-// One ring stage: packed weights | activation boxes (4, or 4 hi + 4 lo) | scales | biases |
-// activation group sums fp32 [16 tokens][4 groups]; a 1024-byte multiple.  The scale and
-// bias tables hold, per weight row, the 8 groups of the 16-byte-aligned window that
-// contains the stage's 4 groups ([256][8] bf16), or with 4 groups per row ([256][4]) the
-// whole row.  A gate/up-only launch has room for 4 of its smaller stages; launches that run
-// down tiles use 3 stages sized for them.
+// One ring stage: packed weights | activation boxes (4, or 4 hi + 4 lo; one row per token of
+// the chunk) | scales | biases | activation group sums fp32 [chunk tokens][4 groups]; a
+// 1024-byte multiple.  The scale and bias tables hold, per weight row, the 8 groups of the
+// 16-byte-aligned window that contains the stage's 4 groups ([256][8] bf16), or with 4 groups
+// per row ([256][4]) the whole row.  A gate/up-only launch has room for 4 of its smaller
+// stages; a down-only launch takes chunks of at most 8 tokens (8-row boxes), which also leaves
+// room for 4 stages; the both-pass launch uses 3 stages sized for 16-token down chunks.
 template <int MODE>
 struct StageCfg {
-    static constexpr int kCount = gate_up_only(MODE) ? 4 : 3;
+    static constexpr int kCount = MODE == kBoth ? 3 : 4;
+    static constexpr int kChunk = down_only(MODE) ? 8 : kTokChunk;   // tokens per pass over the weights
+    static constexpr int kBox = kChunk * 128;                        // one activation box: kChunk rows x 64 fp16
     static constexpr int kXOff = kWBytes;
-    static constexpr int kSOff = kXOff + (gate_up_only(MODE) ? 4 : 8) * kXBoxBytes;
+    static constexpr int kSOff = kXOff + (gate_up_only(MODE) ? 4 : 8) * kBox;
     static constexpr int kBOff = kSOff + kSbBytes;
     static constexpr int kSumOff = kBOff + kSbBytes;
-    static constexpr int kSumBytes = kTokChunk * 4 * 4;
+    static constexpr int kSumBytes = kChunk * 4 * 4;
     static constexpr int kBytes = (kSumOff + kSumBytes + 1023) / 1024 * 1024;
     static constexpr int kSmem = kCount * kBytes + 1024;
     // TMA bytes of a pass's stage, without the scale / bias tables
-    static constexpr int tx(int pass) { return kWBytes + (pass ? 8 : 4) * kXBoxBytes + kSumBytes; }
+    static constexpr int tx(int pass) { return kWBytes + (pass ? 8 : 4) * kBox + kSumBytes; }
 };
 static_assert(StageCfg<kGateUp>::kSmem <= 227 * 1024 - 3072, "gate/up pass shared memory");
+static_assert(StageCfg<kDown>::kSmem <= 227 * 1024 - 3072, "down pass shared memory");
 static_assert(StageCfg<kBoth>::kSmem <= 227 * 1024 - 3072, "expert pass shared memory");
 
 
@@ -308,11 +311,12 @@ struct Tile {
 // columns 0-3 the hi terms of tokens 0-3 and columns 4-7 their lo terms, so each k-step is
 // one mma instead of two.  The lo columns get no bias term (S = 0 there: the group sum
 // already covers hi + lo); the caller adds column j + 4 into column j at the end.
-template <int NT, bool LO, bool PK>
+template <int NT, bool LO, bool PK, int XB>
 __device__ __forceinline__ void consume_stage(float (&acc)[2][NT][4], uint32_t wb0, uint32_t wb1, uint32_t xs,
                                               const uint2 (&sc)[2][2], const uint2 (&bi)[2][2], uint32_t sums,
                                               int g, int c) {
     static_assert(!PK || (LO && NT == 1), "packed hi/lo columns: down pass, one n-tile");
+    static_assert(NT * 8 * 128 <= XB, "the chunk's tokens fit the activation box");
     constexpr int NB = (LO && !PK) ? 2 : 1;   // activation terms per input (separate n-tiles)
     float4 S[NT][2];                 // group sums of tokens 2c and 2c+1 of each n-tile, 4 groups
 #pragma unroll
@@ -340,7 +344,7 @@ __device__ __forceinline__ void consume_stage(float (&acc)[2][NT][4], uint32_t w
 #pragma unroll
             for (int hl = 0; hl < NB; ++hl) {
                 const int box = PK ? (g >> 2) * 4 + q : hl * 4 + q;
-                const uint32_t rb = xs + box * kXBoxBytes + r * 128;
+                const uint32_t rb = xs + box * XB + r * 128;
                 const uint4 v0 = lds_u4(rb + (((2 * c) ^ sw) << 4));
                 const uint4 v1 = lds_u4(rb + (((2 * c + 1) ^ sw) << 4));
                 bf[nt][hl][0] = v0.x; bf[nt][hl][1] = v0.y; bf[nt][hl][2] = v0.z; bf[nt][hl][3] = v0.w;
@@ -487,7 +491,7 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
         bi[0][1] = lds_u2(tb + (uint32_t)(lrow0 + g + 8) * rs);
         bi[1][0] = lds_u2(tb + (uint32_t)(lrow1 + g) * rs);
         bi[1][1] = lds_u2(tb + (uint32_t)(lrow1 + g + 8) * rs);
-        consume_stage<NT, PASS == 1, PK>(acc, base + wrow_off0, base + wrow_off1, base + C::kXOff, sc, bi,
+        consume_stage<NT, PASS == 1, PK, C::kBox>(acc, base + wrow_off0, base + wrow_off1, base + C::kXOff, sc, bi,
                                      base + C::kSumOff, g, c);
         __syncwarp();   // the warp's reads of the slot, then one arrival for the warp
         if (lane == 0) mbar_arrive(R.empty + 8 * slot);
@@ -766,7 +770,7 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
                     prefetch_l2(a.s0 + r0 * G, bytes); prefetch_l2(a.b0 + r0 * G, bytes);
                     if (cur.pass == 0) { prefetch_l2(a.s1 + r1 * G, bytes); prefetch_l2(a.b1 + r1 * G, bytes); }
                     const int ty0 = (int)(packed ? r0 / 2 : r0), ty1 = (int)(packed ? r1 / 2 : r1);
-                    for (int pc = T.p0; pc < T.p1 && !poisoned; pc += kTokChunk) {
+                    for (int pc = T.p0; pc < T.p1 && !poisoned; pc += C::kChunk) {
                         for (int st = 0; st < nst; ++st) {
                             const uint32_t slot = it % C::kCount;
                             if (it >= C::kCount && !mbar_wait(R.empty + 8 * slot, ((it / C::kCount) - 1) & 1u)) {
@@ -793,7 +797,7 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
                                 tma_load_2d(base + C::kBOff + 128 * rs, &map_bu, tx0, ty1, full);
 #pragma unroll
                                 for (int q = 0; q < 4; ++q)
-                                    tma_load_2d(base + C::kXOff + q * kXBoxBytes, &map_xg, (st * 4 + q) * 64, pc,
+                                    tma_load_2d(base + C::kXOff + q * C::kBox, &map_xg, (st * 4 + q) * 64, pc,
                                                 full);
                                 tma_load_2d(base + C::kSumOff, &map_sx, st * 4, pc, full);
                             } else if (!gate_up_only(MODE)) {
@@ -802,8 +806,8 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
                                 tma_load_2d(base + C::kBOff, &map_bd, tx0, ty0, full);
 #pragma unroll
                                 for (int q = 0; q < 4; ++q) {   // h hi, then its lo terms (columns F..)
-                                    tma_load_2d(base + C::kXOff + q * kXBoxBytes, &map_h, (st * 4 + q) * 64, pc, full);
-                                    tma_load_2d(base + C::kXOff + (4 + q) * kXBoxBytes, &map_h,
+                                    tma_load_2d(base + C::kXOff + q * C::kBox, &map_h, (st * 4 + q) * 64, pc, full);
+                                    tma_load_2d(base + C::kXOff + (4 + q) * C::kBox, &map_h,
                                                 a.F + (st * 4 + q) * 64, pc, full);
                                 }
                                 tma_load_2d(base + C::kSumOff, &map_sh, st * 4, pc, full);
@@ -856,12 +860,12 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
         T.p0 = meta[3];
         T.p1 = meta[4];
         T.row = meta[5];
-        const int n = min(kTokChunk, T.p1 - pc);
+        const int n = min(C::kChunk, T.p1 - pc);
         const bool gate_up = gate_up_only(MODE) || (MODE == kBoth && item < n0);
         if constexpr (!down_only(MODE)) {
             if (gate_up) {
                 // both passes in this launch: publish the tile after its last chunk
-                const int done_uu = has_publisher(MODE) && pc + kTokChunk >= T.p1 ? item / t0 : -1;
+                const int done_uu = has_publisher(MODE) && pc + C::kChunk >= T.p1 ? item / t0 : -1;
                 if (n <= 8) consume_chunk<1, 0, MODE>(f.p[0], R, it, poisoned, T, pc, n, warp, lane, red, done_uu, M);
                 else consume_chunk<2, 0, MODE>(f.p[0], R, it, poisoned, T, pc, n, warp, lane, red, done_uu, M);
             }
@@ -870,6 +874,8 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
             if (!gate_up) {
                 if (n <= 4)
                     consume_chunk<1, 1, MODE, true>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
+                else if constexpr (C::kChunk <= 8)   // down-only launch: chunks of at most 8 tokens
+                    consume_chunk<1, 1, MODE>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
                 else if (n <= 8)
                     consume_chunk<1, 1, MODE>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
                 else consume_chunk<2, 1, MODE>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
@@ -1047,13 +1053,19 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     const int sms = sm_count[dev & 63] > 0 ? sm_count[dev & 63] : 1;
 
     // activation / group-sum maps over this call's workspace rows
-    CUtensorMap map_xg, map_h, map_sx, map_sh;
-    if (!encode_map_2d(&map_xg, xg, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, d, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_map_2d(&map_h, h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, 2 * F, 64, 16,
+    // activation boxes of one chunk: 16 token rows; the down-only launch's chunks: 8 (map_h8, map_sh8)
+    CUtensorMap map_xg, map_h, map_sx, map_sh, map_h8, map_sh8;
+    if (!encode_map_2d(&map_xg, xg, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, d, 64, kTokChunk,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_map_2d(&map_h, h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, 2 * F, 64, kTokChunk,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_map_2d(&map_sx, sx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BK, d / kGroup, 4, kTokChunk,
                        CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_map_2d(&map_sh, sh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BK, F / kGroup, 4, kTokChunk,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_map_2d(&map_h8, h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, 2 * F, 64, StageCfg<kDown>::kChunk,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_map_2d(&map_sh8, sh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BK, F / kGroup, 4, StageCfg<kDown>::kChunk,
                        CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
 
@@ -1111,7 +1123,7 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
                                     stream>>>(W.map_gate, W.map_up, W.map_down, map_xg, map_h, map_sx, map_sh,
                                               W.map_sg, W.map_su, W.map_bg, W.map_bu, W.map_sd, W.map_bd, fa);
         ffn_expert_kernel<kDown><<<std::min(sms, max_u * t1), pass_threads(kDown), StageCfg<kDown>::kSmem,
-                                  stream>>>(W.map_gate, W.map_up, W.map_down, map_xg, map_h, map_sx, map_sh,
+                                  stream>>>(W.map_gate, W.map_up, W.map_down, map_xg, map_h8, map_sx, map_sh8,
                                             W.map_sg, W.map_su, W.map_bg, W.map_bu, W.map_sd, W.map_bd, fa);
     }
     if (tc_min > 0) {
