@@ -246,34 +246,39 @@ constexpr bool claims(int mode) { return mode == kBoth; }   // atomic queue, dow
 // consumer warps + a producer warp (+ a publisher warp when both passes share a launch)
 constexpr int pass_threads(int mode) { return 32 * (kConsumerWarps + 1 + has_publisher(mode)); }
 constexpr int kWBytes = 256 * 128;         // 256 weight rows x 32 u32 words (4 groups)
-constexpr int kTokChunk = 16;              // tokens per pass over the weights (down-only launches: 8)
+constexpr int kTokChunk = 16;              // tokens per pass over the weights (or 8, see StageCfg)
 constexpr int kSbBytes = 256 * 16;         // 256 rows x up to 8 bf16 (a table of scales or biases)
 
 // One ring stage: packed weights | activation boxes (4, or 4 hi + 4 lo; one row per token of
 // the chunk) | scales | biases | activation group sums fp32 [chunk tokens][4 groups]; a
 // 1024-byte multiple.  The scale and bias tables hold, per weight row, the 8 groups of the
 // 16-byte-aligned window that contains the stage's 4 groups ([256][8] bf16), or with 4 groups
-// per row ([256][4]) the whole row.  A gate/up-only launch has room for 4 of its smaller
-// stages; a down-only launch takes chunks of at most 8 tokens (8-row boxes), which also leaves
-// room for 4 stages; the both-pass launch uses 3 stages sized for 16-token down chunks.
-template <int MODE>
+// per row ([256][4]) the whole row.  CH tokens per chunk (a pass over the weights): 16, or for
+// a down-only launch whose experts average at most 4 tokens 8 (8-row boxes).  As many stages
+// as fit, up to 4: 4 for gate/up and for 8-token down chunks, 3 for 16-token down chunks
+// (a down-only launch with many tokens per expert, and the both-pass launch).
+constexpr int kMaxDynSmem = 227 * 1024 - 3072;   // the rest of a CTA's 227 KB holds the static arrays
+template <int MODE, int CH>
 struct StageCfg {
-    static constexpr int kCount = MODE == kBoth ? 3 : 4;
-    static constexpr int kChunk = down_only(MODE) ? 8 : kTokChunk;   // tokens per pass over the weights
-    static constexpr int kBox = kChunk * 128;                        // one activation box: kChunk rows x 64 fp16
+    static constexpr int kChunk = CH;                                // tokens per pass over the weights
+    static constexpr int kBox = kChunk * 128;                        // one activation box: CH rows x 64 fp16
     static constexpr int kXOff = kWBytes;
     static constexpr int kSOff = kXOff + (gate_up_only(MODE) ? 4 : 8) * kBox;
     static constexpr int kBOff = kSOff + kSbBytes;
     static constexpr int kSumOff = kBOff + kSbBytes;
     static constexpr int kSumBytes = kChunk * 4 * 4;
     static constexpr int kBytes = (kSumOff + kSumBytes + 1023) / 1024 * 1024;
+    static constexpr int kFit = (kMaxDynSmem - 1024) / kBytes;
+    static constexpr int kCount = kFit < 4 ? kFit : 4;
     static constexpr int kSmem = kCount * kBytes + 1024;
     // TMA bytes of a pass's stage, without the scale / bias tables
     static constexpr int tx(int pass) { return kWBytes + (pass ? 8 : 4) * kBox + kSumBytes; }
 };
-static_assert(StageCfg<kGateUp>::kSmem <= 227 * 1024 - 3072, "gate/up pass shared memory");
-static_assert(StageCfg<kDown>::kSmem <= 227 * 1024 - 3072, "down pass shared memory");
-static_assert(StageCfg<kBoth>::kSmem <= 227 * 1024 - 3072, "expert pass shared memory");
+static_assert(StageCfg<kGateUp, 16>::kCount == 4 && StageCfg<kDown, 8>::kCount == 4, "ring depth");
+static_assert(StageCfg<kDown, 16>::kCount == 3 && StageCfg<kBoth, 16>::kCount == 3, "ring depth");
+static_assert(StageCfg<kGateUp, 16>::kSmem <= kMaxDynSmem && StageCfg<kDown, 8>::kSmem <= kMaxDynSmem &&
+                  StageCfg<kDown, 16>::kSmem <= kMaxDynSmem && StageCfg<kBoth, 16>::kSmem <= kMaxDynSmem,
+              "expert pass shared memory");
 
 
 struct PassArgs {
@@ -425,11 +430,11 @@ __device__ __forceinline__ bool mailbox_post(Mailbox& M, int uu) {
 // posts the tile to the publisher, which makes them visible device-wide and counts the tile
 // for the expert's down tiles.  Publishing from a warp of its own keeps the fence's wait for
 // outstanding stores off the consumers.
-template <int NT, int PASS, int MODE, bool PK = false>
+template <int NT, int PASS, int MODE, int CH, bool PK = false>
 __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, uint32_t& it, bool& poisoned,
                                               const Tile& T, int pc, int n, int warp, int lane, float* red,
                                               int done_uu, Mailbox& M) {
-    using C = StageCfg<MODE>;
+    using C = StageCfg<MODE, CH>;
     const int g = lane >> 2, c = lane & 3;
     const int nst = a.kdim / kGroup / 4;
     float acc[2][NT][4];
@@ -652,7 +657,7 @@ __device__ __forceinline__ Claim claim_item(const FusedArgs& f, int item, int n0
     return c;
 }
 
-template <int MODE>
+template <int MODE, int CH>
 __global__ void __launch_bounds__(pass_threads(MODE), 1)
     ffn_expert_kernel(const __grid_constant__ CUtensorMap map_gate, const __grid_constant__ CUtensorMap map_up,
                      const __grid_constant__ CUtensorMap map_down, const __grid_constant__ CUtensorMap map_xg,
@@ -661,7 +666,7 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
                      const __grid_constant__ CUtensorMap map_su, const __grid_constant__ CUtensorMap map_bg,
                      const __grid_constant__ CUtensorMap map_bu, const __grid_constant__ CUtensorMap map_sd,
                      const __grid_constant__ CUtensorMap map_bd, FusedArgs f) {
-    using C = StageCfg<MODE>;
+    using C = StageCfg<MODE, CH>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[2 * C::kCount];
     // per stage: item (< 0: stop), chunk start, and the decoded tile (expert, list range, row)
@@ -866,19 +871,19 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
             if (gate_up) {
                 // both passes in this launch: publish the tile after its last chunk
                 const int done_uu = has_publisher(MODE) && pc + C::kChunk >= T.p1 ? item / t0 : -1;
-                if (n <= 8) consume_chunk<1, 0, MODE>(f.p[0], R, it, poisoned, T, pc, n, warp, lane, red, done_uu, M);
-                else consume_chunk<2, 0, MODE>(f.p[0], R, it, poisoned, T, pc, n, warp, lane, red, done_uu, M);
+                if (n <= 8) consume_chunk<1, 0, MODE, CH>(f.p[0], R, it, poisoned, T, pc, n, warp, lane, red, done_uu, M);
+                else consume_chunk<2, 0, MODE, CH>(f.p[0], R, it, poisoned, T, pc, n, warp, lane, red, done_uu, M);
             }
         }
         if constexpr (!gate_up_only(MODE)) {
             if (!gate_up) {
                 if (n <= 4)
-                    consume_chunk<1, 1, MODE, true>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
-                else if constexpr (C::kChunk <= 8)   // down-only launch: chunks of at most 8 tokens
-                    consume_chunk<1, 1, MODE>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
+                    consume_chunk<1, 1, MODE, CH, true>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
+                else if constexpr (CH <= 8)   // chunks of at most 8 tokens
+                    consume_chunk<1, 1, MODE, CH>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
                 else if (n <= 8)
-                    consume_chunk<1, 1, MODE>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
-                else consume_chunk<2, 1, MODE>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
+                    consume_chunk<1, 1, MODE, CH>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
+                else consume_chunk<2, 1, MODE, CH>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
             }
         }
         if (poisoned) break;
@@ -1037,35 +1042,41 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_done.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(ffn_expert_kernel<kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             StageCfg<kGateUp>::kSmem);
-
+        cudaError_t e = cudaFuncSetAttribute(ffn_expert_kernel<kGateUp, 16>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, StageCfg<kGateUp, 16>::kSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(ffn_expert_kernel<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     StageCfg<kDown>::kSmem);
+            e = cudaFuncSetAttribute(ffn_expert_kernel<kDown, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     StageCfg<kDown, 8>::kSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(ffn_expert_kernel<kBoth>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     StageCfg<kBoth>::kSmem);
+            e = cudaFuncSetAttribute(ffn_expert_kernel<kDown, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     StageCfg<kDown, 16>::kSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(ffn_expert_kernel<kBoth, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     StageCfg<kBoth, 16>::kSmem);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count[dev & 63], cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit);
     }
     const int sms = sm_count[dev & 63] > 0 ? sm_count[dev & 63] : 1;
 
-    // activation / group-sum maps over this call's workspace rows
-    // activation boxes of one chunk: 16 token rows; the down-only launch's chunks: 8 (map_h8, map_sh8)
-    CUtensorMap map_xg, map_h, map_sx, map_sh, map_h8, map_sh8;
+    // experts with many tokens go to the tcgen05 path; with fewer than 256 tokens in the chunk
+    // a routed expert rarely reaches the threshold, so the extra launches are skipped (the
+    // slices of a shared expert hold every token and take it from kTcMinTokens tokens on)
+    const int tc_min = (tc_path_supported(D) && (B >= 256 || (all_tokens && B >= kTcMinTokens))) ? kTcMinTokens : 0;
+    const bool both = tc_min > 0;
+    // tokens per down chunk: 8 while the experts average at most 4 tokens (then nearly all have
+    // at most 8, and the smaller stages make a 4-stage ring), else 16
+    const int ch_dn = !both && (int64_t)BK <= 4 * (int64_t)E ? 8 : kTokChunk;
+
+    // activation / group-sum maps over this call's workspace rows, one box row per chunk token
+    CUtensorMap map_xg, map_h, map_sx, map_sh;
     if (!encode_map_2d(&map_xg, xg, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, d, 64, kTokChunk,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_map_2d(&map_h, h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, 2 * F, 64, kTokChunk,
+        !encode_map_2d(&map_h, h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, 2 * F, 64, ch_dn,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_map_2d(&map_sx, sx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BK, d / kGroup, 4, kTokChunk,
                        CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_map_2d(&map_sh, sh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BK, F / kGroup, 4, kTokChunk,
-                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_map_2d(&map_h8, h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, BK, 2 * F, 64, StageCfg<kDown>::kChunk,
-                       CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_map_2d(&map_sh8, sh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BK, F / kGroup, 4, StageCfg<kDown>::kChunk,
+        !encode_map_2d(&map_sh, sh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BK, F / kGroup, 4, ch_dn,
                        CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
 
@@ -1081,10 +1092,6 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
                                                                           xg, sx, ws_ptr<__half>(ws, L.s16x), BK,
                                                                           ticket, E + 2);
 
-    // experts with many tokens go to the tcgen05 path; with fewer than 256 tokens in the chunk
-    // a routed expert rarely reaches the threshold, so the extra launches are skipped (the
-    // slices of a shared expert hold every token and take it from kTcMinTokens tokens on)
-    const int tc_min = (tc_path_supported(D) && (B >= 256 || (all_tokens && B >= kTcMinTokens))) ? kTcMinTokens : 0;
     FfnTcWeights TW{};
     TW.map_gate = W.tc_gate; TW.map_up = W.tc_up; TW.map_down = W.tc_down;
     TW.sg = W.sg; TW.bg = W.bg; TW.g_rows = W.g_rows_per_expert;
@@ -1112,21 +1119,28 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     fa.ticket = ticket;
     const int t0 = a.tiles_per_expert, t1 = b.tiles_per_expert;
 
-    if (tc_min > 0) {
+    if (both) {
         // long prompts: experts with a few tokens each run both passes from one queue
         const int grid = std::min(sms, max_u * (t0 + t1));
-        ffn_expert_kernel<kBoth><<<grid, pass_threads(kBoth), StageCfg<kBoth>::kSmem, stream>>>(
+        ffn_expert_kernel<kBoth, 16><<<grid, pass_threads(kBoth), StageCfg<kBoth, 16>::kSmem, stream>>>(
             W.map_gate, W.map_up, W.map_down, map_xg, map_h, map_sx, map_sh, W.map_sg, W.map_su, W.map_bg, W.map_bu,
             W.map_sd, W.map_bd, fa);
     } else {
-        ffn_expert_kernel<kGateUp><<<std::min(sms, max_u * t0), pass_threads(kGateUp), StageCfg<kGateUp>::kSmem,
-                                    stream>>>(W.map_gate, W.map_up, W.map_down, map_xg, map_h, map_sx, map_sh,
-                                              W.map_sg, W.map_su, W.map_bg, W.map_bu, W.map_sd, W.map_bd, fa);
-        ffn_expert_kernel<kDown><<<std::min(sms, max_u * t1), pass_threads(kDown), StageCfg<kDown>::kSmem,
-                                  stream>>>(W.map_gate, W.map_up, W.map_down, map_xg, map_h8, map_sx, map_sh8,
-                                            W.map_sg, W.map_su, W.map_bg, W.map_bu, W.map_sd, W.map_bd, fa);
+        ffn_expert_kernel<kGateUp, 16><<<std::min(sms, max_u * t0), pass_threads(kGateUp),
+                                        StageCfg<kGateUp, 16>::kSmem, stream>>>(
+            W.map_gate, W.map_up, W.map_down, map_xg, map_h, map_sx, map_sh, W.map_sg, W.map_su, W.map_bg, W.map_bu,
+            W.map_sd, W.map_bd, fa);
+        const int g1 = std::min(sms, max_u * t1);
+        if (ch_dn == 8)
+            ffn_expert_kernel<kDown, 8><<<g1, pass_threads(kDown), StageCfg<kDown, 8>::kSmem, stream>>>(
+                W.map_gate, W.map_up, W.map_down, map_xg, map_h, map_sx, map_sh, W.map_sg, W.map_su, W.map_bg,
+                W.map_bu, W.map_sd, W.map_bd, fa);
+        else
+            ffn_expert_kernel<kDown, 16><<<g1, pass_threads(kDown), StageCfg<kDown, 16>::kSmem, stream>>>(
+                W.map_gate, W.map_up, W.map_down, map_xg, map_h, map_sx, map_sh, W.map_sg, W.map_su, W.map_bg,
+                W.map_bu, W.map_sd, W.map_bd, fa);
     }
-    if (tc_min > 0) {
+    if (both) {
         for (int pass = 0; pass < 2; ++pass) {
             cudaError_t e = launch_ffn_tc(D, TW, B, pass, union_ids, n_union, offsets, token_list, slot_list, ws, L,
                                           tc_min, sms, stream);
