@@ -162,6 +162,20 @@ smoe_status check_weights(const smoe_layer_desc& D, const smoe_expert_weights* W
         P->map_su = P->map_sg;
         P->map_bu = P->map_bg;
     }
+    P->wide = F % 192 == 0;
+    if (P->wide) {
+        const uint32_t* wg = sep ? W->w_gate : W->w_gate_up;
+        const uint32_t* wu = sep ? W->w_up : W->w_gate_up;
+        const uint16_t* sg = sep ? W->s_gate : W->s_gate_up;
+        const uint16_t* bg = sep ? W->b_gate : W->b_gate_up;
+        const uint16_t* su = sep ? W->s_up : W->s_gate_up;
+        const uint16_t* bu = sep ? W->b_up : W->b_gate_up;
+        const int64_t rows = sep ? E * F : E * 2 * F;
+        if (!encode_weight_map(&P->wide_gate, wg, rows, d, 192) || !encode_weight_map(&P->wide_up, wu, rows, d, 192) ||
+            !encode_group_map(&P->wide_sg, sg, rows, d, 192) || !encode_group_map(&P->wide_bg, bg, rows, d, 192) ||
+            !encode_group_map(&P->wide_su, su, rows, d, 192) || !encode_group_map(&P->wide_bu, bu, rows, d, 192))
+            return SMOE_ERR_CUDA;
+    }
     return SMOE_OK;
 }
 

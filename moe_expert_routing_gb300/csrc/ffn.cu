@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
 }
 
 // ----------------------------------------------------------------------------- expert passes
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 8;                           // down and both-pass launches; gate/up: 8 or 12
 constexpr int kMailbox = 4;                                // finished gate/up tiles awaiting publication
 
 // Which passes a launch of the expert-pass kernel runs.
@@ -243,11 +243,9 @@ constexpr bool has_publisher(int mode) { return mode == kBoth; }
 constexpr bool gate_up_only(int mode) { return mode == kGateUp; }
 constexpr bool down_only(int mode) { return mode == kDown; }
 constexpr bool claims(int mode) { return mode == kBoth; }   // atomic queue, down tiles wait per expert
-// consumer warps + a producer warp (+ a publisher warp when both passes share a launch)
-constexpr int pass_threads(int mode) { return 32 * (kConsumerWarps + 1 + has_publisher(mode)); }
-constexpr int kWBytes = 256 * 128;         // 256 weight rows x 32 u32 words (4 groups)
+// NW consumer warps + a producer warp (+ a publisher warp when both passes share a launch)
+constexpr int pass_threads(int mode, int nw) { return 32 * (nw + 1 + has_publisher(mode)); }
 constexpr int kTokChunk = 16;              // tokens per pass over the weights (or 8, see StageCfg)
-constexpr int kSbBytes = 256 * 16;         // 256 rows x up to 8 bf16 (a table of scales or biases)
 
 // One ring stage: packed weights | activation boxes (4, or 4 hi + 4 lo; one row per token of
 // the chunk) | scales | biases | activation group sums fp32 [chunk tokens][4 groups]; a
@@ -257,9 +255,14 @@ constexpr int kSbBytes = 256 * 16;         // 256 rows x up to 8 bf16 (a table o
 // a down-only launch whose experts average at most 4 tokens 8 (8-row boxes).  As many stages
 // as fit, up to 4: 4 for gate/up and for 8-token down chunks, 3 for 16-token down chunks
 // (a down-only launch with many tokens per expert, and the both-pass launch).
+// A tile holds 32 NW weight rows (gate/up: 16 NW gate rows above 16 NW up rows; down: 32 NW
+// output rows), consumer warp w taking rows 16w.. and 16 NW + 16w.. (gate/up) or 32w.. (down).
 constexpr int kMaxDynSmem = 227 * 1024 - 3072;   // the rest of a CTA's 227 KB holds the static arrays
-template <int MODE, int CH>
+template <int MODE, int CH, int NW>
 struct StageCfg {
+    static constexpr int kRows = 32 * NW;                            // weight rows of a tile
+    static constexpr int kWBytes = kRows * 128;                      // kRows x 32 u32 words (4 groups)
+    static constexpr int kSbBytes = kRows * 16;                      // kRows x up to 8 bf16 (scales or biases)
     static constexpr int kChunk = CH;                                // tokens per pass over the weights
     static constexpr int kBox = kChunk * 128;                        // one activation box: CH rows x 64 fp16
     static constexpr int kXOff = kWBytes;
@@ -274,10 +277,12 @@ struct StageCfg {
     // TMA bytes of a pass's stage, without the scale / bias tables
     static constexpr int tx(int pass) { return kWBytes + (pass ? 8 : 4) * kBox + kSumBytes; }
 };
-static_assert(StageCfg<kGateUp, 16>::kCount == 4 && StageCfg<kDown, 8>::kCount == 4, "ring depth");
-static_assert(StageCfg<kDown, 16>::kCount == 3 && StageCfg<kBoth, 16>::kCount == 3, "ring depth");
-static_assert(StageCfg<kGateUp, 16>::kSmem <= kMaxDynSmem && StageCfg<kDown, 8>::kSmem <= kMaxDynSmem &&
-                  StageCfg<kDown, 16>::kSmem <= kMaxDynSmem && StageCfg<kBoth, 16>::kSmem <= kMaxDynSmem,
+static_assert(StageCfg<kGateUp, 16, 8>::kCount == 4 && StageCfg<kDown, 8, 8>::kCount == 4, "ring depth");
+static_assert(StageCfg<kDown, 16, 8>::kCount == 3 && StageCfg<kBoth, 16, 8>::kCount == 3, "ring depth");
+static_assert(StageCfg<kGateUp, 16, 12>::kCount == 3, "ring depth (12 consumer warps: stages of 1.5x the work)");
+static_assert(StageCfg<kGateUp, 16, 8>::kSmem <= kMaxDynSmem && StageCfg<kDown, 8, 8>::kSmem <= kMaxDynSmem &&
+                  StageCfg<kDown, 16, 8>::kSmem <= kMaxDynSmem && StageCfg<kBoth, 16, 8>::kSmem <= kMaxDynSmem &&
+                  StageCfg<kGateUp, 16, 12>::kSmem <= kMaxDynSmem,
               "expert pass shared memory");
 
 
@@ -430,11 +435,11 @@ __device__ __forceinline__ bool mailbox_post(Mailbox& M, int uu) {
 // posts the tile to the publisher, which makes them visible device-wide and counts the tile
 // for the expert's down tiles.  Publishing from a warp of its own keeps the fence's wait for
 // outstanding stores off the consumers.
-template <int NT, int PASS, int MODE, int CH, bool PK = false>
+template <int NT, int PASS, int MODE, int CH, int NW, bool PK = false>
 __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, uint32_t& it, bool& poisoned,
                                               const Tile& T, int pc, int n, int warp, int lane, float* red,
                                               int done_uu, Mailbox& M) {
-    using C = StageCfg<MODE, CH>;
+    using C = StageCfg<MODE, CH, NW>;
     const int g = lane >> 2, c = lane & 3;
     const int nst = a.kdim / kGroup / 4;
     float acc[2][NT][4];
@@ -449,8 +454,8 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
     uint32_t wrow_off0, wrow_off1;
     int lrow0, lrow1;
     if (PASS == 0) {
-        lrow0 = warp * 16;          // gate rows 16w.. of the tile
-        lrow1 = 128 + warp * 16;    // up rows
+        lrow0 = warp * 16;               // gate rows 16w.. of the tile
+        lrow1 = 16 * NW + warp * 16;     // up rows
     } else {
         lrow0 = warp * 32;
         lrow1 = warp * 32 + 16;
@@ -547,17 +552,18 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
                 red[warp * 16 + nt * 8 + 2 * c + 1] = hs[nt][1];
             }
         }
-        asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kConsumerWarps) : "memory");
+        asm volatile("bar.sync 1, %0;\n" ::"r"(32 * NW) : "memory");
         const int tid = warp * 32 + lane;
-        if (tid < 32) {
-            const int half = tid >> 4, slot = tid & 15;   // 128 columns = two 64-column groups
+        if (tid < 4 * NW) {
+            // 16 NW columns = NW / 4 groups of 64 columns, four warps each
+            const int grp = tid >> 4, slot = tid & 15;
             if (slot < n) {
-                const float s = red[(4 * half) * 16 + slot] + red[(4 * half + 1) * 16 + slot] +
-                                red[(4 * half + 2) * 16 + slot] + red[(4 * half + 3) * 16 + slot];
-                a.hsum_out[(size_t)(pc + slot) * (a.F / kGroup) + T.row / kGroup + half] = s;
+                const float s = red[(4 * grp) * 16 + slot] + red[(4 * grp + 1) * 16 + slot] +
+                                red[(4 * grp + 2) * 16 + slot] + red[(4 * grp + 3) * 16 + slot];
+                a.hsum_out[(size_t)(pc + slot) * (a.F / kGroup) + T.row / kGroup + grp] = s;
             }
         }
-        asm volatile("bar.sync 1, %0;\n" ::"r"(32 * kConsumerWarps) : "memory");
+        asm volatile("bar.sync 1, %0;\n" ::"r"(32 * NW) : "memory");
         // every consumer thread's h / sum stores happen before this point (named barrier);
         // the fence makes them visible device-wide before the count
         if (done_uu >= 0 && tid == 0 && !mailbox_post(M, done_uu)) atomicOr(a.status, SMOE_FAULT_TIMEOUT);
@@ -583,9 +589,11 @@ __device__ __forceinline__ void consume_chunk(const PassArgs& a, const Ring& R, 
 }
 
 // The expert passes as persistent kernels with a device-side work queue.  Work items, in this
-// order: the gate/up tiles (128 h columns of one union expert: consumer warp w takes gate and
-// up rows 16w..16w+15), then the down tiles (256 output rows of one union expert: consumer
-// warp w takes rows 32w..32w+31), expert-major.  A launch runs the gate/up items, the down
+// order: the gate/up tiles (16 NW h columns of one union expert: consumer warp w takes gate and
+// up rows 16w..16w+15; NW = 8, or 12 where ffn_dim is a multiple of 192 and the tiles fill the
+// SMs twice: three consumer warps per scheduler instead of two hide more of each warp's
+// latency), then the down tiles (256 output rows of one union expert: consumer warp w takes
+// rows 32w..32w+31), expert-major.  A launch runs the gate/up items, the down
 // items, or both (MODE).  The producer thread takes the next item with an atomic ticket, so
 // CTAs that draw long items (experts with many tokens) do not hold up the rest.  With both
 // passes in one launch, items are claimed in order and every item a CTA waits for has been
@@ -599,13 +607,14 @@ struct FusedArgs {
                           // down launch; [2 + u]: published gate/up tiles of union expert u
 };
 
-// OR of v over the consumer threads (named barrier 1).
+// OR of v over the NW consumer warps' threads (named barrier 1).
+template <int NW>
 __device__ __forceinline__ bool consumers_any(bool v) {
     uint32_t r;
     asm volatile(
         "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
         : "=r"(r)
-        : "r"((uint32_t)v), "r"(32 * kConsumerWarps)
+        : "r"((uint32_t)v), "r"(32 * NW)
         : "memory");
     return r != 0;
 }
@@ -657,8 +666,8 @@ __device__ __forceinline__ Claim claim_item(const FusedArgs& f, int item, int n0
     return c;
 }
 
-template <int MODE, int CH>
-__global__ void __launch_bounds__(pass_threads(MODE), 1)
+template <int MODE, int CH, int NW>
+__global__ void __launch_bounds__(pass_threads(MODE, NW), 1)
     ffn_expert_kernel(const __grid_constant__ CUtensorMap map_gate, const __grid_constant__ CUtensorMap map_up,
                      const __grid_constant__ CUtensorMap map_down, const __grid_constant__ CUtensorMap map_xg,
                      const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_sx,
@@ -666,12 +675,13 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
                      const __grid_constant__ CUtensorMap map_su, const __grid_constant__ CUtensorMap map_bg,
                      const __grid_constant__ CUtensorMap map_bu, const __grid_constant__ CUtensorMap map_sd,
                      const __grid_constant__ CUtensorMap map_bd, FusedArgs f) {
-    using C = StageCfg<MODE, CH>;
+    using C = StageCfg<MODE, CH, NW>;
+    static_assert(NW % 4 == 0 && (NW == kConsumerWarps || gate_up_only(MODE)), "consumer warps");
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[2 * C::kCount];
     // per stage: item (< 0: stop), chunk start, and the decoded tile (expert, list range, row)
     __shared__ int slot_meta[C::kCount][6];
-    __shared__ float red[kConsumerWarps * 16];
+    __shared__ float red[NW * 16];
     __shared__ __align__(8) uint64_t mbars[2 * kMailbox];
     __shared__ int mail[kMailbox];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -688,7 +698,7 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kCount; ++s) {
             mbar_init(R.full + 8 * s, 1);
-            mbar_init(R.empty + 8 * s, kConsumerWarps);   // one arrival per consumer warp
+            mbar_init(R.empty + 8 * s, NW);   // one arrival per consumer warp
         }
         for (int s = 0; s < kMailbox; ++s) {
             mbar_init(M.full + 8 * s, 1);
@@ -706,7 +716,7 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
     uint32_t it = 0;
     bool poisoned = false;
 
-    if (has_publisher(MODE) && warp == kConsumerWarps + 1) {
+    if (has_publisher(MODE) && warp == NW + 1) {
         // ---------------------------------------------------------------- publisher (one thread)
         if (lane == 0) {
             for (uint32_t k = 0;; ++k) {
@@ -725,7 +735,7 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
         return;
     }
 
-    if (warp == kConsumerWarps) {
+    if (warp == NW) {
         // ---------------------------------------------------------------- producer (one thread)
         if (lane == 0) {
             // tickets run two items ahead and the globals of an item are loaded one item ahead,
@@ -746,7 +756,7 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
                 T.e = cur.e;
                 T.p0 = cur.p0;
                 T.p1 = cur.p1;
-                T.row = (cur.j - cur.uu * a.tiles_per_expert) * (cur.pass ? 256 : 128);
+                T.row = (cur.j - cur.uu * a.tiles_per_expert) * (cur.pass ? 32 * NW : 16 * NW);
                 T.ok = T.e >= 0 && T.e < a.E && T.p0 >= 0 && T.p1 >= T.p0 && T.p1 <= a.B * a.K;
                 T.mine = a.tc_min <= 0 || T.p1 - T.p0 < a.tc_min;
                 if (!T.ok) atomicOr(a.status, SMOE_FAULT_EXPERT_INDEX);
@@ -766,12 +776,12 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
                     const int G = a.kdim / kGroup, nst = G / 4;
                     const bool packed = G == 4;
                     const uint32_t rs = packed ? 8u : 16u;
-                    const uint32_t tx = (uint32_t)C::tx(cur.pass) + 2u * 256u * rs;
+                    const uint32_t tx = (uint32_t)C::tx(cur.pass) + 2u * (uint32_t)C::kRows * rs;
                     // first rows of the tile in the weight maps
                     const int64_t r0 = (int64_t)T.e * a.wrow0 + T.row;
                     const int64_t r1 = cur.pass == 0 ? (int64_t)T.e * a.wrow1 + a.woff1 + T.row : r0;
                     // the tile's scale / bias rows into L2 ahead of the table copies
-                    const uint32_t bytes = (uint32_t)((cur.pass ? 256 : 128) * G * 2);
+                    const uint32_t bytes = (uint32_t)((cur.pass ? 32 * NW : 16 * NW) * G * 2);
                     prefetch_l2(a.s0 + r0 * G, bytes); prefetch_l2(a.b0 + r0 * G, bytes);
                     if (cur.pass == 0) { prefetch_l2(a.s1 + r1 * G, bytes); prefetch_l2(a.b1 + r1 * G, bytes); }
                     const int ty0 = (int)(packed ? r0 / 2 : r0), ty1 = (int)(packed ? r1 / 2 : r1);
@@ -795,11 +805,11 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
                             const int tx0 = packed ? 0 : (st * 4) & ~7;   // 16-byte window of the stage's groups
                             if (gate_up_only(MODE) || (MODE == kBoth && cur.pass == 0)) {
                                 tma_load_2d(base, &map_gate, st * 32, (int)r0, full);
-                                tma_load_2d(base + 128 * 128, &map_up, st * 32, (int)r1, full);
+                                tma_load_2d(base + 16 * NW * 128, &map_up, st * 32, (int)r1, full);
                                 tma_load_2d(base + C::kSOff, &map_sg, tx0, ty0, full);
-                                tma_load_2d(base + C::kSOff + 128 * rs, &map_su, tx0, ty1, full);
+                                tma_load_2d(base + C::kSOff + 16 * NW * rs, &map_su, tx0, ty1, full);
                                 tma_load_2d(base + C::kBOff, &map_bg, tx0, ty0, full);
-                                tma_load_2d(base + C::kBOff + 128 * rs, &map_bu, tx0, ty1, full);
+                                tma_load_2d(base + C::kBOff + 16 * NW * rs, &map_bu, tx0, ty1, full);
 #pragma unroll
                                 for (int q = 0; q < 4; ++q)
                                     tma_load_2d(base + C::kXOff + q * C::kBox, &map_xg, (st * 4 + q) * 64, pc,
@@ -851,7 +861,7 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
         // they run the same chunks and meet at the same named barriers; a down-only launch has
         // none, and each warp decides for itself (no cross-warp sync per chunk)
         const bool late = !mbar_wait(R.full + 8 * slot, (it / C::kCount) & 1u);
-        if (down_only(MODE) ? __any_sync(0xffffffffu, late) : consumers_any(late)) {
+        if (down_only(MODE) ? __any_sync(0xffffffffu, late) : consumers_any<NW>(late)) {
             if (threadIdx.x == 0) atomicOr(f.p[0].status, SMOE_FAULT_TIMEOUT);
             break;
         }
@@ -871,19 +881,19 @@ __global__ void __launch_bounds__(pass_threads(MODE), 1)
             if (gate_up) {
                 // both passes in this launch: publish the tile after its last chunk
                 const int done_uu = has_publisher(MODE) && pc + C::kChunk >= T.p1 ? item / t0 : -1;
-                if (n <= 8) consume_chunk<1, 0, MODE, CH>(f.p[0], R, it, poisoned, T, pc, n, warp, lane, red, done_uu, M);
-                else consume_chunk<2, 0, MODE, CH>(f.p[0], R, it, poisoned, T, pc, n, warp, lane, red, done_uu, M);
+                if (n <= 8) consume_chunk<1, 0, MODE, CH, NW>(f.p[0], R, it, poisoned, T, pc, n, warp, lane, red, done_uu, M);
+                else consume_chunk<2, 0, MODE, CH, NW>(f.p[0], R, it, poisoned, T, pc, n, warp, lane, red, done_uu, M);
             }
         }
         if constexpr (!gate_up_only(MODE)) {
             if (!gate_up) {
                 if (n <= 4)
-                    consume_chunk<1, 1, MODE, CH, true>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
+                    consume_chunk<1, 1, MODE, CH, NW, true>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
                 else if constexpr (CH <= 8)   // chunks of at most 8 tokens
-                    consume_chunk<1, 1, MODE, CH>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
+                    consume_chunk<1, 1, MODE, CH, NW>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
                 else if (n <= 8)
-                    consume_chunk<1, 1, MODE, CH>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
-                else consume_chunk<2, 1, MODE, CH>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
+                    consume_chunk<1, 1, MODE, CH, NW>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
+                else consume_chunk<2, 1, MODE, CH, NW>(f.p[1], R, it, poisoned, T, pc, n, warp, lane, red, -1, M);
             }
         }
         if (poisoned) break;
@@ -1042,17 +1052,21 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_done.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(ffn_expert_kernel<kGateUp, 16>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, StageCfg<kGateUp, 16>::kSmem);
+        cudaError_t e = cudaFuncSetAttribute(ffn_expert_kernel<kGateUp, 16, 8>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             StageCfg<kGateUp, 16, 8>::kSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(ffn_expert_kernel<kDown, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     StageCfg<kDown, 8>::kSmem);
+            e = cudaFuncSetAttribute(ffn_expert_kernel<kGateUp, 16, 12>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     StageCfg<kGateUp, 16, 12>::kSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(ffn_expert_kernel<kDown, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     StageCfg<kDown, 16>::kSmem);
+            e = cudaFuncSetAttribute(ffn_expert_kernel<kDown, 8, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     StageCfg<kDown, 8, 8>::kSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(ffn_expert_kernel<kBoth, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     StageCfg<kBoth, 16>::kSmem);
+            e = cudaFuncSetAttribute(ffn_expert_kernel<kDown, 16, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     StageCfg<kDown, 16, 8>::kSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(ffn_expert_kernel<kBoth, 16, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     StageCfg<kBoth, 16, 8>::kSmem);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count[dev & 63], cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(bit);
@@ -1102,7 +1116,10 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     a.wrow0 = W.g_rows_per_expert; a.wrow1 = W.u_rows_per_expert; a.woff1 = W.u_row_offset;
     a.s0 = W.sg; a.b0 = W.bg; a.s1 = W.su; a.b1 = W.bu;
     a.kdim = d; a.F = F; a.d = d; a.K = K; a.E = E; a.B = B;
-    a.tiles_per_expert = F / 128;
+    // gate/up tiles of 16 NW h columns: 12 consumer warps (192 columns) where ffn_dim allows it and
+    // the tiles fill the SMs at least twice, else 8 (128 columns); the both-pass launch takes 8
+    const int nw_gu = !both && W.wide && (int64_t)max_u * (F / 192) >= 2 * (int64_t)sms ? 12 : kConsumerWarps;
+    a.tiles_per_expert = F / (16 * nw_gu);
     a.tc_min = tc_min;
     a.union_ids = union_ids; a.n_union = n_union; a.offsets = offsets;
     a.token_list = token_list; a.slot_list = slot_list;
@@ -1122,21 +1139,27 @@ cudaError_t launch_ffn(const smoe_layer_desc& D, const FfnPointers& W, const uin
     if (both) {
         // long prompts: experts with a few tokens each run both passes from one queue
         const int grid = std::min(sms, max_u * (t0 + t1));
-        ffn_expert_kernel<kBoth, 16><<<grid, pass_threads(kBoth), StageCfg<kBoth, 16>::kSmem, stream>>>(
+        ffn_expert_kernel<kBoth, 16, 8><<<grid, pass_threads(kBoth, 8), StageCfg<kBoth, 16, 8>::kSmem, stream>>>(
             W.map_gate, W.map_up, W.map_down, map_xg, map_h, map_sx, map_sh, W.map_sg, W.map_su, W.map_bg, W.map_bu,
             W.map_sd, W.map_bd, fa);
     } else {
-        ffn_expert_kernel<kGateUp, 16><<<std::min(sms, max_u * t0), pass_threads(kGateUp),
-                                        StageCfg<kGateUp, 16>::kSmem, stream>>>(
-            W.map_gate, W.map_up, W.map_down, map_xg, map_h, map_sx, map_sh, W.map_sg, W.map_su, W.map_bg, W.map_bu,
-            W.map_sd, W.map_bd, fa);
+        if (nw_gu == 12)
+            ffn_expert_kernel<kGateUp, 16, 12><<<std::min(sms, max_u * t0), pass_threads(kGateUp, 12),
+                                                StageCfg<kGateUp, 16, 12>::kSmem, stream>>>(
+                W.wide_gate, W.wide_up, W.map_down, map_xg, map_h, map_sx, map_sh, W.wide_sg, W.wide_su, W.wide_bg,
+                W.wide_bu, W.map_sd, W.map_bd, fa);
+        else
+            ffn_expert_kernel<kGateUp, 16, 8><<<std::min(sms, max_u * t0), pass_threads(kGateUp, 8),
+                                               StageCfg<kGateUp, 16, 8>::kSmem, stream>>>(
+                W.map_gate, W.map_up, W.map_down, map_xg, map_h, map_sx, map_sh, W.map_sg, W.map_su, W.map_bg,
+                W.map_bu, W.map_sd, W.map_bd, fa);
         const int g1 = std::min(sms, max_u * t1);
         if (ch_dn == 8)
-            ffn_expert_kernel<kDown, 8><<<g1, pass_threads(kDown), StageCfg<kDown, 8>::kSmem, stream>>>(
+            ffn_expert_kernel<kDown, 8, 8><<<g1, pass_threads(kDown, 8), StageCfg<kDown, 8, 8>::kSmem, stream>>>(
                 W.map_gate, W.map_up, W.map_down, map_xg, map_h, map_sx, map_sh, W.map_sg, W.map_su, W.map_bg,
                 W.map_bu, W.map_sd, W.map_bd, fa);
         else
-            ffn_expert_kernel<kDown, 16><<<g1, pass_threads(kDown), StageCfg<kDown, 16>::kSmem, stream>>>(
+            ffn_expert_kernel<kDown, 16, 8><<<g1, pass_threads(kDown, 8), StageCfg<kDown, 16, 8>::kSmem, stream>>>(
                 W.map_gate, W.map_up, W.map_down, map_xg, map_h, map_sx, map_sh, W.map_sg, W.map_su, W.map_bg,
                 W.map_bu, W.map_sd, W.map_bd, fa);
     }

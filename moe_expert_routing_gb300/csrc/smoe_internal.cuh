@@ -83,6 +83,10 @@ struct FfnPointers {
     // scale / bias tables of the expert passes: bf16 [rows, in/64], box 8 groups x 128 rows
     // (gate, up) or 256 rows (down); see encode_group_map
     CUtensorMap map_sg, map_bg, map_su, map_bu, map_sd, map_bd;
+    // the gate/up views and tables again with boxes of 192 rows (a gate/up launch with 12
+    // consumer warps); set when ffn_dim is a multiple of 192 (wide)
+    bool wide;
+    CUtensorMap wide_gate, wide_up, wide_sg, wide_bg, wide_su, wide_bu;
     const uint16_t* sg; const uint16_t* bg; int64_t g_rows_per_expert;
     const uint16_t* su; const uint16_t* bu; int64_t u_rows_per_expert; int64_t u_row_offset;
     const uint16_t* sd; const uint16_t* bd;

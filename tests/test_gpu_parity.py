@@ -393,6 +393,19 @@ def test_hot_experts_many_tokens_per_expert(B, same):
 
 
 @pytest.mark.parametrize("layout", ["separate", "fused"])
+def test_wide_gate_up_tiles(layout):
+    """ffn_dim 1536 (a multiple of 192) over 64 experts with 64 tokens: 8 gate/up tiles of 192 h
+    columns per expert and more than two waves of them, so the gate/up pass runs with 12
+    consumer warps; both weight layouts (separate tensors, fused gate_up with gate rows on top)."""
+    w = W.scaled(W.WORKLOADS["toy"], num_experts=64, top_k=8, ffn_dim=1536, tokens=64, layout=layout)
+    c = Case(w)
+    out, idx, _ = c.run_layer()
+    o64, oidx, _, _ = c.oracle_layer()
+    assert np.array_equal(idx.numpy(), oidx)
+    check_outputs(out.numpy(), o64, c.x.float().numpy())
+
+
+@pytest.mark.parametrize("layout", ["separate", "fused"])
 def test_tensor_core_path_many_tokens_per_expert(layout):
     """512 tokens over 16 experts (top-4): every expert has ~128 entries (>= 32) and runs on
     the tcgen05 path (d and ffn_dim multiples of 512, B >= 256)."""
