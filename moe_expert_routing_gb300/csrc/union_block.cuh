@@ -1,5 +1,5 @@
-// Step 2 inside one CTA: the expert union of a chunk and its per-expert token lists, as device
-// functions that the standalone union kernels (union.cu) and the fused router (route.cu) share.
+// Step 2 inside one CTA: the expert union of a chunk and its per-expert token lists, as the
+// device functions of the one-warp and one-CTA union kernels (union.cu).
 //
 // Page "Layer-Major Batched Prefill", "The Inversion": the chunk's routed experts are
 // deduplicated into a UNION and every union expert is applied to each token routed to it.
@@ -9,8 +9,8 @@
 // the flat entry order t*K + k, so the output is deterministic.  An id outside [0, E) sets
 // SMOE_FAULT_EXPERT_INDEX and n_union = 0.
 //
-// The routing indices are read with ld.global.cg (L2, not the non-coherent path): in the
-// fused router they were written by other CTAs of the same kernel.
+// The routing indices are read with ld.global.cg (L2, not the non-coherent path), so the
+// functions also hold where the indices were written by other CTAs of the calling kernel.
 #pragma once
 
 #include "smoe_internal.cuh"
