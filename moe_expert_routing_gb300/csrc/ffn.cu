@@ -11,17 +11,19 @@
 // on the device):
 //   gather_kernel      x rows of every (expert, token) entry -> fp16, pair-permuted,
 //                      with per-64-group sums (xg, sx)
-//   ffn_expert_kernel  the experts with few tokens, persistent, from a device-side work
-//                      queue: gate/up projections + SwiGLU, 128 h columns of one expert per
-//                      tile, writing h (fp16, pair-permuted) and its per-group sums; the down
-//                      projection, 256 output rows of one expert per tile, writing y.  One
-//                      launch per pass, or both passes in one launch for long prompts
+//   ffn_expert_kernel  the experts with few tokens, persistent: gate/up projections + SwiGLU,
+//                      128 or 192 h columns of one expert per tile, writing h (fp16, pair-
+//                      permuted) and its per-group sums; the down projection, 256 output rows
+//                      of one expert per tile, writing the weighted slots of y.  One launch per
+//                      pass (static tile order), or both passes in one launch for long
+//                      prompts (a device-side queue)
 //   combine_kernel     residual[t] += sum_k w[t][k] * y[t*K + k], k in rank order
 //
 // The pass kernels are persistent and warp-specialised: one producer warp streams, for
 // every tile and every 256-input k-slice, the packed weight rows and the activation rows
 // (TMA, 128-byte swizzle), the activations' group sums and the rows' scales and biases (TMA)
-// into a shared-memory ring; eight consumer warps decode and multiply.
+// into a shared-memory ring; eight (or, for 192-column gate/up tiles, twelve) consumer warps
+// decode and multiply.
 // Full/empty mbarriers hand the stages back and forth, so the weight stream never drains
 // between tiles and the consumers never wait on a global load.
 //
