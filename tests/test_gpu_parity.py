@@ -392,12 +392,13 @@ def test_hot_experts_many_tokens_per_expert(B, same):
         assert torch.all(out[a:b] == out[a])
 
 
-@pytest.mark.parametrize("layout", ["separate", "fused"])
-def test_wide_gate_up_tiles(layout):
+@pytest.mark.parametrize("layout,d", [("separate", 512), ("fused", 512), ("separate", 256)])
+def test_wide_gate_up_tiles(layout, d):
     """ffn_dim 1536 (a multiple of 192) over 64 experts with 64 tokens: 8 gate/up tiles of 192 h
     columns per expert and more than two waves of them, so the gate/up pass runs with 12
-    consumer warps; both weight layouts (separate tensors, fused gate_up with gate rows on top)."""
-    w = W.scaled(W.WORKLOADS["toy"], num_experts=64, top_k=8, ffn_dim=1536, tokens=64, layout=layout)
+    consumer warps; both weight layouts (separate tensors, fused gate_up with gate rows on top),
+    and d_model 256, whose 4-group scale rows travel as the packed [rows / 2, 8] tables."""
+    w = W.scaled(W.WORKLOADS["toy"], d_model=d, num_experts=64, top_k=8, ffn_dim=1536, tokens=64, layout=layout)
     c = Case(w)
     out, idx, _ = c.run_layer()
     o64, oidx, _, _ = c.oracle_layer()
