@@ -252,11 +252,12 @@ constexpr int kTokChunk = 16;              // tokens per pass over the weights (
 // One ring stage: packed weights | activation boxes (4, or 4 hi + 4 lo; one row per token of
 // the chunk) | scales | biases | activation group sums fp32 [chunk tokens][4 groups]; a
 // 1024-byte multiple.  The scale and bias tables hold, per weight row, the 8 groups of the
-// 16-byte-aligned window that contains the stage's 4 groups ([256][8] bf16), or with 4 groups
-// per row ([256][4]) the whole row.  CH tokens per chunk (a pass over the weights): 16, or for
+// 16-byte-aligned window that contains the stage's 4 groups ([rows][8] bf16), or with 4 groups
+// per row ([rows][4]) the whole row.  CH tokens per chunk (a pass over the weights): 16, or for
 // a down-only launch whose experts average at most 4 tokens 8 (8-row boxes).  As many stages
-// as fit, up to 4: 4 for gate/up and for 8-token down chunks, 3 for 16-token down chunks
-// (a down-only launch with many tokens per expert, and the both-pass launch).
+// as fit, up to 4: 4 for 8-warp gate/up and for 8-token down chunks, 3 for 12-warp gate/up
+// (stages of 1.5x the rows) and for 16-token down chunks (a down-only launch with many tokens
+// per expert, and the both-pass launch).
 // A tile holds 32 NW weight rows (gate/up: 16 NW gate rows above 16 NW up rows; down: 32 NW
 // output rows), consumer warp w taking rows 16w.. and 16 NW + 16w.. (gate/up) or 32w.. (down).
 constexpr int kMaxDynSmem = 227 * 1024 - 3072;   // the rest of a CTA's 227 KB holds the static arrays
